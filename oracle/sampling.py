@@ -1,0 +1,367 @@
+"""Plain, slow CPU oracle of the decode-time sampling chain and the logprobs entry point.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` may import this module.  It shares no code with the CUDA library and imports
+nothing from it; both sides take their inputs from ``synth``.
+
+Every step is the plain definition from the pages, cited by page title and section:
+
+* "#19 serve: per-request temperature/top_p/top_k/min_p/penalties sampling" (the sampled chain),
+  sections "What changed" -> "min_p and the penalties", "The sampled chain is one block per
+  token", "A persistent per-request draw counter; sampled requests default top_k=20",
+  "server.py forwards the block to the engine".
+* "#3200 [Engine] OpenAI logprobs / top_logprobs / allowed_token_ids for the CUDA/HIP engine",
+  sections "Problem and result" and "Approach" (logprobs on the raw head logits before
+  penalties and temperature; top 0..20; allowed_token_ids renormalised over the named ids).
+* "#1916 OpenAI logprobs on /v1/chat/completions for the CUDA/HIP engine", "What changed".
+* "#559 Several conversations at once: batch slots, a pipelined layer split, per-stage dense
+  weights", "What it adds" item 1 (one row per batch slot, each slot sampled with its own keys
+  and Philox(seed, position)).
+
+Precision: the penalty arithmetic, the ranking it feeds and the min_p cut are float32 (IEEE
+round-to-nearest, no fused multiply-add), because they decide integers (which ids are kept and in
+what order) and the pages state them on float logits with ``logf``.  Everything on the softmax
+side (top_p mass, the draw's cumulative weights, log-sum-exp, log-probabilities) is float64.
+
+Readings taken where the pages are silent (each is listed in the design notes):
+  * the penalty applies to every vocabulary entry before top_k (the ~318M-compare figure is
+    k * V * hlen, so every entry was evaluated in every round);
+  * inside the penalty: repeat first (multiply if l <= 0, divide if l > 0), then subtract
+    count*freq + [count>0]*present in one subtraction (the llama.cpp chain the page names);
+  * top_p is measured on temperature-1 probabilities renormalised over the min_p survivors and
+    keeps the smallest prefix whose mass reaches top_p; temperature applies after both cuts;
+  * the draw picks the first survivor whose inclusive cumulative weight exceeds u * W;
+  * greedy rows (temperature <= 0) take the first entry of the penalised order;
+  * ties rank the lower index first; -0.0 equals +0.0; NaN ranks below -inf.
+"""
+from __future__ import annotations
+
+import ctypes
+import ctypes.util
+from dataclasses import dataclass
+
+import numpy as np
+
+from .philox import row_uniform
+
+BOUNDARY_EPS = 1e-6          # a top_p or draw decision this close to a boundary is "flagged"
+DEFAULT_SAMPLED_TOP_K = 20   # "#19 ...": sampled requests default to the sampler's own top_k=20
+MAX_TOP_K = 64               # "#19 ...": the sampled path requires top_k in 1..64
+MAX_TOP_LOGPROBS = 20        # "#3200 ...": top_logprobs 0..20
+
+_libm = ctypes.CDLL(ctypes.util.find_library("m"))
+_libm.logf.restype = ctypes.c_float
+_libm.logf.argtypes = [ctypes.c_float]
+
+
+def c_logf(x: float) -> np.float32:
+    """The host C library's single-precision logf, as the min_p formula names it."""
+    return np.float32(_libm.logf(ctypes.c_float(x)))
+
+
+# -------------------------------------------------------------------------------------------
+# Request keys
+# -------------------------------------------------------------------------------------------
+
+@dataclass
+class Params:
+    temperature: float = 0.0
+    top_k: int = 0
+    top_p: float = 1.0
+    min_p: float = 0.0
+    penalty_repeat: float = 1.0
+    penalty_freq: float = 0.0
+    penalty_present: float = 0.0
+    penalty_last_n: int = 64
+    seed: int = 0
+
+    @classmethod
+    def from_dict(cls, d):
+        return cls(**{k: d[k] for k in cls.__dataclass_fields__})
+
+    @property
+    def greedy(self) -> bool:
+        # "#19 ...", "server.py forwards the block": an absent temperature keeps greedy and
+        # temperature=0 means the same thing.
+        return not (np.float32(self.temperature) > 0)
+
+    @property
+    def k(self) -> int:
+        # "#19 ...", "A persistent per-request draw counter; sampled requests default top_k=20".
+        return DEFAULT_SAMPLED_TOP_K if self.top_k == 0 else int(self.top_k)
+
+
+def params_valid(p: Params) -> bool:
+    """Whether the engine can honour these keys (it refuses the rest instead of changing them)."""
+    vals = [p.temperature, p.top_p, p.min_p, p.penalty_repeat, p.penalty_freq, p.penalty_present]
+    if not all(np.isfinite(np.float32(v)) for v in vals):
+        return False
+    if not (0 <= p.top_k <= MAX_TOP_K):
+        return False
+    if not (np.float32(p.penalty_repeat) > 0):
+        return False
+    if np.float32(p.min_p) < 0:
+        return False
+    if p.penalty_last_n < 0:
+        return False
+    return True
+
+
+# -------------------------------------------------------------------------------------------
+# Steps of the chain
+# -------------------------------------------------------------------------------------------
+
+def widen(row, dtype: str) -> np.ndarray:
+    """bf16 -> fp32 is exact (the bf16 bits are the high half of the fp32 bits)."""
+    if dtype == "bf16":
+        return (np.asarray(row, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return np.asarray(row, dtype=np.float32)
+
+
+def history_counts(hist_ids, last_n: int, V: int) -> dict:
+    """Multiplicity of each id over the request's last `penalty_last_n` history tokens.
+
+    "#19 ...", "min_p and the penalties": the serve loop uploads the request's last
+    penalty_last_n tokens; ids outside [0, V) are not vocabulary entries and are skipped.
+    """
+    hist_ids = np.asarray(hist_ids, dtype=np.int64)
+    h = min(int(last_n), hist_ids.size)
+    window = hist_ids[hist_ids.size - h:] if h > 0 else hist_ids[:0]
+    counts = {}
+    for t in window.tolist():
+        if 0 <= t < V:
+            counts[t] = counts.get(t, 0) + 1
+    return counts
+
+
+def penalties_neutral(p: Params) -> bool:
+    return (np.float32(p.penalty_repeat) == 1 and np.float32(p.penalty_freq) == 0
+            and np.float32(p.penalty_present) == 0)
+
+
+def apply_penalties(row32: np.ndarray, counts: dict, r: float, f: float, pres: float) -> np.ndarray:
+    """The llama.cpp-style penalty set on every id with count c > 0, in float32.
+
+    "#19 ...", "min_p and the penalties": the repeat penalty multiplies non-positive logits and
+    divides positive ones; the frequency penalty is freq * count; the presence penalty is a
+    boolean (present when the count is positive), not the count.
+    """
+    out = np.array(row32, dtype=np.float32, copy=True)
+    if not counts:
+        return out
+    ids = np.fromiter(counts.keys(), dtype=np.int64)
+    c = np.fromiter(counts.values(), dtype=np.int64)
+    r32, f32_, p32 = np.float32(r), np.float32(f), np.float32(pres)
+    x = out[ids]
+    x = np.where(x <= np.float32(0), x * r32, x / r32).astype(np.float32)
+    sub = (c.astype(np.float32) * f32_ + np.where(c > 0, p32, np.float32(0))).astype(np.float32)
+    out[ids] = (x - sub).astype(np.float32)
+    return out
+
+
+def rank_order(values32: np.ndarray) -> np.ndarray:
+    """All ids ordered by value descending, ties to the lowest index, NaN last.
+
+    "#19 ...", "The sampled chain is one block per token": k argmax rounds whose ties resolve to
+    the lowest index (the serial scan's strict >); the first k entries of this order are the k
+    rounds' winners in order.
+    """
+    v = np.asarray(values32, dtype=np.float32).astype(np.float64)
+    idx = np.arange(v.size)
+    return np.lexsort((idx, -v))
+
+
+def min_p_cut(sel: np.ndarray, min_p: float) -> int:
+    """Kept prefix length after min_p, in logit space, float32.
+
+    "#19 ...", "min_p and the penalties": keep the prefix with sel_logit >= sel_logit[0] +
+    logf(min_p); 0 disables; the head always survives so the kept count never reaches zero.
+    """
+    k = sel.size
+    if not (np.float32(min_p) > 0):
+        return k
+    thr = np.float32(sel[0]) + c_logf(float(np.float32(min_p)))
+    kept = int(np.count_nonzero(sel.astype(np.float32) >= np.float32(thr)))
+    return max(1, kept)
+
+
+def top_p_cut(sel: np.ndarray, m1: int, top_p: float):
+    """Kept prefix length after top_p over the min_p survivors; returns (m2, flagged).
+
+    Reading: probabilities at temperature 1 renormalised over the m1 survivors (min_p runs
+    first "so the two cuts compose"); keep the smallest prefix whose mass reaches top_p.
+    """
+    tp = float(np.float32(top_p))
+    if tp >= 1.0:
+        return m1, False
+    if tp <= 0.0:
+        return 1, False
+    v = sel[:m1].astype(np.float64)
+    q = np.exp(v - v[0])
+    cum = np.cumsum(q) / np.sum(q)
+    m2 = int(np.argmax(cum >= tp)) + 1 if np.any(cum >= tp) else m1
+    flagged = bool(np.any(np.abs(cum - tp) < BOUNDARY_EPS))
+    return m2, flagged
+
+
+def draw_index(sel: np.ndarray, m2: int, temperature: float, u: float):
+    """Index of the drawn survivor; returns (j, flagged).
+
+    Temperature scales the kept logits, the weights are exp((l_i - l_0) / T), and the pick is the
+    first survivor whose inclusive cumulative weight exceeds u * W.
+    """
+    v = sel[:m2].astype(np.float64)
+    w = np.exp((v - v[0]) / float(np.float32(temperature)))
+    cum = np.cumsum(w)
+    W = cum[-1]
+    hit = np.nonzero(cum > u * W)[0]
+    j = int(hit[0]) if hit.size else m2 - 1
+    flagged = bool(np.any(np.abs(cum / W - u) < BOUNDARY_EPS))
+    return j, flagged
+
+
+def log_softmax(raw32: np.ndarray) -> np.ndarray:
+    """log-probabilities of the raw head logits in float64 (LSE with the max subtracted)."""
+    l = np.asarray(raw32, dtype=np.float32).astype(np.float64)
+    m = np.max(l)
+    lse = m + np.log(np.sum(np.exp(l - m)))
+    return l - lse
+
+
+def allowed_renorm(raw32: np.ndarray, allowed) -> np.ndarray:
+    """log-probabilities renormalised over exactly the named ids, in the caller's order.
+
+    "#3200 ...", "Problem and result": allowed_token_ids returns a distribution renormalised over
+    exactly the ids the caller named.  Reading: a repeated id counts once in the normaliser and is
+    reported at every place it was named; an id outside [0, V) is reported as NaN and ignored.
+    """
+    l = np.asarray(raw32, dtype=np.float32).astype(np.float64)
+    a = np.asarray(allowed, dtype=np.int64)
+    V = l.size
+    ok = (a >= 0) & (a < V)
+    out = np.full(a.size, np.nan)
+    if not np.any(ok):
+        return out
+    uniq = np.unique(a[ok])
+    m = np.max(l[uniq])
+    lse_a = m + np.log(np.sum(np.exp(l[uniq] - m)))
+    out[ok] = l[a[ok]] - lse_a
+    return out
+
+
+# -------------------------------------------------------------------------------------------
+# Whole rows
+# -------------------------------------------------------------------------------------------
+
+def sample_row(raw32, p: Params, hist_ids, position: int, counter: int):
+    """One row of the sampled chain (or the greedy argmax); returns a dict of every decision.
+
+    Chain order from "#19 ...": penalties over the history window -> top_k (ties to the lowest
+    index) -> min_p -> top_p -> temperature -> Philox(seed, position) draw at the slot's counter.
+    """
+    V = raw32.size
+    if penalties_neutral(p) or p.penalty_last_n <= 0 or hist_ids is None:
+        counts = {}
+    else:
+        counts = history_counts(hist_ids, p.penalty_last_n, V)
+    pen = apply_penalties(raw32, counts, p.penalty_repeat, p.penalty_freq, p.penalty_present)
+    order = rank_order(pen)
+    res = dict(greedy=p.greedy, flag_top_p=False, flag_draw=False, u=None)
+    if p.greedy:
+        res.update(id=int(order[0]), topk_ids=order[:1].copy(), topk_vals=pen[order[:1]],
+                   m1=1, m2=1, j=0)
+        return res
+    k = min(p.k, V)
+    sel_ids = order[:k]
+    sel = pen[sel_ids]
+    m1 = min_p_cut(sel, p.min_p)
+    m2, f_tp = top_p_cut(sel, m1, p.top_p)
+    u = row_uniform(p.seed, position, counter)
+    j, f_dr = draw_index(sel, m2, p.temperature, u)
+    res.update(id=int(sel_ids[j]), topk_ids=sel_ids.copy(), topk_vals=sel.copy(), m1=m1, m2=m2,
+               j=j, u=u, flag_top_p=f_tp, flag_draw=f_dr)
+    return res
+
+
+def logprobs_row(raw32, chosen, top_n: int, allowed=None):
+    """The logprobs of one row from its raw (pre-penalty, pre-temperature) logits.
+
+    "#3200 ...", "Approach": the value comes from the verify window's head logits before
+    sampling, penalties and temperature; one entry per token with up to 20 top alternatives.
+    """
+    lp = log_softmax(raw32)
+    V = lp.size
+    res = {}
+    if chosen is not None:
+        res["chosen_lp"] = float(lp[chosen]) if 0 <= chosen < V else float("nan")
+    n = int(top_n)
+    order = rank_order(raw32)[:n]
+    ids = np.full(n, -1, dtype=np.int64)
+    lps = np.full(n, -np.inf)
+    ids[:order.size] = order
+    lps[:order.size] = lp[order]
+    res["top_ids"], res["top_lps"] = ids, lps
+    if allowed is not None:
+        res["allowed_lps"] = allowed_renorm(raw32, allowed)
+    return res
+
+
+# -------------------------------------------------------------------------------------------
+# Whole calls, with the per-slot counter semantics
+# -------------------------------------------------------------------------------------------
+
+def _slot_history(w, s):
+    if w.get("hist") is None or w.get("hist_off") is None or s >= w["n_hist_slots"]:
+        return None
+    off = w["hist_off"]
+    return w["hist"][off[s]:off[s + 1]]
+
+
+def sample_call(w, counters=None, top_n=None, with_allowed=True):
+    """One batched sampling call over workload dict `w` (see ``synth``); mirrors the library call.
+
+    Every row reads its slot's draw counter as it stood before the call; afterwards each slot
+    that had at least one sampled row advances by exactly one ("#19 ...": the Philox draw
+    counter persists across a request's verify windows).  Returns (rows, new_counters).
+    """
+    counters = dict(w["counters"] if counters is None else counters)
+    top_n = w["top_n"] if top_n is None else top_n
+    V, dtype = w["V"], w["dtype"]
+    rows = []
+    sampled_slots = set()
+    for b in range(w["B"]):
+        s = int(w["row_slot"][b])
+        raw = widen(w["logits"][b, :V], dtype)
+        if s not in w["slot_params"]:
+            rows.append(dict(id=-1, invalid=True))
+            continue
+        p = Params.from_dict(w["slot_params"][s])
+        r = sample_row(raw, p, _slot_history(w, s), int(w["row_pos"][b]), counters.get(s, 0))
+        if not p.greedy:
+            sampled_slots.add(s)
+        allowed = None
+        if with_allowed and w.get("allowed_off") is not None:
+            off = w["allowed_off"]
+            allowed = w["allowed"][off[b]:off[b + 1]]
+        r.update(logprobs_row(raw, r["id"], top_n, allowed))
+        rows.append(r)
+    for s in sampled_slots:
+        counters[s] = counters.get(s, 0) + 1
+    return rows, counters
+
+
+def logprobs_call(w, chosen=None, top_n=None):
+    """One batched logprobs call (no sampling): chosen lp, top-N raw alternatives, allowed subset."""
+    top_n = w["top_n"] if top_n is None else top_n
+    V, dtype = w["V"], w["dtype"]
+    chosen = w.get("chosen") if chosen is None else chosen
+    out = []
+    for b in range(w["B"]):
+        raw = widen(w["logits"][b, :V], dtype)
+        allowed = None
+        if w.get("allowed_off") is not None:
+            off = w["allowed_off"]
+            allowed = w["allowed"][off[b]:off[b + 1]]
+        c = None if chosen is None else int(chosen[b])
+        out.append(logprobs_row(raw, c, top_n, allowed))
+    return out

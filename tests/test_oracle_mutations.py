@@ -1,0 +1,57 @@
+"""Planted mistakes in a copy of the oracle must each fail the pin suite (CPU only).
+
+Every mutation below is a plausible slip in writing the chain down (a swapped branch, a dropped
+or extra term, a flipped sign or comparison, a wrong index or word, the cuts in the wrong order).
+The test copies ``oracle/``, ``synth/`` and ``tests/`` to a temporary folder, plants one mistake,
+runs ``test_oracle_pins.py`` there and requires it to fail.  Nothing here touches a GPU.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = [
+    ("sampling.py", "x * r32, x / r32", "x / r32, x * r32"),
+    ("sampling.py", "np.where(c > 0, p32, np.float32(0))", "c.astype(np.float32) * p32"),
+    ("sampling.py", "(x - sub)", "(x + sub)"),
+    ("sampling.py", "window = hist_ids[hist_ids.size - h:]", "window = hist_ids[:h]"),
+    ("sampling.py", "np.lexsort((idx, -v))", "np.lexsort((-idx, -v))"),
+    ("sampling.py", "sel.astype(np.float32) >= np.float32(thr)", "sel.astype(np.float32) > np.float32(thr)"),
+    ("sampling.py", "thr = np.float32(sel[0]) + c_logf", "thr = np.float32(sel[0]) - c_logf"),
+    ("sampling.py", "q = np.exp(v - v[0])", "q = np.exp((v - v[0]) / 0.7)"),
+    ("sampling.py", "cum = np.cumsum(q) / np.sum(q)", "cum = np.cumsum(q[::-1])[::-1] / np.sum(q)"),
+    ("sampling.py", "hit = np.nonzero(cum > u * W)[0]", "hit = np.nonzero(cum >= u * W)[0]"),
+    ("sampling.py", "w = np.exp((v - v[0]) / float(np.float32(temperature)))",
+     "w = np.exp((v - v[0]) * float(np.float32(temperature)))"),
+    ("sampling.py", "lse = m + np.log(np.sum(np.exp(l - m)))", "lse = np.log(np.sum(np.exp(l - m)))"),
+    ("sampling.py", "uniq = np.unique(a[ok])", "uniq = a[ok]"),
+    ("sampling.py", "m1 = min_p_cut(sel, p.min_p)\n    m2, f_tp = top_p_cut(sel, m1, p.top_p)",
+     "m2, f_tp = top_p_cut(sel, k, p.top_p)\n    m1 = min(m2, min_p_cut(sel, p.min_p)); m2 = m1"),
+    ("sampling.py", "counters[s] = counters.get(s, 0) + 1", "counters[s] = counters.get(s, 0) + 2"),
+    ("sampling.py", "return DEFAULT_SAMPLED_TOP_K if self.top_k == 0 else int(self.top_k)",
+     "return int(self.top_k) or 1"),
+    ("philox.py", "c0, c1, c2, c3 = (hi1 ^ c1 ^ k0) & MASK32, lo1, (hi0 ^ c3 ^ k1) & MASK32, lo0",
+     "c0, c1, c2, c3 = (hi0 ^ c1 ^ k0) & MASK32, lo1, (hi1 ^ c3 ^ k1) & MASK32, lo0"),
+    ("philox.py", "(position & MASK32, position >> 32, counter & MASK32, counter >> 32)",
+     "(counter & MASK32, counter >> 32, position & MASK32, position >> 32)"),
+    ("philox.py", "return (out[0] >> 8) * (2.0 ** -24)", "return (out[1] >> 8) * (2.0 ** -24)"),
+]
+
+
+@pytest.mark.parametrize("fn,old,new", MUTATIONS, ids=[f"{m[0]}:{i}" for i, m in enumerate(MUTATIONS)])
+def test_planted_mistake_is_caught(tmp_path, fn, old, new):
+    for d in ("oracle", "synth", "tests"):
+        shutil.copytree(os.path.join(ROOT, d), tmp_path / d,
+                        ignore=shutil.ignore_patterns("__pycache__", "*.pyc"))
+    target = tmp_path / "oracle" / fn
+    src = target.read_text()
+    assert old in src, "mutation anchor vanished from the oracle"
+    target.write_text(src.replace(old, new))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        str(tmp_path / "tests" / "test_oracle_pins.py")],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"planted mistake survived: {new!r}"
