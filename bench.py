@@ -1,0 +1,436 @@
+"""Throughput of the fused decode-time sampler on GB300.
+
+One step = one strata_sample_rows call over one batch: the logprobs workload (8 fp32 rows, V=248,320,
+N(0,3^2) logits with 1-5 spikes), every row a sampled request with the single-row request's keys
+(penalties over a 64-token history, top_k 20, min_p 0.05, top_p 0.95, T 0.8, Philox draw), fused
+with top_logprobs=20, the sampled token's log-probability and allowed_token_ids subsets of 5, 100 and
+1000 ids.  That runs every step of the hot path in one launch.
+
+  value      rows/s over exactly K timed steps: one CUDA graph holding the K calls, replayed once;
+             inputs rotate over enough distinct batches to exceed 4x the L2 size (HBM serves reads).
+  e2e        the same metric through the C ABI from pinned host buffers: every step copies its
+             inputs host->device, runs the call and copies every output back.
+  roofline   algorithmic bytes per launch / average launch time, against the measured HBM copy
+             bandwidth; `traffic` is the DRAM bytes per launch from the committed ncu summary when
+             the kernel source still matches it.
+  cpu_baseline  the CPU oracle (plain numpy) on a bounded sample of the same workload, 1 core.
+
+`--impl reference` times the CPU oracle alone on the same workload (one row per step).
+Multi-GPU (torchrun): every rank runs its own batch stream (weak scaling, no collective on the data
+path); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "sampled rows/s and achieved HBM GB/s (fraction of GB300 peak) at V=248,320"
+UNIT = "rows/s"
+WORKLOAD = ("logprobs workload fused with sampling: B=8 fp32 rows x V=248,320, N(0,3^2)+1..5 spikes; "
+            "per-row keys top_k=20 T=0.8 top_p=0.95 min_p=0.05 repeat=1.1 freq=0.1 presence=0.1 "
+            "penalty_last_n=64; top_logprobs=20, chosen-token logprob, allowed_token_ids of 5/100/1000")
+KERNEL_SOURCES = ("request_token_sampling_gb300/csrc/strata_kernel.cuh",
+                  "request_token_sampling_gb300/csrc/strata_device.cuh",
+                  "request_token_sampling_gb300/csrc/strata_sample.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_config4_fused.json")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes a launch must move at least: logits once, history windows, allowed ids, row arrays,
+    slot keys and counters, and every output."""
+    B, V = w["B"], w["V"]
+    esz = 4 if w["dtype"] == "f32" else 2
+    n = B * V * esz
+    for s in range(w["n_hist_slots"]):
+        ln = w["slot_params"][s]["penalty_last_n"]
+        n += 4 * min(ln, int(w["hist_off"][s + 1] - w["hist_off"][s]))
+    n_allowed = int(w["allowed_off"][-1]) if w.get("allowed_off") is not None else 0
+    n += 4 * n_allowed + 4 * (B + 1) + 4 * (w["n_hist_slots"] + 1)          # allowed ids, offsets
+    n += B * (4 + 8)                                                          # row slot + position
+    n += len(w["slot_params"]) * (48 + 8 + 4)                                 # slot keys, counter
+    n += B * (4 + 4 + w["top_n"] * 8) + 4 * n_allowed                         # outputs
+    return n
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank number over all ranks (the slowest rank sets the job's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: every rank processes its own rows (weak scaling)."""
+    return world * rows_per_rank / seconds
+
+
+# ------------------------------------------------------------------------------ clocks (NVML)
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str | None):
+        self.ok = False
+        self.samples = []
+        self._stop = threading.Event()
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            rc = -1
+            if pci_bus_id:
+                rc = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h))
+            if rc != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            pass
+
+    def _read(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c))
+        self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r))
+        return int(c.value), int(r.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.samples.append(self._read())
+            time.sleep(0.001)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+            self.samples.append(self._read())
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        mhz = [m for m, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = [n for b, n in self.REASONS.items() if bits & b]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle timing
+def oracle_rows_per_s(w, budget_s=15.0, max_rows=400):
+    """Time the unmodified oracle on rows of the workload (fused sample + logprobs + allowed)."""
+    import oracle
+    t0 = time.perf_counter()
+    rows = 0
+    counters = dict(w["counters"])
+    while True:
+        b = rows % w["B"]
+        wb = dict(w)
+        wb["B"] = 1
+        wb["logits"] = w["logits"][b:b + 1]
+        wb["row_slot"] = w["row_slot"][b:b + 1]
+        wb["row_pos"] = w["row_pos"][b:b + 1]
+        off = w["allowed_off"]
+        wb["allowed"] = w["allowed"][off[b]:off[b + 1]]
+        wb["allowed_off"] = np.array([0, off[b + 1] - off[b]], np.int32)
+        _, counters = oracle.sample_call(wb, counters=counters)
+        rows += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or rows >= max_rows:
+            return rows / el, rows, el
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = synth.config4(fused=True)
+    import oracle
+    counters = dict(w["counters"])
+
+    def step(i):
+        nonlocal counters
+        b = i % w["B"]
+        wb = dict(w)
+        wb["B"] = 1
+        wb["logits"] = w["logits"][b:b + 1]
+        wb["row_slot"] = w["row_slot"][b:b + 1]
+        wb["row_pos"] = w["row_pos"][b:b + 1]
+        off = w["allowed_off"]
+        wb["allowed"] = w["allowed"][off[b]:off[b + 1]]
+        wb["allowed_off"] = np.array([0, off[b + 1] - off[b]], np.int32)
+        _, counters = oracle.sample_call(wb, counters=counters)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    v = args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32(penalty,ranking)+f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "rows_per_step": 1},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} timed rows of the 8-row batch, one row per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def make_batches(w, R, dev):
+    """R distinct device batches with the workload's recipe (batch 0 is the workload itself)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(0x5EED0004)
+    out = [torch.from_numpy(w["logits"]).to(dev)]
+    B, V = w["B"], w["V"]
+    for _ in range(R - 1):
+        x = torch.randn((B, V), generator=g, device=dev) * 3.0
+        n = torch.randint(1, 6, (B,), generator=g, device=dev)
+        for b in range(B):
+            ids = torch.randint(0, V, (int(n[b]),), generator=g, device=dev)
+            x[b, ids] = torch.rand((int(n[b]),), generator=g, device=dev) * 7.0 + 8.0
+        out.append(x.contiguous())
+    return out
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from request_token_sampling_gb300 import STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL, Sampler
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    w = synth.config4(fused=True)
+    B = w["B"]
+    step_bytes = B * w["V"] * 4
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    R = max(2, -(-4 * l2 // step_bytes))
+    flags = 0 if args.no_pdl else (STRATA_FLAG_PDL | (STRATA_FLAG_EARLY_LOAD if args.early_load else 0))
+
+    s = Sampler(device=local, max_slots=16, max_vocab=w["V"], max_rows=B)
+    for slot, p in w["slot_params"].items():
+        s.restore_slot(slot, p, 0)
+    ten = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    row_slot, row_pos = ten(w["row_slot"]), ten(w["row_pos"])
+    hist, hist_off = ten(w["hist"]), ten(w["hist_off"])
+    allowed, allowed_off = ten(w["allowed"]), ten(w["allowed_off"])
+    batches = make_batches(w, R, dev)
+    out = s.sample(batches[0], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
+                   chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags)
+    torch.cuda.synchronize()
+    if s.errors() != 0:
+        raise RuntimeError("device error bits set")
+    shape = s.shape(0, 0, B, w["V"], w["top_n"], flags)
+
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def call(i):
+        s.sample(batches[i % R], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
+                 chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags, stream=stream, out=out)
+
+    # the K timed steps as one CUDA graph (the calls advance the device counters on replay)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                call(i)
+        warm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(warm, stream=stream):
+            for i in range(max(args.warmup, 1)):
+                call(i)
+    torch.cuda.synchronize()
+    # untimed: bring clocks up, then exactly W warm-up steps
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 0.5
+        while time.perf_counter() < t_end:
+            warm.replay()
+            stream.synchronize()
+        warm.replay()
+    stream.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    bus = getattr(props, "pci_bus_id", None)
+    bus_str = None
+    if bus is not None:
+        bus_str = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), bus, getattr(props, "pci_device_id", 0))
+    clk = ClockSampler(bus_str)
+    with clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    if world > 1:
+        dist.barrier()
+    if s.errors() != 0:
+        raise RuntimeError("device error bits set after the timed region")
+    per_launch_s = ms / 1e3 / args.steps
+    value = job_rows_per_s(B * args.steps, world, ms / 1e3)
+
+    # ---- e2e through the C ABI from pinned host buffers -------------------------------------
+    K_e2e = max(3, min(args.steps, 200))
+    h_logits = [torch.from_numpy(w["logits"]).pin_memory()]
+    h_small = {k: torch.from_numpy(np.ascontiguousarray(w[k])).pin_memory()
+               for k in ("row_slot", "row_pos", "hist", "hist_off", "allowed", "allowed_off")}
+    d_logits = torch.empty_like(batches[0])
+    d_small = {k: torch.empty_like(v, device=dev) for k, v in h_small.items()}
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = int(h_logits[0].numel() * 4 + sum(v.numel() * v.element_size() for v in h_small.values()))
+    d2h = int(sum(v.numel() * v.element_size() for v in out.values()))
+
+    def e2e_step():
+        d_logits.copy_(h_logits[0], non_blocking=True)
+        for k, v in h_small.items():
+            d_small[k].copy_(v, non_blocking=True)
+        s.sample(d_logits, d_small["row_slot"], d_small["row_pos"], hist=d_small["hist"],
+                 hist_off=d_small["hist_off"], top_n=w["top_n"], chosen_lp=True, allowed=d_small["allowed"],
+                 allowed_off=d_small["allowed_off"], flags=flags, stream=stream, out=out)
+        for k, v in out.items():
+            h_out[k].copy_(v, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(K_e2e):
+            e2e_step()
+        a1.record(stream)
+        stream.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), dev)
+    e2e_value = job_rows_per_s(B * K_e2e, world, e2e_ms / 1e3)
+
+    if rank != 0:
+        s.close()
+        return
+    alg = algorithmic_bytes(w)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+    achieved = alg / per_launch_s / 1e9
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        tj = json.load(open(TRAFFIC_FILE))
+        if tj.get("kernel_hash") == kernel_hash():
+            traffic = tj.get("dram_bytes_per_launch")
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rps, nrows, el = oracle_rows_per_s(w, budget_s=args.cpu_budget)
+        cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{nrows} rows of the same 8-row workload (fused sample + logprobs + allowed), "
+                         f"{el:.1f} s on 1 host core"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows_per_step": B, "V": w["V"], "logits_dtype": "f32",
+                   "l2_policy": f"inputs rotate over {R} distinct batches ({R * step_bytes / 1e6:.0f} MB, "
+                                f">= 4x the {l2 / 1e6:.0f} MB L2)",
+                   "launch": "one CUDA graph of the K calls" + (", programmatic dependent launch" if flags & 1 else "")
+                             + (", early logit loads" if flags & 2 else ""),
+                   "split": shape["split"], "chunk_elems": shape["chunk"], "smem_bytes": shape["smem"],
+                   "grid": shape["grid"], "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": alg, "launch_us": per_launch_s * 1e6},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": K_e2e},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    s.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["own", "reference"], default="own")
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--early-load", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * strata_sample.h -- C ABI of the GB300 decode-time token sampler.
+ *
+ * One library call samples one token for each of B head-logit rows (verify-window positions or
+ * batch slots) in a single kernel launch, and optionally reports raw-logit log-probabilities.
+ * Definitions follow the pages of the engine this library serves:
+ *   [P19]   "#19 serve: per-request temperature/top_p/top_k/min_p/penalties sampling",
+ *           section "What changed" (paragraphs "min_p and the penalties", "The sampled chain is
+ *           one block per token", "A persistent per-request draw counter; sampled requests
+ *           default top_k=20", "server.py forwards the block to the engine").
+ *   [P3200] "#3200 [Engine] OpenAI logprobs / top_logprobs / allowed_token_ids for the CUDA/HIP
+ *           engine", sections "Problem and result" and "Approach".
+ *   [P1916] "#1916 OpenAI logprobs on /v1/chat/completions for the CUDA/HIP engine",
+ *           section "What changed".
+ *   [P559]  "#559 Several conversations at once: batch slots, a pipelined layer split, per-stage
+ *           dense weights", section "What it adds", item 1 (one row per slot, per-slot keys,
+ *           Philox(seed, position)).
+ *
+ * Conventions for every call:
+ *   - Device pointers are plain CUDA device addresses owned by the caller; the library reads and
+ *     writes them only from work it enqueues on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream).  Host pointers are read before the call returns.
+ *   - Calls that take a stream are asynchronous unless stated otherwise: outputs are valid once
+ *     the stream has reached the call's work.
+ *   - Every call returns STRATA_OK (0) or a negative STRATA_E* code; strata_last_error() then
+ *     holds a one-line message for the calling thread.  Argument checks run before any work is
+ *     enqueued, so a call that returns an error has launched nothing and written nothing.
+ *   - A context serves one stream at a time: calls on one context must be ordered (one stream,
+ *     or synchronised streams).  Calls on different contexts are independent.
+ *   - The calling thread's current CUDA device must be the context's device.
+ */
+#ifndef STRATA_SAMPLE_H
+#define STRATA_SAMPLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---------------------------------------------------------------------- */
+#define STRATA_OK        0
+#define STRATA_EINVAL  (-1)   /* a parameter or shape is invalid                                 */
+#define STRATA_EALIGN  (-2)   /* a logit pointer or row stride is not 16-byte aligned            */
+#define STRATA_ERANGE  (-3)   /* slot, rows or vocabulary above the limits given at create time  */
+#define STRATA_ECUDA   (-4)   /* a CUDA runtime call failed (message in strata_last_error)       */
+#define STRATA_ENOMEM  (-5)   /* device or host allocation failed at create time                 */
+
+/* ---- logit element types ----------------------------------------------------------------- */
+#define STRATA_DTYPE_F32   0  /* IEEE float32 rows                                               */
+#define STRATA_DTYPE_BF16  1  /* bfloat16 rows; widened to float32 exactly                       */
+
+/* ---- limits ------------------------------------------------------------------------------ */
+#define STRATA_MAX_TOP_K           64   /* [P19]: the sampled path requires top_k in 1..64       */
+#define STRATA_DEFAULT_TOP_K       20   /* [P19]: sampled requests default to top_k=20           */
+#define STRATA_MAX_TOP_N           20   /* [P3200]: top_logprobs 0..20                           */
+#define STRATA_DEFAULT_LAST_N      64   /* [P19]: a penalty without a window uses 64 tokens      */
+#define STRATA_MAX_PENALTY_LAST_N  4096 /* library limit on the penalty history window           */
+#define STRATA_MAX_VOCAB           524288 /* library limit on V (per-row split over <= 16 SMs)   */
+
+/* ---- launch flags (strata_sample_rows / strata_logprobs_rows `flags`) --------------------- */
+/* Launch with programmatic dependent launch: the kernel may be scheduled while the previous
+ * kernel on the stream finishes; it waits for that kernel before reading any input.            */
+#define STRATA_FLAG_PDL         0x1u
+/* With STRATA_FLAG_PDL: the caller asserts that the logit rows were complete before the previous
+ * kernel on the stream started (they are not that kernel's output).  The kernel then starts its
+ * logit loads before waiting for the previous kernel; slot state is still read after the wait.  */
+#define STRATA_FLAG_EARLY_LOAD  0x2u
+/* Testing aid: force the number of thread blocks (1..16) that split each row; 0 = automatic.   */
+#define STRATA_FLAG_SPLIT(n)    (((uint32_t)(n) & 0x1Fu) << 8)
+
+/* ---- device error bits (strata_read_errors) ---------------------------------------------- */
+#define STRATA_DEVERR_SLOT      0x01u  /* a row named a slot outside [0, max_slots): out id -1  */
+#define STRATA_DEVERR_ALLOWED   0x02u  /* an allowed id outside [0, V): its output is NaN       */
+#define STRATA_DEVERR_CHOSEN    0x04u  /* a chosen id outside [0, V): its logprob is NaN        */
+#define STRATA_DEVERR_TIMEOUT   0x08u  /* a bounded device wait ran out (outputs of that call
+                                          are not valid)                                        */
+#define STRATA_DEVERR_NOCAND    0x10u  /* a row had no orderable logit (all NaN): out id -1     */
+#define STRATA_DEVERR_HISTORY   0x20u  /* the history table of a row overflowed (not expected)  */
+#define STRATA_DEVERR_SHAPE     0x40u  /* a slot's top_k exceeded the launch shape: a call captured
+                                          in a CUDA graph before the slot's keys grew; the row kept
+                                          fewer survivors.  Re-capture after raising top_k.      */
+
+typedef struct strata_ctx strata_ctx;
+
+/*
+ * A request's sampling keys [P19, "What changed": the GEN keys temperature=, top_p=, top_k=,
+ * min_p=, penalty_repeat=, penalty_freq=, penalty_present=, penalty_last_n=, seed=].
+ * Plain data; `struct_size` must be at least sizeof(strata_sampling_params) as defined here
+ * (a larger value from a newer caller is accepted and the unknown tail is ignored).
+ */
+typedef struct strata_sampling_params {
+  uint32_t struct_size;
+  float    temperature;      /* > 0: sampled row.  <= 0: greedy argmax of the penalised logits
+                                ([P19]: absent temperature and temperature=0 both mean greedy)   */
+  int32_t  top_k;            /* sampled rows: 1..64 survivors; 0 means 20 [P19]; else EINVAL     */
+  float    top_p;            /* nucleus mass over the min_p survivors; >= 1 disables; <= 0 keeps
+                                the head only                                                     */
+  float    min_p;            /* >= 0; 0 disables; keep sel_logit >= sel_logit[0] + logf(min_p),
+                                the head always kept [P19]                                        */
+  float    penalty_repeat;   /* > 0; 1 is neutral.  l <= 0: l*r, l > 0: l/r [P19]                 */
+  float    penalty_freq;     /* finite; 0 is neutral.  subtract freq * count [P19]                */
+  float    penalty_present;  /* finite; 0 is neutral.  subtract present if count > 0 [P19]        */
+  int32_t  penalty_last_n;   /* 0..4096 history tokens counted; 0 disables the penalties          */
+  uint32_t reserved;         /* must be 0                                                         */
+  uint64_t seed;             /* Philox key [P19], [P559]                                          */
+} strata_sampling_params;
+
+/* Library version: major*10000 + minor*100 + patch. */
+int strata_version(void);
+
+/* Message of the calling thread's last failed call ("" if none).  Owned by the library. */
+const char *strata_last_error(void);
+
+/* Fill *p with the neutral greedy defaults: temperature 0, top_k 0, top_p 1, min_p 0, repeat 1,
+ * freq 0, present 0, penalty_last_n 64, seed 0, struct_size set.  Host only. */
+void strata_default_params(strata_sampling_params *p);
+
+/* Check keys without a context: STRATA_OK or STRATA_EINVAL (reason in strata_last_error).
+ * A value the engine cannot honour is refused rather than changed [P19, "server.py ...":
+ * a typo'd config should not quietly change sampling].  Host only, no CUDA call. */
+int strata_validate_params(const strata_sampling_params *p);
+
+/*
+ * Create a context on `device` (must be the calling thread's current device) for up to
+ * `max_slots` request slots (1..65536), vocabularies up to `max_vocab` (1..STRATA_MAX_VOCAB)
+ * and up to `max_rows` rows per call (1..65536).  Allocates the device slot table (keys and
+ * 64-bit draw counters, all slots greedy-neutral with counter 0) and a device error word.
+ * Synchronous.  Returns STRATA_ECUDA when no usable device is present.
+ */
+int strata_create(strata_ctx **out, int device, int max_slots, int max_vocab, int max_rows);
+
+/* Free a context and its device memory.  Synchronises the device first.  NULL is a no-op. */
+void strata_destroy(strata_ctx *ctx);
+
+/*
+ * Set a slot's keys (validated as strata_validate_params) and, with reset_counter != 0, its
+ * draw counter to 0.  The device copy is updated by a copy enqueued on `stream`, so sample calls
+ * enqueued later on that stream see the new keys.  Without reset the counter keeps counting
+ * [P19: the draw counter persists across a request's verify windows].
+ */
+int strata_set_slot_params(strata_ctx *ctx, int slot, const strata_sampling_params *p,
+                           int reset_counter, void *stream);
+
+/* Read a slot's keys and its current draw counter.  Synchronises `stream` (counters live on the
+ * device and advance inside sample calls).  Either output pointer may be NULL. */
+int strata_get_slot_state(strata_ctx *ctx, int slot, strata_sampling_params *p,
+                          uint64_t *counter, void *stream);
+
+/* Restore a slot's keys and counter exactly (checkpoint/resume of a request); asynchronous on
+ * `stream` like strata_set_slot_params. */
+int strata_set_slot_state(strata_ctx *ctx, int slot, const strata_sampling_params *p,
+                          uint64_t counter, void *stream);
+
+/*
+ * Sample one token per row: penalties over the slot's history window -> top_k (value
+ * descending, ties to the lowest index) -> min_p -> top_p -> temperature -> one draw from
+ * Philox(seed, position) at the slot's draw counter [P19]; greedy rows take the first entry of
+ * the penalised order.  One kernel launch on `stream`.
+ *
+ *   logits      device, [B][ld] elements of `dtype`, row b at logits + b*ld; base address and
+ *               ld*sizeof(element) must be multiples of 16 bytes (else STRATA_EALIGN); ld >= V.
+ *               Logits must be finite or -inf; NaN is outside the contract.
+ *   row_slot    device int32[B]: the slot whose keys, history and counter row b uses.
+ *   row_pos     device int64[B]: row b's absolute token position (the Philox counter word).
+ *   hist        device int32[]: concatenated history ids of slots 0..n_hist_slots-1;
+ *   hist_off    device int32[n_hist_slots+1]: slot s owns hist[hist_off[s] .. hist_off[s+1]).
+ *               The penalties count the last min(penalty_last_n, length) ids of the slot's run;
+ *               ids outside [0, V) are ignored.  hist/hist_off NULL (or a slot >= n_hist_slots)
+ *               means no history: the byte-for-byte neutral path [P19].
+ *   out_ids     device int32[B]: the sampled id of each row (always written; -1 for a row whose
+ *               slot is out of range, with STRATA_DEVERR_SLOT).
+ *   Optional fused logprobs of the raw (pre-penalty, pre-temperature) logits [P3200, P1916];
+ *   every NULL output switches its part off at no cost:
+ *   top_n       0..20 alternatives per row.
+ *   chosen_lp   device float[B]: log-probability of out_ids[b] under the raw softmax.
+ *   top_ids     device int32[B][top_n] and top_lps float[B][top_n]: the top_n raw logits
+ *               (ties to the lowest index) and their log-probabilities; rows with V < top_n are
+ *               padded with id -1 and -inf.
+ *   allowed     device int32[]: concatenated allowed_token_ids of rows 0..B-1;
+ *   allowed_off device int32[B+1]: row b names allowed[allowed_off[b] .. allowed_off[b+1]);
+ *   allowed_lps device float[allowed_off[B]]: log-probabilities renormalised over exactly the
+ *               named ids, in the caller's order (a repeated id counts once in the normaliser).
+ *   Optional debug outputs (NULL = off): topk_ids int32[B][64] and topk_vals float[B][64] (the
+ *   ordered survivors of top_k and their penalised logits, padded with -1 / NaN), kept
+ *   int32[B][2] (survivors after min_p, after top_p).
+ *   flags       STRATA_FLAG_* bits.
+ *
+ * Counter rule: each slot that has at least one sampled row in the call advances its draw
+ * counter by exactly 1; all rows of the call read the counter as it was before the call (rows of
+ * one slot differ by position).  The advance happens on the device inside the launch, so the
+ * call can be captured in a CUDA graph and every replay draws fresh numbers.
+ */
+int strata_sample_rows(strata_ctx *ctx, const void *logits, int dtype, int B, int V, int64_t ld,
+                       const int32_t *row_slot, const int64_t *row_pos,
+                       const int32_t *hist, const int32_t *hist_off, int n_hist_slots,
+                       int32_t *out_ids,
+                       int top_n, float *chosen_lp, int32_t *top_ids, float *top_lps,
+                       const int32_t *allowed, const int32_t *allowed_off, float *allowed_lps,
+                       int32_t *topk_ids, float *topk_vals, int32_t *kept,
+                       uint32_t flags, void *stream);
+
+/*
+ * Logprobs without sampling [P3200, "Approach": the head logits before sampling, penalties and
+ * temperature; P1916, "What changed"].  Same layouts as above; `chosen` (device int32[B], or
+ * NULL) names the id whose log-probability goes to chosen_lp[b] (NaN and STRATA_DEVERR_CHOSEN
+ * for an id outside [0, V)).  No slot state is read or changed.
+ */
+int strata_logprobs_rows(strata_ctx *ctx, const void *logits, int dtype, int B, int V, int64_t ld,
+                         const int32_t *chosen, float *chosen_lp,
+                         int top_n, int32_t *top_ids, float *top_lps,
+                         const int32_t *allowed, const int32_t *allowed_off, float *allowed_lps,
+                         uint32_t flags, void *stream);
+
+/* Synchronise `stream`, return the accumulated STRATA_DEVERR_* bits in *bits and clear them. */
+int strata_read_errors(strata_ctx *ctx, uint32_t *bits, void *stream);
+
+/*
+ * The launch shape a call with these arguments would use (host only, nothing enqueued):
+ * blocks per row (the thread-block cluster size), elements per block, dynamic shared memory
+ * bytes and the total grid size.  mode 0 = strata_sample_rows, 1 = strata_logprobs_rows.
+ */
+int strata_launch_shape(strata_ctx *ctx, int mode, int dtype, int B, int V, int top_n,
+                        uint32_t flags, int *split, int *chunk_elems, int *smem_bytes, int *grid);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* STRATA_SAMPLE_H */

@@ -1,0 +1,913 @@
+// strata_kernel.cuh -- the fused row kernel: one HBM pass per logit row.
+//
+// Each logit row is split over a thread-block cluster of `cs` CTAs (one chunk per CTA).  A CTA
+//   1. bulk-copies its chunk into shared memory (16 KiB pieces, one mbarrier each), and while the
+//      bytes land builds the row's history table for its id range (bitmap + open-addressing
+//      counts) and, as each piece completes, runs the first pass: the per-thread running max and
+//      sum of exp (log-sum-exp of the raw logits);
+//   2. derives a selection threshold t_c: the q-th largest per-thread maximum of the logits that
+//      carry no penalty (q = ceil(K/cs), K = max(top_k, top_n)).  q distinct elements of the
+//      chunk reach t_c, so min over the cluster of t_c bounds the row's K-th largest value from
+//      below; the CTAs exchange t_c and their (max, sum) pairs through DSMEM (cluster barrier B0);
+//   3. rescans only the threads whose maximum reaches the row threshold, adds the penalised ids
+//      from the history table, keeps its best <= K candidates and sends them to the cluster's
+//      leader CTA through DSMEM (cluster barrier B1);
+//   4. the leader ranks the <= cs*K received keys exactly, then one warp runs the tail of the
+//      chain on <= 64 survivors: min_p, top_p, temperature, the Philox draw.
+// Every CTA writes the allowed-subset and chosen-id log-probabilities of its own id range.
+//
+// The chain it computes is defined on the pages "#19 serve: per-request temperature/top_p/top_k/
+// min_p/penalties sampling" (section "What changed") and "#3200 [Engine] OpenAI logprobs /
+// top_logprobs / allowed_token_ids for the CUDA/HIP engine" (sections "Problem and result",
+// "Approach").  The pages' own kernel ran k full-vocabulary argmax rounds per token; this one
+// reads each row from HBM once and selects in a single pass plus a small exact merge.
+#pragma once
+
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/strata_sample.h"
+#include "strata_device.cuh"
+
+namespace strata {
+
+constexpr int NT = 512;                      // threads per CTA
+constexpr int NW = NT / 32;                  // warps per CTA
+constexpr int VR = 2;                        // 16-byte vectors per thread per piece
+constexpr int PIECE_VECS = NT * VR;
+constexpr int PIECE_BYTES = PIECE_VECS * 16; // 16 KiB per bulk copy
+constexpr int MAX_PIECES = 12;               // chunk <= 192 KiB
+constexpr int MAX_CS = 16;                   // CTAs per row (non-portable cluster size)
+constexpr int KMAX = STRATA_MAX_TOP_K;
+constexpr int NMAX = STRATA_MAX_TOP_N;
+constexpr int QMAX = 8;                      // per-CTA threshold rank handled by the warp stage
+constexpr int LOCAL_CAP = 512;               // per-CTA candidate buffer (beyond: exact rounds)
+constexpr int HASH_CNT_BITS = 13;            // history table entry = (local id << 13) | count
+constexpr uint32_t HASH_EMPTY = 0xFFFFFFFFu;
+constexpr int MODE_SAMPLE = 0;
+constexpr int MODE_LOGPROBS = 1;
+constexpr uint32_t SLOT_SAMPLED = 1u;
+constexpr uint32_t SLOT_PENAL = 2u;
+constexpr long long WAIT_CYCLES = 4000000000LL;  // bounded waits: ~2 s at GB300 clocks
+
+// Control words in shared memory.
+enum : int {
+  CTL_CAND_PEN = 0,
+  CTL_CAND_RAW = 1,
+  CTL_TC = 2,
+  CTL_CTR_LO = 3,
+  CTL_CTR_HI = 4,
+  CTL_TIMEOUT = 5,
+  CTL_WORDS = 16
+};
+
+// A slot's keys as the kernel reads them (prepared and validated by the host).
+struct __align__(16) SlotDev {
+  float temperature;  // > 0 for sampled slots
+  float top_p;
+  float min_p;
+  float logminp;      // host logf(min_p) when min_p > 0
+  float rep, freq, pres;
+  int32_t k;          // survivors: top_k (0 -> 20) for sampled slots, 1 for greedy slots
+  int32_t last_n;     // history window
+  uint32_t flags;     // SLOT_SAMPLED | SLOT_PENAL
+  uint64_t seed;
+};
+static_assert(sizeof(SlotDev) == 48, "SlotDev layout");
+
+struct KParams {
+  const void* logits;
+  long long ld;
+  int B, V, cs, chunk, mode;
+  const int32_t* row_slot;
+  const long long* row_pos;
+  const int32_t* hist;
+  const int32_t* hist_off;
+  int n_hist_slots;
+  int32_t* out_ids;
+  int top_n;          // row stride of top_ids / top_lps
+  int nmax;           // alternatives to compute (top_n if requested, else 0)
+  int kmax;           // receive entries per CTA for the penalised list (>= every row's k)
+  float* chosen_lp;
+  int32_t* top_ids;
+  float* top_lps;
+  const int32_t* chosen;
+  const int32_t* allowed;
+  const int32_t* allowed_off;
+  float* allowed_lps;
+  int32_t* topk_ids;
+  float* topk_vals;
+  int32_t* kept;
+  const SlotDev* slots;
+  unsigned long long* ctr;
+  uint32_t* arrivals;
+  int max_slots;
+  uint32_t* err;
+  int hash_cap, hash_bits;
+  uint32_t flags;
+};
+
+struct Layout {
+  uint32_t data, mbar, hbits, abits, hash, dirty, tc, ms, wtop, red, ctl;
+  uint32_t cand_pen, cand_raw, recv_pen, recv_raw, recv_cnt, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory layout of one CTA; identical in every CTA of a launch.
+__host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, int cs, int kmax,
+                                              int nmax) {
+  Layout L;
+  uint32_t o = 0;
+  L.data = o;
+  o += align_up(static_cast<uint32_t>(chunk) * esz, 128);
+  L.mbar = o;
+  o += MAX_PIECES * 8;
+  const uint32_t bw = align_up((static_cast<uint32_t>(chunk) + 31) / 32 * 4, 16);
+  L.hbits = o;
+  o += bw;
+  L.abits = o;
+  o += bw;
+  L.hash = o;
+  o += static_cast<uint32_t>(hash_cap) * 4;
+  L.dirty = o;
+  o += NT / 8;
+  L.tc = o;
+  o += MAX_CS * 4;
+  o = align_up(o, 16);
+  L.ms = o;
+  o += MAX_CS * 16;
+  L.wtop = o;
+  o += NW * QMAX * 4;
+  L.red = o;
+  o += NW * 16 + 64;
+  L.ctl = o;
+  o += CTL_WORDS * 4;
+  o = align_up(o, 16);
+  L.cand_pen = o;
+  o += LOCAL_CAP * 16;
+  L.cand_raw = o;
+  o += LOCAL_CAP * 8;
+  L.recv_pen = o;
+  o += static_cast<uint32_t>(cs * kmax) * 16;
+  L.recv_raw = o;
+  o += static_cast<uint32_t>(cs * nmax) * 8;
+  L.recv_cnt = o;
+  o += MAX_CS * 8;
+  L.total = align_up(o, 128);
+  return L;
+}
+
+// ------------------------------------------------------------------------------ helpers
+template <int DT>
+__device__ __forceinline__ void load_vec(const unsigned char* data, int v, float (&x)[16 / (DT == 0 ? 4 : 2)]) {
+  if constexpr (DT == 0) {
+    const float4 f = reinterpret_cast<const float4*>(data)[v];
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+  } else {
+    const uint4 u = reinterpret_cast<const uint4*>(data)[v];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float elem_at(const unsigned char* data, uint32_t loc) {
+  if constexpr (DT == 0) {
+    return reinterpret_cast<const float*>(data)[loc];
+  } else {
+    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(data)[loc]) << 16);
+  }
+}
+
+__device__ __forceinline__ bool bit_at(const uint32_t* bits, uint32_t loc) {
+  return (bits[loc >> 5] >> (loc & 31)) & 1u;
+}
+
+__device__ __forceinline__ uint32_t hash_slot(uint32_t loc, int bits) {
+  return (loc * 0x9E3779B1u) >> (32 - bits);
+}
+
+// Count one occurrence of chunk-local id `loc`; false if the table is full.
+__device__ bool hash_add(uint32_t* tab, int bits, uint32_t loc) {
+  const uint32_t mask = (1u << bits) - 1u;
+  uint32_t h = hash_slot(loc, bits);
+  for (uint32_t n = 0; n <= mask; ++n) {
+    uint32_t cur = *reinterpret_cast<volatile uint32_t*>(&tab[h]);
+    if (cur == HASH_EMPTY) {
+      const uint32_t prev = atomicCAS(&tab[h], HASH_EMPTY, (loc << HASH_CNT_BITS) | 1u);
+      if (prev == HASH_EMPTY) return true;
+      cur = prev;
+    }
+    if ((cur >> HASH_CNT_BITS) == loc) {
+      atomicAdd(&tab[h], 1u);
+      return true;
+    }
+    h = (h + 1u) & mask;
+  }
+  return false;
+}
+
+__device__ uint32_t hash_count(const uint32_t* tab, int bits, uint32_t loc) {
+  const uint32_t mask = (1u << bits) - 1u;
+  uint32_t h = hash_slot(loc, bits);
+  for (uint32_t n = 0; n <= mask; ++n) {
+    const uint32_t cur = tab[h];
+    if (cur == HASH_EMPTY) return 0u;
+    if ((cur >> HASH_CNT_BITS) == loc) return cur & ((1u << HASH_CNT_BITS) - 1u);
+    h = (h + 1u) & mask;
+  }
+  return 0u;
+}
+
+// Bounded wait on piece `p` (phase 0).  On timeout the error word and a shared flag are set and
+// the caller carries on, so every thread still reaches every cluster barrier.
+__device__ __forceinline__ void wait_piece(uint64_t* mbar, int p, uint32_t* ctl, uint32_t* err) {
+  if (mbar_try_wait(&mbar[p], 0)) return;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(&mbar[p], 0)) {
+    if (clock64() - t0 > WAIT_CYCLES) {
+      atomicOr(err, STRATA_DEVERR_TIMEOUT);
+      ctl[CTL_TIMEOUT] = 1u;
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void online_add(MaxSum& a, float v) {
+  if (v == -INFINITY || v != v) return;
+  if (v > a.m) {
+    a.s = (a.m == -INFINITY) ? 1.0f : a.s * ex2_approx((a.m - v) * LOG2E) + 1.0f;
+    a.m = v;
+  } else {
+    a.s += ex2_approx((v - a.m) * LOG2E);
+  }
+}
+
+// Block-wide max of a 64-bit key (all threads call; result in every thread).
+__device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int lane, int wid) {
+  x = warp_max_u64(x);
+  __syncthreads();
+  if (lane == 0) red[wid] = x;
+  __syncthreads();
+  uint64_t r = red[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) r = red[w] > r ? red[w] : r;
+  return r;
+}
+
+// ------------------------------------------------------------------------------ the kernel
+template <int DT>
+__global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  constexpr int ESZ = DT == 0 ? 4 : 2;
+  constexpr int EPV = 16 / ESZ;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const uint32_t crank = cluster_ctarank();
+  const int cs = P.cs;
+  const int row = blockIdx.x / cs;
+  const Layout L = make_layout(P.chunk, ESZ, P.hash_cap, cs, P.kmax, P.nmax);
+
+  const int lo = static_cast<int>(crank) * P.chunk;
+  const int hi = min(P.V, lo + P.chunk);
+  const int n_el = max(0, hi - lo);
+  const int bytes = n_el * ESZ;
+  const int bytes_al = bytes & ~15;
+  const int n_vec = (bytes + 15) >> 4;
+  const int n_pieces = (bytes_al + PIECE_BYTES - 1) / PIECE_BYTES;
+
+  unsigned char* data = sm + L.data;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + L.mbar);
+  uint32_t* hbits = reinterpret_cast<uint32_t*>(sm + L.hbits);
+  uint32_t* abits = reinterpret_cast<uint32_t*>(sm + L.abits);
+  uint32_t* htab = reinterpret_cast<uint32_t*>(sm + L.hash);
+  uint32_t* dirty = reinterpret_cast<uint32_t*>(sm + L.dirty);
+  uint32_t* tc_arr = reinterpret_cast<uint32_t*>(sm + L.tc);
+  float4* ms_arr = reinterpret_cast<float4*>(sm + L.ms);
+  uint32_t* wtop = reinterpret_cast<uint32_t*>(sm + L.wtop);
+  uint64_t* red64 = reinterpret_cast<uint64_t*>(sm + L.red);
+  float4* red4 = reinterpret_cast<float4*>(sm + L.red);
+  uint32_t* ctl = reinterpret_cast<uint32_t*>(sm + L.ctl);
+  uint4* cand_pen = reinterpret_cast<uint4*>(sm + L.cand_pen);
+  uint64_t* cand_raw = reinterpret_cast<uint64_t*>(sm + L.cand_raw);
+  const uint4* recv_pen = reinterpret_cast<const uint4*>(sm + L.recv_pen);
+  const uint64_t* recv_raw = reinterpret_cast<const uint64_t*>(sm + L.recv_raw);
+  const uint2* recv_cnt = reinterpret_cast<const uint2*>(sm + L.recv_cnt);
+
+  const char* grow = static_cast<const char*>(P.logits) + (static_cast<long long>(row) * P.ld + lo) * ESZ;
+  const bool early = (P.flags & STRATA_FLAG_EARLY_LOAD) != 0u;
+
+  // ---- 1. start the bulk copies of this chunk ------------------------------------------------
+  if (tid == 0) {
+    for (int p = 0; p < n_pieces; ++p) mbar_init(&mbar[p], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!early) grid_dep_wait();
+  if (tid == 0) {
+    for (int p = 0; p < n_pieces; ++p) {
+      const uint32_t nb = static_cast<uint32_t>(min(PIECE_BYTES, bytes_al - p * PIECE_BYTES));
+      mbar_arrive_expect_tx(&mbar[p], nb);
+      bulk_g2s(data + p * PIECE_BYTES, grow + p * PIECE_BYTES, nb, &mbar[p]);
+    }
+  }
+  if (early) grid_dep_wait();
+  grid_dep_launch();
+
+  // The ragged last vector (chunk bytes not a multiple of 16) is read with plain loads by its
+  // owner thread, padded with -inf.
+  if (bytes > bytes_al && tid == (n_vec - 1) % NT) {
+    const int tv = n_vec - 1;
+    if constexpr (DT == 0) {
+      const float* g = reinterpret_cast<const float*>(grow);
+      float* d = reinterpret_cast<float*>(data);
+      for (int e = 0; e < EPV; ++e) {
+        const int idx = tv * EPV + e;
+        d[idx] = idx < n_el ? g[idx] : -INFINITY;
+      }
+    } else {
+      const uint16_t* g = reinterpret_cast<const uint16_t*>(grow);
+      uint16_t* d = reinterpret_cast<uint16_t*>(data);
+      for (int e = 0; e < EPV; ++e) {
+        const int idx = tv * EPV + e;
+        d[idx] = idx < n_el ? g[idx] : static_cast<uint16_t>(0xFF80u);
+      }
+    }
+  }
+
+  const int bw_words = (P.chunk + 31) >> 5;
+  for (int i = tid; i < bw_words; i += NT) {
+    hbits[i] = 0u;
+    abits[i] = 0u;
+  }
+  for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
+  if (tid < NT / 32) dirty[tid] = 0u;
+  if (tid < CTL_WORDS) ctl[tid] = 0u;
+  __syncthreads();
+  cluster_arrive();  // every CTA of the cluster is running before any DSMEM store (waited below)
+
+  // ---- row metadata -------------------------------------------------------------------------
+  int slot = -1;
+  bool valid = true;
+  SlotDev sp{};
+  if (P.mode == MODE_SAMPLE) {
+    slot = P.row_slot[row];
+    valid = static_cast<unsigned>(slot) < static_cast<unsigned>(P.max_slots);
+    if (valid) sp = P.slots[slot];
+  }
+  const bool sampled = valid && (sp.flags & SLOT_SAMPLED);
+  const int k_row = (P.mode == MODE_SAMPLE && valid) ? min(max(sp.k, 1), P.kmax) : 0;
+  if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
+  const int n_row = P.nmax;
+  const int kp = max(k_row, n_row);
+  const int q = (kp + cs - 1) / cs;
+  const bool penal = (P.mode == MODE_SAMPLE) && valid && (sp.flags & SLOT_PENAL) && P.hist_off != nullptr &&
+                     slot < P.n_hist_slots && P.hash_cap > 0;
+
+  // ---- history table of this chunk's id range ------------------------------------------------
+  if (penal) {
+    const int hb = P.hist_off[slot], he = P.hist_off[slot + 1];
+    const int h = min(sp.last_n, max(0, he - hb));
+    const int start = he - h;
+    for (int i = tid; i < h; i += NT) {
+      const int id = P.hist[start + i];
+      if (id >= lo && id < hi) {
+        const uint32_t loc = static_cast<uint32_t>(id - lo);
+        atomicOr(&hbits[loc >> 5], 1u << (loc & 31));
+        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
+        const uint32_t owner = (loc / EPV) % NT;
+        atomicOr(&dirty[owner >> 5], 1u << (owner & 31));
+      }
+    }
+  }
+
+  // allowed ids of this row (first two per thread prefetched) and the chosen id
+  int a_beg = 0, a_end = 0;
+  if (P.allowed_off != nullptr) {
+    a_beg = P.allowed_off[row];
+    a_end = P.allowed_off[row + 1];
+  }
+  const int aid0 = (a_beg + tid < a_end) ? P.allowed[a_beg + tid] : -1;
+  const int aid1 = (a_beg + tid + NT < a_end) ? P.allowed[a_beg + tid + NT] : -1;
+  const int chosen_id = (P.mode == MODE_LOGPROBS && P.chosen != nullptr) ? P.chosen[row] : -1;
+
+  // ---- the draw counter: read once, the last row of the slot advances it ----------------------
+  if (crank == 0 && sampled) {
+    int cnt = 0;
+    for (int b0 = 0; b0 < P.B; b0 += NT) {
+      const int b = b0 + tid;
+      cnt += __syncthreads_count(b < P.B && P.row_slot[b] == slot);
+    }
+    if (tid == 0) {
+      const unsigned long long c = *reinterpret_cast<volatile unsigned long long*>(&P.ctr[slot]);
+      __threadfence();
+      const unsigned a = atomicAdd(&P.arrivals[slot], 1u);
+      __threadfence();
+      if (a + 1u == static_cast<unsigned>(cnt)) {
+        P.ctr[slot] = c + 1ull;
+        P.arrivals[slot] = 0u;
+      }
+      ctl[CTL_CTR_LO] = static_cast<uint32_t>(c);
+      ctl[CTL_CTR_HI] = static_cast<uint32_t>(c >> 32);
+    }
+  }
+
+  // ---- 1b. first pass as pieces land: running max and sum of exp ----------------------------
+  MaxSum acc{-INFINITY, 0.0f};
+  {
+    int waited = -1;
+    int i = 0;
+    for (int v = tid; v < n_vec; v += NT, ++i) {
+      const int p = i / VR;
+      if (p < n_pieces && p != waited) {
+        wait_piece(mbar, p, ctl, P.err);
+        waited = p;
+      }
+      float x[EPV];
+      load_vec<DT>(data, v, x);
+      float vm = x[0];
+#pragma unroll
+      for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
+      if (vm > acc.m) {
+        acc.s = (acc.m == -INFINITY) ? 0.0f : acc.s * ex2_approx((acc.m - vm) * LOG2E);
+        acc.m = vm;
+      }
+      if (acc.m != -INFINITY) {
+        const float mb = acc.m * LOG2E;
+        float t = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) t += ex2_approx(fmaf(x[e], LOG2E, -mb));
+        acc.s += t;
+      }
+    }
+  }
+  for (int p = 0; p < n_pieces; ++p) wait_piece(mbar, p, ctl, P.err);  // all pieces visible
+  __syncthreads();
+
+  // per-thread maximum over the ids that carry no penalty (the threshold's elements)
+  bool has_m = tid < n_vec;
+  float mm = acc.m;
+  if (penal && ((dirty[tid >> 5] >> (tid & 31)) & 1u)) {
+    mm = -INFINITY;
+    has_m = false;
+    for (int v = tid; v < n_vec; v += NT) {
+      float x[EPV];
+      load_vec<DT>(data, v, x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+        if (loc < static_cast<uint32_t>(n_el) && !bit_at(hbits, loc)) {
+          mm = fmaxf(mm, x[e]);
+          has_m = true;
+        }
+      }
+    }
+  }
+  const uint32_t ord_t = has_m ? order_key(mm) : 0u;
+
+  // ---- 2. threshold t_c, block (max,sum) of the row and of the allowed subset -----------------
+  if (kp > 0 && q <= QMAX) {
+    uint32_t key = ord_t;
+    for (int r = 0; r < q; ++r) {
+      const uint32_t mx = __reduce_max_sync(FULL_MASK, key);
+      if (lane == 0) wtop[wid * QMAX + r] = mx;
+      const uint32_t bal = __ballot_sync(FULL_MASK, key == mx);
+      if (lane == __ffs(bal) - 1) key = 0u;
+    }
+  }
+  MaxSum al{-INFINITY, 0.0f};
+  {
+    auto add_allowed = [&](int id) {
+      if (id >= lo && id < hi) {
+        const uint32_t loc = static_cast<uint32_t>(id - lo);
+        const uint32_t bit = 1u << (loc & 31);
+        const uint32_t old = atomicOr(&abits[loc >> 5], bit);
+        if (!(old & bit)) online_add(al, elem_at<DT>(data, loc));
+      }
+    };
+    add_allowed(aid0);
+    add_allowed(aid1);
+    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) add_allowed(P.allowed[j]);
+  }
+  const MaxSum wrow = warp_ms(acc);
+  const MaxSum wal = warp_ms(al);
+  if (lane == 0) red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
+  __syncthreads();
+  if (wid == 0) {
+    MaxSum r1{-INFINITY, 0.0f}, r2{-INFINITY, 0.0f};
+    if (lane < NW) {
+      const float4 t = red4[lane];
+      r1 = {t.x, t.y};
+      r2 = {t.z, t.w};
+    }
+    r1 = warp_ms(r1);
+    r2 = warp_ms(r2);
+    uint32_t tq = 0u;
+    if (kp > 0 && q <= QMAX) {
+      uint32_t vals[4];
+      const int nv = NW * q;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int f = lane + 32 * j;
+        vals[j] = (f < nv) ? wtop[(f / q) * QMAX + (f % q)] : 0u;
+      }
+      for (int r = 0; r < q; ++r) {
+        uint32_t lm = vals[0];
+#pragma unroll
+        for (int j = 1; j < 4; ++j) lm = vals[j] > lm ? vals[j] : lm;
+        const uint32_t mx = __reduce_max_sync(FULL_MASK, lm);
+        const uint32_t bal = __ballot_sync(FULL_MASK, lm == mx);
+        if (lane == __ffs(bal) - 1) {
+          bool done = false;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (!done && vals[j] == mx) {
+              vals[j] = 0u;
+              done = true;
+            }
+          }
+        }
+        tq = mx;
+      }
+    }
+    if (lane == 0) {
+      ctl[CTL_TC] = tq;
+      red4[NW] = make_float4(r1.m, r1.s, r2.m, r2.s);
+    }
+  }
+  __syncthreads();
+
+  // ---- exchange through DSMEM (cluster barrier B0) ---------------------------------------------
+  cluster_wait();
+  if (tid < cs) {
+    const float4 t = red4[NW];
+    const uint32_t r = static_cast<uint32_t>(tid);
+    dsmem_st_u32(dsmem_addr(smem_u32(tc_arr + crank), r), ctl[CTL_TC]);
+    dsmem_st_v4(dsmem_addr(smem_u32(ms_arr + crank), r), __float_as_uint(t.x), __float_as_uint(t.y),
+                __float_as_uint(t.z), __float_as_uint(t.w));
+  }
+  cluster_arrive();
+  cluster_wait();
+
+  uint32_t T = 0xFFFFFFFFu;
+  MaxSum g{-INFINITY, 0.0f}, ga{-INFINITY, 0.0f};
+  for (int c = 0; c < cs; ++c) {
+    T = min(T, tc_arr[c]);
+    const float4 t = ms_arr[c];
+    g = ms_combine(g, MaxSum{t.x, t.y});
+    ga = ms_combine(ga, MaxSum{t.z, t.w});
+  }
+  const float lse = (g.m == -INFINITY || !(g.s > 0.0f)) ? -INFINITY : g.m + logf(g.s);
+  const float lse_a = (ga.m == -INFINITY || !(ga.s > 0.0f)) ? -INFINITY : ga.m + logf(ga.s);
+
+  // allowed-subset log-probabilities and the given chosen id, for this chunk's ids
+  if (P.allowed_off != nullptr && P.allowed_lps != nullptr) {
+    auto out_allowed = [&](int j, int id) {
+      if (id >= lo && id < hi) {
+        P.allowed_lps[j] = elem_at<DT>(data, static_cast<uint32_t>(id - lo)) - lse_a;
+      } else if ((id < 0 || id >= P.V) && crank == 0) {
+        P.allowed_lps[j] = __int_as_float(0x7FC00000);
+        atomicOr(P.err, STRATA_DEVERR_ALLOWED);
+      }
+    };
+    if (a_beg + tid < a_end) out_allowed(a_beg + tid, aid0);
+    if (a_beg + tid + NT < a_end) out_allowed(a_beg + tid + NT, aid1);
+    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) out_allowed(j, P.allowed[j]);
+  }
+  if (P.mode == MODE_LOGPROBS && P.chosen_lp != nullptr && P.chosen != nullptr && tid == 0) {
+    if (chosen_id >= lo && chosen_id < hi) {
+      P.chosen_lp[row] = elem_at<DT>(data, static_cast<uint32_t>(chosen_id - lo)) - lse;
+    } else if ((chosen_id < 0 || chosen_id >= P.V) && crank == 0) {
+      P.chosen_lp[row] = __int_as_float(0x7FC00000);
+      atomicOr(P.err, STRATA_DEVERR_CHOSEN);
+    }
+  }
+
+  // ---- 3. candidates of this chunk -------------------------------------------------------------
+  if (kp > 0) {
+    if (q > QMAX) T = 0u;  // no usable bound: every element is a candidate (exact rounds below)
+    if (has_m && ord_t >= T) {
+      for (int v = tid; v < n_vec; v += NT) {
+        float x[EPV];
+        load_vec<DT>(data, v, x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+          const uint32_t o = order_key(x[e]);
+          if (loc >= static_cast<uint32_t>(n_el) || o == 0u || o < T) continue;
+          if (penal && bit_at(hbits, loc)) continue;
+          const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
+          if (n_row > 0) {
+            const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
+            if (i < LOCAL_CAP) cand_raw[i] = key;
+          }
+          if (k_row > 0) {
+            const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+            if (i < LOCAL_CAP)
+              cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
+                                       __float_as_uint(x[e]), 0u);
+          }
+        }
+      }
+    }
+    if (penal) {
+      for (int i = tid; i < P.hash_cap; i += NT) {
+        const uint32_t ent = htab[i];
+        if (ent == HASH_EMPTY) continue;
+        const uint32_t loc = ent >> HASH_CNT_BITS;
+        const uint32_t c = ent & ((1u << HASH_CNT_BITS) - 1u);
+        const float raw = elem_at<DT>(data, loc);
+        const uint32_t id = static_cast<uint32_t>(lo) + loc;
+        const uint32_t o = order_key(raw);
+        if (n_row > 0 && o != 0u && o >= T) {
+          const uint32_t j = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
+          if (j < LOCAL_CAP) cand_raw[j] = sel_key(o, id);
+        }
+        const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
+        const uint32_t op = order_key(pv);
+        if (k_row > 0 && op != 0u && op >= T) {
+          const uint32_t j = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+          const uint64_t key = sel_key(op, id);
+          if (j < LOCAL_CAP)
+            cand_pen[j] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
+                                     __float_as_uint(raw), 0u);
+        }
+      }
+    }
+    __syncthreads();
+
+    const uint32_t recv_pen_base = smem_u32(sm + L.recv_pen) + crank * static_cast<uint32_t>(P.kmax) * 16u;
+    const uint32_t recv_raw_base = smem_u32(sm + L.recv_raw) + crank * static_cast<uint32_t>(P.nmax) * 8u;
+    uint32_t sent_pen = 0, sent_raw = 0;
+
+    // -- penalised list: keep this chunk's best k_row and send them to the leader
+    if (k_row > 0) {
+      const int np = static_cast<int>(ctl[CTL_CAND_PEN]);
+      if (np <= LOCAL_CAP) {
+        for (int i = tid; i < np; i += NT) {
+          const uint4 ent = cand_pen[i];
+          int slot_out = i;
+          if (np > k_row) {
+            const uint64_t ki = (static_cast<uint64_t>(ent.y) << 32) | ent.x;
+            int rank = 0;
+            for (int j = 0; j < np; ++j) {
+              const uint4 o = cand_pen[j];
+              rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
+            }
+            slot_out = rank;
+          }
+          if (slot_out < k_row) dsmem_st_v4(dsmem_addr(recv_pen_base + slot_out * 16u, 0), ent.x, ent.y, ent.z, 0u);
+        }
+        sent_pen = static_cast<uint32_t>(min(np, k_row));
+      } else {
+        // more candidates than the buffer holds (heavy ties): k exact argmax rounds
+        uint64_t prev = ~0ull;
+        for (int r = 0; r < k_row; ++r) {
+          uint64_t best = 0ull;
+          for (int v = tid; v < n_vec; v += NT) {
+            float x[EPV];
+            load_vec<DT>(data, v, x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+              if (loc >= static_cast<uint32_t>(n_el)) continue;
+              float pv = x[e];
+              if (penal && bit_at(hbits, loc))
+                pv = penalize(pv, hash_count(htab, P.hash_bits, loc), sp.rep, sp.freq, sp.pres);
+              const uint32_t o = order_key(pv);
+              if (o == 0u) continue;
+              const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
+              if (key < prev && key > best) best = key;
+            }
+          }
+          best = block_max_u64(best, red64, lane, wid);
+          if (best == 0ull) break;
+          if (tid == 0) {
+            const float raw = elem_at<DT>(data, key_id(best) - static_cast<uint32_t>(lo));
+            dsmem_st_v4(dsmem_addr(recv_pen_base + r * 16u, 0), static_cast<uint32_t>(best),
+                        static_cast<uint32_t>(best >> 32), __float_as_uint(raw), 0u);
+          }
+          prev = best;
+          sent_pen = static_cast<uint32_t>(r + 1);
+        }
+      }
+    }
+    // -- raw list: this chunk's best n_row raw logits
+    if (n_row > 0) {
+      const int nr = static_cast<int>(ctl[CTL_CAND_RAW]);
+      if (nr <= LOCAL_CAP) {
+        for (int i = tid; i < nr; i += NT) {
+          const uint64_t ki = cand_raw[i];
+          int slot_out = i;
+          if (nr > n_row) {
+            int rank = 0;
+            for (int j = 0; j < nr; ++j) rank += cand_raw[j] > ki;
+            slot_out = rank;
+          }
+          if (slot_out < n_row)
+            dsmem_st_v2(dsmem_addr(recv_raw_base + slot_out * 8u, 0), static_cast<uint32_t>(ki),
+                        static_cast<uint32_t>(ki >> 32));
+        }
+        sent_raw = static_cast<uint32_t>(min(nr, n_row));
+      } else {
+        uint64_t prev = ~0ull;
+        for (int r = 0; r < n_row; ++r) {
+          uint64_t best = 0ull;
+          for (int v = tid; v < n_vec; v += NT) {
+            float x[EPV];
+            load_vec<DT>(data, v, x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+              if (loc >= static_cast<uint32_t>(n_el)) continue;
+              const uint32_t o = order_key(x[e]);
+              if (o == 0u) continue;
+              const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
+              if (key < prev && key > best) best = key;
+            }
+          }
+          best = block_max_u64(best, red64, lane, wid);
+          if (best == 0ull) break;
+          if (tid == 0)
+            dsmem_st_v2(dsmem_addr(recv_raw_base + r * 8u, 0), static_cast<uint32_t>(best),
+                        static_cast<uint32_t>(best >> 32));
+          prev = best;
+          sent_raw = static_cast<uint32_t>(r + 1);
+        }
+      }
+    }
+    if (tid == 0) dsmem_st_v2(dsmem_addr(smem_u32(sm + L.recv_cnt) + crank * 8u, 0), sent_pen, sent_raw);
+    cluster_arrive();
+    cluster_wait();  // B1: the leader holds every CTA's candidates
+
+    // ---- 4. the leader ranks the received keys exactly -----------------------------------------
+    if (crank == 0) {
+      int tot_p = 0, tot_r = 0;
+      for (int c = 0; c < cs; ++c) {
+        tot_p += static_cast<int>(recv_cnt[c].x);
+        tot_r += static_cast<int>(recv_cnt[c].y);
+      }
+      uint4* sorted_pen = cand_pen;
+      uint64_t* sorted_raw = cand_raw;
+      __syncthreads();  // candidate buffers are reused for the sorted lists
+      for (int f = tid; f < tot_p + tot_r; f += NT) {
+        if (f < tot_p) {
+          int c = 0, j = f;
+          while (j >= static_cast<int>(recv_cnt[c].x)) {
+            j -= static_cast<int>(recv_cnt[c].x);
+            ++c;
+          }
+          const uint4 ent = recv_pen[c * P.kmax + j];
+          const uint64_t ki = (static_cast<uint64_t>(ent.y) << 32) | ent.x;
+          int rank = 0;
+          for (int c2 = 0; c2 < cs; ++c2) {
+            const int n2 = static_cast<int>(recv_cnt[c2].x);
+            const uint4* base = recv_pen + c2 * P.kmax;
+            for (int j2 = 0; j2 < n2; ++j2) rank += ((static_cast<uint64_t>(base[j2].y) << 32) | base[j2].x) > ki;
+          }
+          if (rank < k_row) sorted_pen[rank] = ent;
+        } else {
+          int c = 0, j = f - tot_p;
+          while (j >= static_cast<int>(recv_cnt[c].y)) {
+            j -= static_cast<int>(recv_cnt[c].y);
+            ++c;
+          }
+          const uint64_t ki = recv_raw[c * P.nmax + j];
+          int rank = 0;
+          for (int c2 = 0; c2 < cs; ++c2) {
+            const int n2 = static_cast<int>(recv_cnt[c2].y);
+            const uint64_t* base = recv_raw + c2 * P.nmax;
+            for (int j2 = 0; j2 < n2; ++j2) rank += base[j2] > ki;
+          }
+          if (rank < n_row) sorted_raw[rank] = ki;
+        }
+      }
+      __syncthreads();
+      const int k_eff = min(k_row, tot_p);
+      const int n_eff = min(n_row, tot_r);
+
+      // top-N raw alternatives and their log-probabilities
+      if (n_row > 0 && P.top_ids != nullptr) {
+        for (int i = tid; i < n_row; i += NT) {
+          const long long o = static_cast<long long>(row) * P.top_n + i;
+          if (i < n_eff) {
+            const uint64_t key = sorted_raw[i];
+            P.top_ids[o] = static_cast<int32_t>(key_id(key));
+            P.top_lps[o] = key_value(static_cast<uint32_t>(key >> 32)) - lse;
+          } else {
+            P.top_ids[o] = -1;
+            P.top_lps[o] = -INFINITY;
+          }
+        }
+      }
+
+      // ---- the tail of the chain on <= 64 survivors (one warp) --------------------------------
+      if (P.mode == MODE_SAMPLE && wid == 0) {
+        int out = -1, m1 = 0, m2 = 0;
+        float chosen_raw = __int_as_float(0x7FC00000);
+        const uint4 ea = (lane < k_eff) ? sorted_pen[lane] : make_uint4(0, 0, 0, 0);
+        const uint4 eb = (lane + 32 < k_eff) ? sorted_pen[lane + 32] : make_uint4(0, 0, 0, 0);
+        const float va = key_value(ea.y), vb = key_value(eb.y);
+        if (!valid) {
+          if (lane == 0) atomicOr(P.err, STRATA_DEVERR_SLOT);
+        } else if (k_eff == 0) {
+          if (lane == 0) atomicOr(P.err, STRATA_DEVERR_NOCAND);
+        } else {
+          int j = 0;
+          m1 = m2 = 1;
+          if (sampled) {
+            const float v0 = __shfl_sync(FULL_MASK, va, 0);
+            m1 = k_eff;
+            if (sp.min_p > 0.0f) {  // min_p in logit space, float32
+              const float thr = __fadd_rn(v0, sp.logminp);
+              const uint32_t ba = __ballot_sync(FULL_MASK, lane < k_eff && va >= thr);
+              const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && vb >= thr);
+              m1 = max(1, __popc(ba) + __popc(bb));
+            }
+            m2 = m1;
+            if (!(sp.top_p >= 1.0f)) {
+              if (!(sp.top_p > 0.0f)) {
+                m2 = 1;
+              } else {  // temperature-1 mass over the min_p survivors
+                const double qa = (lane < m1) ? static_cast<double>(expf(__fsub_rn(va, v0))) : 0.0;
+                const double qb = (lane + 32 < m1) ? static_cast<double>(expf(__fsub_rn(vb, v0))) : 0.0;
+                const double ca = warp_scan_incl(qa, lane);
+                const double cb = warp_scan_incl(qb, lane) + __shfl_sync(FULL_MASK, ca, 31);
+                const double tot = __shfl_sync(FULL_MASK, cb, 31);
+                const double target = static_cast<double>(sp.top_p) * tot;
+                const uint32_t la = __ballot_sync(FULL_MASK, lane < m1 && ca < target);
+                const uint32_t lb = __ballot_sync(FULL_MASK, lane + 32 < m1 && cb < target);
+                m2 = min(m1, __popc(la) + __popc(lb) + 1);
+              }
+            }
+            const unsigned long long ctr =
+                (static_cast<unsigned long long>(ctl[CTL_CTR_HI]) << 32) | ctl[CTL_CTR_LO];
+            const unsigned long long pos = static_cast<unsigned long long>(P.row_pos[row]);
+            const uint32_t x0 = philox_word0(sp.seed, pos, ctr);
+            const double u = static_cast<double>(x0 >> 8) * 0x1p-24;
+            const float Tm = sp.temperature;
+            const double wa = (lane < m2) ? static_cast<double>(expf(__fdiv_rn(__fsub_rn(va, v0), Tm))) : 0.0;
+            const double wb = (lane + 32 < m2) ? static_cast<double>(expf(__fdiv_rn(__fsub_rn(vb, v0), Tm))) : 0.0;
+            const double Ca = warp_scan_incl(wa, lane);
+            const double Cb = warp_scan_incl(wb, lane) + __shfl_sync(FULL_MASK, Ca, 31);
+            const double W = __shfl_sync(FULL_MASK, Cb, 31);
+            const double tgt = u * W;
+            const uint32_t ja = __ballot_sync(FULL_MASK, lane < m2 && Ca <= tgt);
+            const uint32_t jb = __ballot_sync(FULL_MASK, lane + 32 < m2 && Cb <= tgt);
+            j = min(__popc(ja) + __popc(jb), m2 - 1);
+          }
+          const uint32_t id_a = key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x);
+          const uint32_t id_b = key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x);
+          const uint32_t sel_id = __shfl_sync(FULL_MASK, j < 32 ? id_a : id_b, j & 31);
+          const float sel_raw = __shfl_sync(FULL_MASK, __uint_as_float(j < 32 ? ea.z : eb.z), j & 31);
+          out = static_cast<int>(sel_id);
+          chosen_raw = sel_raw;
+        }
+        if (lane == 0) {
+          P.out_ids[row] = out;
+          if (P.kept != nullptr) {
+            P.kept[2 * row] = m1;
+            P.kept[2 * row + 1] = m2;
+          }
+          if (P.chosen_lp != nullptr) P.chosen_lp[row] = (out >= 0) ? chosen_raw - lse : __int_as_float(0x7FC00000);
+        }
+        if (P.topk_ids != nullptr) {
+          const long long o = static_cast<long long>(row) * KMAX;
+          const bool ia = valid && lane < k_eff, ib = valid && lane + 32 < k_eff;
+          P.topk_ids[o + lane] = ia ? static_cast<int32_t>(key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x)) : -1;
+          P.topk_ids[o + lane + 32] =
+              ib ? static_cast<int32_t>(key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x)) : -1;
+          if (P.topk_vals != nullptr) {
+            P.topk_vals[o + lane] = ia ? va : __int_as_float(0x7FC00000);
+            P.topk_vals[o + lane + 32] = ib ? vb : __int_as_float(0x7FC00000);
+          }
+        }
+      }
+    }
+  } else if (P.mode == MODE_SAMPLE && crank == 0 && tid == 0) {
+    // no selection in this row: only an out-of-range slot gets here
+    P.out_ids[row] = -1;
+    if (P.kept != nullptr) {
+      P.kept[2 * row] = 0;
+      P.kept[2 * row + 1] = 0;
+    }
+    if (P.chosen_lp != nullptr) P.chosen_lp[row] = __int_as_float(0x7FC00000);
+    atomicOr(P.err, STRATA_DEVERR_SLOT);
+  }
+  if (P.mode == MODE_SAMPLE && crank == 0 && P.topk_ids != nullptr && kp == 0 && tid < KMAX) {
+    P.topk_ids[static_cast<long long>(row) * KMAX + tid] = -1;
+    if (P.topk_vals != nullptr) P.topk_vals[static_cast<long long>(row) * KMAX + tid] = __int_as_float(0x7FC00000);
+  }
+  if (ctl[CTL_TIMEOUT] != 0u) {  // a copy may still be in flight into this CTA: bounded wait again
+    for (int p = 0; p < n_pieces; ++p) wait_piece(mbar, p, ctl, P.err);
+  }
+}
+
+}  // namespace strata

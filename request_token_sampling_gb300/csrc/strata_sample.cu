@@ -1,0 +1,527 @@
+// strata_sample.cu -- host side of the C ABI declared in include/strata_sample.h.
+//
+// The context owns the device slot table (each request slot's prepared keys and its 64-bit draw
+// counter), the per-slot arrival words the kernel uses to advance the counters, and a device
+// error word.  Keys are validated and prepared here (top_k 0 -> 20, logf(min_p) once on the host,
+// penalty activity), mirrored on the host, and copied to the device on the caller's stream.
+// Every sampling or logprobs call is one launch of the fused row kernel.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/strata_sample.h"
+#include "strata_kernel.cuh"
+
+using strata::KParams;
+using strata::Layout;
+using strata::SlotDev;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(STRATA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int CHUNK_TARGET_BYTES = 64 * 1024;  // preferred bytes of logits per CTA
+constexpr int MIN_CHUNK_ELEMS = 2048;          // do not split a row finer than this
+constexpr int KEY_BINS = STRATA_MAX_TOP_K + 1;
+constexpr int LASTN_BINS = STRATA_MAX_PENALTY_LAST_N + 1;
+
+}  // namespace
+
+struct strata_ctx {
+  int device = 0;
+  int num_sms = 0;
+  int max_slots = 0, max_vocab = 0, max_rows = 0;
+  int max_cluster = 8;
+  int max_smem = 0;
+  SlotDev* d_slots = nullptr;
+  unsigned long long* d_ctr = nullptr;
+  uint32_t* d_arrivals = nullptr;
+  uint32_t* d_err = nullptr;
+  std::vector<strata_sampling_params> h_params;
+  std::vector<SlotDev> h_slots;
+  // histograms over slots, for the launch shape: top_k of sampled slots, window of penal slots
+  std::vector<int> k_bins, lastn_bins;
+};
+
+namespace {
+
+SlotDev prepare(const strata_sampling_params& p) {
+  SlotDev s{};
+  const bool sampled = p.temperature > 0.0f;
+  s.temperature = p.temperature;
+  s.top_p = p.top_p;
+  s.min_p = p.min_p;
+  // "#19 ...", "min_p and the penalties": sel_logit >= sel_logit[0] + logf(min_p).  The host C
+  // library's logf is evaluated once here so the device never computes it.
+  s.logminp = p.min_p > 0.0f ? logf(p.min_p) : -INFINITY;
+  s.rep = p.penalty_repeat;
+  s.freq = p.penalty_freq;
+  s.pres = p.penalty_present;
+  s.k = sampled ? (p.top_k == 0 ? STRATA_DEFAULT_TOP_K : p.top_k) : 1;
+  const bool neutral = p.penalty_repeat == 1.0f && p.penalty_freq == 0.0f && p.penalty_present == 0.0f;
+  s.last_n = p.penalty_last_n;
+  s.flags = (sampled ? strata::SLOT_SAMPLED : 0u) | ((!neutral && p.penalty_last_n > 0) ? strata::SLOT_PENAL : 0u);
+  s.seed = p.seed;
+  return s;
+}
+
+void bins_update(strata_ctx* c, const SlotDev& s, int delta) {
+  if (s.flags & strata::SLOT_SAMPLED) c->k_bins[s.k] += delta;
+  if (s.flags & strata::SLOT_PENAL) c->lastn_bins[s.last_n] += delta;
+}
+
+int max_k_sampled(const strata_ctx* c) {
+  for (int k = STRATA_MAX_TOP_K; k >= 1; --k)
+    if (c->k_bins[k] > 0) return k;
+  return 0;
+}
+
+int max_lastn_penal(const strata_ctx* c) {
+  for (int n = STRATA_MAX_PENALTY_LAST_N; n >= 1; --n)
+    if (c->lastn_bins[n] > 0) return n;
+  return 0;
+}
+
+int check_device(const strata_ctx* c) {
+  int cur = -1;
+  const cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != c->device) return fail(STRATA_EINVAL, "current device %d is not the context's device %d", cur, c->device);
+  return STRATA_OK;
+}
+
+struct Shape {
+  int cs, chunk, smem, kmax, nmax, hash_cap, hash_bits;
+};
+
+int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int top_n_eff, bool with_hist,
+                  uint32_t flags, Shape* s) {
+  const int esz = dtype == STRATA_DTYPE_F32 ? 4 : 2;
+  const long long row_bytes = static_cast<long long>(V) * esz;
+  s->nmax = top_n_eff;
+  s->kmax = mode == strata::MODE_SAMPLE ? std::max(1, max_k_sampled(c)) : 0;
+  const int kp_max = std::max(s->kmax, s->nmax);
+  const int forced = static_cast<int>((flags >> 8) & 0x1Fu);
+  int cs;
+  if (forced > 0) {
+    if (forced > c->max_cluster) return fail(STRATA_ERANGE, "forced split %d above the cluster limit %d", forced, c->max_cluster);
+    cs = forced;
+  } else {
+    const int cs_bytes = static_cast<int>((row_bytes + CHUNK_TARGET_BYTES - 1) / CHUNK_TARGET_BYTES);
+    const int cs_q = (kp_max + strata::QMAX - 1) / strata::QMAX;
+    const int cs_fill = (c->num_sms + B - 1) / std::max(1, B);
+    const int cs_small = std::max(1, (V + MIN_CHUNK_ELEMS - 1) / MIN_CHUNK_ELEMS);
+    cs = std::max({cs_bytes, cs_q, std::min(cs_fill, cs_small), 1});
+    cs = std::min(cs, c->max_cluster);
+  }
+  int chunk = (V + cs - 1) / cs;
+  chunk = (chunk + 15) / 16 * 16;
+  if (static_cast<long long>(chunk) * esz > static_cast<long long>(strata::MAX_PIECES) * strata::PIECE_BYTES)
+    return fail(STRATA_ERANGE, "V=%d needs %d bytes per block (limit %d)", V, chunk * esz,
+                strata::MAX_PIECES * strata::PIECE_BYTES);
+  s->cs = cs;
+  s->chunk = chunk;
+  s->hash_cap = 0;
+  s->hash_bits = 0;
+  if (mode == strata::MODE_SAMPLE && with_hist) {
+    const int ln = max_lastn_penal(c);
+    if (ln > 0) {
+      int bits = 6;
+      while ((1 << bits) < 2 * ln) ++bits;
+      s->hash_bits = bits;
+      s->hash_cap = 1 << bits;
+    }
+  }
+  const Layout L = strata::make_layout(chunk, esz, s->hash_cap, cs, s->kmax, s->nmax);
+  s->smem = static_cast<int>(L.total);
+  if (s->smem > c->max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit %d", s->smem, c->max_smem);
+  return STRATA_OK;
+}
+
+int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t flags, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(P.B * sh.cs), 1, 1);
+  cfg.blockDim = dim3(strata::NT, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(sh.smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeClusterDimension;
+  attrs[na].val.clusterDim.x = static_cast<unsigned>(sh.cs);
+  attrs[na].val.clusterDim.y = 1;
+  attrs[na].val.clusterDim.z = 1;
+  ++na;
+  if (flags & STRATA_FLAG_PDL) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  cudaError_t e;
+  if (dtype == STRATA_DTYPE_F32)
+    e = cudaLaunchKernelEx(&cfg, strata::rows_kernel<0>, P);
+  else
+    e = cudaLaunchKernelEx(&cfg, strata::rows_kernel<1>, P);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  (void)c;
+  return STRATA_OK;
+}
+
+int check_rows_common(const strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld, int top_n,
+                      const float* chosen_lp, const int32_t* top_ids, const float* top_lps,
+                      const int32_t* allowed, const int32_t* allowed_off, const float* allowed_lps) {
+  if (c == nullptr) return fail(STRATA_EINVAL, "null context");
+  if (dtype != STRATA_DTYPE_F32 && dtype != STRATA_DTYPE_BF16) return fail(STRATA_EINVAL, "dtype %d", dtype);
+  if (B < 0) return fail(STRATA_EINVAL, "B=%d", B);
+  if (B > c->max_rows) return fail(STRATA_ERANGE, "B=%d above max_rows %d", B, c->max_rows);
+  if (V < 1) return fail(STRATA_EINVAL, "V=%d", V);
+  if (V > c->max_vocab) return fail(STRATA_ERANGE, "V=%d above max_vocab %d", V, c->max_vocab);
+  if (ld < V) return fail(STRATA_EINVAL, "ld=%lld below V=%d", static_cast<long long>(ld), V);
+  if (top_n < 0 || top_n > STRATA_MAX_TOP_N) return fail(STRATA_EINVAL, "top_n=%d outside 0..%d", top_n, STRATA_MAX_TOP_N);
+  if (B > 0 && logits == nullptr) return fail(STRATA_EINVAL, "null logits");
+  const int esz = dtype == STRATA_DTYPE_F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(logits) & 15u) != 0) return fail(STRATA_EALIGN, "logits not 16-byte aligned");
+  if ((static_cast<long long>(ld) * esz) % 16 != 0) return fail(STRATA_EALIGN, "row stride of %lld bytes not a multiple of 16", static_cast<long long>(ld) * esz);
+  if (top_n > 0 && ((top_ids == nullptr) != (top_lps == nullptr)))
+    return fail(STRATA_EINVAL, "top_ids and top_lps must be given together");
+  if (allowed_off != nullptr && (allowed == nullptr || allowed_lps == nullptr))
+    return fail(STRATA_EINVAL, "allowed_off needs allowed and allowed_lps");
+  (void)chosen_lp;
+  return STRATA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int strata_version(void) { return 10000; }
+
+const char* strata_last_error(void) { return g_err; }
+
+void strata_default_params(strata_sampling_params* p) {
+  if (p == nullptr) return;
+  std::memset(p, 0, sizeof(*p));
+  p->struct_size = sizeof(strata_sampling_params);
+  p->temperature = 0.0f;
+  p->top_k = 0;
+  p->top_p = 1.0f;
+  p->min_p = 0.0f;
+  p->penalty_repeat = 1.0f;
+  p->penalty_freq = 0.0f;
+  p->penalty_present = 0.0f;
+  p->penalty_last_n = STRATA_DEFAULT_LAST_N;
+  p->seed = 0;
+}
+
+int strata_validate_params(const strata_sampling_params* p) {
+  if (p == nullptr) return fail(STRATA_EINVAL, "null params");
+  if (p->struct_size < sizeof(strata_sampling_params))
+    return fail(STRATA_EINVAL, "struct_size %u below %zu", p->struct_size, sizeof(strata_sampling_params));
+  const float fs[6] = {p->temperature, p->top_p, p->min_p, p->penalty_repeat, p->penalty_freq, p->penalty_present};
+  const char* names[6] = {"temperature", "top_p", "min_p", "penalty_repeat", "penalty_freq", "penalty_present"};
+  for (int i = 0; i < 6; ++i)
+    if (!std::isfinite(fs[i])) return fail(STRATA_EINVAL, "%s is not finite", names[i]);
+  if (p->top_k < 0 || p->top_k > STRATA_MAX_TOP_K)
+    return fail(STRATA_EINVAL, "top_k=%d outside 0..%d (0 means %d)", p->top_k, STRATA_MAX_TOP_K, STRATA_DEFAULT_TOP_K);
+  if (!(p->penalty_repeat > 0.0f)) return fail(STRATA_EINVAL, "penalty_repeat must be > 0");
+  if (p->min_p < 0.0f) return fail(STRATA_EINVAL, "min_p must be >= 0");
+  if (p->penalty_last_n < 0 || p->penalty_last_n > STRATA_MAX_PENALTY_LAST_N)
+    return fail(STRATA_EINVAL, "penalty_last_n=%d outside 0..%d", p->penalty_last_n, STRATA_MAX_PENALTY_LAST_N);
+  if (p->reserved != 0u) return fail(STRATA_EINVAL, "reserved field must be 0");
+  return STRATA_OK;
+}
+
+int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, int max_rows) {
+  if (out == nullptr) return fail(STRATA_EINVAL, "null output pointer");
+  *out = nullptr;
+  if (max_slots < 1 || max_slots > 65536) return fail(STRATA_EINVAL, "max_slots=%d outside 1..65536", max_slots);
+  if (max_vocab < 1 || max_vocab > STRATA_MAX_VOCAB) return fail(STRATA_EINVAL, "max_vocab=%d outside 1..%d", max_vocab, STRATA_MAX_VOCAB);
+  if (max_rows < 1 || max_rows > 65536) return fail(STRATA_EINVAL, "max_rows=%d outside 1..65536", max_rows);
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device < 0 || device >= ndev) return fail(STRATA_EINVAL, "device %d of %d", device, ndev);
+  int cur = -1;
+  if ((e = cudaGetDevice(&cur)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != device) return fail(STRATA_EINVAL, "device %d is not the calling thread's current device %d", device, cur);
+  cudaDeviceProp prop;
+  if ((e = cudaGetDeviceProperties(&prop, device)) != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (prop.major < 10) return fail(STRATA_ECUDA, "device %s (sm_%d%d) is not a Blackwell GPU", prop.name, prop.major, prop.minor);
+
+  strata_ctx* c = new (std::nothrow) strata_ctx();
+  if (c == nullptr) return fail(STRATA_ENOMEM, "host allocation");
+  c->device = device;
+  c->num_sms = prop.multiProcessorCount;
+  c->max_slots = max_slots;
+  c->max_vocab = max_vocab;
+  c->max_rows = max_rows;
+  c->max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
+  c->k_bins.assign(KEY_BINS, 0);
+  c->lastn_bins.assign(LASTN_BINS, 0);
+
+  auto cleanup = [&](int code) {
+    strata_destroy(c);
+    return code;
+  };
+  const void* kernels[2] = {reinterpret_cast<const void*>(strata::rows_kernel<0>),
+                            reinterpret_cast<const void*>(strata::rows_kernel<1>)};
+  for (const void* k : kernels) {
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->max_smem)) != cudaSuccess)
+      return cleanup(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+      return cleanup(cuda_fail(e, "cudaFuncSetAttribute(cluster)"));
+  }
+  // The largest cluster the device can place with a typical shared-memory footprint.
+  c->max_cluster = 8;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(strata::MAX_CS, 1, 1);
+    cfg.blockDim = dim3(strata::NT, 1, 1);
+    cfg.dynamicSmemBytes = 128 * 1024;
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = strata::MAX_CS;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, strata::rows_kernel<0>, &cfg) == cudaSuccess && nclusters > 0)
+      c->max_cluster = strata::MAX_CS;
+    cudaGetLastError();
+  }
+
+  c->h_params.resize(max_slots);
+  c->h_slots.resize(max_slots);
+  strata_sampling_params d;
+  strata_default_params(&d);
+  const SlotDev sd = prepare(d);
+  for (int i = 0; i < max_slots; ++i) {
+    c->h_params[i] = d;
+    c->h_slots[i] = sd;
+  }
+  if ((e = cudaMalloc(&c->d_slots, sizeof(SlotDev) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc slots: %s", cudaGetErrorString(e)));
+  if ((e = cudaMalloc(&c->d_ctr, sizeof(unsigned long long) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc counters: %s", cudaGetErrorString(e)));
+  if ((e = cudaMalloc(&c->d_arrivals, sizeof(uint32_t) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc arrivals: %s", cudaGetErrorString(e)));
+  if ((e = cudaMalloc(&c->d_err, sizeof(uint32_t))) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc error word: %s", cudaGetErrorString(e)));
+  if ((e = cudaMemcpy(c->d_slots, c->h_slots.data(), sizeof(SlotDev) * max_slots, cudaMemcpyHostToDevice)) != cudaSuccess) return cleanup(cuda_fail(e, "slot table upload"));
+  if ((e = cudaMemset(c->d_ctr, 0, sizeof(unsigned long long) * max_slots)) != cudaSuccess) return cleanup(cuda_fail(e, "counter reset"));
+  if ((e = cudaMemset(c->d_arrivals, 0, sizeof(uint32_t) * max_slots)) != cudaSuccess) return cleanup(cuda_fail(e, "arrival reset"));
+  if ((e = cudaMemset(c->d_err, 0, sizeof(uint32_t))) != cudaSuccess) return cleanup(cuda_fail(e, "error word reset"));
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cleanup(cuda_fail(e, "create sync"));
+  *out = c;
+  return STRATA_OK;
+}
+
+void strata_destroy(strata_ctx* c) {
+  if (c == nullptr) return;
+  cudaDeviceSynchronize();
+  cudaFree(c->d_slots);
+  cudaFree(c->d_ctr);
+  cudaFree(c->d_arrivals);
+  cudaFree(c->d_err);
+  delete c;
+}
+
+static int set_slot(strata_ctx* c, int slot, const strata_sampling_params* p, bool set_ctr, uint64_t ctr,
+                    void* stream) {
+  if (c == nullptr) return fail(STRATA_EINVAL, "null context");
+  if (slot < 0 || slot >= c->max_slots) return fail(STRATA_ERANGE, "slot %d outside 0..%d", slot, c->max_slots - 1);
+  int rc = strata_validate_params(p);
+  if (rc != STRATA_OK) return rc;
+  if ((rc = check_device(c)) != STRATA_OK) return rc;
+  strata_sampling_params q = *p;
+  q.struct_size = sizeof(strata_sampling_params);
+  const SlotDev sd = prepare(q);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(c->d_slots + slot, &sd, sizeof(SlotDev), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "slot upload");
+  if (set_ctr) {
+    const unsigned long long v = ctr;
+    if ((e = cudaMemcpyAsync(c->d_ctr + slot, &v, sizeof(v), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail(e, "counter upload");
+    if ((e = cudaMemsetAsync(c->d_arrivals + slot, 0, sizeof(uint32_t), s)) != cudaSuccess)
+      return cuda_fail(e, "arrival reset");
+  }
+  bins_update(c, c->h_slots[slot], -1);
+  c->h_slots[slot] = sd;
+  c->h_params[slot] = q;
+  bins_update(c, sd, +1);
+  return STRATA_OK;
+}
+
+int strata_set_slot_params(strata_ctx* c, int slot, const strata_sampling_params* p, int reset_counter,
+                           void* stream) {
+  return set_slot(c, slot, p, reset_counter != 0, 0ull, stream);
+}
+
+int strata_set_slot_state(strata_ctx* c, int slot, const strata_sampling_params* p, uint64_t counter,
+                          void* stream) {
+  return set_slot(c, slot, p, true, counter, stream);
+}
+
+int strata_get_slot_state(strata_ctx* c, int slot, strata_sampling_params* p, uint64_t* counter, void* stream) {
+  if (c == nullptr) return fail(STRATA_EINVAL, "null context");
+  if (slot < 0 || slot >= c->max_slots) return fail(STRATA_ERANGE, "slot %d outside 0..%d", slot, c->max_slots - 1);
+  int rc = check_device(c);
+  if (rc != STRATA_OK) return rc;
+  if (p != nullptr) *p = c->h_params[slot];
+  if (counter != nullptr) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned long long v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, c->d_ctr + slot, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "counter read");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "counter read sync");
+    *counter = v;
+  }
+  return STRATA_OK;
+}
+
+int strata_read_errors(strata_ctx* c, uint32_t* bits, void* stream) {
+  if (c == nullptr || bits == nullptr) return fail(STRATA_EINVAL, "null argument");
+  int rc = check_device(c);
+  if (rc != STRATA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, c->d_err, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "error word read");
+  if ((e = cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), s)) != cudaSuccess) return cuda_fail(e, "error word clear");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "error word sync");
+  *bits = v;
+  return STRATA_OK;
+}
+
+int strata_launch_shape(strata_ctx* c, int mode, int dtype, int B, int V, int top_n, uint32_t flags, int* split,
+                        int* chunk_elems, int* smem_bytes, int* grid) {
+  if (c == nullptr) return fail(STRATA_EINVAL, "null context");
+  if (mode != strata::MODE_SAMPLE && mode != strata::MODE_LOGPROBS) return fail(STRATA_EINVAL, "mode %d", mode);
+  if (dtype != STRATA_DTYPE_F32 && dtype != STRATA_DTYPE_BF16) return fail(STRATA_EINVAL, "dtype %d", dtype);
+  if (B < 1 || V < 1 || V > c->max_vocab || top_n < 0 || top_n > STRATA_MAX_TOP_N) return fail(STRATA_EINVAL, "shape");
+  Shape sh;
+  const int rc = compute_shape(c, mode, dtype, B, V, top_n, true, flags, &sh);
+  if (rc != STRATA_OK) return rc;
+  if (split) *split = sh.cs;
+  if (chunk_elems) *chunk_elems = sh.chunk;
+  if (smem_bytes) *smem_bytes = sh.smem;
+  if (grid) *grid = B * sh.cs;
+  return STRATA_OK;
+}
+
+int strata_sample_rows(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
+                       const int32_t* row_slot, const int64_t* row_pos, const int32_t* hist,
+                       const int32_t* hist_off, int n_hist_slots, int32_t* out_ids, int top_n, float* chosen_lp,
+                       int32_t* top_ids, float* top_lps, const int32_t* allowed, const int32_t* allowed_off,
+                       float* allowed_lps, int32_t* topk_ids, float* topk_vals, int32_t* kept, uint32_t flags,
+                       void* stream) {
+  int rc = check_rows_common(c, logits, dtype, B, V, ld, top_n, chosen_lp, top_ids, top_lps, allowed, allowed_off,
+                             allowed_lps);
+  if (rc != STRATA_OK) return rc;
+  if (B > 0 && (row_slot == nullptr || row_pos == nullptr || out_ids == nullptr))
+    return fail(STRATA_EINVAL, "row_slot, row_pos and out_ids are required");
+  if (hist_off != nullptr && (hist == nullptr || n_hist_slots < 1))
+    return fail(STRATA_EINVAL, "hist_off needs hist and n_hist_slots >= 1");
+  if (hist_off == nullptr) n_hist_slots = 0;
+  if ((rc = check_device(c)) != STRATA_OK) return rc;
+  if (B == 0) return STRATA_OK;
+  const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
+  Shape sh;
+  if ((rc = compute_shape(c, strata::MODE_SAMPLE, dtype, B, V, top_n_eff, hist_off != nullptr, flags, &sh)) != STRATA_OK)
+    return rc;
+  KParams P{};
+  P.logits = logits;
+  P.ld = ld;
+  P.B = B;
+  P.V = V;
+  P.cs = sh.cs;
+  P.chunk = sh.chunk;
+  P.mode = strata::MODE_SAMPLE;
+  P.row_slot = row_slot;
+  P.row_pos = reinterpret_cast<const long long*>(row_pos);
+  P.hist = hist;
+  P.hist_off = hist_off;
+  P.n_hist_slots = n_hist_slots;
+  P.out_ids = out_ids;
+  P.top_n = top_n;
+  P.nmax = sh.nmax;
+  P.kmax = sh.kmax;
+  P.chosen_lp = chosen_lp;
+  P.top_ids = top_n_eff > 0 ? top_ids : nullptr;
+  P.top_lps = top_n_eff > 0 ? top_lps : nullptr;
+  P.chosen = nullptr;
+  P.allowed = allowed;
+  P.allowed_off = allowed_off;
+  P.allowed_lps = allowed_lps;
+  P.topk_ids = topk_ids;
+  P.topk_vals = topk_vals;
+  P.kept = kept;
+  P.slots = c->d_slots;
+  P.ctr = c->d_ctr;
+  P.arrivals = c->d_arrivals;
+  P.max_slots = c->max_slots;
+  P.err = c->d_err;
+  P.hash_cap = sh.hash_cap;
+  P.hash_bits = sh.hash_bits;
+  P.flags = flags;
+  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream));
+}
+
+int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
+                         const int32_t* chosen, float* chosen_lp, int top_n, int32_t* top_ids, float* top_lps,
+                         const int32_t* allowed, const int32_t* allowed_off, float* allowed_lps, uint32_t flags,
+                         void* stream) {
+  int rc = check_rows_common(c, logits, dtype, B, V, ld, top_n, chosen_lp, top_ids, top_lps, allowed, allowed_off,
+                             allowed_lps);
+  if (rc != STRATA_OK) return rc;
+  if ((chosen == nullptr) != (chosen_lp == nullptr)) return fail(STRATA_EINVAL, "chosen and chosen_lp must be given together");
+  if ((rc = check_device(c)) != STRATA_OK) return rc;
+  if (B == 0) return STRATA_OK;
+  const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
+  Shape sh;
+  if ((rc = compute_shape(c, strata::MODE_LOGPROBS, dtype, B, V, top_n_eff, false, flags, &sh)) != STRATA_OK) return rc;
+  KParams P{};
+  P.logits = logits;
+  P.ld = ld;
+  P.B = B;
+  P.V = V;
+  P.cs = sh.cs;
+  P.chunk = sh.chunk;
+  P.mode = strata::MODE_LOGPROBS;
+  P.top_n = top_n;
+  P.nmax = sh.nmax;
+  P.kmax = 0;
+  P.chosen_lp = chosen_lp;
+  P.top_ids = top_n_eff > 0 ? top_ids : nullptr;
+  P.top_lps = top_n_eff > 0 ? top_lps : nullptr;
+  P.chosen = chosen;
+  P.allowed = allowed;
+  P.allowed_off = allowed_off;
+  P.allowed_lps = allowed_lps;
+  P.slots = c->d_slots;
+  P.ctr = c->d_ctr;
+  P.arrivals = c->d_arrivals;
+  P.max_slots = c->max_slots;
+  P.err = c->d_err;
+  P.flags = flags;
+  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

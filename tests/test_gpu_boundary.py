@@ -1,0 +1,198 @@
+"""GPU tests of the boundary: argument errors, the per-slot counter rule, save/restore, graph capture,
+launch flags, and the invariants the pages state (greedy unchanged by neutral keys, same seed replays,
+a batch row equals the row alone, logprobs off changes nothing)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+from _harness import compare_sample, dev_tensor, gpu_sample, set_slots, upload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sampler():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from request_token_sampling_gb300 import Sampler
+    s = Sampler(device=0, max_slots=16, max_vocab=synth.V_FULL, max_rows=64)
+    yield s
+    s.close()
+
+
+def _small(seed=0, B=6, V=5000, n_slots=3, **kw):
+    return synth.random_case(seed, B=B, V=V, n_slots=n_slots, sampled_frac=1.0, hist_len=40, **kw)
+
+
+def test_argument_errors_launch_nothing(sampler):
+    import request_token_sampling_gb300 as S
+    w = _small()
+    d = upload(w)
+    out = torch.full((w["B"],), 777, dtype=torch.int32, device="cuda:0")
+    ctx = sampler.ctx
+    cases = []
+    raw = torch.zeros(w["B"] * w["ld"] + 4, dtype=torch.float32, device="cuda:0")
+    misaligned = raw[1:1 + w["B"] * w["ld"]].view(w["B"], w["ld"])
+    cases.append((dict(logits=misaligned), S.STRATA_EALIGN))
+    cases.append((dict(top_n=21), S.STRATA_EINVAL))
+    cases.append((dict(V=w["ld"] + 1), S.STRATA_EINVAL))
+    big = torch.zeros((65, w["ld"]), dtype=torch.float32, device="cuda:0")
+    cases.append((dict(logits=big, row_slot=torch.zeros(65, dtype=torch.int32, device="cuda:0"),
+                       row_pos=torch.zeros(65, dtype=torch.int64, device="cuda:0"),
+                       out_ids=torch.zeros(65, dtype=torch.int32, device="cuda:0")), S.STRATA_ERANGE))
+    for over, code in cases:
+        args = dict(logits=d["logits"], row_slot=d["row_slot"], row_pos=d["row_pos"], out_ids=out, V=w["V"])
+        args.update(over)
+        with pytest.raises(S.StrataError) as ei:
+            S.strata_sample_rows(ctx, **args)
+        assert ei.value.code == code
+    torch.cuda.synchronize()
+    assert (out == 777).all()                        # nothing ran
+    bad = dict(synth.make_params(temperature=1.0, top_k=65))
+    with pytest.raises(S.StrataError):
+        sampler.set_slot(0, bad)
+    with pytest.raises(S.StrataError):
+        sampler.set_slot(99, synth.make_params())
+
+
+def test_every_output_written(sampler):
+    w = _small(1)
+    set_slots(sampler, w)
+    d = upload(w)
+    o = {"ids": torch.full((w["B"],), 0x7EADBEEF, dtype=torch.int32, device="cuda:0")}
+    sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=d["hist"], hist_off=d["hist_off"], out=o)
+    torch.cuda.synchronize()
+    assert (o["ids"] >= 0).all() and (o["ids"] < w["V"]).all()
+
+
+def test_counter_rule_and_restore(sampler):
+    w = _small(2, B=7, n_slots=3)
+    w["row_slot"] = np.array([0, 0, 1, 2, 0, 1, 2], np.int32)
+    w["slot_params"][2]["temperature"] = 0.0         # greedy slot: its counter never moves
+    set_slots(sampler, w, {0: 5, 1: 0, 2: 9})
+    d = upload(w)
+    counters = {0: 5, 1: 0, 2: 9}
+    for _ in range(4):
+        g = gpu_sample(sampler, w, d=d, top_n=0)
+        rows, counters = oracle.sample_call(w, counters=counters)
+        compare_sample(w, rows, g, top_n=0)
+    assert counters == {0: 9, 1: 4, 2: 9}
+    assert [sampler.slot_state(s)[1] for s in range(3)] == [9, 4, 9]
+    # save slot 0, run two more calls, restore, replay: identical ids
+    p0, c0 = sampler.slot_state(0)
+    a = gpu_sample(sampler, w, d=d, top_n=0)["ids"]
+    gpu_sample(sampler, w, d=d, top_n=0)
+    sampler.restore_slot(0, p0, c0)
+    sampler.restore_slot(1, w["slot_params"][1], 4)
+    b = gpu_sample(sampler, w, d=d, top_n=0)["ids"]
+    assert np.array_equal(a, b)
+    # reset_counter sets 0
+    sampler.set_slot(0, p0, reset_counter=True)
+    assert sampler.slot_state(0)[1] == 0
+    # set without reset keeps counting
+    sampler.set_slot(1, w["slot_params"][1])
+    assert sampler.slot_state(1)[1] == 5
+
+
+def test_same_seed_replays_and_counter_moves_draws(sampler):
+    w = synth.config1()
+    p = dict(w["slot_params"][0], temperature=1.5, top_k=64, top_p=1.0, min_p=0.0)
+    w["slot_params"][0] = p
+    d = upload(w)
+    set_slots(sampler, w, {0: 0})
+    first = [int(gpu_sample(sampler, w, d=d, top_n=0)["ids"][0]) for _ in range(16)]
+    set_slots(sampler, w, {0: 0})
+    again = [int(gpu_sample(sampler, w, d=d, top_n=0)["ids"][0]) for _ in range(16)]
+    assert first == again
+    assert len(set(first)) > 1
+
+
+def test_neutral_keys_are_greedy_byte_for_byte(sampler):
+    w = synth.config4(fused=True)
+    for s in w["slot_params"]:
+        w["slot_params"][s] = synth.make_params(temperature=0.0, penalty_last_n=64, seed=s)
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w, top_n=0)
+    raw = oracle.widen(w["logits"][:, :w["V"]], "f32")
+    assert g["ids"].tolist() == [int(np.argmax(r)) for r in raw]
+    # a sampled request with top_k=1 and no history is greedy too
+    for s in w["slot_params"]:
+        w["slot_params"][s] = synth.make_params(temperature=0.9, top_k=1, penalty_last_n=0, seed=s)
+    set_slots(sampler, w)
+    g1 = gpu_sample(sampler, w, top_n=0)
+    assert g1["ids"].tolist() == g["ids"].tolist()
+
+
+def test_batch_row_equals_solo_row(sampler):
+    w = synth.config5()
+    set_slots(sampler, w)
+    batch = gpu_sample(sampler, w)
+    for b in (0, 9, 33, 63):
+        wb = dict(w)
+        wb["B"] = 1
+        wb["logits"] = w["logits"][b:b + 1]
+        wb["row_slot"] = w["row_slot"][b:b + 1]
+        wb["row_pos"] = w["row_pos"][b:b + 1]
+        set_slots(sampler, w)
+        solo = gpu_sample(sampler, wb)
+        for k in ("ids", "chosen_lp", "top_ids", "top_lps", "topk_ids", "topk_vals", "kept"):
+            assert np.array_equal(solo[k][0], batch[k][b], equal_nan=(k == "topk_vals")), (b, k)
+
+
+def test_logprobs_off_changes_nothing(sampler):
+    w = synth.config4(fused=True)
+    set_slots(sampler, w)
+    with_lp = gpu_sample(sampler, w)
+    set_slots(sampler, w)
+    without = gpu_sample(sampler, w, top_n=0, with_allowed=False, chosen_lp=False, debug=False)
+    assert np.array_equal(with_lp["ids"], without["ids"])
+
+
+@pytest.mark.parametrize("flags", [1, 3])
+def test_pdl_flags_same_results(sampler, flags):
+    w = synth.config3()
+    set_slots(sampler, w)
+    a = gpu_sample(sampler, w)
+    set_slots(sampler, w)
+    b = gpu_sample(sampler, w, flags=flags)
+    for k in a:
+        assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+def test_graph_capture_replays_draw_fresh_numbers(sampler):
+    """A captured call advances the device counters on every replay (the pages moved sampling out of
+    the captured graph because a captured sampler replayed the same draws)."""
+    w = synth.config4(fused=True)
+    for s in w["slot_params"]:
+        w["slot_params"][s] = dict(w["slot_params"][s], temperature=2.0, top_k=64, top_p=1.0, min_p=0.0)
+    set_slots(sampler, w, {s: 0 for s in w["slot_params"]})
+    d = upload(w)
+    out = {"ids": torch.empty(w["B"], dtype=torch.int32, device="cuda:0")}
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=d["hist"],
+                       hist_off=d["hist_off"], out=out, stream=stream)   # warm-up call: counter 0
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=d["hist"],
+                           hist_off=d["hist_off"], out=out, stream=stream)
+    torch.cuda.synchronize()
+    counters = {s: 1 for s in w["slot_params"]}
+    seen = []
+    for _ in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        rows, counters = oracle.sample_call(w, counters=counters, top_n=0, with_allowed=False)
+        ids = out["ids"].cpu().numpy()
+        for b, r in enumerate(rows):
+            if not (r["flag_top_p"] or r["flag_draw"]):
+                assert int(ids[b]) == r["id"]
+        seen.append(ids.tolist())
+    assert seen[0] != seen[1] or seen[1] != seen[2]
+    assert sampler.slot_state(0)[1] == 4

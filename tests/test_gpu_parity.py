@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle on the same seeded inputs.
+
+Rules (written in the comparisons of tests/_harness.py): greedy ids, the top_k id sequence, the
+penalised values and the min_p survivor count bit-exact; top_p survivors and sampled ids exact
+except rows the oracle flags (a top_p or draw decision within 1e-6 of a boundary, counted and
+printed); log-probabilities within 1e-5 absolute.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+from _harness import Stats, compare_logprobs, compare_sample, gpu_logprobs, gpu_sample, set_slots, upload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sampler():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from request_token_sampling_gb300 import Sampler
+    s = Sampler(device=0, max_slots=64, max_vocab=synth.V_FULL, max_rows=256)
+    yield s
+    s.close()
+
+
+def _check_no_errors(sampler, allowed_bits=0):
+    bits = sampler.errors()
+    assert bits & ~allowed_bits == 0, hex(bits)
+
+
+def test_config1_single_row(sampler):
+    w = synth.config1()
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w)
+    rows, ctr = oracle.sample_call(w)
+    st = compare_sample(w, rows, g)
+    _check_no_errors(sampler)
+    assert sampler.slot_state(0)[1] == ctr[0] == 1
+    print("config1", st)
+
+
+def test_config2_verify_windows_counter_persists(sampler):
+    """100 consecutive 5-row windows of one request; the device counter carries across calls."""
+    w0 = synth.config2_window(0)
+    set_slots(sampler, w0, {0: 0})
+    st = Stats()
+    counters = {0: 0}
+    for win in range(synth.CONFIG2_WINDOWS):
+        w = synth.config2_window(win, counter=counters[0])
+        g = gpu_sample(sampler, w, top_n=0, chosen_lp=False)
+        rows, counters = oracle.sample_call(w, counters=counters)
+        compare_sample(w, rows, g, top_n=0, stats=st)
+    _check_no_errors(sampler)
+    assert sampler.slot_state(0)[1] == counters[0] == synth.CONFIG2_WINDOWS
+    print("config2", st)
+
+
+def test_config3_batch_slots_bf16(sampler):
+    w = synth.config3()
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w, top_n=0, chosen_lp=True)
+    rows, ctr = oracle.sample_call(w)
+    st = compare_sample(w, rows, g, top_n=0)
+    _check_no_errors(sampler)
+    for s in range(8):
+        assert sampler.slot_state(s)[1] == ctr[s]
+    print("config3", st)
+
+
+def test_config4_logprobs_entry(sampler):
+    w = synth.config4(fused=False)
+    g = gpu_logprobs(sampler, w)
+    ref = oracle.logprobs_call(w)
+    st = compare_logprobs(w, ref, g)
+    _check_no_errors(sampler)
+    print("config4 logprobs", st)
+
+
+def test_config4_fused_sample_and_logprobs(sampler):
+    w = synth.config4(fused=True)
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w)
+    rows, _ = oracle.sample_call(w)
+    st = compare_sample(w, rows, g)
+    _check_no_errors(sampler)
+    print("config4 fused", st)
+
+
+def test_config5_stress_bf16_ties(sampler):
+    w = synth.config5()
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w)
+    rows, ctr = oracle.sample_call(w)
+    st = compare_sample(w, rows, g)
+    _check_no_errors(sampler)
+    for s in range(8):
+        assert sampler.slot_state(s)[1] == ctr[s] == 1
+    print("config5", st)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_edge_cases(sampler, seed):
+    """Small, ragged and tie-heavy cases across row splits, dtypes, strides and slot mixes."""
+    rng = np.random.default_rng(1000 + seed)
+    V = int(rng.choice([1, 3, 17, 64, 65, 300, 1023, 4099, 20011, 70001]))
+    B = int(rng.integers(1, 12))
+    dtype = "bf16" if seed % 3 == 1 else "f32"
+    pad = int(rng.choice([0, 8, 24]))
+    w = synth.random_case(seed, B=B, V=V, dtype=dtype, ld=V + (-V % 8) + pad, n_slots=int(rng.integers(1, 6)),
+                          sampled_frac=0.7, hist_len=int(rng.choice([0, 5, 64, 300])),
+                          top_n=int(rng.integers(0, 21)), allowed_sizes=[0, 3, 50] if seed % 2 else None,
+                          ties=(seed % 4 == 0))
+    if seed % 5 == 2:
+        w["row_slot"][0] = 999          # an out-of-range slot: id -1 and the SLOT error bit
+    set_slots(sampler, w)
+    from request_token_sampling_gb300 import STRATA_FLAG_SPLIT
+    split = int(rng.choice([0, 0, 1, 2, 3, 16]))
+    esz = 2 if dtype == "bf16" else 4
+    if split and -(-V // split) * esz > 190_000:
+        split = 0
+    g = gpu_sample(sampler, w, flags=STRATA_FLAG_SPLIT(split))
+    rows, ctr = oracle.sample_call(w)
+    compare_sample(w, rows, g)
+    bits = sampler.errors()
+    expect = 0x01 if seed % 5 == 2 else 0
+    assert bits == expect, hex(bits)
+    for s in w["slot_params"]:
+        assert sampler.slot_state(s)[1] == ctr[s]
+
+
+@pytest.mark.parametrize("split", [6, 8, 13, 16])
+def test_full_vocab_every_split(sampler, split):
+    """The 248,320-id rows give the same answer whatever the number of CTAs per row."""
+    from request_token_sampling_gb300 import STRATA_FLAG_SPLIT
+    w = synth.config4(fused=True)
+    w["B"] = 3
+    w["logits"] = w["logits"][:3]
+    w["row_slot"], w["row_pos"] = w["row_slot"][:3], w["row_pos"][:3]
+    w["allowed_off"] = w["allowed_off"][:4]
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w, flags=STRATA_FLAG_SPLIT(split))
+    rows, _ = oracle.sample_call(w)
+    compare_sample(w, rows, g)
+    _check_no_errors(sampler)
+
+
+def test_heavy_ties_fallback(sampler):
+    """All-equal and two-level rows: more candidates than the per-CTA buffer (exact rounds path)."""
+    V = 50000
+    rows_np = np.zeros((4, V), np.float32)
+    rows_np[1, ::7] = 1.0
+    rows_np[2] = -0.0
+    rows_np[3, 12345] = 2.0
+    w = synth._workload("ties", "f32", V, rows_np,
+                        {s: synth.make_params(temperature=1.0, top_k=64, seed=9 + s, penalty_repeat=1.5,
+                                              penalty_last_n=8) for s in range(4)},
+                        [0, 1, 2, 3], [0, 1, 2, 3],
+                        [np.array([0, 7, 14, 40000], np.int32)] * 4, 20)
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w)
+    rows, _ = oracle.sample_call(w)
+    compare_sample(w, rows, g)
+    _check_no_errors(sampler)
+
+
+def test_logprobs_edge_cases(sampler):
+    rng = np.random.default_rng(5)
+    for V in (1, 7, 20, 21, 333, 40000):
+        B = 3
+        x = np.full((B, V + (-V % 4)), -7.0, np.float32)
+        x[:, :V] = (rng.standard_normal((B, V)) * 4).astype(np.float32)
+        allowed = [np.array([0, V - 1, 0], np.int32), np.zeros(0, np.int32),
+                   np.concatenate([rng.integers(0, V, 40), [-1, V]]).astype(np.int32)]
+        w = synth._workload("lp", "f32", V, x, {}, [0] * B, [0] * B, [], 20, allowed_lists=allowed,
+                            chosen=np.array([0, V - 1, V], np.int32))
+        g = gpu_logprobs(sampler, w)
+        ref = oracle.logprobs_call(w)
+        compare_logprobs(w, ref, g)
+        assert sampler.errors() == 0x02 | 0x04     # out-of-range allowed and chosen ids flagged
