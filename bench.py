@@ -248,8 +248,8 @@ def run_gpu(args, rank, world):
     B = w["B"]
     step_bytes = B * w["V"] * 4
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-    R = max(2, -(-4 * l2 // step_bytes))
-    flags = 0 if args.no_pdl else (STRATA_FLAG_PDL | (STRATA_FLAG_EARLY_LOAD if args.early_load else 0))
+    R = max(2, -(-4 * l2 // step_bytes)) if args.batches <= 0 else args.batches
+    flags = 0 if args.no_pdl else (STRATA_FLAG_PDL | (0 if args.no_early_load else STRATA_FLAG_EARLY_LOAD))
 
     s = Sampler(device=local, max_slots=16, max_vocab=w["V"], max_rows=B)
     for slot, p in w["slot_params"].items():
@@ -385,9 +385,10 @@ def run_gpu(args, rank, world):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "rows_per_step": B, "V": w["V"], "logits_dtype": "f32",
                    "l2_policy": f"inputs rotate over {R} distinct batches ({R * step_bytes / 1e6:.0f} MB, "
-                                f">= 4x the {l2 / 1e6:.0f} MB L2)",
+                                f"{R * step_bytes / l2:.1f}x the {l2 / 1e6:.0f} MB L2)",
                    "launch": "one CUDA graph of the K calls" + (", programmatic dependent launch" if flags & 1 else "")
-                             + (", early logit loads" if flags & 2 else ""),
+                             + (", logit loads start before the previous call ends (inputs resident)"
+                                if flags & 2 else ""),
                    "split": shape["split"], "chunk_elems": shape["chunk"], "smem_bytes": shape["smem"],
                    "grid": shape["grid"], "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -410,9 +411,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["own", "reference"], default="own")
     ap.add_argument("--no-pdl", action="store_true")
-    ap.add_argument("--early-load", action="store_true")
+    ap.add_argument("--no-early-load", action="store_true",
+                    help="with PDL, wait for the previous kernel before loading logits (inputs produced by it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--batches", type=int, default=0,
+                    help="distinct input batches to rotate over (0: enough for 4x the L2 size)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -117,15 +117,15 @@ const char *strata_last_error(void);
 void strata_default_params(strata_sampling_params *p);
 
 /* Check keys without a context: STRATA_OK or STRATA_EINVAL (reason in strata_last_error).
- * A value the engine cannot honour is refused rather than changed [P19, "server.py ...":
- * a typo'd config should not quietly change sampling].  Host only, no CUDA call. */
+ * An invalid key is rejected, never silently adjusted [P19, "server.py forwards the block to
+ * the engine"].  Host only, no CUDA call. */
 int strata_validate_params(const strata_sampling_params *p);
 
 /*
  * Create a context on `device` (must be the calling thread's current device) for up to
  * `max_slots` request slots (1..65536), vocabularies up to `max_vocab` (1..STRATA_MAX_VOCAB)
- * and up to `max_rows` rows per call (1..65536).  Allocates the device slot table (keys and
- * 64-bit draw counters, all slots greedy-neutral with counter 0) and a device error word.
+ * and up to `max_rows` rows per call (1..65535).  Allocates the device slot table (keys and
+ * 48-bit draw counters, all slots greedy-neutral with counter 0) and a device error word.
  * Synchronous.  Returns STRATA_ECUDA when no usable device is present.
  */
 int strata_create(strata_ctx **out, int device, int max_slots, int max_vocab, int max_rows);
@@ -148,7 +148,7 @@ int strata_get_slot_state(strata_ctx *ctx, int slot, strata_sampling_params *p,
                           uint64_t *counter, void *stream);
 
 /* Restore a slot's keys and counter exactly (checkpoint/resume of a request); asynchronous on
- * `stream` like strata_set_slot_params. */
+ * `stream` like strata_set_slot_params.  Counters are 48-bit: a value >= 2^48 is STRATA_ERANGE. */
 int strata_set_slot_state(strata_ctx *ctx, int slot, const strata_sampling_params *p,
                           uint64_t counter, void *stream);
 
@@ -167,7 +167,7 @@ int strata_set_slot_state(strata_ctx *ctx, int slot, const strata_sampling_param
  *   hist_off    device int32[n_hist_slots+1]: slot s owns hist[hist_off[s] .. hist_off[s+1]).
  *               The penalties count the last min(penalty_last_n, length) ids of the slot's run;
  *               ids outside [0, V) are ignored.  hist/hist_off NULL (or a slot >= n_hist_slots)
- *               means no history: the byte-for-byte neutral path [P19].
+ *               means no history: the penalty stage is skipped and the logits are used unchanged [P19].
  *   out_ids     device int32[B]: the sampled id of each row (always written; -1 for a row whose
  *               slot is out of range, with STRATA_DEVERR_SLOT).
  *   Optional fused logprobs of the raw (pre-penalty, pre-temperature) logits [P3200, P1916];
@@ -179,7 +179,7 @@ int strata_set_slot_state(strata_ctx *ctx, int slot, const strata_sampling_param
  *               padded with id -1 and -inf.
  *   allowed     device int32[]: concatenated allowed_token_ids of rows 0..B-1;
  *   allowed_off device int32[B+1]: row b names allowed[allowed_off[b] .. allowed_off[b+1]);
- *   allowed_lps device float[allowed_off[B]]: log-probabilities renormalised over exactly the
+ *   allowed_lps device float[allowed_off[B]]: log-probabilities normalised over only the
  *               named ids, in the caller's order (a repeated id counts once in the normaliser).
  *   Optional debug outputs (NULL = off): topk_ids int32[B][64] and topk_vals float[B][64] (the
  *   ordered survivors of top_k and their penalised logits, padded with -1 / NaN), kept

@@ -163,7 +163,7 @@ def rank_order(values32: np.ndarray) -> np.ndarray:
     """All ids ordered by value descending, ties to the lowest index, NaN last.
 
     "#19 ...", "The sampled chain is one block per token": k argmax rounds whose ties resolve to
-    the lowest index (the serial scan's strict >); the first k entries of this order are the k
+    the lowest index (a serial scan that only replaces on a strictly larger value); the first k entries of this order are the k
     rounds' winners in order.
     """
     v = np.asarray(values32, dtype=np.float32).astype(np.float64)
@@ -175,7 +175,7 @@ def min_p_cut(sel: np.ndarray, min_p: float) -> int:
     """Kept prefix length after min_p, in logit space, float32.
 
     "#19 ...", "min_p and the penalties": keep the prefix with sel_logit >= sel_logit[0] +
-    logf(min_p); 0 disables; the head always survives so the kept count never reaches zero.
+    logf(min_p); 0 disables; the top survivor is never cut, so at least one id is kept.
     """
     k = sel.size
     if not (np.float32(min_p) > 0):
@@ -189,7 +189,7 @@ def top_p_cut(sel: np.ndarray, m1: int, top_p: float):
     """Kept prefix length after top_p over the min_p survivors; returns (m2, flagged).
 
     Reading: probabilities at temperature 1 renormalised over the m1 survivors (min_p runs
-    first "so the two cuts compose"); keep the smallest prefix whose mass reaches top_p.
+    first and the page has the two cuts compose); keep the smallest prefix whose mass reaches top_p.
     """
     tp = float(np.float32(top_p))
     if tp >= 1.0:
@@ -229,7 +229,7 @@ def log_softmax(raw32: np.ndarray) -> np.ndarray:
 
 
 def allowed_renorm(raw32: np.ndarray, allowed) -> np.ndarray:
-    """log-probabilities renormalised over exactly the named ids, in the caller's order.
+    """log-probabilities normalised over the caller's subset of ids only, in the caller's order.
 
     "#3200 ...", "Problem and result": allowed_token_ids returns a distribution renormalised over
     exactly the ids the caller named.  Reading: a repeated id counts once in the normaliser and is

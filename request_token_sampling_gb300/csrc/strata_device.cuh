@@ -84,6 +84,13 @@ __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, uint32_t a, uint32_t 
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
+// Atomic add on a cluster CTA's shared memory word; returns the previous value.
+__device__ __forceinline__ uint32_t dsmem_atomic_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void dsmem_st_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
@@ -174,12 +181,69 @@ __device__ __forceinline__ MaxSum warp_ms(MaxSum x) {
   return x;
 }
 
-__device__ __forceinline__ double warp_scan_incl(double x, int lane) {
+// Warp (max, sum of exp) of per-lane pairs: the max by one redux on order keys, then every
+// lane's sum rescaled to it and added by butterfly shuffles (short dependency chain).
+__device__ __forceinline__ MaxSum warp_ms_fast(MaxSum x) {
+  const uint32_t km = __reduce_max_sync(FULL_MASK, order_key(x.m));
+  const float M = (km == 0u) ? -INFINITY : key_value(km);
+  float s = (x.m == -INFINITY || M == -INFINITY || !(x.s > 0.0f)) ? 0.0f : x.s * ex2_approx((x.m - M) * LOG2E);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(FULL_MASK, s, off);
+  return {M, s};
+}
+
+// ------------------------------------------------------------------------------ double-word fp32
+// A value carried as an unevaluated sum hi + lo of two floats, added with Knuth's TwoSum (an
+// error-free transformation), so a prefix sum of <= 64 terms keeps ~44 significant bits without
+// FP64 arithmetic.
+struct DW {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DW two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+__device__ __forceinline__ DW dw_add(DW x, DW y) {
+  const DW s = two_sum(x.hi, y.hi);
+  const float lo = __fadd_rn(__fadd_rn(x.lo, y.lo), s.lo);
+  const float hi = __fadd_rn(s.hi, lo);
+  return {hi, __fsub_rn(lo, __fsub_rn(hi, s.hi))};
+}
+
+// x * y for a float y, with the product's rounding error recovered by a fused multiply-add.
+__device__ __forceinline__ DW dw_mul_f(DW x, float y) {
+  const float p = __fmul_rn(x.hi, y);
+  const float e = __fmaf_rn(x.hi, y, -p);
+  const float lo = __fadd_rn(e, __fmul_rn(x.lo, y));
+  const float hi = __fadd_rn(p, lo);
+  return {hi, __fsub_rn(lo, __fsub_rn(hi, p))};
+}
+
+// Sign of a - b for double-word values (the high parts are close whenever the sign is in doubt).
+__device__ __forceinline__ bool dw_less(DW a, DW b) {
+  return __fadd_rn(__fsub_rn(a.hi, b.hi), __fsub_rn(a.lo, b.lo)) < 0.0f;
+}
+
+__device__ __forceinline__ DW warp_scan_dw(DW x, int lane) {
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const double y = __shfl_up_sync(FULL_MASK, x, off);
-    if (lane >= off) x += y;
+    const DW y{__shfl_up_sync(FULL_MASK, x.hi, off), __shfl_up_sync(FULL_MASK, x.lo, off)};
+    if (lane >= off) x = dw_add(y, x);
   }
+  return x;
+}
+
+__device__ __forceinline__ DW shfl_dw(DW x, int src) {
+  return {__shfl_sync(FULL_MASK, x.hi, src), __shfl_sync(FULL_MASK, x.lo, src)};
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(FULL_MASK, x, off);
   return x;
 }
 

@@ -58,6 +58,11 @@ enum : int {
   CTL_CTR_LO = 3,
   CTL_CTR_HI = 4,
   CTL_TIMEOUT = 5,
+  CTL_X0 = 6,        // first Philox word of the leader's row
+  CTL_RECV_NP = 7,   // leader: entries received in the flat penalised / raw lists
+  CTL_RECV_NR = 8,
+  CTL_BASE_P = 9,    // this CTA's slice of the leader's lists
+  CTL_BASE_R = 10,
   CTL_WORDS = 16
 };
 
@@ -99,8 +104,7 @@ struct KParams {
   float* topk_vals;
   int32_t* kept;
   const SlotDev* slots;
-  unsigned long long* ctr;
-  uint32_t* arrivals;
+  unsigned long long* ctr;  // per slot: (draw counter << 16) | arrivals of the current call
   int max_slots;
   uint32_t* err;
   int hash_cap, hash_bits;
@@ -265,16 +269,18 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int
 
 // ------------------------------------------------------------------------------ the kernel
 template <int DT>
-__global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
+__global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char sm[];
   constexpr int ESZ = DT == 0 ? 4 : 2;
   constexpr int EPV = 16 / ESZ;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool early = (P.flags & STRATA_FLAG_EARLY_LOAD) != 0u;
+  if (!early) grid_dep_wait();  // inputs may be the previous kernel's outputs
+
   const uint32_t crank = cluster_ctarank();
   const int cs = P.cs;
   const int row = blockIdx.x / cs;
   const Layout L = make_layout(P.chunk, ESZ, P.hash_cap, cs, P.kmax, P.nmax);
-
   const int lo = static_cast<int>(crank) * P.chunk;
   const int hi = min(P.V, lo + P.chunk);
   const int n_el = max(0, hi - lo);
@@ -285,10 +291,26 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
 
   unsigned char* data = sm + L.data;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + L.mbar);
+  const char* grow = static_cast<const char*>(P.logits) + (static_cast<long long>(row) * P.ld + lo) * ESZ;
+
+  // ---- 1. the bulk copies of this chunk go out first ---------------------------------------
+  if (wid == 0) {  // lane 0 initialises the piece barriers, lane p issues piece p
+    if (lane == 0) {
+      for (int p = 0; p < n_pieces; ++p) mbar_init(&mbar[p], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    for (int p = lane; p < n_pieces; p += 32) {
+      const uint32_t nb = static_cast<uint32_t>(min(PIECE_BYTES, bytes_al - p * PIECE_BYTES));
+      mbar_arrive_expect_tx(&mbar[p], nb);
+      bulk_g2s(data + p * PIECE_BYTES, grow + p * PIECE_BYTES, nb, &mbar[p]);
+    }
+  }
+  grid_dep_launch();
+
   uint32_t* hbits = reinterpret_cast<uint32_t*>(sm + L.hbits);
   uint32_t* abits = reinterpret_cast<uint32_t*>(sm + L.abits);
   uint32_t* htab = reinterpret_cast<uint32_t*>(sm + L.hash);
-  uint32_t* dirty = reinterpret_cast<uint32_t*>(sm + L.dirty);
   uint32_t* tc_arr = reinterpret_cast<uint32_t*>(sm + L.tc);
   float4* ms_arr = reinterpret_cast<float4*>(sm + L.ms);
   uint32_t* wtop = reinterpret_cast<uint32_t*>(sm + L.wtop);
@@ -299,27 +321,6 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
   uint64_t* cand_raw = reinterpret_cast<uint64_t*>(sm + L.cand_raw);
   const uint4* recv_pen = reinterpret_cast<const uint4*>(sm + L.recv_pen);
   const uint64_t* recv_raw = reinterpret_cast<const uint64_t*>(sm + L.recv_raw);
-  const uint2* recv_cnt = reinterpret_cast<const uint2*>(sm + L.recv_cnt);
-
-  const char* grow = static_cast<const char*>(P.logits) + (static_cast<long long>(row) * P.ld + lo) * ESZ;
-  const bool early = (P.flags & STRATA_FLAG_EARLY_LOAD) != 0u;
-
-  // ---- 1. start the bulk copies of this chunk ------------------------------------------------
-  if (tid == 0) {
-    for (int p = 0; p < n_pieces; ++p) mbar_init(&mbar[p], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (!early) grid_dep_wait();
-  if (tid == 0) {
-    for (int p = 0; p < n_pieces; ++p) {
-      const uint32_t nb = static_cast<uint32_t>(min(PIECE_BYTES, bytes_al - p * PIECE_BYTES));
-      mbar_arrive_expect_tx(&mbar[p], nb);
-      bulk_g2s(data + p * PIECE_BYTES, grow + p * PIECE_BYTES, nb, &mbar[p]);
-    }
-  }
-  if (early) grid_dep_wait();
-  grid_dep_launch();
 
   // The ragged last vector (chunk bytes not a multiple of 16) is read with plain loads by its
   // owner thread, padded with -inf.
@@ -348,12 +349,11 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
     abits[i] = 0u;
   }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
-  if (tid < NT / 32) dirty[tid] = 0u;
   if (tid < CTL_WORDS) ctl[tid] = 0u;
-  __syncthreads();
-  cluster_arrive();  // every CTA of the cluster is running before any DSMEM store (waited below)
+  __syncthreads();   // tables zeroed, piece barriers initialised
+  cluster_arrive();  // every CTA of the cluster is running before any DSMEM access (waited below)
 
-  // ---- row metadata -------------------------------------------------------------------------
+  // ---- row metadata (inputs only: slot keys are never written by a kernel) -------------------
   int slot = -1;
   bool valid = true;
   SlotDev sp{};
@@ -364,63 +364,68 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
   }
   const bool sampled = valid && (sp.flags & SLOT_SAMPLED);
   const int k_row = (P.mode == MODE_SAMPLE && valid) ? min(max(sp.k, 1), P.kmax) : 0;
-  if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
   const int n_row = P.nmax;
   const int kp = max(k_row, n_row);
   const int q = (kp + cs - 1) / cs;
   const bool penal = (P.mode == MODE_SAMPLE) && valid && (sp.flags & SLOT_PENAL) && P.hist_off != nullptr &&
                      slot < P.n_hist_slots && P.hash_cap > 0;
-
-  // ---- history table of this chunk's id range ------------------------------------------------
-  if (penal) {
-    const int hb = P.hist_off[slot], he = P.hist_off[slot + 1];
-    const int h = min(sp.last_n, max(0, he - hb));
-    const int start = he - h;
-    for (int i = tid; i < h; i += NT) {
-      const int id = P.hist[start + i];
-      if (id >= lo && id < hi) {
-        const uint32_t loc = static_cast<uint32_t>(id - lo);
-        atomicOr(&hbits[loc >> 5], 1u << (loc & 31));
-        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
-        const uint32_t owner = (loc / EPV) % NT;
-        atomicOr(&dirty[owner >> 5], 1u << (owner & 31));
-      }
-    }
-  }
-
-  // allowed ids of this row (first two per thread prefetched) and the chosen id
+  const unsigned long long pos = (P.mode == MODE_SAMPLE) ? static_cast<unsigned long long>(P.row_pos[row]) : 0ull;
+  const int chosen_id = (P.mode == MODE_LOGPROBS && P.chosen != nullptr) ? P.chosen[row] : -1;
   int a_beg = 0, a_end = 0;
   if (P.allowed_off != nullptr) {
     a_beg = P.allowed_off[row];
     a_end = P.allowed_off[row + 1];
   }
-  const int aid0 = (a_beg + tid < a_end) ? P.allowed[a_beg + tid] : -1;
-  const int aid1 = (a_beg + tid + NT < a_end) ? P.allowed[a_beg + tid + NT] : -1;
-  const int chosen_id = (P.mode == MODE_LOGPROBS && P.chosen != nullptr) ? P.chosen[row] : -1;
-
-  // ---- the draw counter: read once, the last row of the slot advances it ----------------------
-  if (crank == 0 && sampled) {
-    int cnt = 0;
-    for (int b0 = 0; b0 < P.B; b0 += NT) {
-      const int b = b0 + tid;
-      cnt += __syncthreads_count(b < P.B && P.row_slot[b] == slot);
-    }
-    if (tid == 0) {
-      const unsigned long long c = *reinterpret_cast<volatile unsigned long long*>(&P.ctr[slot]);
-      __threadfence();
-      const unsigned a = atomicAdd(&P.arrivals[slot], 1u);
-      __threadfence();
-      if (a + 1u == static_cast<unsigned>(cnt)) {
-        P.ctr[slot] = c + 1ull;
-        P.arrivals[slot] = 0u;
-      }
-      ctl[CTL_CTR_LO] = static_cast<uint32_t>(c);
-      ctl[CTL_CTR_HI] = static_cast<uint32_t>(c >> 32);
+  // the first two allowed ids of this thread: mark the chunk's dedup bits now (before the data)
+  int aid[2];
+  bool acount[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int j = a_beg + tid + t * NT;
+    aid[t] = j < a_end ? P.allowed[j] : -1;
+    acount[t] = false;
+    if (aid[t] >= lo && aid[t] < hi) {
+      const uint32_t loc = static_cast<uint32_t>(aid[t] - lo);
+      const uint32_t bit = 1u << (loc & 31);
+      acount[t] = !(atomicOr(&abits[loc >> 5], bit) & bit);
     }
   }
 
-  // ---- 1b. first pass as pieces land: running max and sum of exp ----------------------------
+  // The draw counter: each sampled row adds one arrival to its slot's packed word (counter << 16 |
+  // arrivals) and reads the counter from the returned value; the row that completes the slot's
+  // arrivals also advances the counter and clears them, so every row of the call sees the value
+  // from before the call.  Issued early, consumed just before the leader's merge.
+  const bool ctr_warp = k_row > 0 && wid == 0 && crank == 0 && sampled;
+  const bool ctr_thread = ctr_warp && lane == 0;
+  int r_s = 0;
+  unsigned long long ctr_old = 0ull;
+  if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
+  if (ctr_warp) {
+    for (int b0 = 0; b0 < P.B; b0 += 32) {
+      const int b = b0 + lane;
+      r_s += __popc(__ballot_sync(FULL_MASK, b < P.B && P.row_slot[b] == slot));
+    }
+  }
+
+  // ---- history table of this chunk's id range ------------------------------------------------
+  if (penal) {
+    const int hb = P.hist_off[slot], he = P.hist_off[slot + 1];
+    const int h_len = min(sp.last_n, max(0, he - hb));
+    const int h_start = he - h_len;
+    for (int i = tid; i < h_len; i += NT) {
+      const int id = P.hist[h_start + i];
+      if (id >= lo && id < hi) {
+        const uint32_t loc = static_cast<uint32_t>(id - lo);
+        atomicOr(&hbits[loc >> 5], 1u << (loc & 31));
+        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
+      }
+    }
+  }
+
+  // ---- 1b. first pass as pieces land: running (max, sum of exp) and this thread's top two ------
   MaxSum acc{-INFINITY, 0.0f};
+  float v1 = -INFINITY, v2 = -INFINITY;
+  int i1 = -1, i2 = -1;
   {
     int waited = -1;
     int i = 0;
@@ -446,60 +451,86 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
         for (int e = 0; e < EPV; ++e) t += ex2_approx(fmaf(x[e], LOG2E, -mb));
         acc.s += t;
       }
+      if (vm > v2) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const int loc = v * EPV + e;
+          if (x[e] > v2 && loc < n_el) {
+            if (x[e] > v1) {
+              v2 = v1;
+              i2 = i1;
+              v1 = x[e];
+              i1 = loc;
+            } else {
+              v2 = x[e];
+              i2 = loc;
+            }
+          }
+        }
+      }
     }
   }
-  for (int p = 0; p < n_pieces; ++p) wait_piece(mbar, p, ctl, P.err);  // all pieces visible
-  __syncthreads();
+  for (int p = 0; p < n_pieces; ++p) wait_piece(mbar, p, ctl, P.err);  // all pieces visible here
+  __syncthreads();  // history table and allowed dedup bits complete
 
-  // per-thread maximum over the ids that carry no penalty (the threshold's elements)
-  bool has_m = tid < n_vec;
-  float mm = acc.m;
-  if (penal && ((dirty[tid >> 5] >> (tid & 31)) & 1u)) {
-    mm = -INFINITY;
-    has_m = false;
+  // this thread's top two over the ids that carry no penalty (the threshold's elements)
+  if (penal && ((i1 >= 0 && bit_at(hbits, static_cast<uint32_t>(i1))) ||
+                (i2 >= 0 && bit_at(hbits, static_cast<uint32_t>(i2))))) {
+    v1 = v2 = -INFINITY;
+    i1 = i2 = -1;
     for (int v = tid; v < n_vec; v += NT) {
       float x[EPV];
       load_vec<DT>(data, v, x);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-        if (loc < static_cast<uint32_t>(n_el) && !bit_at(hbits, loc)) {
-          mm = fmaxf(mm, x[e]);
-          has_m = true;
+        const int loc = v * EPV + e;
+        if (loc < n_el && x[e] > v2 && !bit_at(hbits, static_cast<uint32_t>(loc))) {
+          if (x[e] > v1) {
+            v2 = v1;
+            i2 = i1;
+            v1 = x[e];
+            i1 = loc;
+          } else {
+            v2 = x[e];
+            i2 = loc;
+          }
         }
       }
     }
   }
-  const uint32_t ord_t = has_m ? order_key(mm) : 0u;
+  const uint32_t o1 = (i1 >= 0) ? order_key(v1) : 0u;
+  const uint32_t o2 = (i2 >= 0) ? order_key(v2) : 0u;
 
-  // ---- 2. threshold t_c, block (max,sum) of the row and of the allowed subset -----------------
+  // ---- 2. threshold t_c and the CTA's (max, sum) of the row and of the allowed subset ---------
   if (kp > 0 && q <= QMAX) {
-    uint32_t key = ord_t;
+    uint32_t key = o1;
     for (int r = 0; r < q; ++r) {
       const uint32_t mx = __reduce_max_sync(FULL_MASK, key);
-      if (lane == 0) wtop[wid * QMAX + r] = mx;
+      if (lane == 0) wtop[wid * q + r] = mx;
       const uint32_t bal = __ballot_sync(FULL_MASK, key == mx);
       if (lane == __ffs(bal) - 1) key = 0u;
     }
   }
   MaxSum al{-INFINITY, 0.0f};
-  {
-    auto add_allowed = [&](int id) {
-      if (id >= lo && id < hi) {
-        const uint32_t loc = static_cast<uint32_t>(id - lo);
-        const uint32_t bit = 1u << (loc & 31);
-        const uint32_t old = atomicOr(&abits[loc >> 5], bit);
-        if (!(old & bit)) online_add(al, elem_at<DT>(data, loc));
-      }
-    };
-    add_allowed(aid0);
-    add_allowed(aid1);
-    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) add_allowed(P.allowed[j]);
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    if (acount[t]) online_add(al, elem_at<DT>(data, static_cast<uint32_t>(aid[t] - lo)));
+  for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) {
+    const int id = P.allowed[j];
+    if (id >= lo && id < hi) {
+      const uint32_t loc = static_cast<uint32_t>(id - lo);
+      const uint32_t bit = 1u << (loc & 31);
+      if (!(atomicOr(&abits[loc >> 5], bit) & bit)) online_add(al, elem_at<DT>(data, loc));
+    }
   }
-  const MaxSum wrow = warp_ms(acc);
-  const MaxSum wal = warp_ms(al);
-  if (lane == 0) red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
+  {
+    const MaxSum wrow = warp_ms_fast(acc);
+    const MaxSum wal = warp_ms_fast(al);
+    if (lane == 0) red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
+  }
   __syncthreads();
+  float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
+  uint32_t tq = 0u;
   if (wid == 0) {
     MaxSum r1{-INFINITY, 0.0f}, r2{-INFINITY, 0.0f};
     if (lane < NW) {
@@ -507,65 +538,312 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
       r1 = {t.x, t.y};
       r2 = {t.z, t.w};
     }
-    r1 = warp_ms(r1);
-    r2 = warp_ms(r2);
-    uint32_t tq = 0u;
+    r1 = warp_ms_fast(r1);
+    r2 = warp_ms_fast(r2);
+    mine = make_float4(r1.m, r1.s, r2.m, r2.s);
     if (kp > 0 && q <= QMAX) {
       uint32_t vals[4];
       const int nv = NW * q;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int f = lane + 32 * j;
-        vals[j] = (f < nv) ? wtop[(f / q) * QMAX + (f % q)] : 0u;
-      }
+      for (int j = 0; j < 4; ++j) vals[j] = (lane + 32 * j < nv) ? wtop[lane + 32 * j] : 0u;
       for (int r = 0; r < q; ++r) {
-        uint32_t lm = vals[0];
-#pragma unroll
-        for (int j = 1; j < 4; ++j) lm = vals[j] > lm ? vals[j] : lm;
+        const uint32_t lm = max(max(vals[0], vals[1]), max(vals[2], vals[3]));
         const uint32_t mx = __reduce_max_sync(FULL_MASK, lm);
         const uint32_t bal = __ballot_sync(FULL_MASK, lm == mx);
         if (lane == __ffs(bal) - 1) {
-          bool done = false;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (!done && vals[j] == mx) {
-              vals[j] = 0u;
-              done = true;
-            }
-          }
+          if (vals[0] == mx) vals[0] = 0u;
+          else if (vals[1] == mx) vals[1] = 0u;
+          else if (vals[2] == mx) vals[2] = 0u;
+          else vals[3] = 0u;
         }
         tq = mx;
       }
     }
-    if (lane == 0) {
-      ctl[CTL_TC] = tq;
-      red4[NW] = make_float4(r1.m, r1.s, r2.m, r2.s);
-    }
   }
-  __syncthreads();
 
   // ---- exchange through DSMEM (cluster barrier B0) ---------------------------------------------
   cluster_wait();
-  if (tid < cs) {
-    const float4 t = red4[NW];
-    const uint32_t r = static_cast<uint32_t>(tid);
-    dsmem_st_u32(dsmem_addr(smem_u32(tc_arr + crank), r), ctl[CTL_TC]);
-    dsmem_st_v4(dsmem_addr(smem_u32(ms_arr + crank), r), __float_as_uint(t.x), __float_as_uint(t.y),
-                __float_as_uint(t.z), __float_as_uint(t.w));
+  if (wid == 0 && lane < cs) {
+    const uint32_t r = static_cast<uint32_t>(lane);
+    dsmem_st_u32(dsmem_addr(smem_u32(tc_arr + crank), r), tq);
+    dsmem_st_v4(dsmem_addr(smem_u32(ms_arr + crank), r), __float_as_uint(mine.x), __float_as_uint(mine.y),
+                __float_as_uint(mine.z), __float_as_uint(mine.w));
   }
   cluster_arrive();
   cluster_wait();
 
-  uint32_t T = 0xFFFFFFFFu;
-  MaxSum g{-INFINITY, 0.0f}, ga{-INFINITY, 0.0f};
-  for (int c = 0; c < cs; ++c) {
-    T = min(T, tc_arr[c]);
-    const float4 t = ms_arr[c];
-    g = ms_combine(g, MaxSum{t.x, t.y});
-    ga = ms_combine(ga, MaxSum{t.z, t.w});
+  // every warp reduces the cluster's contributions itself (lane c holds CTA c's)
+  uint32_t T;
+  float lse, lse_a;
+  {
+    const bool in = lane < cs;
+    const float4 t = in ? ms_arr[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    T = __reduce_min_sync(FULL_MASK, in ? tc_arr[lane] : 0xFFFFFFFFu);
+    const MaxSum g = warp_ms_fast(MaxSum{t.x, t.y});
+    const MaxSum ga = warp_ms_fast(MaxSum{t.z, t.w});
+    lse = (g.m == -INFINITY || !(g.s > 0.0f)) ? -INFINITY : g.m + logf(g.s);
+    lse_a = (ga.m == -INFINITY || !(ga.s > 0.0f)) ? -INFINITY : ga.m + logf(ga.s);
   }
-  const float lse = (g.m == -INFINITY || !(g.s > 0.0f)) ? -INFINITY : g.m + logf(g.s);
-  const float lse_a = (ga.m == -INFINITY || !(ga.s > 0.0f)) ? -INFINITY : ga.m + logf(ga.s);
+  // state of the tail, carried across the wait for the previous kernel (leader, warp 0)
+  int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0;
+  DW Ca{0.0f, 0.0f}, Cb{0.0f, 0.0f}, W{0.0f, 0.0f};
+  uint4 ea = make_uint4(0, 0, 0, 0), eb = make_uint4(0, 0, 0, 0);
+  float va = 0.0f, vb = 0.0f;
+
+  // ---- 3. candidates of this chunk: every element at or above the row threshold T ------------
+  if (kp > 0) {
+    if (q > QMAX) T = 0u;  // no usable bound: every element is a candidate
+    auto put = [&](uint64_t key, float raw, bool to_raw, bool to_pen) {
+      if (to_raw && n_row > 0) {
+        const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
+        if (i < LOCAL_CAP) cand_raw[i] = key;
+      }
+      if (to_pen && k_row > 0) {
+        const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+        if (i < LOCAL_CAP)
+          cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
+                                   __float_as_uint(raw), 0u);
+      }
+    };
+    // a thread whose second best reaches T may hold more: it rescans its own elements
+    const bool full = (T == 0u && tid < n_vec) || (o2 != 0u && o2 >= T);
+    if (full) {
+      for (int v = tid; v < n_vec; v += NT) {
+        float x[EPV];
+        load_vec<DT>(data, v, x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+          const uint32_t o = order_key(x[e]);
+          if (loc >= static_cast<uint32_t>(n_el) || o == 0u || o < T) continue;
+          if (penal && bit_at(hbits, loc)) continue;
+          put(sel_key(o, static_cast<uint32_t>(lo) + loc), x[e], true, true);
+        }
+      }
+    }
+    {  // the common case: at most this thread's best reaches T (one warp-wide append per list)
+      const bool one = !full && o1 != 0u && o1 >= T;
+      const uint32_t bal = __ballot_sync(FULL_MASK, one);
+      if (bal != 0u) {
+        const int leader = __ffs(bal) - 1;
+        const uint32_t before = __popc(bal & ((1u << lane) - 1u));
+        uint32_t base_r = 0, base_p = 0;
+        if (lane == leader) {
+          if (n_row > 0) base_r = atomicAdd(&ctl[CTL_CAND_RAW], static_cast<uint32_t>(__popc(bal)));
+          if (k_row > 0) base_p = atomicAdd(&ctl[CTL_CAND_PEN], static_cast<uint32_t>(__popc(bal)));
+        }
+        base_r = __shfl_sync(FULL_MASK, base_r, leader) + before;
+        base_p = __shfl_sync(FULL_MASK, base_p, leader) + before;
+        if (one) {
+          const uint64_t key = sel_key(o1, static_cast<uint32_t>(lo + i1));
+          if (n_row > 0 && base_r < LOCAL_CAP) cand_raw[base_r] = key;
+          if (k_row > 0 && base_p < LOCAL_CAP)
+            cand_pen[base_p] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
+                                          __float_as_uint(v1), 0u);
+        }
+      }
+    }
+    if (penal) {  // penalised ids: raw value for the raw list, penalised value for the other
+      for (int i = tid; i < P.hash_cap; i += NT) {
+        const uint32_t ent = htab[i];
+        if (ent == HASH_EMPTY) continue;
+        const uint32_t loc = ent >> HASH_CNT_BITS;
+        const uint32_t c = ent & ((1u << HASH_CNT_BITS) - 1u);
+        const float raw = elem_at<DT>(data, loc);
+        const uint32_t id = static_cast<uint32_t>(lo) + loc;
+        const uint32_t o = order_key(raw);
+        if (o != 0u && o >= T) put(sel_key(o, id), raw, true, false);
+        const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
+        const uint32_t op = order_key(pv);
+        if (op != 0u && op >= T) put(sel_key(op, id), raw, false, true);
+      }
+    }
+    __syncthreads();
+
+    int np = static_cast<int>(ctl[CTL_CAND_PEN]);
+    int nr = static_cast<int>(ctl[CTL_CAND_RAW]);
+    // more candidates than the buffer holds (heavy ties): exact argmax rounds write the chunk's
+    // best k_row / n_row in order into the candidate buffers
+    if ((k_row > 0 && np > LOCAL_CAP) || (n_row > 0 && nr > LOCAL_CAP)) {
+      const bool do_p = k_row > 0 && np > LOCAL_CAP, do_r = n_row > 0 && nr > LOCAL_CAP;
+      for (int list = 0; list < 2; ++list) {
+        if (list == 0 ? !do_p : !do_r) continue;
+        const int need = list == 0 ? k_row : n_row;
+        uint64_t prev = ~0ull;
+        int got = 0;
+        for (int r = 0; r < need; ++r) {
+          uint64_t best = 0ull;
+          for (int v = tid; v < n_vec; v += NT) {
+            float x[EPV];
+            load_vec<DT>(data, v, x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+              if (loc >= static_cast<uint32_t>(n_el)) continue;
+              float pv = x[e];
+              if (list == 0 && penal && bit_at(hbits, loc))
+                pv = penalize(pv, hash_count(htab, P.hash_bits, loc), sp.rep, sp.freq, sp.pres);
+              const uint32_t o = order_key(pv);
+              if (o == 0u) continue;
+              const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
+              if (key < prev && key > best) best = key;
+            }
+          }
+          best = block_max_u64(best, red64, lane, wid);
+          if (best == 0ull) break;
+          if (tid == 0) {
+            if (list == 0) {
+              const float raw = elem_at<DT>(data, key_id(best) - static_cast<uint32_t>(lo));
+              cand_pen[r] = make_uint4(static_cast<uint32_t>(best), static_cast<uint32_t>(best >> 32),
+                                       __float_as_uint(raw), 0u);
+            } else {
+              cand_raw[r] = best;
+            }
+          }
+          prev = best;
+          got = r + 1;
+        }
+        if (list == 0) np = got;
+        else nr = got;
+      }
+      __syncthreads();
+    }
+
+    // keep this chunk's best k_row / n_row and reserve their slice of the leader's lists
+    const int sent_pen = min(np, k_row), sent_raw = min(nr, n_row);
+    if (tid == 0) {
+      const uint32_t ctl_leader = dsmem_addr(smem_u32(ctl), 0);
+      ctl[CTL_BASE_P] = sent_pen > 0 ? dsmem_atomic_add(ctl_leader + 4u * CTL_RECV_NP, sent_pen) : 0u;
+      ctl[CTL_BASE_R] = sent_raw > 0 ? dsmem_atomic_add(ctl_leader + 4u * CTL_RECV_NR, sent_raw) : 0u;
+    }
+    int out_p = -1, out_r = -1;
+    uint4 ent_p = make_uint4(0, 0, 0, 0);
+    uint64_t ent_r = 0ull;
+    if (tid < np && k_row > 0) {
+      ent_p = cand_pen[tid];
+      out_p = tid;
+      if (np > k_row) {
+        const uint64_t ki = (static_cast<uint64_t>(ent_p.y) << 32) | ent_p.x;
+        const uint2* keys = reinterpret_cast<const uint2*>(cand_pen);
+        int rank = 0;
+#pragma unroll 4
+        for (int j = 0; j < np; ++j) {
+          const uint2 o = keys[2 * j];
+          rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
+        }
+        out_p = rank < k_row ? rank : -1;
+      }
+    }
+    if (tid < nr && n_row > 0) {
+      ent_r = cand_raw[tid];
+      out_r = tid;
+      if (nr > n_row) {
+        int rank = 0;
+#pragma unroll 4
+        for (int j = 0; j < nr; ++j) rank += cand_raw[j] > ent_r;
+        out_r = rank < n_row ? rank : -1;
+      }
+    }
+    __syncthreads();
+    if (out_p >= 0)
+      dsmem_st_v4(dsmem_addr(smem_u32(sm + L.recv_pen) + (ctl[CTL_BASE_P] + out_p) * 16u, 0), ent_p.x, ent_p.y,
+                  ent_p.z, 0u);
+    if (out_r >= 0)
+      dsmem_st_v2(dsmem_addr(smem_u32(sm + L.recv_raw) + (ctl[CTL_BASE_R] + out_r) * 8u, 0),
+                  static_cast<uint32_t>(ent_r), static_cast<uint32_t>(ent_r >> 32));
+    cluster_arrive();
+    cluster_wait();  // B1: the leader holds every CTA's best candidates in two dense lists
+
+    // ---- 4. the leader ranks the received keys exactly -----------------------------------------
+    if (crank == 0) {
+      const int tot_p = static_cast<int>(ctl[CTL_RECV_NP]);
+      const int tot_r = static_cast<int>(ctl[CTL_RECV_NR]);
+      const int tot = tot_p + tot_r;
+      uint4* sorted_pen = cand_pen;   // the leader's own candidates were sent before B1
+      uint64_t* sorted_raw = cand_raw;
+      int G = 1;  // threads per ranked key (a power of two)
+      while (G < 32 && 2 * G * tot <= NT) G *= 2;
+      const uint2* pkeys = reinterpret_cast<const uint2*>(recv_pen);
+      for (int base = 0; base < tot; base += NT / G) {
+        const int f = base + tid / G, sub = tid & (G - 1);
+        int rank = 0;
+        uint64_t ki = 0ull;
+        if (f < tot_p) {
+          const uint2 k2 = pkeys[2 * f];
+          ki = (static_cast<uint64_t>(k2.y) << 32) | k2.x;
+          for (int j = sub; j < tot_p; j += G) {
+            const uint2 o = pkeys[2 * j];
+            rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
+          }
+        } else if (f < tot) {
+          ki = recv_raw[f - tot_p];
+          for (int j = sub; j < tot_r; j += G) rank += recv_raw[j] > ki;
+        }
+        for (int off = G >> 1; off > 0; off >>= 1) rank += __shfl_xor_sync(FULL_MASK, rank, off);
+        if (sub == 0) {
+          if (f < tot_p) {
+            if (rank < k_row) sorted_pen[rank] = recv_pen[f];
+          } else if (f < tot && rank < n_row) {
+            sorted_raw[rank] = ki;
+          }
+        }
+      }
+      __syncthreads();
+      k_eff = min(k_row, tot_p);
+      n_eff = min(n_row, tot_r);
+
+      // the tail's first half on <= 64 survivors (one warp): min_p and top_p cuts and the
+      // tempered cumulative weights; nothing here depends on the draw counter
+      if (P.mode == MODE_SAMPLE && wid == 0 && valid && k_eff > 0) {
+        ea = (lane < k_eff) ? sorted_pen[lane] : make_uint4(0, 0, 0, 0);
+        eb = (lane + 32 < k_eff) ? sorted_pen[lane + 32] : make_uint4(0, 0, 0, 0);
+        va = key_value(ea.y);
+        vb = key_value(eb.y);
+        m1 = m2 = 1;
+        if (sampled) {
+          const float v0 = __shfl_sync(FULL_MASK, va, 0);
+          m1 = k_eff;
+          if (sp.min_p > 0.0f) {  // min_p in logit space, float32
+            const float thr = __fadd_rn(v0, sp.logminp);
+            const uint32_t ba = __ballot_sync(FULL_MASK, lane < k_eff && va >= thr);
+            const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && vb >= thr);
+            m1 = max(1, __popc(ba) + __popc(bb));
+          }
+          // temperature-1 mass (top_p) and tempered weights (draw) over the min_p survivors, as
+          // double-word prefix sums; the draw only ever reads prefixes below m2
+          const bool ina = lane < m1, inb = lane + 32 < m1;
+          const float da = __fsub_rn(va, v0), db = __fsub_rn(vb, v0);
+          const float Tm = sp.temperature;
+          const DW qa{ina ? expf(da) : 0.0f, 0.0f}, qb{inb ? expf(db) : 0.0f, 0.0f};
+          const DW wa{ina ? expf(__fdiv_rn(da, Tm)) : 0.0f, 0.0f};
+          const DW wb{inb ? expf(__fdiv_rn(db, Tm)) : 0.0f, 0.0f};
+          const DW ca = warp_scan_dw(qa, lane);
+          Ca = warp_scan_dw(wa, lane);
+          const DW cb = dw_add(shfl_dw(ca, 31), warp_scan_dw(qb, lane));
+          Cb = dw_add(shfl_dw(Ca, 31), warp_scan_dw(wb, lane));
+          m2 = m1;
+          if (!(sp.top_p >= 1.0f)) {
+            if (!(sp.top_p > 0.0f)) {
+              m2 = 1;
+            } else {
+              const DW target = dw_mul_f(shfl_dw(cb, 31), sp.top_p);
+              const uint32_t la = __ballot_sync(FULL_MASK, ina && dw_less(ca, target));
+              const uint32_t lb = __ballot_sync(FULL_MASK, inb && dw_less(cb, target));
+              m2 = min(m1, __popc(la) + __popc(lb) + 1);
+            }
+          }
+          const int last = m2 - 1;
+          W = (last < 32) ? shfl_dw(Ca, last) : shfl_dw(Cb, last - 32);
+        }
+      }
+    }
+  }
+
+  // ---- outputs: with early loads the previous kernel owns outputs and counters until it ends --
+  if (early) {
+    grid_dep_wait();
+    if (ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
+  }
 
   // allowed-subset log-probabilities and the given chosen id, for this chunk's ids
   if (P.allowed_off != nullptr && P.allowed_lps != nullptr) {
@@ -577,8 +855,8 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
         atomicOr(P.err, STRATA_DEVERR_ALLOWED);
       }
     };
-    if (a_beg + tid < a_end) out_allowed(a_beg + tid, aid0);
-    if (a_beg + tid + NT < a_end) out_allowed(a_beg + tid + NT, aid1);
+    if (a_beg + tid < a_end) out_allowed(a_beg + tid, aid[0]);
+    if (a_beg + tid + NT < a_end) out_allowed(a_beg + tid + NT, aid[1]);
     for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) out_allowed(j, P.allowed[j]);
   }
   if (P.mode == MODE_LOGPROBS && P.chosen_lp != nullptr && P.chosen != nullptr && tid == 0) {
@@ -590,308 +868,71 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
     }
   }
 
-  // ---- 3. candidates of this chunk -------------------------------------------------------------
-  if (kp > 0) {
-    if (q > QMAX) T = 0u;  // no usable bound: every element is a candidate (exact rounds below)
-    if (has_m && ord_t >= T) {
-      for (int v = tid; v < n_vec; v += NT) {
-        float x[EPV];
-        load_vec<DT>(data, v, x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-          const uint32_t o = order_key(x[e]);
-          if (loc >= static_cast<uint32_t>(n_el) || o == 0u || o < T) continue;
-          if (penal && bit_at(hbits, loc)) continue;
-          const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
-          if (n_row > 0) {
-            const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
-            if (i < LOCAL_CAP) cand_raw[i] = key;
-          }
-          if (k_row > 0) {
-            const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
-            if (i < LOCAL_CAP)
-              cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
-                                       __float_as_uint(x[e]), 0u);
-          }
-        }
-      }
-    }
-    if (penal) {
-      for (int i = tid; i < P.hash_cap; i += NT) {
-        const uint32_t ent = htab[i];
-        if (ent == HASH_EMPTY) continue;
-        const uint32_t loc = ent >> HASH_CNT_BITS;
-        const uint32_t c = ent & ((1u << HASH_CNT_BITS) - 1u);
-        const float raw = elem_at<DT>(data, loc);
-        const uint32_t id = static_cast<uint32_t>(lo) + loc;
-        const uint32_t o = order_key(raw);
-        if (n_row > 0 && o != 0u && o >= T) {
-          const uint32_t j = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
-          if (j < LOCAL_CAP) cand_raw[j] = sel_key(o, id);
-        }
-        const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
-        const uint32_t op = order_key(pv);
-        if (k_row > 0 && op != 0u && op >= T) {
-          const uint32_t j = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
-          const uint64_t key = sel_key(op, id);
-          if (j < LOCAL_CAP)
-            cand_pen[j] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
-                                     __float_as_uint(raw), 0u);
-        }
-      }
-    }
-    __syncthreads();
-
-    const uint32_t recv_pen_base = smem_u32(sm + L.recv_pen) + crank * static_cast<uint32_t>(P.kmax) * 16u;
-    const uint32_t recv_raw_base = smem_u32(sm + L.recv_raw) + crank * static_cast<uint32_t>(P.nmax) * 8u;
-    uint32_t sent_pen = 0, sent_raw = 0;
-
-    // -- penalised list: keep this chunk's best k_row and send them to the leader
-    if (k_row > 0) {
-      const int np = static_cast<int>(ctl[CTL_CAND_PEN]);
-      if (np <= LOCAL_CAP) {
-        for (int i = tid; i < np; i += NT) {
-          const uint4 ent = cand_pen[i];
-          int slot_out = i;
-          if (np > k_row) {
-            const uint64_t ki = (static_cast<uint64_t>(ent.y) << 32) | ent.x;
-            int rank = 0;
-            for (int j = 0; j < np; ++j) {
-              const uint4 o = cand_pen[j];
-              rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
-            }
-            slot_out = rank;
-          }
-          if (slot_out < k_row) dsmem_st_v4(dsmem_addr(recv_pen_base + slot_out * 16u, 0), ent.x, ent.y, ent.z, 0u);
-        }
-        sent_pen = static_cast<uint32_t>(min(np, k_row));
-      } else {
-        // more candidates than the buffer holds (heavy ties): k exact argmax rounds
-        uint64_t prev = ~0ull;
-        for (int r = 0; r < k_row; ++r) {
-          uint64_t best = 0ull;
-          for (int v = tid; v < n_vec; v += NT) {
-            float x[EPV];
-            load_vec<DT>(data, v, x);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-              if (loc >= static_cast<uint32_t>(n_el)) continue;
-              float pv = x[e];
-              if (penal && bit_at(hbits, loc))
-                pv = penalize(pv, hash_count(htab, P.hash_bits, loc), sp.rep, sp.freq, sp.pres);
-              const uint32_t o = order_key(pv);
-              if (o == 0u) continue;
-              const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
-              if (key < prev && key > best) best = key;
-            }
-          }
-          best = block_max_u64(best, red64, lane, wid);
-          if (best == 0ull) break;
-          if (tid == 0) {
-            const float raw = elem_at<DT>(data, key_id(best) - static_cast<uint32_t>(lo));
-            dsmem_st_v4(dsmem_addr(recv_pen_base + r * 16u, 0), static_cast<uint32_t>(best),
-                        static_cast<uint32_t>(best >> 32), __float_as_uint(raw), 0u);
-          }
-          prev = best;
-          sent_pen = static_cast<uint32_t>(r + 1);
-        }
-      }
-    }
-    // -- raw list: this chunk's best n_row raw logits
-    if (n_row > 0) {
-      const int nr = static_cast<int>(ctl[CTL_CAND_RAW]);
-      if (nr <= LOCAL_CAP) {
-        for (int i = tid; i < nr; i += NT) {
-          const uint64_t ki = cand_raw[i];
-          int slot_out = i;
-          if (nr > n_row) {
-            int rank = 0;
-            for (int j = 0; j < nr; ++j) rank += cand_raw[j] > ki;
-            slot_out = rank;
-          }
-          if (slot_out < n_row)
-            dsmem_st_v2(dsmem_addr(recv_raw_base + slot_out * 8u, 0), static_cast<uint32_t>(ki),
-                        static_cast<uint32_t>(ki >> 32));
-        }
-        sent_raw = static_cast<uint32_t>(min(nr, n_row));
-      } else {
-        uint64_t prev = ~0ull;
-        for (int r = 0; r < n_row; ++r) {
-          uint64_t best = 0ull;
-          for (int v = tid; v < n_vec; v += NT) {
-            float x[EPV];
-            load_vec<DT>(data, v, x);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-              if (loc >= static_cast<uint32_t>(n_el)) continue;
-              const uint32_t o = order_key(x[e]);
-              if (o == 0u) continue;
-              const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
-              if (key < prev && key > best) best = key;
-            }
-          }
-          best = block_max_u64(best, red64, lane, wid);
-          if (best == 0ull) break;
-          if (tid == 0)
-            dsmem_st_v2(dsmem_addr(recv_raw_base + r * 8u, 0), static_cast<uint32_t>(best),
-                        static_cast<uint32_t>(best >> 32));
-          prev = best;
-          sent_raw = static_cast<uint32_t>(r + 1);
-        }
-      }
-    }
-    if (tid == 0) dsmem_st_v2(dsmem_addr(smem_u32(sm + L.recv_cnt) + crank * 8u, 0), sent_pen, sent_raw);
-    cluster_arrive();
-    cluster_wait();  // B1: the leader holds every CTA's candidates
-
-    // ---- 4. the leader ranks the received keys exactly -----------------------------------------
-    if (crank == 0) {
-      int tot_p = 0, tot_r = 0;
-      for (int c = 0; c < cs; ++c) {
-        tot_p += static_cast<int>(recv_cnt[c].x);
-        tot_r += static_cast<int>(recv_cnt[c].y);
-      }
-      uint4* sorted_pen = cand_pen;
-      uint64_t* sorted_raw = cand_raw;
-      __syncthreads();  // candidate buffers are reused for the sorted lists
-      for (int f = tid; f < tot_p + tot_r; f += NT) {
-        if (f < tot_p) {
-          int c = 0, j = f;
-          while (j >= static_cast<int>(recv_cnt[c].x)) {
-            j -= static_cast<int>(recv_cnt[c].x);
-            ++c;
-          }
-          const uint4 ent = recv_pen[c * P.kmax + j];
-          const uint64_t ki = (static_cast<uint64_t>(ent.y) << 32) | ent.x;
-          int rank = 0;
-          for (int c2 = 0; c2 < cs; ++c2) {
-            const int n2 = static_cast<int>(recv_cnt[c2].x);
-            const uint4* base = recv_pen + c2 * P.kmax;
-            for (int j2 = 0; j2 < n2; ++j2) rank += ((static_cast<uint64_t>(base[j2].y) << 32) | base[j2].x) > ki;
-          }
-          if (rank < k_row) sorted_pen[rank] = ent;
+  if (kp > 0 && crank == 0) {
+    const uint64_t* sorted_raw = cand_raw;
+    // top-N raw alternatives and their log-probabilities
+    if (n_row > 0 && P.top_ids != nullptr) {
+      for (int i = tid; i < n_row; i += NT) {
+        const long long o = static_cast<long long>(row) * P.top_n + i;
+        if (i < n_eff) {
+          const uint64_t key = sorted_raw[i];
+          P.top_ids[o] = static_cast<int32_t>(key_id(key));
+          P.top_lps[o] = key_value(static_cast<uint32_t>(key >> 32)) - lse;
         } else {
-          int c = 0, j = f - tot_p;
-          while (j >= static_cast<int>(recv_cnt[c].y)) {
-            j -= static_cast<int>(recv_cnt[c].y);
-            ++c;
-          }
-          const uint64_t ki = recv_raw[c * P.nmax + j];
-          int rank = 0;
-          for (int c2 = 0; c2 < cs; ++c2) {
-            const int n2 = static_cast<int>(recv_cnt[c2].y);
-            const uint64_t* base = recv_raw + c2 * P.nmax;
-            for (int j2 = 0; j2 < n2; ++j2) rank += base[j2] > ki;
-          }
-          if (rank < n_row) sorted_raw[rank] = ki;
-        }
-      }
-      __syncthreads();
-      const int k_eff = min(k_row, tot_p);
-      const int n_eff = min(n_row, tot_r);
-
-      // top-N raw alternatives and their log-probabilities
-      if (n_row > 0 && P.top_ids != nullptr) {
-        for (int i = tid; i < n_row; i += NT) {
-          const long long o = static_cast<long long>(row) * P.top_n + i;
-          if (i < n_eff) {
-            const uint64_t key = sorted_raw[i];
-            P.top_ids[o] = static_cast<int32_t>(key_id(key));
-            P.top_lps[o] = key_value(static_cast<uint32_t>(key >> 32)) - lse;
-          } else {
-            P.top_ids[o] = -1;
-            P.top_lps[o] = -INFINITY;
-          }
-        }
-      }
-
-      // ---- the tail of the chain on <= 64 survivors (one warp) --------------------------------
-      if (P.mode == MODE_SAMPLE && wid == 0) {
-        int out = -1, m1 = 0, m2 = 0;
-        float chosen_raw = __int_as_float(0x7FC00000);
-        const uint4 ea = (lane < k_eff) ? sorted_pen[lane] : make_uint4(0, 0, 0, 0);
-        const uint4 eb = (lane + 32 < k_eff) ? sorted_pen[lane + 32] : make_uint4(0, 0, 0, 0);
-        const float va = key_value(ea.y), vb = key_value(eb.y);
-        if (!valid) {
-          if (lane == 0) atomicOr(P.err, STRATA_DEVERR_SLOT);
-        } else if (k_eff == 0) {
-          if (lane == 0) atomicOr(P.err, STRATA_DEVERR_NOCAND);
-        } else {
-          int j = 0;
-          m1 = m2 = 1;
-          if (sampled) {
-            const float v0 = __shfl_sync(FULL_MASK, va, 0);
-            m1 = k_eff;
-            if (sp.min_p > 0.0f) {  // min_p in logit space, float32
-              const float thr = __fadd_rn(v0, sp.logminp);
-              const uint32_t ba = __ballot_sync(FULL_MASK, lane < k_eff && va >= thr);
-              const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && vb >= thr);
-              m1 = max(1, __popc(ba) + __popc(bb));
-            }
-            m2 = m1;
-            if (!(sp.top_p >= 1.0f)) {
-              if (!(sp.top_p > 0.0f)) {
-                m2 = 1;
-              } else {  // temperature-1 mass over the min_p survivors
-                const double qa = (lane < m1) ? static_cast<double>(expf(__fsub_rn(va, v0))) : 0.0;
-                const double qb = (lane + 32 < m1) ? static_cast<double>(expf(__fsub_rn(vb, v0))) : 0.0;
-                const double ca = warp_scan_incl(qa, lane);
-                const double cb = warp_scan_incl(qb, lane) + __shfl_sync(FULL_MASK, ca, 31);
-                const double tot = __shfl_sync(FULL_MASK, cb, 31);
-                const double target = static_cast<double>(sp.top_p) * tot;
-                const uint32_t la = __ballot_sync(FULL_MASK, lane < m1 && ca < target);
-                const uint32_t lb = __ballot_sync(FULL_MASK, lane + 32 < m1 && cb < target);
-                m2 = min(m1, __popc(la) + __popc(lb) + 1);
-              }
-            }
-            const unsigned long long ctr =
-                (static_cast<unsigned long long>(ctl[CTL_CTR_HI]) << 32) | ctl[CTL_CTR_LO];
-            const unsigned long long pos = static_cast<unsigned long long>(P.row_pos[row]);
-            const uint32_t x0 = philox_word0(sp.seed, pos, ctr);
-            const double u = static_cast<double>(x0 >> 8) * 0x1p-24;
-            const float Tm = sp.temperature;
-            const double wa = (lane < m2) ? static_cast<double>(expf(__fdiv_rn(__fsub_rn(va, v0), Tm))) : 0.0;
-            const double wb = (lane + 32 < m2) ? static_cast<double>(expf(__fdiv_rn(__fsub_rn(vb, v0), Tm))) : 0.0;
-            const double Ca = warp_scan_incl(wa, lane);
-            const double Cb = warp_scan_incl(wb, lane) + __shfl_sync(FULL_MASK, Ca, 31);
-            const double W = __shfl_sync(FULL_MASK, Cb, 31);
-            const double tgt = u * W;
-            const uint32_t ja = __ballot_sync(FULL_MASK, lane < m2 && Ca <= tgt);
-            const uint32_t jb = __ballot_sync(FULL_MASK, lane + 32 < m2 && Cb <= tgt);
-            j = min(__popc(ja) + __popc(jb), m2 - 1);
-          }
-          const uint32_t id_a = key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x);
-          const uint32_t id_b = key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x);
-          const uint32_t sel_id = __shfl_sync(FULL_MASK, j < 32 ? id_a : id_b, j & 31);
-          const float sel_raw = __shfl_sync(FULL_MASK, __uint_as_float(j < 32 ? ea.z : eb.z), j & 31);
-          out = static_cast<int>(sel_id);
-          chosen_raw = sel_raw;
-        }
-        if (lane == 0) {
-          P.out_ids[row] = out;
-          if (P.kept != nullptr) {
-            P.kept[2 * row] = m1;
-            P.kept[2 * row + 1] = m2;
-          }
-          if (P.chosen_lp != nullptr) P.chosen_lp[row] = (out >= 0) ? chosen_raw - lse : __int_as_float(0x7FC00000);
-        }
-        if (P.topk_ids != nullptr) {
-          const long long o = static_cast<long long>(row) * KMAX;
-          const bool ia = valid && lane < k_eff, ib = valid && lane + 32 < k_eff;
-          P.topk_ids[o + lane] = ia ? static_cast<int32_t>(key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x)) : -1;
-          P.topk_ids[o + lane + 32] =
-              ib ? static_cast<int32_t>(key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x)) : -1;
-          if (P.topk_vals != nullptr) {
-            P.topk_vals[o + lane] = ia ? va : __int_as_float(0x7FC00000);
-            P.topk_vals[o + lane + 32] = ib ? vb : __int_as_float(0x7FC00000);
-          }
+          P.top_ids[o] = -1;
+          P.top_lps[o] = -INFINITY;
         }
       }
     }
-  } else if (P.mode == MODE_SAMPLE && crank == 0 && tid == 0) {
+    // the tail's second half: Philox(seed, position) at the slot's counter, the pick, the outputs
+    if (P.mode == MODE_SAMPLE && wid == 0) {
+      int out = -1;
+      float chosen_raw = __int_as_float(0x7FC00000);
+      if (!valid) {
+        if (lane == 0) atomicOr(P.err, STRATA_DEVERR_SLOT);
+      } else if (k_eff == 0) {
+        if (lane == 0) atomicOr(P.err, STRATA_DEVERR_NOCAND);
+      } else {
+        int j = 0;
+        if (sampled) {
+          uint32_t x0 = 0u;
+          if (ctr_thread) {
+            if ((ctr_old & 0xFFFFull) + 1ull == static_cast<unsigned long long>(r_s))
+              atomicAdd(&P.ctr[slot], (1ull << 16) - static_cast<unsigned long long>(r_s));
+            x0 = philox_word0(sp.seed, pos, ctr_old >> 16);
+          }
+          x0 = __shfl_sync(FULL_MASK, x0, 0);
+          const float u = static_cast<float>(x0 >> 8) * 0x1p-24f;
+          const DW tgt = dw_mul_f(W, u);
+          const uint32_t ja = __ballot_sync(FULL_MASK, lane < m2 && !dw_less(tgt, Ca));
+          const uint32_t jb = __ballot_sync(FULL_MASK, lane + 32 < m2 && !dw_less(tgt, Cb));
+          j = min(__popc(ja) + __popc(jb), m2 - 1);
+        }
+        const uint32_t id_a = key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x);
+        const uint32_t id_b = key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x);
+        out = static_cast<int>(__shfl_sync(FULL_MASK, j < 32 ? id_a : id_b, j & 31));
+        chosen_raw = __shfl_sync(FULL_MASK, __uint_as_float(j < 32 ? ea.z : eb.z), j & 31);
+      }
+      if (lane == 0) {
+        P.out_ids[row] = out;
+        if (P.kept != nullptr) {
+          P.kept[2 * row] = m1;
+          P.kept[2 * row + 1] = m2;
+        }
+        if (P.chosen_lp != nullptr) P.chosen_lp[row] = (out >= 0) ? chosen_raw - lse : __int_as_float(0x7FC00000);
+      }
+      if (P.topk_ids != nullptr) {
+        const long long o = static_cast<long long>(row) * KMAX;
+        const bool ia = valid && lane < k_eff, ib = valid && lane + 32 < k_eff;
+        P.topk_ids[o + lane] = ia ? static_cast<int32_t>(key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x)) : -1;
+        P.topk_ids[o + lane + 32] = ib ? static_cast<int32_t>(key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x)) : -1;
+        if (P.topk_vals != nullptr) {
+          P.topk_vals[o + lane] = ia ? va : __int_as_float(0x7FC00000);
+          P.topk_vals[o + lane + 32] = ib ? vb : __int_as_float(0x7FC00000);
+        }
+      }
+    }
+  } else if (kp == 0 && P.mode == MODE_SAMPLE && crank == 0 && tid == 0) {
     // no selection in this row: only an out-of-range slot gets here
     P.out_ids[row] = -1;
     if (P.kept != nullptr) {
@@ -905,6 +946,7 @@ __global__ void __launch_bounds__(NT, 1) rows_kernel(const KParams P) {
     P.topk_ids[static_cast<long long>(row) * KMAX + tid] = -1;
     if (P.topk_vals != nullptr) P.topk_vals[static_cast<long long>(row) * KMAX + tid] = __int_as_float(0x7FC00000);
   }
+  if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
   if (ctl[CTL_TIMEOUT] != 0u) {  // a copy may still be in flight into this CTA: bounded wait again
     for (int p = 0; p < n_pieces; ++p) wait_piece(mbar, p, ctl, P.err);
   }

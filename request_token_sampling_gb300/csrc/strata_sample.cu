@@ -1,8 +1,8 @@
 // strata_sample.cu -- host side of the C ABI declared in include/strata_sample.h.
 //
-// The context owns the device slot table (each request slot's prepared keys and its 64-bit draw
-// counter), the per-slot arrival words the kernel uses to advance the counters, and a device
-// error word.  Keys are validated and prepared here (top_k 0 -> 20, logf(min_p) once on the host,
+// The context owns the device slot table (each request slot's prepared keys), one packed 64-bit
+// word per slot holding its 48-bit draw counter and the 16-bit arrival count the kernel uses to
+// advance it, and a device error word.  Keys are validated and prepared here (top_k 0 -> 20, logf(min_p) once on the host,
 // penalty activity), mirrored on the host, and copied to the device on the caller's stream.
 // Every sampling or logprobs call is one launch of the fused row kernel.
 #include <cuda_runtime.h>
@@ -53,7 +53,6 @@ struct strata_ctx {
   int max_smem = 0;
   SlotDev* d_slots = nullptr;
   unsigned long long* d_ctr = nullptr;
-  uint32_t* d_arrivals = nullptr;
   uint32_t* d_err = nullptr;
   std::vector<strata_sampling_params> h_params;
   std::vector<SlotDev> h_slots;
@@ -255,7 +254,7 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
   *out = nullptr;
   if (max_slots < 1 || max_slots > 65536) return fail(STRATA_EINVAL, "max_slots=%d outside 1..65536", max_slots);
   if (max_vocab < 1 || max_vocab > STRATA_MAX_VOCAB) return fail(STRATA_EINVAL, "max_vocab=%d outside 1..%d", max_vocab, STRATA_MAX_VOCAB);
-  if (max_rows < 1 || max_rows > 65536) return fail(STRATA_EINVAL, "max_rows=%d outside 1..65536", max_rows);
+  if (max_rows < 1 || max_rows > 65535) return fail(STRATA_EINVAL, "max_rows=%d outside 1..65535", max_rows);
   int ndev = 0;
   cudaError_t e = cudaGetDeviceCount(&ndev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
@@ -321,11 +320,9 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
   }
   if ((e = cudaMalloc(&c->d_slots, sizeof(SlotDev) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc slots: %s", cudaGetErrorString(e)));
   if ((e = cudaMalloc(&c->d_ctr, sizeof(unsigned long long) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc counters: %s", cudaGetErrorString(e)));
-  if ((e = cudaMalloc(&c->d_arrivals, sizeof(uint32_t) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc arrivals: %s", cudaGetErrorString(e)));
   if ((e = cudaMalloc(&c->d_err, sizeof(uint32_t))) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc error word: %s", cudaGetErrorString(e)));
   if ((e = cudaMemcpy(c->d_slots, c->h_slots.data(), sizeof(SlotDev) * max_slots, cudaMemcpyHostToDevice)) != cudaSuccess) return cleanup(cuda_fail(e, "slot table upload"));
   if ((e = cudaMemset(c->d_ctr, 0, sizeof(unsigned long long) * max_slots)) != cudaSuccess) return cleanup(cuda_fail(e, "counter reset"));
-  if ((e = cudaMemset(c->d_arrivals, 0, sizeof(uint32_t) * max_slots)) != cudaSuccess) return cleanup(cuda_fail(e, "arrival reset"));
   if ((e = cudaMemset(c->d_err, 0, sizeof(uint32_t))) != cudaSuccess) return cleanup(cuda_fail(e, "error word reset"));
   if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cleanup(cuda_fail(e, "create sync"));
   *out = c;
@@ -337,7 +334,6 @@ void strata_destroy(strata_ctx* c) {
   cudaDeviceSynchronize();
   cudaFree(c->d_slots);
   cudaFree(c->d_ctr);
-  cudaFree(c->d_arrivals);
   cudaFree(c->d_err);
   delete c;
 }
@@ -346,6 +342,7 @@ static int set_slot(strata_ctx* c, int slot, const strata_sampling_params* p, bo
                     void* stream) {
   if (c == nullptr) return fail(STRATA_EINVAL, "null context");
   if (slot < 0 || slot >= c->max_slots) return fail(STRATA_ERANGE, "slot %d outside 0..%d", slot, c->max_slots - 1);
+  if (set_ctr && ctr >= (1ull << 48)) return fail(STRATA_ERANGE, "counter %llu needs more than 48 bits", static_cast<unsigned long long>(ctr));
   int rc = strata_validate_params(p);
   if (rc != STRATA_OK) return rc;
   if ((rc = check_device(c)) != STRATA_OK) return rc;
@@ -356,11 +353,9 @@ static int set_slot(strata_ctx* c, int slot, const strata_sampling_params* p, bo
   cudaError_t e = cudaMemcpyAsync(c->d_slots + slot, &sd, sizeof(SlotDev), cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "slot upload");
   if (set_ctr) {
-    const unsigned long long v = ctr;
+    const unsigned long long v = static_cast<unsigned long long>(ctr) << 16;  // arrivals cleared
     if ((e = cudaMemcpyAsync(c->d_ctr + slot, &v, sizeof(v), cudaMemcpyHostToDevice, s)) != cudaSuccess)
       return cuda_fail(e, "counter upload");
-    if ((e = cudaMemsetAsync(c->d_arrivals + slot, 0, sizeof(uint32_t), s)) != cudaSuccess)
-      return cuda_fail(e, "arrival reset");
   }
   bins_update(c, c->h_slots[slot], -1);
   c->h_slots[slot] = sd;
@@ -391,7 +386,7 @@ int strata_get_slot_state(strata_ctx* c, int slot, strata_sampling_params* p, ui
     cudaError_t e = cudaMemcpyAsync(&v, c->d_ctr + slot, sizeof(v), cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(e, "counter read");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "counter read sync");
-    *counter = v;
+    *counter = v >> 16;
   }
   return STRATA_OK;
 }
@@ -475,7 +470,6 @@ int strata_sample_rows(strata_ctx* c, const void* logits, int dtype, int B, int 
   P.kept = kept;
   P.slots = c->d_slots;
   P.ctr = c->d_ctr;
-  P.arrivals = c->d_arrivals;
   P.max_slots = c->max_slots;
   P.err = c->d_err;
   P.hash_cap = sh.hash_cap;
@@ -517,7 +511,6 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
   P.allowed_lps = allowed_lps;
   P.slots = c->d_slots;
   P.ctr = c->d_ctr;
-  P.arrivals = c->d_arrivals;
   P.max_slots = c->max_slots;
   P.err = c->d_err;
   P.flags = flags;

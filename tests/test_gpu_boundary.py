@@ -165,7 +165,7 @@ def test_pdl_flags_same_results(sampler, flags):
 
 def test_graph_capture_replays_draw_fresh_numbers(sampler):
     """A captured call advances the device counters on every replay (the pages moved sampling out of
-    the captured graph because a captured sampler replayed the same draws)."""
+    the captured graph since a sampler baked into a graph draws identical numbers on every replay)."""
     w = synth.config4(fused=True)
     for s in w["slot_params"]:
         w["slot_params"][s] = dict(w["slot_params"][s], temperature=2.0, top_k=64, top_p=1.0, min_p=0.0)
