@@ -44,9 +44,8 @@ UNIT = "rows/s"
 WORKLOAD = ("logprobs workload fused with sampling: B=8 fp32 rows x V=248,320, N(0,3^2)+1..5 spikes; "
             "per-row keys top_k=20 T=0.8 top_p=0.95 min_p=0.05 repeat=1.1 freq=0.1 presence=0.1 "
             "penalty_last_n=64; top_logprobs=20, chosen-token logprob, allowed_token_ids of 5/100/1000")
-KERNEL_SOURCES = ("request_token_sampling_gb300/csrc/strata_kernel.cuh",
-                  "request_token_sampling_gb300/csrc/strata_device.cuh",
-                  "request_token_sampling_gb300/csrc/strata_sample.cu")
+KERNEL_SOURCES = ("request_token_sampling_gb300/csrc/strata_kernel.cuh",   # the device code the
+                  "request_token_sampling_gb300/csrc/strata_device.cuh")   # ncu counters describe
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_config4_fused.json")
 
 

@@ -223,6 +223,35 @@ int strata_read_errors(strata_ctx *ctx, uint32_t *bits, void *stream);
 int strata_launch_shape(strata_ctx *ctx, int mode, int dtype, int B, int V, int top_n,
                         uint32_t flags, int *split, int *chunk_elems, int *smem_bytes, int *grid);
 
+/*
+ * Allocation-free sampling, for callers that cannot call cudaMalloc (code running inside a
+ * framework whose allocator owns all device memory, or a process that must not grow its device
+ * footprint once serving has started).  The pages have no counterpart of this call; it is a
+ * library addition.
+ *
+ * Same chain and kernel as strata_sample_rows, with no context: row b is its own request slot,
+ * its keys come from the host array row_params[b] and its draw counter value from the host array
+ * row_counters[b] (< 2^48).  The caller owns the counters: after a call, advance every sampled
+ * row's counter by one itself (greedy rows draw nothing).  hist/hist_off is CSR per row
+ * ([B+1] offsets; NULL = no history).  Outputs as in strata_sample_rows (no allowed subsets, no
+ * debug outputs).  B is at most STRATA_NOALLOC_MAX_ROWS; more rows is STRATA_ERANGE.
+ *
+ * Memory: nothing is allocated, on the device or the host heap.  The per-row key records, counter
+ * words, the row-to-slot table and the device error word live in one static device array of about
+ * 60 KiB that every GPU loading this library holds until the process exits.  Every call shares
+ * that array and it keeps the last call's contents; each call rewrites (and zeroes) what it reads,
+ * but calls that overlap on the GPU race, so issue them on one stream.  Device error bits of these
+ * calls are not reported.  The first call on each device sets that device up synchronously (finds
+ * the array's device address, sets kernel attributes, uploads the row table); make that first call
+ * before capturing any stream.
+ */
+#define STRATA_NOALLOC_MAX_ROWS 1024
+int strata_sample_rows_noalloc(const void *logits, int dtype, int B, int V, int64_t ld,
+                               const strata_sampling_params *row_params, const uint64_t *row_counters,
+                               const int64_t *row_pos, const int32_t *hist, const int32_t *hist_off,
+                               int32_t *out_ids, int top_n, float *chosen_lp, int32_t *top_ids,
+                               float *top_lps, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

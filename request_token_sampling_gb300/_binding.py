@@ -27,6 +27,7 @@ STRATA_MAX_TOP_K = 64
 STRATA_DEFAULT_TOP_K = 20
 STRATA_MAX_TOP_N = 20
 STRATA_MAX_PENALTY_LAST_N = 4096
+STRATA_NOALLOC_MAX_ROWS = 1024
 
 STRATA_FLAG_PDL = 0x1
 STRATA_FLAG_EARLY_LOAD = 0x2
@@ -48,7 +49,7 @@ EXPORTED = (
     "strata_version", "strata_last_error", "strata_default_params", "strata_validate_params",
     "strata_create", "strata_destroy", "strata_set_slot_params", "strata_get_slot_state",
     "strata_set_slot_state", "strata_sample_rows", "strata_logprobs_rows", "strata_read_errors",
-    "strata_launch_shape",
+    "strata_launch_shape", "strata_sample_rows_noalloc",
 )
 
 
@@ -101,6 +102,8 @@ def _load() -> ctypes.CDLL:
         "strata_read_errors": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], i32),
         "strata_launch_shape": ([vp, i32, i32, i32, i32, i32, u32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
+        "strata_sample_rows_noalloc": ([vp, i32, i32, i32, i64, P, ctypes.POINTER(ctypes.c_uint64), vp, vp, vp, vp,
+                                        i32, vp, vp, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -267,3 +270,23 @@ def strata_launch_shape(ctx, mode: int, dtype: int, B: int, V: int, top_n: int =
     _check(lib.strata_launch_shape(ctx, mode, dtype, B, V, top_n, flags, ctypes.byref(s), ctypes.byref(c),
                                    ctypes.byref(m), ctypes.byref(g)))
     return dict(split=s.value, chunk=c.value, smem=m.value, grid=g.value)
+
+
+def strata_sample_rows_noalloc(logits, row_params, row_counters, row_pos, out_ids, V=None, hist=None,
+                               hist_off=None, top_n: int = 0, chosen_lp=None, top_ids=None, top_lps=None,
+                               stream=None) -> None:
+    """Allocation-free sampling: row b is its own slot with keys row_params[b] (dicts) and draw
+    counter row_counters[b]; the caller advances the counters.  See the C header for the rules."""
+    import torch
+    ptr, dt, B, V, ld = _logits_args(logits, V)
+    if len(row_params) != B or len(row_counters) != B:
+        raise ValueError("one key set and one counter per row")
+    params = (strata_sampling_params * max(B, 1))()
+    for b, p in enumerate(row_params):
+        params[b] = to_c_params(p)
+    ctrs = (ctypes.c_uint64 * max(B, 1))(*[int(c) for c in row_counters])
+    _check(lib.strata_sample_rows_noalloc(
+        ptr, dt, B, V, ld, params, ctrs, _typed(row_pos, torch.int64, "row_pos"), _typed(hist, torch.int32, "hist"),
+        _typed(hist_off, torch.int32, "hist_off"), _typed(out_ids, torch.int32, "out_ids"), int(top_n),
+        _typed(chosen_lp, torch.float32, "chosen_lp"), _typed(top_ids, torch.int32, "top_ids"),
+        _typed(top_lps, torch.float32, "top_lps"), _stream(stream)))

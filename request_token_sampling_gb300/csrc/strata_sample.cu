@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -518,3 +519,202 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// strata_sample_rows_noalloc: the sampling call for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all: code running inside a framework whose allocator owns
+// every byte of device memory, or a process that must not grow its device footprint once serving
+// has started.  This entry point needs no context.  The only global memory it uses beyond the
+// caller's inputs and outputs (one prepared key record and one packed counter word per row, the
+// identity row-to-slot table and the device error word) lives in the file-scope array below,
+// which every GPU that loads this library holds until the process exits.  Every call shares the
+// array and it keeps the last call's contents; each call rewrites the parts it reads, so calls
+// that overlap on the GPU (two streams at once) race and must not be issued.
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+constexpr int NA_MAX_ROWS = STRATA_NOALLOC_MAX_ROWS;
+constexpr size_t NA_CTR = 256;                                          // error word at offset 0
+constexpr size_t NA_SLOTS = NA_CTR + sizeof(unsigned long long) * NA_MAX_ROWS;
+constexpr size_t NA_ROWSLOT = NA_SLOTS + sizeof(SlotDev) * NA_MAX_ROWS;
+constexpr size_t NA_BYTES = NA_ROWSLOT + sizeof(int32_t) * NA_MAX_ROWS;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NA_BYTES];
+
+namespace {
+
+struct NoallocDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int num_sms = 0, max_cluster = 8, max_smem = 0;
+};
+constexpr int NA_MAX_DEVICES = 64;
+NoallocDevice g_na[NA_MAX_DEVICES];
+std::mutex g_na_mu;
+
+// Once per device, with that device current: the array's device address, kernel attributes and
+// the identity row-to-slot table.  Runs inside the first call on the device (synchronously).
+int noalloc_setup(int dev, NoallocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_na_mu);
+  NoallocDevice& d = g_na[dev];
+  if (!d.ready) {
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.scratch), g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major < 10) return fail(STRATA_ECUDA, "device %s is not a Blackwell GPU", prop.name);
+    d.num_sms = prop.multiProcessorCount;
+    d.max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
+    const void* kernels[2] = {reinterpret_cast<const void*>(strata::rows_kernel<0>),
+                              reinterpret_cast<const void*>(strata::rows_kernel<1>)};
+    for (const void* k : kernels) {
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(smem)");
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(cluster)");
+    }
+    d.max_cluster = 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(strata::MAX_CS, 1, 1);
+    cfg.blockDim = dim3(strata::NT, 1, 1);
+    cfg.dynamicSmemBytes = 128 * 1024;
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = strata::MAX_CS;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, strata::rows_kernel<0>, &cfg) == cudaSuccess && nclusters > 0)
+      d.max_cluster = strata::MAX_CS;
+    cudaGetLastError();
+    static int32_t identity[NA_MAX_ROWS];
+    for (int i = 0; i < NA_MAX_ROWS; ++i) identity[i] = i;
+    if ((e = cudaMemcpy(d.scratch + NA_ROWSLOT, identity, sizeof(identity), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "row table upload");
+    d.ready = true;
+  }
+  *out = &d;
+  return STRATA_OK;
+}
+
+// Host staging of one call's key records and counter words (per thread, no heap).
+struct NoallocStage {
+  unsigned char head[NA_CTR + sizeof(unsigned long long) * NA_MAX_ROWS];
+  SlotDev slots[NA_MAX_ROWS];
+};
+thread_local NoallocStage g_na_stage;
+
+}  // namespace
+
+extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, int V, int64_t ld,
+                                          const strata_sampling_params* row_params, const uint64_t* row_counters,
+                                          const int64_t* row_pos, const int32_t* hist, const int32_t* hist_off,
+                                          int32_t* out_ids, int top_n, float* chosen_lp, int32_t* top_ids,
+                                          float* top_lps, void* stream) {
+  if (dtype != STRATA_DTYPE_F32 && dtype != STRATA_DTYPE_BF16) return fail(STRATA_EINVAL, "dtype %d", dtype);
+  if (B < 0) return fail(STRATA_EINVAL, "B=%d", B);
+  if (B > NA_MAX_ROWS) return fail(STRATA_ERANGE, "B=%d above the %d rows this call's static scratch holds", B, NA_MAX_ROWS);
+  if (V < 1 || V > STRATA_MAX_VOCAB) return fail(STRATA_ERANGE, "V=%d outside 1..%d", V, STRATA_MAX_VOCAB);
+  if (ld < V) return fail(STRATA_EINVAL, "ld=%lld below V=%d", static_cast<long long>(ld), V);
+  if (top_n < 0 || top_n > STRATA_MAX_TOP_N) return fail(STRATA_EINVAL, "top_n=%d outside 0..%d", top_n, STRATA_MAX_TOP_N);
+  if (top_n > 0 && ((top_ids == nullptr) != (top_lps == nullptr)))
+    return fail(STRATA_EINVAL, "top_ids and top_lps must be given together");
+  if (B == 0) return STRATA_OK;
+  if (logits == nullptr || row_params == nullptr || row_counters == nullptr || row_pos == nullptr || out_ids == nullptr)
+    return fail(STRATA_EINVAL, "logits, row_params, row_counters, row_pos and out_ids are required");
+  if (hist_off != nullptr && hist == nullptr) return fail(STRATA_EINVAL, "hist_off needs hist");
+  const int esz = dtype == STRATA_DTYPE_F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(logits) & 15u) != 0) return fail(STRATA_EALIGN, "logits not 16-byte aligned");
+  if ((static_cast<long long>(ld) * esz) % 16 != 0) return fail(STRATA_EALIGN, "row stride not a multiple of 16 bytes");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= NA_MAX_DEVICES) return fail(STRATA_ERANGE, "device %d", dev);
+
+  // keys and counters of this call, one slot per row
+  NoallocStage& st = g_na_stage;
+  std::memset(st.head, 0, NA_CTR);  // the device error word starts at zero
+  unsigned long long* ctr = reinterpret_cast<unsigned long long*>(st.head + NA_CTR);
+  int kmax_sampled = 0, max_lastn = 0;
+  for (int b = 0; b < B; ++b) {
+    int rc = strata_validate_params(&row_params[b]);
+    if (rc != STRATA_OK) return rc;
+    if (row_counters[b] >= (1ull << 48)) return fail(STRATA_ERANGE, "row %d counter needs more than 48 bits", b);
+    strata_sampling_params q = row_params[b];
+    q.struct_size = sizeof(strata_sampling_params);
+    st.slots[b] = prepare(q);
+    ctr[b] = static_cast<unsigned long long>(row_counters[b]) << 16;
+    if (st.slots[b].flags & strata::SLOT_SAMPLED) kmax_sampled = std::max(kmax_sampled, st.slots[b].k);
+    if (st.slots[b].flags & strata::SLOT_PENAL) max_lastn = std::max(max_lastn, st.slots[b].last_n);
+  }
+  NoallocDevice* nd = nullptr;
+  int rc = noalloc_setup(dev, &nd);
+  if (rc != STRATA_OK) return rc;
+
+  // launch shape (same rules as a context's)
+  const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
+  Shape sh;
+  sh.nmax = top_n_eff;
+  sh.kmax = std::max(1, kmax_sampled);
+  const int kp_max = std::max(sh.kmax, sh.nmax);
+  const long long row_bytes = static_cast<long long>(V) * esz;
+  int cs = std::max({static_cast<int>((row_bytes + CHUNK_TARGET_BYTES - 1) / CHUNK_TARGET_BYTES),
+                     (kp_max + strata::QMAX - 1) / strata::QMAX,
+                     std::min((nd->num_sms + B - 1) / B, std::max(1, (V + MIN_CHUNK_ELEMS - 1) / MIN_CHUNK_ELEMS)), 1});
+  cs = std::min(cs, nd->max_cluster);
+  int chunk = ((V + cs - 1) / cs + 15) / 16 * 16;
+  if (static_cast<long long>(chunk) * esz > static_cast<long long>(strata::MAX_PIECES) * strata::PIECE_BYTES)
+    return fail(STRATA_ERANGE, "V=%d needs %d bytes per block", V, chunk * esz);
+  sh.cs = cs;
+  sh.chunk = chunk;
+  sh.hash_cap = 0;
+  sh.hash_bits = 0;
+  if (hist_off != nullptr && max_lastn > 0) {
+    int bits = 6;
+    while ((1 << bits) < 2 * max_lastn) ++bits;
+    sh.hash_bits = bits;
+    sh.hash_cap = 1 << bits;
+  }
+  sh.smem = static_cast<int>(strata::make_layout(chunk, esz, sh.hash_cap, cs, sh.kmax, sh.nmax).total);
+  if (sh.smem > nd->max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit", sh.smem);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((e = cudaMemcpyAsync(nd->scratch, st.head, NA_CTR + sizeof(unsigned long long) * B, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "counter upload");
+  if ((e = cudaMemcpyAsync(nd->scratch + NA_SLOTS, st.slots, sizeof(SlotDev) * B, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "key upload");
+
+  KParams P{};
+  P.logits = logits;
+  P.ld = ld;
+  P.B = B;
+  P.V = V;
+  P.cs = sh.cs;
+  P.chunk = sh.chunk;
+  P.mode = strata::MODE_SAMPLE;
+  P.row_slot = reinterpret_cast<const int32_t*>(nd->scratch + NA_ROWSLOT);
+  P.row_pos = reinterpret_cast<const long long*>(row_pos);
+  P.hist = hist;
+  P.hist_off = hist_off;
+  P.n_hist_slots = hist_off != nullptr ? B : 0;
+  P.out_ids = out_ids;
+  P.top_n = top_n;
+  P.nmax = sh.nmax;
+  P.kmax = sh.kmax;
+  P.chosen_lp = chosen_lp;
+  P.top_ids = top_n_eff > 0 ? top_ids : nullptr;
+  P.top_lps = top_n_eff > 0 ? top_lps : nullptr;
+  P.slots = reinterpret_cast<const SlotDev*>(nd->scratch + NA_SLOTS);
+  P.ctr = reinterpret_cast<unsigned long long*>(nd->scratch + NA_CTR);
+  P.max_slots = B;
+  P.err = reinterpret_cast<uint32_t*>(nd->scratch);
+  P.hash_cap = sh.hash_cap;
+  P.hash_bits = sh.hash_bits;
+  P.flags = 0;
+  return launch(nullptr, P, dtype, sh, 0u, s);
+}
