@@ -33,10 +33,10 @@ namespace strata {
 
 constexpr int NT = 512;                      // threads per CTA
 constexpr int NW = NT / 32;                  // warps per CTA
-constexpr int VR = 2;                        // 16-byte vectors per thread per piece
+constexpr int VR = 4;                        // 16-byte vectors per thread per piece
 constexpr int PIECE_VECS = NT * VR;
-constexpr int PIECE_BYTES = PIECE_VECS * 16; // 16 KiB per bulk copy
-constexpr int MAX_PIECES = 12;               // chunk <= 192 KiB
+constexpr int PIECE_BYTES = PIECE_VECS * 16; // 32 KiB per bulk copy
+constexpr int MAX_PIECES = 6;                // chunk <= 192 KiB
 constexpr int MAX_CS = 16;                   // CTAs per row (non-portable cluster size)
 constexpr int KMAX = STRATA_MAX_TOP_K;
 constexpr int NMAX = STRATA_MAX_TOP_N;
@@ -63,6 +63,10 @@ enum : int {
   CTL_RECV_NR = 8,
   CTL_BASE_P = 9,    // this CTA's slice of the leader's lists
   CTL_BASE_R = 10,
+  CTL_MAXP = 11,     // leader: largest high key word received per list, refined thresholds
+  CTL_MAXR = 12,
+  CTL_TP = 13,
+  CTL_TR = 14,
   CTL_WORDS = 16
 };
 
@@ -267,6 +271,141 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int
   return r;
 }
 
+// Exact argmax rounds over this CTA's chunk: the `need` largest keys in order (penalised values
+// for list 0, raw values for list 1), written to the candidate buffer.  Only taken when more
+// candidates reach the row threshold than the buffer holds (heavy ties); kept out of line so the
+// common path stays small.  Every thread of the CTA calls it.  Returns the number found.
+template <int DT>
+__device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, int n_el, int lo, int list, int need,
+                                         bool penal, const uint32_t* hbits, const uint32_t* htab, int hash_bits,
+                                         float rep, float freq, float pres, uint64_t* red64, uint4* cand_pen,
+                                         uint64_t* cand_raw) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  uint64_t prev = ~0ull;
+  int got = 0;
+  for (int r = 0; r < need; ++r) {
+    uint64_t best = 0ull;
+    for (int v = tid; v < n_vec; v += NT) {
+      float x[EPV];
+      load_vec<DT>(data, v, x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+        if (loc >= static_cast<uint32_t>(n_el)) continue;
+        float pv = x[e];
+        if (list == 0 && penal && bit_at(hbits, loc)) pv = penalize(pv, hash_count(htab, hash_bits, loc), rep, freq, pres);
+        const uint32_t o = order_key(pv);
+        if (o == 0u) continue;
+        const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
+        if (key < prev && key > best) best = key;
+      }
+    }
+    best = block_max_u64(best, red64, lane, wid);
+    if (best == 0ull) break;
+    if (tid == 0) {
+      if (list == 0) {
+        const float raw = elem_at<DT>(data, key_id(best) - static_cast<uint32_t>(lo));
+        cand_pen[r] = make_uint4(static_cast<uint32_t>(best), static_cast<uint32_t>(best >> 32), __float_as_uint(raw), 0u);
+      } else {
+        cand_raw[r] = best;
+      }
+    }
+    prev = best;
+    got = r + 1;
+  }
+  __syncthreads();
+  return got;
+}
+
+// This thread's top two over the ids that carry no penalty (rare: taken only when the plain top
+// two hold a penalised id).  Out of line to keep the common path's code small.
+template <int DT>
+__device__ __noinline__ void masked_top2(const unsigned char* data, int n_vec, int n_el, const uint32_t* hbits,
+                                         float* v1o, int* i1o, float* v2o, int* i2o) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+  float v1 = -INFINITY, v2 = -INFINITY;
+  int i1 = -1, i2 = -1;
+#pragma unroll 1
+  for (int v = threadIdx.x; v < n_vec; v += NT) {
+    float x[EPV];
+    load_vec<DT>(data, v, x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const int loc = v * EPV + e;
+      if (loc < n_el && x[e] > v2 && !bit_at(hbits, static_cast<uint32_t>(loc))) {
+        if (x[e] > v1) {
+          v2 = v1;
+          i2 = i1;
+          v1 = x[e];
+          i1 = loc;
+        } else {
+          v2 = x[e];
+          i2 = loc;
+        }
+      }
+    }
+  }
+  *v1o = v1;
+  *i1o = i1;
+  *v2o = v2;
+  *i2o = i2;
+}
+
+// Every element of this thread at or above T (a thread whose second best reaches T): appended to
+// both candidate lists one by one.  Out of line (rare).
+template <int DT>
+__device__ __noinline__ void rescan_thread(const unsigned char* data, int n_vec, int n_el, int lo, uint32_t T,
+                                           bool penal, const uint32_t* hbits, uint32_t* ctl, uint4* cand_pen,
+                                           uint64_t* cand_raw, bool to_raw, bool to_pen) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+#pragma unroll 1
+  for (int v = threadIdx.x; v < n_vec; v += NT) {
+    float x[EPV];
+    load_vec<DT>(data, v, x);
+#pragma unroll 1
+    for (int e = 0; e < EPV; ++e) {
+      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+      const uint32_t o = order_key(x[e]);
+      if (loc >= static_cast<uint32_t>(n_el) || o == 0u || o < T) continue;
+      if (penal && bit_at(hbits, loc)) continue;
+      const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
+      if (to_raw) {
+        const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
+        if (i < LOCAL_CAP) cand_raw[i] = key;
+      }
+      if (to_pen) {
+        const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+        if (i < LOCAL_CAP)
+          cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(x[e]), 0u);
+      }
+    }
+  }
+}
+
+// top_p survivors with double-word prefix sums (rare: the fp32 decision was within 1e-5 of its
+// boundary).  Warp-wide: every lane of the warp calls it.
+__device__ __noinline__ int top_p_dw(float qa, float qb, bool ina, bool inb, float top_p, int m1, int lane) {
+  const DW a = warp_scan_dw(DW{qa, 0.0f}, lane);
+  const DW b = dw_add(shfl_dw(a, 31), warp_scan_dw(DW{qb, 0.0f}, lane));
+  const DW tg = dw_mul_f(shfl_dw(b, 31), top_p);
+  const uint32_t la = __ballot_sync(FULL_MASK, ina && dw_less(a, tg));
+  const uint32_t lb = __ballot_sync(FULL_MASK, inb && dw_less(b, tg));
+  return min(m1, __popc(la) + __popc(lb) + 1);
+}
+
+// The draw's pick with double-word prefix sums (rare, as above).  Warp-wide.
+__device__ __noinline__ int draw_dw(float wa, float wb, int m2, float u, int lane) {
+  const DW a = warp_scan_dw(DW{wa, 0.0f}, lane);
+  const DW b = dw_add(shfl_dw(a, 31), warp_scan_dw(DW{wb, 0.0f}, lane));
+  const int last = m2 - 1;
+  const DW Wd = (last < 32) ? shfl_dw(a, last) : shfl_dw(b, last - 32);
+  const DW td = dw_mul_f(Wd, u);
+  const uint32_t ja = __ballot_sync(FULL_MASK, lane < m2 && !dw_less(td, a));
+  const uint32_t jb = __ballot_sync(FULL_MASK, lane + 32 < m2 && !dw_less(td, b));
+  return min(__popc(ja) + __popc(jb), m2 - 1);
+}
+
 // ------------------------------------------------------------------------------ the kernel
 template <int DT>
 __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
@@ -350,8 +489,8 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
   if (tid < CTL_WORDS) ctl[tid] = 0u;
-  __syncthreads();   // tables zeroed, piece barriers initialised
-  cluster_arrive();  // every CTA of the cluster is running before any DSMEM access (waited below)
+  __syncthreads();           // tables zeroed, piece barriers initialised
+  cluster_arrive_relaxed();  // this CTA is running (DSMEM access waits for every CTA, below)
 
   // ---- row metadata (inputs only: slot keys are never written by a kernel) -------------------
   int slot = -1;
@@ -429,6 +568,7 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   {
     int waited = -1;
     int i = 0;
+#pragma unroll 1
     for (int v = tid; v < n_vec; v += NT, ++i) {
       const int p = i / VR;
       if (p < n_pieces && p != waited) {
@@ -475,29 +615,8 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
 
   // this thread's top two over the ids that carry no penalty (the threshold's elements)
   if (penal && ((i1 >= 0 && bit_at(hbits, static_cast<uint32_t>(i1))) ||
-                (i2 >= 0 && bit_at(hbits, static_cast<uint32_t>(i2))))) {
-    v1 = v2 = -INFINITY;
-    i1 = i2 = -1;
-    for (int v = tid; v < n_vec; v += NT) {
-      float x[EPV];
-      load_vec<DT>(data, v, x);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const int loc = v * EPV + e;
-        if (loc < n_el && x[e] > v2 && !bit_at(hbits, static_cast<uint32_t>(loc))) {
-          if (x[e] > v1) {
-            v2 = v1;
-            i2 = i1;
-            v1 = x[e];
-            i1 = loc;
-          } else {
-            v2 = x[e];
-            i2 = loc;
-          }
-        }
-      }
-    }
-  }
+                (i2 >= 0 && bit_at(hbits, static_cast<uint32_t>(i2)))))
+    masked_top2<DT>(data, n_vec, n_el, hbits, &v1, &i1, &v2, &i2);
   const uint32_t o1 = (i1 >= 0) ? order_key(v1) : 0u;
   const uint32_t o2 = (i2 >= 0) ? order_key(v2) : 0u;
 
@@ -585,8 +704,8 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     lse_a = (ga.m == -INFINITY || !(ga.s > 0.0f)) ? -INFINITY : ga.m + logf(ga.s);
   }
   // state of the tail, carried across the wait for the previous kernel (leader, warp 0)
-  int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0;
-  DW Ca{0.0f, 0.0f}, Cb{0.0f, 0.0f}, W{0.0f, 0.0f};
+  int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0, n_recv_p = 0;
+  float Ca = 0.0f, Cb = 0.0f, wa = 0.0f, wb = 0.0f;  // tempered weights and their fp32 prefix sums
   uint4 ea = make_uint4(0, 0, 0, 0), eb = make_uint4(0, 0, 0, 0);
   float va = 0.0f, vb = 0.0f;
 
@@ -607,20 +726,7 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     };
     // a thread whose second best reaches T may hold more: it rescans its own elements
     const bool full = (T == 0u && tid < n_vec) || (o2 != 0u && o2 >= T);
-    if (full) {
-      for (int v = tid; v < n_vec; v += NT) {
-        float x[EPV];
-        load_vec<DT>(data, v, x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-          const uint32_t o = order_key(x[e]);
-          if (loc >= static_cast<uint32_t>(n_el) || o == 0u || o < T) continue;
-          if (penal && bit_at(hbits, loc)) continue;
-          put(sel_key(o, static_cast<uint32_t>(lo) + loc), x[e], true, true);
-        }
-      }
-    }
+    if (full) rescan_thread<DT>(data, n_vec, n_el, lo, T, penal, hbits, ctl, cand_pen, cand_raw, n_row > 0, k_row > 0);
     {  // the common case: at most this thread's best reaches T (one warp-wide append per list)
       const bool one = !full && o1 != 0u && o1 >= T;
       const uint32_t bal = __ballot_sync(FULL_MASK, one);
@@ -664,50 +770,12 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     int nr = static_cast<int>(ctl[CTL_CAND_RAW]);
     // more candidates than the buffer holds (heavy ties): exact argmax rounds write the chunk's
     // best k_row / n_row in order into the candidate buffers
-    if ((k_row > 0 && np > LOCAL_CAP) || (n_row > 0 && nr > LOCAL_CAP)) {
-      const bool do_p = k_row > 0 && np > LOCAL_CAP, do_r = n_row > 0 && nr > LOCAL_CAP;
-      for (int list = 0; list < 2; ++list) {
-        if (list == 0 ? !do_p : !do_r) continue;
-        const int need = list == 0 ? k_row : n_row;
-        uint64_t prev = ~0ull;
-        int got = 0;
-        for (int r = 0; r < need; ++r) {
-          uint64_t best = 0ull;
-          for (int v = tid; v < n_vec; v += NT) {
-            float x[EPV];
-            load_vec<DT>(data, v, x);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-              if (loc >= static_cast<uint32_t>(n_el)) continue;
-              float pv = x[e];
-              if (list == 0 && penal && bit_at(hbits, loc))
-                pv = penalize(pv, hash_count(htab, P.hash_bits, loc), sp.rep, sp.freq, sp.pres);
-              const uint32_t o = order_key(pv);
-              if (o == 0u) continue;
-              const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
-              if (key < prev && key > best) best = key;
-            }
-          }
-          best = block_max_u64(best, red64, lane, wid);
-          if (best == 0ull) break;
-          if (tid == 0) {
-            if (list == 0) {
-              const float raw = elem_at<DT>(data, key_id(best) - static_cast<uint32_t>(lo));
-              cand_pen[r] = make_uint4(static_cast<uint32_t>(best), static_cast<uint32_t>(best >> 32),
-                                       __float_as_uint(raw), 0u);
-            } else {
-              cand_raw[r] = best;
-            }
-          }
-          prev = best;
-          got = r + 1;
-        }
-        if (list == 0) np = got;
-        else nr = got;
-      }
-      __syncthreads();
-    }
+    if (k_row > 0 && np > LOCAL_CAP)
+      np = exact_rounds<DT>(data, n_vec, n_el, lo, 0, k_row, penal, hbits, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+                            red64, cand_pen, cand_raw);
+    if (n_row > 0 && nr > LOCAL_CAP)
+      nr = exact_rounds<DT>(data, n_vec, n_el, lo, 1, n_row, penal, hbits, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+                            red64, cand_pen, cand_raw);
 
     // keep this chunk's best k_row / n_row and reserve their slice of the leader's lists
     const int sent_pen = min(np, k_row), sent_raw = min(nr, n_row);
@@ -758,37 +826,173 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     if (crank == 0) {
       const int tot_p = static_cast<int>(ctl[CTL_RECV_NP]);
       const int tot_r = static_cast<int>(ctl[CTL_RECV_NR]);
-      const int tot = tot_p + tot_r;
       uint4* sorted_pen = cand_pen;   // the leader's own candidates were sent before B1
-      uint64_t* sorted_raw = cand_raw;
+      uint64_t* sorted_raw = reinterpret_cast<uint64_t*>(cand_pen + KMAX);
+      const uint2* pkeys = reinterpret_cast<const uint2*>(recv_pen);
+      if (tot_p <= 256 && tot_r <= 256) {
+        // common case: warp 0 sorts the penalised list, warp 1 the raw list, each in registers;
+        // no block barrier, each warp then reads its own sorted list back
+        if (wid < 2) {
+          const int n = wid == 0 ? tot_p : tot_r;
+          const int need = wid == 0 ? k_row : n_row;
+          if (n <= 128) {
+            uint64_t kk[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int i = lane * 4 + r;
+              kk[r] = i < n ? (wid == 0 ? ((static_cast<uint64_t>(pkeys[2 * i].y) << 32) | pkeys[2 * i].x) : recv_raw[i]) : 0ull;
+            }
+            warp_sort_desc<4>(kk, lane);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int i = lane * 4 + r;
+              if (i < need && i < n) {
+                if (wid == 0) sorted_pen[i] = make_uint4(static_cast<uint32_t>(kk[r]), static_cast<uint32_t>(kk[r] >> 32), 0u, 0u);
+                else sorted_raw[i] = kk[r];
+              }
+            }
+          } else {
+            uint64_t kk[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const int i = lane * 8 + r;
+              kk[r] = i < n ? (wid == 0 ? ((static_cast<uint64_t>(pkeys[2 * i].y) << 32) | pkeys[2 * i].x) : recv_raw[i]) : 0ull;
+            }
+            warp_sort_desc<8>(kk, lane);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const int i = lane * 8 + r;
+              if (i < need && i < n) {
+                if (wid == 0) sorted_pen[i] = make_uint4(static_cast<uint32_t>(kk[r]), static_cast<uint32_t>(kk[r] >> 32), 0u, 0u);
+                else sorted_raw[i] = kk[r];
+              }
+            }
+          }
+          __syncwarp();
+        }
+      } else {
+      uint32_t* hist = reinterpret_cast<uint32_t*>(cand_raw);            // 2 x 256 bins
+      uint16_t* surv = reinterpret_cast<uint16_t*>(hist + 512);          // survivors of both lists
+      // A long list is first cut by a threshold on the high key word: a 256-bin histogram of
+      // (hi - T) over the list's range, scanned from the top, keeps the bin holding the
+      // need-th largest value and everything above it (all of the top `need`, plus that bin).
+      const bool cut_p = tot_p > max(2 * k_row, 32), cut_r = tot_r > max(2 * n_row, 32);
+      const uint32_t Thi = T;
+      if (cut_p || cut_r) {
+        if (tid < 512 / 2) reinterpret_cast<uint2*>(hist)[tid] = make_uint2(0u, 0u);
+        uint32_t mp = 0u, mr = 0u;
+        for (int f = tid; f < tot_p; f += NT) mp = max(mp, pkeys[2 * f].y);
+        for (int f = tid; f < tot_r; f += NT) mr = max(mr, static_cast<uint32_t>(recv_raw[f] >> 32));
+        mp = __reduce_max_sync(FULL_MASK, mp);
+        mr = __reduce_max_sync(FULL_MASK, mr);
+        if (lane == 0) {
+          atomicMax(&ctl[CTL_MAXP], mp);
+          atomicMax(&ctl[CTL_MAXR], mr);
+        }
+        __syncthreads();
+        const uint32_t span_p = ctl[CTL_MAXP] - Thi, span_r = ctl[CTL_MAXR] - Thi;
+        const int sh_p = max(0, 32 - __clz(static_cast<int>(span_p | 1u)) - 8);
+        const int sh_r = max(0, 32 - __clz(static_cast<int>(span_r | 1u)) - 8);
+        if (cut_p)
+          for (int f = tid; f < tot_p; f += NT) atomicAdd(&hist[(pkeys[2 * f].y - Thi) >> sh_p], 1u);
+        if (cut_r)
+          for (int f = tid; f < tot_r; f += NT) atomicAdd(&hist[256 + ((static_cast<uint32_t>(recv_raw[f] >> 32) - Thi) >> sh_r)], 1u);
+        __syncthreads();
+        if (wid < 2 && (wid == 0 ? cut_p : cut_r)) {  // warp 0: penalised list, warp 1: raw list
+          const uint32_t* hh = hist + 256 * wid;
+          const int need = wid == 0 ? k_row : n_row;
+          uint32_t c[8], tsum = 0u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {  // lane l holds bins 255-8l .. 248-8l (from the top)
+            c[j] = hh[255 - (8 * lane + j)];
+            tsum += c[j];
+          }
+          uint32_t incl = tsum;  // inclusive prefix over lanes = count in bins above this lane's
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t y = __shfl_up_sync(FULL_MASK, incl, off);
+            if (lane >= off) incl += y;
+          }
+          uint32_t run = incl - tsum;
+          int bstar = -1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            run += c[j];
+            if (bstar < 0 && run >= static_cast<uint32_t>(need)) bstar = 255 - (8 * lane + j);
+          }
+          const uint32_t has = __ballot_sync(FULL_MASK, bstar >= 0);
+          const int first = __ffs(has) - 1;  // lowest lane = highest bins
+          const int b = __shfl_sync(FULL_MASK, bstar, first < 0 ? 0 : first);
+          if (lane == 0) ctl[wid == 0 ? CTL_TP : CTL_TR] = first < 0 ? Thi : Thi + (static_cast<uint32_t>(b) << (wid == 0 ? sh_p : sh_r));
+        }
+        __syncthreads();
+      }
+      // survivors (indices into the received lists), then exact ranks among them; a cut that keeps
+      // more than the survivor buffer holds (ties) is dropped and the whole list is ranked
+      constexpr uint32_t SURV = 512;
+      const uint32_t tp = cut_p ? ctl[CTL_TP] : 0u, tr = cut_r ? ctl[CTL_TR] : 0u;
+      int n_sp = tot_p, n_sr = tot_r;
+      bool use_sp = false, use_sr = false;
+      if (cut_p || cut_r) {
+        if (tid == 0) {
+          ctl[CTL_BASE_P] = 0u;
+          ctl[CTL_BASE_R] = 0u;
+        }
+        __syncthreads();
+        for (int f0 = 0; f0 < max(tot_p, tot_r); f0 += NT) {
+          const int f = f0 + tid;
+          const bool kp_ = cut_p && f < tot_p && pkeys[2 * f].y >= tp;
+          const bool kr_ = cut_r && f < tot_r && static_cast<uint32_t>(recv_raw[f] >> 32) >= tr;
+          const uint32_t bp = __ballot_sync(FULL_MASK, kp_), br = __ballot_sync(FULL_MASK, kr_);
+          uint32_t basep = 0, baser = 0;
+          if (lane == 0) {
+            if (bp) basep = atomicAdd(&ctl[CTL_BASE_P], static_cast<uint32_t>(__popc(bp)));
+            if (br) baser = atomicAdd(&ctl[CTL_BASE_R], static_cast<uint32_t>(__popc(br)));
+          }
+          basep = __shfl_sync(FULL_MASK, basep, 0) + __popc(bp & ((1u << lane) - 1u));
+          baser = __shfl_sync(FULL_MASK, baser, 0) + __popc(br & ((1u << lane) - 1u));
+          if (kp_ && basep < SURV) surv[basep] = static_cast<uint16_t>(f);
+          if (kr_ && baser < SURV) surv[SURV + baser] = static_cast<uint16_t>(f);
+        }
+        __syncthreads();
+        use_sp = cut_p && ctl[CTL_BASE_P] <= SURV;
+        use_sr = cut_r && ctl[CTL_BASE_R] <= SURV;
+        if (use_sp) n_sp = static_cast<int>(ctl[CTL_BASE_P]);
+        if (use_sr) n_sr = static_cast<int>(ctl[CTL_BASE_R]);
+      }
+      const int tot = n_sp + n_sr;
       int G = 1;  // threads per ranked key (a power of two)
       while (G < 32 && 2 * G * tot <= NT) G *= 2;
-      const uint2* pkeys = reinterpret_cast<const uint2*>(recv_pen);
       for (int base = 0; base < tot; base += NT / G) {
-        const int f = base + tid / G, sub = tid & (G - 1);
+        const int g = base + tid / G, sub = tid & (G - 1);
         int rank = 0;
         uint64_t ki = 0ull;
-        if (f < tot_p) {
-          const uint2 k2 = pkeys[2 * f];
+        int src = -1;
+        if (g < n_sp) {
+          src = use_sp ? surv[g] : g;
+          const uint2 k2 = pkeys[2 * src];
           ki = (static_cast<uint64_t>(k2.y) << 32) | k2.x;
-          for (int j = sub; j < tot_p; j += G) {
-            const uint2 o = pkeys[2 * j];
+          for (int j = sub; j < n_sp; j += G) {
+            const uint2 o = pkeys[2 * (use_sp ? surv[j] : j)];
             rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
           }
-        } else if (f < tot) {
-          ki = recv_raw[f - tot_p];
-          for (int j = sub; j < tot_r; j += G) rank += recv_raw[j] > ki;
+        } else if (g < tot) {
+          src = use_sr ? surv[SURV + (g - n_sp)] : g - n_sp;
+          ki = recv_raw[src];
+          for (int j = sub; j < n_sr; j += G) rank += recv_raw[use_sr ? surv[SURV + j] : j] > ki;
         }
         for (int off = G >> 1; off > 0; off >>= 1) rank += __shfl_xor_sync(FULL_MASK, rank, off);
         if (sub == 0) {
-          if (f < tot_p) {
-            if (rank < k_row) sorted_pen[rank] = recv_pen[f];
-          } else if (f < tot && rank < n_row) {
+          if (g < n_sp) {
+            if (rank < k_row) sorted_pen[rank] = recv_pen[src];
+          } else if (g < tot && rank < n_row) {
             sorted_raw[rank] = ki;
           }
         }
       }
       __syncthreads();
+      }
+      n_recv_p = tot_p;
       k_eff = min(k_row, tot_p);
       n_eff = min(n_row, tot_r);
 
@@ -809,31 +1013,37 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
             const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && vb >= thr);
             m1 = max(1, __popc(ba) + __popc(bb));
           }
-          // temperature-1 mass (top_p) and tempered weights (draw) over the min_p survivors, as
-          // double-word prefix sums; the draw only ever reads prefixes below m2
+          // temperature-1 mass (top_p) and tempered weights (draw) over the min_p survivors.
+          // Prefix sums in fp32 decide unless a decision lies within 1e-5 of its boundary (the fp32
+          // scan is good to ~4e-7 relative); then double-word sums (TwoSum) decide.
           const bool ina = lane < m1, inb = lane + 32 < m1;
           const float da = __fsub_rn(va, v0), db = __fsub_rn(vb, v0);
           const float Tm = sp.temperature;
-          const DW qa{ina ? expf(da) : 0.0f, 0.0f}, qb{inb ? expf(db) : 0.0f, 0.0f};
-          const DW wa{ina ? expf(__fdiv_rn(da, Tm)) : 0.0f, 0.0f};
-          const DW wb{inb ? expf(__fdiv_rn(db, Tm)) : 0.0f, 0.0f};
-          const DW ca = warp_scan_dw(qa, lane);
-          Ca = warp_scan_dw(wa, lane);
-          const DW cb = dw_add(shfl_dw(ca, 31), warp_scan_dw(qb, lane));
-          Cb = dw_add(shfl_dw(Ca, 31), warp_scan_dw(wb, lane));
+          const float qa = ina ? expf(da) : 0.0f, qb = inb ? expf(db) : 0.0f;
+          wa = ina ? expf(__fdiv_rn(da, Tm)) : 0.0f;
+          wb = inb ? expf(__fdiv_rn(db, Tm)) : 0.0f;
+          const float ca = warp_scan_f(qa, lane);
+          Ca = warp_scan_f(wa, lane);
+          const float cb = warp_scan_f(qb, lane) + __shfl_sync(FULL_MASK, ca, 31);
+          Cb = warp_scan_f(wb, lane) + __shfl_sync(FULL_MASK, Ca, 31);
           m2 = m1;
           if (!(sp.top_p >= 1.0f)) {
             if (!(sp.top_p > 0.0f)) {
               m2 = 1;
             } else {
-              const DW target = dw_mul_f(shfl_dw(cb, 31), sp.top_p);
-              const uint32_t la = __ballot_sync(FULL_MASK, ina && dw_less(ca, target));
-              const uint32_t lb = __ballot_sync(FULL_MASK, inb && dw_less(cb, target));
-              m2 = min(m1, __popc(la) + __popc(lb) + 1);
+              const float tot = __shfl_sync(FULL_MASK, cb, 31);
+              const float target = sp.top_p * tot, margin = 1e-5f * tot;
+              const bool near = __any_sync(FULL_MASK, (ina && fabsf(ca - target) <= margin) ||
+                                                          (inb && fabsf(cb - target) <= margin));
+              if (!near) {
+                const uint32_t la = __ballot_sync(FULL_MASK, ina && ca < target);
+                const uint32_t lb = __ballot_sync(FULL_MASK, inb && cb < target);
+                m2 = min(m1, __popc(la) + __popc(lb) + 1);
+              } else {
+                m2 = top_p_dw(qa, qb, ina, inb, sp.top_p, m1, lane);
+              }
             }
           }
-          const int last = m2 - 1;
-          W = (last < 32) ? shfl_dw(Ca, last) : shfl_dw(Cb, last - 32);
         }
       }
     }
@@ -869,10 +1079,10 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   }
 
   if (kp > 0 && crank == 0) {
-    const uint64_t* sorted_raw = cand_raw;
+    const uint64_t* sorted_raw = reinterpret_cast<const uint64_t*>(cand_pen + KMAX);
     // top-N raw alternatives and their log-probabilities
-    if (n_row > 0 && P.top_ids != nullptr) {
-      for (int i = tid; i < n_row; i += NT) {
+    if (n_row > 0 && P.top_ids != nullptr && wid == 1) {  // warp 1 wrote the sorted raw list
+      for (int i = lane; i < n_row; i += 32) {
         const long long o = static_cast<long long>(row) * P.top_n + i;
         if (i < n_eff) {
           const uint64_t key = sorted_raw[i];
@@ -903,15 +1113,35 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
           }
           x0 = __shfl_sync(FULL_MASK, x0, 0);
           const float u = static_cast<float>(x0 >> 8) * 0x1p-24f;
-          const DW tgt = dw_mul_f(W, u);
-          const uint32_t ja = __ballot_sync(FULL_MASK, lane < m2 && !dw_less(tgt, Ca));
-          const uint32_t jb = __ballot_sync(FULL_MASK, lane + 32 < m2 && !dw_less(tgt, Cb));
-          j = min(__popc(ja) + __popc(jb), m2 - 1);
+          const int last = m2 - 1;  // the draw reads prefixes below m2 only; W = C[m2 - 1]
+          const float W = (last < 32) ? __shfl_sync(FULL_MASK, Ca, last) : __shfl_sync(FULL_MASK, Cb, last - 32);
+          const float tgt = u * W, margin = 1e-5f * W;
+          const bool ia = lane < m2, ib = lane + 32 < m2;
+          const bool near = __any_sync(FULL_MASK, (ia && fabsf(Ca - tgt) <= margin) || (ib && fabsf(Cb - tgt) <= margin));
+          if (!near) {
+            const uint32_t ja = __ballot_sync(FULL_MASK, ia && Ca <= tgt);
+            const uint32_t jb = __ballot_sync(FULL_MASK, ib && Cb <= tgt);
+            j = min(__popc(ja) + __popc(jb), m2 - 1);
+          } else {
+            j = draw_dw(wa, wb, m2, u, lane);
+          }
         }
         const uint32_t id_a = key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x);
         const uint32_t id_b = key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x);
         out = static_cast<int>(__shfl_sync(FULL_MASK, j < 32 ? id_a : id_b, j & 31));
-        chosen_raw = __shfl_sync(FULL_MASK, __uint_as_float(j < 32 ? ea.z : eb.z), j & 31);
+        if (P.chosen_lp != nullptr) {  // the raw logit travelled with the received entry
+          const uint32_t kx = __shfl_sync(FULL_MASK, j < 32 ? ea.x : eb.x, j & 31);
+          const uint32_t ky = __shfl_sync(FULL_MASK, j < 32 ? ea.y : eb.y, j & 31);
+          for (int f0 = 0; f0 < n_recv_p; f0 += 32) {
+            const int f = f0 + lane;
+            const uint4 ent = f < n_recv_p ? recv_pen[f] : make_uint4(0, 0, 0, 0);
+            const uint32_t bal = __ballot_sync(FULL_MASK, f < n_recv_p && ent.x == kx && ent.y == ky);
+            if (bal != 0u) {
+              chosen_raw = __shfl_sync(FULL_MASK, __uint_as_float(ent.z), __ffs(bal) - 1);
+              break;
+            }
+          }
+        }
       }
       if (lane == 0) {
         P.out_ids[row] = out;
