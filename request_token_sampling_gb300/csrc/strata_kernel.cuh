@@ -1,20 +1,24 @@
 // strata_kernel.cuh -- the fused row kernel: one HBM pass per logit row.
 //
 // Each logit row is split over a thread-block cluster of `cs` CTAs (one chunk per CTA).  A CTA
-//   1. bulk-copies its chunk into shared memory (16 KiB pieces, one mbarrier each), and while the
-//      bytes land builds the row's history table for its id range (bitmap + open-addressing
-//      counts) and, as each piece completes, runs the first pass: the per-thread running max and
-//      sum of exp (log-sum-exp of the raw logits);
-//   2. derives a selection threshold t_c: the q-th largest per-thread maximum of the logits that
-//      carry no penalty (q = ceil(K/cs), K = max(top_k, top_n)).  q distinct elements of the
-//      chunk reach t_c, so min over the cluster of t_c bounds the row's K-th largest value from
-//      below; the CTAs exchange t_c and their (max, sum) pairs through DSMEM (cluster barrier B0);
-//   3. rescans only the threads whose maximum reaches the row threshold, adds the penalised ids
-//      from the history table, keeps its best <= K candidates and sends them to the cluster's
-//      leader CTA through DSMEM (cluster barrier B1);
-//   4. the leader ranks the <= cs*K received keys exactly, then one warp runs the tail of the
-//      chain on <= 64 survivors: min_p, top_p, temperature, the Philox draw.
+//   1. bulk-copies its chunk into shared memory (32 KiB pieces, one mbarrier each) and, as each
+//      piece lands, runs the first pass: per thread the running maximum and the sum of exp
+//      against a lazily moved reference (log-sum-exp of the raw logits); meanwhile the row's
+//      metadata loads are in flight, and the history table of the chunk's id range (bitmap +
+//      open-addressing counts) and the allowed-subset partial sums follow the last piece;
+//   2. publishes to every CTA of the cluster, with asynchronous DSMEM stores completed on one
+//      mbarrier per CTA, its largest q per-warp maxima of the logits that carry no penalty and its
+//      two (max, sum) pairs (row and allowed subset).  Every CTA then takes T = the K-th largest of
+//      the cs*q published values (K = max(top_k, top_n)): they are K distinct elements of the row,
+//      so the row's K-th largest value (raw, and penalised, since those ids carry no penalty) is
+//      at least T;
+//   3. rescans only the threads whose maximum reaches T, adds the penalised ids of the history
+//      table, keeps its best <= K candidates and stores them into its own slice of the cluster
+//      leader's receive lists (asynchronous DSMEM stores, one transaction-counted arrival per CTA);
+//   4. the leader ranks the received keys by counting (one thread per key), then one warp runs the
+//      tail of the chain on <= 64 survivors: min_p, top_p, temperature, the Philox draw.
 // Every CTA writes the allowed-subset and chosen-id log-probabilities of its own id range.
+// Every wait on another CTA or on a copy is an mbarrier poll with an iteration limit.
 //
 // The chain it computes is defined on the pages "#19 serve: per-request temperature/top_p/top_k/
 // min_p/penalties sampling" (section "What changed") and "#3200 [Engine] OpenAI logprobs /
@@ -40,7 +44,7 @@ constexpr int MAX_PIECES = 6;                // chunk <= 192 KiB
 constexpr int MAX_CS = 16;                   // CTAs per row (non-portable cluster size)
 constexpr int KMAX = STRATA_MAX_TOP_K;
 constexpr int NMAX = STRATA_MAX_TOP_N;
-constexpr int QMAX = 8;                      // per-CTA threshold rank handled by the warp stage
+constexpr int QMAX = 8;                      // the host keeps cs >= ceil(K / QMAX): cs * NW >= 2K
 constexpr int LOCAL_CAP = 512;               // per-CTA candidate buffer (beyond: exact rounds)
 constexpr int HASH_CNT_BITS = 13;            // history table entry = (local id << 13) | count
 constexpr uint32_t HASH_EMPTY = 0xFFFFFFFFu;
@@ -49,25 +53,25 @@ constexpr int MODE_LOGPROBS = 1;
 constexpr uint32_t SLOT_SAMPLED = 1u;
 constexpr uint32_t SLOT_PENAL = 2u;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // bounded waits: ~2 s at GB300 clocks
+constexpr float LAZY_SHIFT = 16.0f;          // the exp reference moves only when the max passes it by this
+constexpr int XREC_WORDS = 20;               // published per CTA: 16 warp-maximum keys + 2 (max, sum) pairs
+constexpr int XREC_BYTES = XREC_WORDS * 4;
+constexpr int HPRE = 2;                      // history ids per thread fetched ahead of the table build
+constexpr int BAR_X0 = MAX_PIECES;           // mbarrier: every CTA's published record has landed
+constexpr int BAR_X1 = MAX_PIECES + 1;       // mbarrier (leader): every CTA's candidates have landed
+constexpr int NBAR = MAX_PIECES + 2;
 
 // Control words in shared memory.
 enum : int {
-  CTL_CAND_PEN = 0,
+  CTL_CAND_PEN = 0,  // candidates appended to this CTA's penalised / raw lists
   CTL_CAND_RAW = 1,
-  CTL_TC = 2,
-  CTL_CTR_LO = 3,
-  CTL_CTR_HI = 4,
-  CTL_TIMEOUT = 5,
-  CTL_X0 = 6,        // first Philox word of the leader's row
-  CTL_RECV_NP = 7,   // leader: entries received in the flat penalised / raw lists
-  CTL_RECV_NR = 8,
-  CTL_BASE_P = 9,    // this CTA's slice of the leader's lists
-  CTL_BASE_R = 10,
-  CTL_MAXP = 11,     // leader: largest high key word received per list, refined thresholds
-  CTL_MAXR = 12,
-  CTL_TP = 13,
-  CTL_TR = 14,
-  CTL_WORDS = 16
+  CTL_T = 2,         // the row threshold (atomicMin target, starts at all ones)
+  CTL_TIMEOUT = 3,
+  CTL_LSE = 4,       // log-sum-exp of the row / of the allowed subset (float bits)
+  CTL_LSE_A = 5,
+  CTL_TOT_P = 6,     // leader: received entries per list
+  CTL_TOT_R = 7,
+  CTL_WORDS = 8
 };
 
 // A slot's keys as the kernel reads them (prepared and validated by the host).
@@ -116,8 +120,8 @@ struct KParams {
 };
 
 struct Layout {
-  uint32_t data, mbar, hbits, abits, hash, dirty, tc, ms, wtop, red, ctl;
-  uint32_t cand_pen, cand_raw, recv_pen, recv_raw, recv_cnt, total;
+  uint32_t data, mbar, hbits, abits, hash, hflag, wmax, red, ctl, xrec;
+  uint32_t cand_pen, cand_raw, recv_cnt, recv_pen, recv_raw, sorted_pen, sorted_raw, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -130,40 +134,51 @@ __host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, 
   L.data = o;
   o += align_up(static_cast<uint32_t>(chunk) * esz, 128);
   L.mbar = o;
-  o += MAX_PIECES * 8;
+  o += NBAR * 8;
   const uint32_t bw = align_up((static_cast<uint32_t>(chunk) + 31) / 32 * 4, 16);
   L.hbits = o;
   o += bw;
   L.abits = o;
   o += bw;
   L.hash = o;
-  o += static_cast<uint32_t>(hash_cap) * 4;
-  L.dirty = o;
+  o += align_up(static_cast<uint32_t>(hash_cap) * 4, 16);
+  L.hflag = o;
   o += NT / 8;
-  L.tc = o;
-  o += MAX_CS * 4;
-  o = align_up(o, 16);
-  L.ms = o;
-  o += MAX_CS * 16;
-  L.wtop = o;
-  o += NW * QMAX * 4;
+  L.wmax = o;
+  o += NW * 4;
   L.red = o;
-  o += NW * 16 + 64;
+  o += NW * 16;
   L.ctl = o;
   o += CTL_WORDS * 4;
   o = align_up(o, 16);
+  L.xrec = o;
+  o += MAX_CS * XREC_BYTES;
   L.cand_pen = o;
   o += LOCAL_CAP * 16;
   L.cand_raw = o;
   o += LOCAL_CAP * 8;
+  L.recv_cnt = o;
+  o += MAX_CS * 8;
   L.recv_pen = o;
   o += static_cast<uint32_t>(cs * kmax) * 16;
   L.recv_raw = o;
   o += static_cast<uint32_t>(cs * nmax) * 8;
-  L.recv_cnt = o;
-  o += MAX_CS * 8;
+  o = align_up(o, 16);
+  L.sorted_pen = o;
+  o += KMAX * 16;
+  L.sorted_raw = o;
+  o += NMAX * 8;
   L.total = align_up(o, 128);
   return L;
+}
+
+// Every region starts on a 16-byte boundary (vector and bulk accesses rely on it).
+__host__ __device__ inline bool layout_aligned(const Layout& L) {
+  const uint32_t r[] = {L.data, L.mbar, L.hbits, L.abits, L.hash, L.hflag, L.wmax, L.red, L.ctl, L.xrec,
+                        L.cand_pen, L.cand_raw, L.recv_cnt, L.recv_pen, L.recv_raw, L.sorted_pen, L.sorted_raw};
+  for (uint32_t x : r)
+    if (x % 16u != 0u) return false;
+  return true;
 }
 
 // ------------------------------------------------------------------------------ helpers
@@ -235,12 +250,12 @@ __device__ uint32_t hash_count(const uint32_t* tab, int bits, uint32_t loc) {
   return 0u;
 }
 
-// Bounded wait on piece `p` (phase 0).  On timeout the error word and a shared flag are set and
-// the caller carries on, so every thread still reaches every cluster barrier.
-__device__ __forceinline__ void wait_piece(uint64_t* mbar, int p, uint32_t* ctl, uint32_t* err) {
-  if (mbar_try_wait(&mbar[p], 0)) return;
+// Bounded poll of an mbarrier phase (parity 0).  On timeout the error word and a shared flag are
+// set and the caller carries on with whatever has landed.
+__device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t* ctl, uint32_t* err, bool cluster_scope) {
+  if (cluster_scope ? mbar_try_wait_cluster(bar, 0) : mbar_try_wait(bar, 0)) return;
   const long long t0 = clock64();
-  while (!mbar_try_wait(&mbar[p], 0)) {
+  while (!(cluster_scope ? mbar_try_wait_cluster(bar, 0) : mbar_try_wait(bar, 0))) {
     if (clock64() - t0 > WAIT_CYCLES) {
       atomicOr(err, STRATA_DEVERR_TIMEOUT);
       ctl[CTL_TIMEOUT] = 1u;
@@ -256,6 +271,100 @@ __device__ __forceinline__ void online_add(MaxSum& a, float v) {
     a.m = v;
   } else {
     a.s += ex2_approx((v - a.m) * LOG2E);
+  }
+}
+
+template <int DT>
+constexpr int BATCH_VECS = DT == 0 ? 4 : 2;  // 16 elements
+
+// First pass over this thread's vectors of one piece, a batch of 16 elements at a time: the
+// running max `mx`, the batch `bmx` that holds it and the largest max `mx2` of the thread's other
+// batches, and the sum of exp(x - ref) in two partial sums.  The reference `ref` moves to the piece's max only when that
+// exceeds it by LAZY_SHIFT (or on the first finite piece), so the common piece costs one compare.
+template <int DT>
+__device__ __forceinline__ void pass1_piece(const unsigned char* data, int p, int v0, int n_vec, float& ref,
+                                            float& mx, float& mx2, int& bmx, float& s0, float& s1) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+  constexpr int RB = BATCH_VECS<DT>;  // vectors held at once: one batch of 16 elements
+#pragma unroll
+  for (int r0 = 0; r0 < VR; r0 += RB) {
+    float x[RB][EPV];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int v = v0 + (r0 + r) * NT;
+      if (v < n_vec) {
+        load_vec<DT>(data, v, x[r]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) x[r][e] = -INFINITY;
+      }
+    }
+    float pm = x[0][0];
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) pm = fmaxf(pm, x[r][e]);
+    if (pm > mx) {  // the batch holding the thread's max, and the best max of its other batches
+      mx2 = mx;
+      mx = pm;
+      bmx = p * (VR / RB) + r0 / RB;
+    } else {
+      mx2 = fmaxf(mx2, pm);
+    }
+    if (pm > ref + LAZY_SHIFT) {
+      const float f = (ref == -INFINITY) ? 0.0f : ex2_approx((ref - pm) * LOG2E);
+      s0 *= f;
+      s1 *= f;
+      ref = pm;
+    }
+    if (ref != -INFINITY) {
+      const float mb = ref * LOG2E;
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int e = 0; e < EPV; e += 2) {
+          s0 += ex2_approx(fmaf(x[r][e], LOG2E, -mb));
+          s1 += ex2_approx(fmaf(x[r][e + 1], LOG2E, -mb));
+        }
+    }
+  }
+}
+
+// Every element of this thread whose key reaches T and that carries no penalty: appended to the
+// raw list (top-N alternatives) and the penalised list (the chain), with its raw logit; this
+// thread's vectors v_first, v_first + NT, ... up to v_last.  Only the few threads whose maximum
+// reaches T call it, usually on the one batch that holds their maximum.  Kept small and out of line: the kernel's code is
+// larger than the instruction cache, so code size on the serial phases costs fetch stalls.
+template <int DT>
+__device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_first, int v_last, int n_vec, int n_el,
+                                               int lo, uint32_t T, bool penal, const uint32_t* hbits, uint32_t* ctl,
+                                               uint4* cand_pen, uint64_t* cand_raw, bool to_raw, bool to_pen) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+#pragma unroll 1
+  for (int v = v_first; v < n_vec && v <= v_last; v += NT) {
+    float x[EPV];
+    load_vec<DT>(data, v, x);
+    uint32_t hit = 0u;  // elements of this vector at or above T
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(order_key(x[e]) >= T) << e;
+#pragma unroll 1
+    for (; hit != 0u; hit &= hit - 1u) {
+      const int e = __ffs(hit) - 1;
+      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+      const float xv = elem_at<DT>(data, loc);
+      const uint32_t o = order_key(xv);
+      if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && bit_at(hbits, loc))) continue;
+      const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
+      if (to_raw) {
+        const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
+        if (i < LOCAL_CAP) cand_raw[i] = key;
+      }
+      if (to_pen) {
+        const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+        if (i < LOCAL_CAP)
+          cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(xv), 0u);
+      }
+    }
   }
 }
 
@@ -318,71 +427,6 @@ __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, i
   return got;
 }
 
-// This thread's top two over the ids that carry no penalty (rare: taken only when the plain top
-// two hold a penalised id).  Out of line to keep the common path's code small.
-template <int DT>
-__device__ __noinline__ void masked_top2(const unsigned char* data, int n_vec, int n_el, const uint32_t* hbits,
-                                         float* v1o, int* i1o, float* v2o, int* i2o) {
-  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
-  float v1 = -INFINITY, v2 = -INFINITY;
-  int i1 = -1, i2 = -1;
-#pragma unroll 1
-  for (int v = threadIdx.x; v < n_vec; v += NT) {
-    float x[EPV];
-    load_vec<DT>(data, v, x);
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      const int loc = v * EPV + e;
-      if (loc < n_el && x[e] > v2 && !bit_at(hbits, static_cast<uint32_t>(loc))) {
-        if (x[e] > v1) {
-          v2 = v1;
-          i2 = i1;
-          v1 = x[e];
-          i1 = loc;
-        } else {
-          v2 = x[e];
-          i2 = loc;
-        }
-      }
-    }
-  }
-  *v1o = v1;
-  *i1o = i1;
-  *v2o = v2;
-  *i2o = i2;
-}
-
-// Every element of this thread at or above T (a thread whose second best reaches T): appended to
-// both candidate lists one by one.  Out of line (rare).
-template <int DT>
-__device__ __noinline__ void rescan_thread(const unsigned char* data, int n_vec, int n_el, int lo, uint32_t T,
-                                           bool penal, const uint32_t* hbits, uint32_t* ctl, uint4* cand_pen,
-                                           uint64_t* cand_raw, bool to_raw, bool to_pen) {
-  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
-#pragma unroll 1
-  for (int v = threadIdx.x; v < n_vec; v += NT) {
-    float x[EPV];
-    load_vec<DT>(data, v, x);
-#pragma unroll 1
-    for (int e = 0; e < EPV; ++e) {
-      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-      const uint32_t o = order_key(x[e]);
-      if (loc >= static_cast<uint32_t>(n_el) || o == 0u || o < T) continue;
-      if (penal && bit_at(hbits, loc)) continue;
-      const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
-      if (to_raw) {
-        const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
-        if (i < LOCAL_CAP) cand_raw[i] = key;
-      }
-      if (to_pen) {
-        const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
-        if (i < LOCAL_CAP)
-          cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(x[e]), 0u);
-      }
-    }
-  }
-}
-
 // top_p survivors with double-word prefix sums (rare: the fp32 decision was within 1e-5 of its
 // boundary).  Warp-wide: every lane of the warp calls it.
 __device__ __noinline__ int top_p_dw(float qa, float qb, bool ina, bool inb, float top_p, int m1, int lane) {
@@ -404,6 +448,53 @@ __device__ __noinline__ int draw_dw(float wa, float wb, int m2, float u, int lan
   const uint32_t ja = __ballot_sync(FULL_MASK, lane < m2 && !dw_less(td, a));
   const uint32_t jb = __ballot_sync(FULL_MASK, lane + 32 < m2 && !dw_less(td, b));
   return min(__popc(ja) + __popc(jb), m2 - 1);
+}
+
+// Entries CTA c stored in list `w` (0: penalised, 1: raw) of the leader, clamped to its slice.
+__device__ __forceinline__ int recv_count(const uint2* recv_cnt, int c, int w, int stride) {
+  const uint2 n = recv_cnt[c];
+  return min(static_cast<int>(w == 0 ? n.x : n.y), stride);
+}
+
+// Rank of `key` among the received entries of one list (slices of `stride` entries per CTA;
+// entry size `esz_words` 32-bit words, key in words 0-1): the number of larger keys.  Keys are
+// distinct (the id is part of the key).
+__device__ __forceinline__ int count_greater(const uint32_t* recv, int esz_words, int stride, const uint2* recv_cnt,
+                                             int w, int cs, uint64_t key) {
+  int rank = 0;
+  for (int c = 0; c < cs; ++c) {
+    const uint32_t* e = recv + static_cast<size_t>(c) * stride * esz_words;
+    const int n = recv_count(recv_cnt, c, w, stride);
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const uint2 o = *reinterpret_cast<const uint2*>(e + j * esz_words);
+      rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > key;
+    }
+  }
+  return rank;
+}
+
+// Rank of `key` in a dense list of `n` entries (entry size `esz_words` 32-bit words, key in words
+// 0-1): the number of larger keys, counted in four independent partial sums (every thread of a
+// warp reads the same entry, a broadcast).
+__device__ __forceinline__ int rank_desc(const uint32_t* list, int esz_words, int n, uint64_t key) {
+  int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+  int j = 0;
+  for (; j + 4 <= n; j += 4) {
+    const uint2 o0 = *reinterpret_cast<const uint2*>(list + (j + 0) * esz_words);
+    const uint2 o1 = *reinterpret_cast<const uint2*>(list + (j + 1) * esz_words);
+    const uint2 o2 = *reinterpret_cast<const uint2*>(list + (j + 2) * esz_words);
+    const uint2 o3 = *reinterpret_cast<const uint2*>(list + (j + 3) * esz_words);
+    r0 += ((static_cast<uint64_t>(o0.y) << 32) | o0.x) > key;
+    r1 += ((static_cast<uint64_t>(o1.y) << 32) | o1.x) > key;
+    r2 += ((static_cast<uint64_t>(o2.y) << 32) | o2.x) > key;
+    r3 += ((static_cast<uint64_t>(o3.y) << 32) | o3.x) > key;
+  }
+  for (; j < n; ++j) {
+    const uint2 o = *reinterpret_cast<const uint2*>(list + j * esz_words);
+    r0 += ((static_cast<uint64_t>(o.y) << 32) | o.x) > key;
+  }
+  return (r0 + r1) + (r2 + r3);
 }
 
 // ------------------------------------------------------------------------------ the kernel
@@ -432,11 +523,30 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + L.mbar);
   const char* grow = static_cast<const char*>(P.logits) + (static_cast<long long>(row) * P.ld + lo) * ESZ;
 
-  // ---- 1. the bulk copies of this chunk go out first ---------------------------------------
-  if (wid == 0) {  // lane 0 initialises the piece barriers, lane p issues piece p
+  // row metadata, first level (independent loads; consumed once the copies are out)
+  int slot = -1;
+  unsigned long long pos = 0ull;
+  int chosen_id = -1;
+  int a_beg = 0, a_end = 0;
+  if (P.mode == MODE_SAMPLE) {
+    slot = P.row_slot[row];
+    pos = static_cast<unsigned long long>(P.row_pos[row]);
+  } else if (P.chosen != nullptr) {
+    chosen_id = P.chosen[row];
+  }
+  if (P.allowed_off != nullptr) {
+    a_beg = P.allowed_off[row];
+    a_end = P.allowed_off[row + 1];
+  }
+
+  // ---- 1. barriers and the bulk copies of this chunk ----------------------------------------
+  if (wid == 0) {
     if (lane == 0) {
       for (int p = 0; p < n_pieces; ++p) mbar_init(&mbar[p], 1);
+      mbar_init(&mbar[BAR_X0], 33);                  // the announced bytes + warp 0 (own record)
+      mbar_init(&mbar[BAR_X1], cs > 1 ? cs - 1 : 1); // one arrival per other CTA (leader only)
       fence_mbar_init();
+      mbar_arrive_expect_tx(&mbar[BAR_X0], static_cast<uint32_t>((cs - 1) * XREC_BYTES));
     }
     __syncwarp();
     for (int p = lane; p < n_pieces; p += 32) {
@@ -450,19 +560,22 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   uint32_t* hbits = reinterpret_cast<uint32_t*>(sm + L.hbits);
   uint32_t* abits = reinterpret_cast<uint32_t*>(sm + L.abits);
   uint32_t* htab = reinterpret_cast<uint32_t*>(sm + L.hash);
-  uint32_t* tc_arr = reinterpret_cast<uint32_t*>(sm + L.tc);
-  float4* ms_arr = reinterpret_cast<float4*>(sm + L.ms);
-  uint32_t* wtop = reinterpret_cast<uint32_t*>(sm + L.wtop);
+  uint32_t* hflag = reinterpret_cast<uint32_t*>(sm + L.hflag);
+  uint32_t* wmax = reinterpret_cast<uint32_t*>(sm + L.wmax);
   uint64_t* red64 = reinterpret_cast<uint64_t*>(sm + L.red);
   float4* red4 = reinterpret_cast<float4*>(sm + L.red);
   uint32_t* ctl = reinterpret_cast<uint32_t*>(sm + L.ctl);
+  uint32_t* xrec = reinterpret_cast<uint32_t*>(sm + L.xrec);
   uint4* cand_pen = reinterpret_cast<uint4*>(sm + L.cand_pen);
   uint64_t* cand_raw = reinterpret_cast<uint64_t*>(sm + L.cand_raw);
-  const uint4* recv_pen = reinterpret_cast<const uint4*>(sm + L.recv_pen);
-  const uint64_t* recv_raw = reinterpret_cast<const uint64_t*>(sm + L.recv_raw);
+  uint2* recv_cnt = reinterpret_cast<uint2*>(sm + L.recv_cnt);
+  uint4* recv_pen = reinterpret_cast<uint4*>(sm + L.recv_pen);
+  uint64_t* recv_raw = reinterpret_cast<uint64_t*>(sm + L.recv_raw);
+  uint4* sorted_pen = reinterpret_cast<uint4*>(sm + L.sorted_pen);
+  uint64_t* sorted_raw = reinterpret_cast<uint64_t*>(sm + L.sorted_raw);
 
-  // The ragged last vector (chunk bytes not a multiple of 16) is read with plain loads by its
-  // owner thread, padded with -inf.
+  // The ragged last vector (chunk bytes not a multiple of 16) is read with plain loads by the
+  // thread that owns it in every pass, padded with -inf.
   if (bytes > bytes_al && tid == (n_vec - 1) % NT) {
     const int tv = n_vec - 1;
     if constexpr (DT == 0) {
@@ -488,16 +601,15 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     abits[i] = 0u;
   }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
-  if (tid < CTL_WORDS) ctl[tid] = 0u;
-  __syncthreads();           // tables zeroed, piece barriers initialised
-  cluster_arrive_relaxed();  // this CTA is running (DSMEM access waits for every CTA, below)
+  if (tid < NT / 32) hflag[tid] = 0u;
+  if (tid < CTL_WORDS) ctl[tid] = (tid == CTL_T) ? 0xFFFFFFFFu : 0u;
+  __syncthreads();           // tables zeroed, barriers initialised
+  cluster_arrive_relaxed();  // this CTA is running (remote stores wait for every CTA, below)
 
-  // ---- row metadata (inputs only: slot keys are never written by a kernel) -------------------
-  int slot = -1;
+  // ---- row metadata, second level ------------------------------------------------------------
   bool valid = true;
   SlotDev sp{};
   if (P.mode == MODE_SAMPLE) {
-    slot = P.row_slot[row];
     valid = static_cast<unsigned>(slot) < static_cast<unsigned>(P.max_slots);
     if (valid) sp = P.slots[slot];
   }
@@ -505,249 +617,218 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   const int k_row = (P.mode == MODE_SAMPLE && valid) ? min(max(sp.k, 1), P.kmax) : 0;
   const int n_row = P.nmax;
   const int kp = max(k_row, n_row);
-  const int q = (kp + cs - 1) / cs;
   const bool penal = (P.mode == MODE_SAMPLE) && valid && (sp.flags & SLOT_PENAL) && P.hist_off != nullptr &&
                      slot < P.n_hist_slots && P.hash_cap > 0;
-  const unsigned long long pos = (P.mode == MODE_SAMPLE) ? static_cast<unsigned long long>(P.row_pos[row]) : 0ull;
-  const int chosen_id = (P.mode == MODE_LOGPROBS && P.chosen != nullptr) ? P.chosen[row] : -1;
-  int a_beg = 0, a_end = 0;
-  if (P.allowed_off != nullptr) {
-    a_beg = P.allowed_off[row];
-    a_end = P.allowed_off[row + 1];
+  int h_len = 0, h_start = 0;
+  if (penal) {
+    const int hb = P.hist_off[slot], he = P.hist_off[slot + 1];
+    h_len = min(sp.last_n, max(0, he - hb));
+    h_start = he - h_len;
   }
-  // the first two allowed ids of this thread: mark the chunk's dedup bits now (before the data)
   int aid[2];
-  bool acount[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int j = a_beg + tid + t * NT;
     aid[t] = j < a_end ? P.allowed[j] : -1;
-    acount[t] = false;
-    if (aid[t] >= lo && aid[t] < hi) {
-      const uint32_t loc = static_cast<uint32_t>(aid[t] - lo);
-      const uint32_t bit = 1u << (loc & 31);
-      acount[t] = !(atomicOr(&abits[loc >> 5], bit) & bit);
-    }
   }
 
   // The draw counter: each sampled row adds one arrival to its slot's packed word (counter << 16 |
   // arrivals) and reads the counter from the returned value; the row that completes the slot's
   // arrivals also advances the counter and clears them, so every row of the call sees the value
-  // from before the call.  Issued early, consumed just before the leader's merge.
+  // from before the call.
   const bool ctr_warp = k_row > 0 && wid == 0 && crank == 0 && sampled;
   const bool ctr_thread = ctr_warp && lane == 0;
-  int r_s = 0;
   unsigned long long ctr_old = 0ull;
   if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
+  int rs_pre[2] = {-1, -1};  // row slots of the call, fetched ahead for the arrival count
   if (ctr_warp) {
-    for (int b0 = 0; b0 < P.B; b0 += 32) {
-      const int b = b0 + lane;
-      r_s += __popc(__ballot_sync(FULL_MASK, b < P.B && P.row_slot[b] == slot));
-    }
+    rs_pre[0] = lane < P.B ? P.row_slot[lane] : -1;
+    rs_pre[1] = lane + 32 < P.B ? P.row_slot[lane + 32] : -1;
   }
 
-  // ---- history table of this chunk's id range ------------------------------------------------
-  if (penal) {
-    const int hb = P.hist_off[slot], he = P.hist_off[slot + 1];
-    const int h_len = min(sp.last_n, max(0, he - hb));
-    const int h_start = he - h_len;
-    for (int i = tid; i < h_len; i += NT) {
-      const int id = P.hist[h_start + i];
-      if (id >= lo && id < hi) {
-        const uint32_t loc = static_cast<uint32_t>(id - lo);
-        atomicOr(&hbits[loc >> 5], 1u << (loc & 31));
-        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
-      }
-    }
-  }
-
-  // ---- 1b. first pass as pieces land: running (max, sum of exp) and this thread's top two ------
-  MaxSum acc{-INFINITY, 0.0f};
-  float v1 = -INFINITY, v2 = -INFINITY;
-  int i1 = -1, i2 = -1;
+  // ---- 1b. first pass as pieces land ----------------------------------------------------------
+  float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
+  int bmx = 0;
+  int hid[HPRE];
+#pragma unroll
+  for (int j = 0; j < HPRE; ++j) hid[j] = -1;
   {
-    int waited = -1;
-    int i = 0;
+    const int n_iter = (n_vec + PIECE_VECS - 1) / PIECE_VECS;
 #pragma unroll 1
-    for (int v = tid; v < n_vec; v += NT, ++i) {
-      const int p = i / VR;
-      if (p < n_pieces && p != waited) {
-        wait_piece(mbar, p, ctl, P.err);
-        waited = p;
-      }
-      float x[EPV];
-      load_vec<DT>(data, v, x);
-      float vm = x[0];
+    for (int p = 0; p < n_iter; ++p) {
+      if (p < n_pieces) wait_bar(&mbar[p], ctl, P.err, false);
+      pass1_piece<DT>(data, p, p * PIECE_VECS + tid, n_vec, ref, mx, mx2, bmx, s0, s1);
+      if (p == 0 && penal) {  // third metadata level: this thread's first history ids
 #pragma unroll
-      for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
-      if (vm > acc.m) {
-        acc.s = (acc.m == -INFINITY) ? 0.0f : acc.s * ex2_approx((acc.m - vm) * LOG2E);
-        acc.m = vm;
-      }
-      if (acc.m != -INFINITY) {
-        const float mb = acc.m * LOG2E;
-        float t = 0.0f;
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) t += ex2_approx(fmaf(x[e], LOG2E, -mb));
-        acc.s += t;
-      }
-      if (vm > v2) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const int loc = v * EPV + e;
-          if (x[e] > v2 && loc < n_el) {
-            if (x[e] > v1) {
-              v2 = v1;
-              i2 = i1;
-              v1 = x[e];
-              i1 = loc;
-            } else {
-              v2 = x[e];
-              i2 = loc;
-            }
-          }
+        for (int j = 0; j < HPRE; ++j) {
+          const int i = tid + j * NT;
+          hid[j] = i < h_len ? P.hist[h_start + i] : -1;
         }
       }
     }
   }
-  for (int p = 0; p < n_pieces; ++p) wait_piece(mbar, p, ctl, P.err);  // all pieces visible here
-  __syncthreads();  // history table and allowed dedup bits complete
+  for (int p = 0; p < n_pieces; ++p) wait_bar(&mbar[p], ctl, P.err, false);  // all pieces visible
 
-  // this thread's top two over the ids that carry no penalty (the threshold's elements)
-  if (penal && ((i1 >= 0 && bit_at(hbits, static_cast<uint32_t>(i1))) ||
-                (i2 >= 0 && bit_at(hbits, static_cast<uint32_t>(i2)))))
-    masked_top2<DT>(data, n_vec, n_el, hbits, &v1, &i1, &v2, &i2);
-  const uint32_t o1 = (i1 >= 0) ? order_key(v1) : 0u;
-  const uint32_t o2 = (i2 >= 0) ? order_key(v2) : 0u;
-
-  // ---- 2. threshold t_c and the CTA's (max, sum) of the row and of the allowed subset ---------
-  if (kp > 0 && q <= QMAX) {
-    uint32_t key = o1;
-    for (int r = 0; r < q; ++r) {
-      const uint32_t mx = __reduce_max_sync(FULL_MASK, key);
-      if (lane == 0) wtop[wid * q + r] = mx;
-      const uint32_t bal = __ballot_sync(FULL_MASK, key == mx);
-      if (lane == __ffs(bal) - 1) key = 0u;
-    }
-  }
-  MaxSum al{-INFINITY, 0.0f};
+  // ---- history table of this chunk's id range, and the owners of its ids ----------------------
+  if (penal) {
+    auto add_hist = [&](int id) {
+      if (id >= lo && id < hi) {
+        const uint32_t loc = static_cast<uint32_t>(id - lo);
+        atomicOr(&hbits[loc >> 5], 1u << (loc & 31));
+        const uint32_t owner = (loc / EPV) % NT;
+        atomicOr(&hflag[owner >> 5], 1u << (owner & 31));
+        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
+      }
+    };
 #pragma unroll
-  for (int t = 0; t < 2; ++t)
-    if (acount[t]) online_add(al, elem_at<DT>(data, static_cast<uint32_t>(aid[t] - lo)));
-  for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) {
-    const int id = P.allowed[j];
-    if (id >= lo && id < hi) {
-      const uint32_t loc = static_cast<uint32_t>(id - lo);
-      const uint32_t bit = 1u << (loc & 31);
-      if (!(atomicOr(&abits[loc >> 5], bit) & bit)) online_add(al, elem_at<DT>(data, loc));
+    for (int j = 0; j < HPRE; ++j) add_hist(hid[j]);
+    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(P.hist[h_start + i]);
+  }
+  // allowed subset: this chunk's ids, each counted once, into (max, sum of exp)
+  MaxSum al{-INFINITY, 0.0f};
+  {
+    auto add_allowed = [&](int id) {
+      if (id >= lo && id < hi) {
+        const uint32_t loc = static_cast<uint32_t>(id - lo);
+        const uint32_t bit = 1u << (loc & 31);
+        if (!(atomicOr(&abits[loc >> 5], bit) & bit)) online_add(al, elem_at<DT>(data, loc));
+      }
+    };
+    add_allowed(aid[0]);
+    add_allowed(aid[1]);
+    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) add_allowed(P.allowed[j]);
+  }
+  __syncthreads();  // history table, owner flags complete
+
+  // ---- 2. this CTA's record: warp maxima (ids without a penalty) and (max, sum) pairs ---------
+  // The candidate test key covers every id of the thread; the threshold key must be the value of
+  // an id without a penalty, so a thread that owns a history id publishes nothing (a valid, very
+  // slightly weaker bound).
+  const uint32_t kall = tid < n_vec ? order_key(mx) : 0u;
+  const uint32_t kthr = (penal && ((hflag[tid >> 5] >> (tid & 31)) & 1u)) ? 0u : kall;
+  {
+    const uint32_t wm = __reduce_max_sync(FULL_MASK, kthr);
+    const MaxSum wrow = warp_ms_fast(MaxSum{ref, s0 + s1});
+    const MaxSum wal = warp_ms_fast(al);
+    if (lane == 0) {
+      wmax[wid] = wm;
+      red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
     }
   }
-  {
-    const MaxSum wrow = warp_ms_fast(acc);
-    const MaxSum wal = warp_ms_fast(al);
-    if (lane == 0) red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
-  }
+  // q: warp maxima published per CTA (all NW when that is no more than 4K/cs)
+  const int q = kp > 0 ? min(NW, max((kp + cs - 1) / cs, (4 * kp + cs - 1) / cs)) : 0;
   __syncthreads();
-  float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);
-  uint32_t tq = 0u;
   if (wid == 0) {
     MaxSum r1{-INFINITY, 0.0f}, r2{-INFINITY, 0.0f};
+    uint32_t w = 0u;
     if (lane < NW) {
       const float4 t = red4[lane];
       r1 = {t.x, t.y};
       r2 = {t.z, t.w};
+      w = wmax[lane];
     }
     r1 = warp_ms_fast(r1);
     r2 = warp_ms_fast(r2);
-    mine = make_float4(r1.m, r1.s, r2.m, r2.s);
-    if (kp > 0 && q <= QMAX) {
-      uint32_t vals[4];
-      const int nv = NW * q;
+    // the q largest warp maxima, in descending order, into words 0..q-1 of this CTA's record
+    // (words q..15 stay zero): rank of each lane's value by comparing it with every other lane's
+    int rank = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) vals[j] = (lane + 32 * j < nv) ? wtop[lane + 32 * j] : 0u;
-      for (int r = 0; r < q; ++r) {
-        const uint32_t lm = max(max(vals[0], vals[1]), max(vals[2], vals[3]));
-        const uint32_t mx = __reduce_max_sync(FULL_MASK, lm);
-        const uint32_t bal = __ballot_sync(FULL_MASK, lm == mx);
-        if (lane == __ffs(bal) - 1) {
-          if (vals[0] == mx) vals[0] = 0u;
-          else if (vals[1] == mx) vals[1] = 0u;
-          else if (vals[2] == mx) vals[2] = 0u;
-          else vals[3] = 0u;
+    for (int m = 0; m < NW; ++m) {
+      const uint32_t o = __shfl_sync(FULL_MASK, w, m);
+      rank += (o > w) || (o == w && m < lane);
+    }
+    uint32_t* own = xrec + crank * XREC_WORDS;
+    if (lane < 16) own[lane] = 0u;
+    if (lane == 16) own[16] = __float_as_uint(r1.m);
+    if (lane == 17) own[17] = __float_as_uint(r1.s);
+    if (lane == 18) own[18] = __float_as_uint(r2.m);
+    if (lane == 19) own[19] = __float_as_uint(r2.s);
+    __syncwarp();
+    if (lane < NW && rank < q) own[rank] = w;
+    mbar_arrive(&mbar[BAR_X0]);  // each lane releases its own word of the record
+    __syncwarp();
+  }
+  cluster_wait();  // every CTA of the cluster is running: remote stores are safe from here on
+  if (wid == 0 && lane < cs && static_cast<uint32_t>(lane) != crank) {
+    const uint4* own = reinterpret_cast<const uint4*>(xrec + crank * XREC_WORDS);
+    const uint32_t dst = dsmem_addr(smem_u32(xrec + crank * XREC_WORDS), static_cast<uint32_t>(lane));
+    const uint32_t bar = dsmem_addr(smem_u32(&mbar[BAR_X0]), static_cast<uint32_t>(lane));
+#pragma unroll
+    for (int i = 0; i < XREC_WORDS / 4; ++i) {
+      const uint4 v = own[i];
+      st_async_v4(dst + 16u * i, v.x, v.y, v.z, v.w, bar);
+    }
+  }
+  wait_bar(&mbar[BAR_X0], ctl, P.err, true);  // every CTA's record is here
+
+  // ---- the row threshold T and the log-normalisers -------------------------------------------
+  // T = the kp-th largest of the cs*q published keys (zeros included, so T = 0 when fewer than
+  // kp real keys exist): the smallest published key with fewer than kp keys above it.  A forced
+  // split can publish fewer than kp keys in all; then there is no bound (T = 0).  Unpublished
+  // record words are zero and never count as above.  Four lanes count for each published key; the
+  // last warp reduces the (max, sum) pairs meanwhile.
+  if (kp > 0) {
+    constexpr int TL = 4;  // lanes per published key; lane `sub` counts records sub, sub+4, ...
+    const int U = cs * q, nq4 = (q + 3) >> 2, sub = tid & (TL - 1);
+    for (int base = 0; base < U; base += NT / TL) {
+      const int i = base + tid / TL;
+      if (i < U) {  // whole groups of TL lanes take this branch together
+        const int c = i / q;
+        const uint32_t u = xrec[c * XREC_WORDS + (i - c * q)];
+        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll 1
+        for (int j4 = 0; j4 < nq4; ++j4) {
+#pragma unroll
+          for (int k = 0; k < MAX_CS / TL; ++k) {
+            const int c2 = sub + k * TL;
+            if (c2 < cs) {
+              const uint4 v = reinterpret_cast<const uint4*>(xrec + c2 * XREC_WORDS)[j4];
+              a0 += v.x > u;
+              a1 += v.y > u;
+              a2 += v.z > u;
+              a3 += v.w > u;
+            }
+          }
         }
-        tq = mx;
+        const unsigned act = __activemask();
+        int above = (a0 + a1) + (a2 + a3);
+        above += __shfl_xor_sync(act, above, 1);
+        above += __shfl_xor_sync(act, above, 2);
+        const uint32_t cand = (sub == 0 && above < kp) ? u : 0xFFFFFFFFu;
+        const uint32_t wmin = __reduce_min_sync(act, cand);
+        if ((tid & 31) == 0) atomicMin(&ctl[CTL_T], wmin);
       }
     }
   }
-
-  // ---- exchange through DSMEM (cluster barrier B0) ---------------------------------------------
-  cluster_wait();
-  if (wid == 0 && lane < cs) {
-    const uint32_t r = static_cast<uint32_t>(lane);
-    dsmem_st_u32(dsmem_addr(smem_u32(tc_arr + crank), r), tq);
-    dsmem_st_v4(dsmem_addr(smem_u32(ms_arr + crank), r), __float_as_uint(mine.x), __float_as_uint(mine.y),
-                __float_as_uint(mine.z), __float_as_uint(mine.w));
-  }
-  cluster_arrive();
-  cluster_wait();
-
-  // every warp reduces the cluster's contributions itself (lane c holds CTA c's)
-  uint32_t T;
-  float lse, lse_a;
-  {
+  if (wid == NW - 1) {
     const bool in = lane < cs;
-    const float4 t = in ? ms_arr[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-    T = __reduce_min_sync(FULL_MASK, in ? tc_arr[lane] : 0xFFFFFFFFu);
-    const MaxSum g = warp_ms_fast(MaxSum{t.x, t.y});
-    const MaxSum ga = warp_ms_fast(MaxSum{t.z, t.w});
-    lse = (g.m == -INFINITY || !(g.s > 0.0f)) ? -INFINITY : g.m + logf(g.s);
-    lse_a = (ga.m == -INFINITY || !(ga.s > 0.0f)) ? -INFINITY : ga.m + logf(ga.s);
+    MaxSum g{-INFINITY, 0.0f}, ga{-INFINITY, 0.0f};
+    if (in) {
+      const float4 t = reinterpret_cast<const float4*>(xrec + lane * XREC_WORDS)[4];
+      g = {t.x, t.y};
+      ga = {t.z, t.w};
+    }
+    g = warp_ms_fast(g);
+    ga = warp_ms_fast(ga);
+    if (lane == 0) {
+      ctl[CTL_LSE] = __float_as_uint((g.m == -INFINITY || !(g.s > 0.0f)) ? -INFINITY : g.m + logf(g.s));
+      ctl[CTL_LSE_A] = __float_as_uint((ga.m == -INFINITY || !(ga.s > 0.0f)) ? -INFINITY : ga.m + logf(ga.s));
+    }
   }
-  // state of the tail, carried across the wait for the previous kernel (leader, warp 0)
-  int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0, n_recv_p = 0;
-  float Ca = 0.0f, Cb = 0.0f, wa = 0.0f, wb = 0.0f;  // tempered weights and their fp32 prefix sums
-  uint4 ea = make_uint4(0, 0, 0, 0), eb = make_uint4(0, 0, 0, 0);
-  float va = 0.0f, vb = 0.0f;
+  __syncthreads();
+  const uint32_t T = cs * q >= kp ? ctl[CTL_T] : 0u;  // fewer than kp published keys: no bound
+  const float lse = __uint_as_float(ctl[CTL_LSE]), lse_a = __uint_as_float(ctl[CTL_LSE_A]);
 
-  // ---- 3. candidates of this chunk: every element at or above the row threshold T ------------
+  // ---- 3. candidates of this chunk: every element at or above T --------------------------------
   if (kp > 0) {
-    if (q > QMAX) T = 0u;  // no usable bound: every element is a candidate
-    auto put = [&](uint64_t key, float raw, bool to_raw, bool to_pen) {
-      if (to_raw && n_row > 0) {
-        const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
-        if (i < LOCAL_CAP) cand_raw[i] = key;
-      }
-      if (to_pen && k_row > 0) {
-        const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
-        if (i < LOCAL_CAP)
-          cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
-                                   __float_as_uint(raw), 0u);
-      }
-    };
-    // a thread whose second best reaches T may hold more: it rescans its own elements
-    const bool full = (T == 0u && tid < n_vec) || (o2 != 0u && o2 >= T);
-    if (full) rescan_thread<DT>(data, n_vec, n_el, lo, T, penal, hbits, ctl, cand_pen, cand_raw, n_row > 0, k_row > 0);
-    {  // the common case: at most this thread's best reaches T (one warp-wide append per list)
-      const bool one = !full && o1 != 0u && o1 >= T;
-      const uint32_t bal = __ballot_sync(FULL_MASK, one);
-      if (bal != 0u) {
-        const int leader = __ffs(bal) - 1;
-        const uint32_t before = __popc(bal & ((1u << lane) - 1u));
-        uint32_t base_r = 0, base_p = 0;
-        if (lane == leader) {
-          if (n_row > 0) base_r = atomicAdd(&ctl[CTL_CAND_RAW], static_cast<uint32_t>(__popc(bal)));
-          if (k_row > 0) base_p = atomicAdd(&ctl[CTL_CAND_PEN], static_cast<uint32_t>(__popc(bal)));
-        }
-        base_r = __shfl_sync(FULL_MASK, base_r, leader) + before;
-        base_p = __shfl_sync(FULL_MASK, base_p, leader) + before;
-        if (one) {
-          const uint64_t key = sel_key(o1, static_cast<uint32_t>(lo + i1));
-          if (n_row > 0 && base_r < LOCAL_CAP) cand_raw[base_r] = key;
-          if (k_row > 0 && base_p < LOCAL_CAP)
-            cand_pen[base_p] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
-                                          __float_as_uint(v1), 0u);
-        }
-      }
+    if (kall != 0u && kall >= T) {
+      // only the batch holding the max, unless another batch also reaches T
+      constexpr int RB = BATCH_VECS<DT>;
+      const bool one = order_key(mx2) < T;
+      const int v_first = one ? (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid : tid;
+      const int v_last = one ? v_first + (RB - 1) * NT : n_vec;
+      rescan_candidates<DT>(data, v_first, v_last, n_vec, n_el, lo, T, penal, hbits, ctl, cand_pen, cand_raw,
+                            n_row > 0, k_row > 0);
     }
     if (penal) {  // penalised ids: raw value for the raw list, penalised value for the other
       for (int i = tid; i < P.hash_cap; i += NT) {
@@ -758,10 +839,18 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
         const float raw = elem_at<DT>(data, loc);
         const uint32_t id = static_cast<uint32_t>(lo) + loc;
         const uint32_t o = order_key(raw);
-        if (o != 0u && o >= T) put(sel_key(o, id), raw, true, false);
+        if (o != 0u && o >= T && n_row > 0) {
+          const uint32_t s = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
+          if (s < LOCAL_CAP) cand_raw[s] = sel_key(o, id);
+        }
         const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
         const uint32_t op = order_key(pv);
-        if (op != 0u && op >= T) put(sel_key(op, id), raw, false, true);
+        if (op != 0u && op >= T && k_row > 0) {
+          const uint32_t s = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+          const uint64_t key = sel_key(op, id);
+          if (s < LOCAL_CAP)
+            cand_pen[s] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
+        }
       }
     }
     __syncthreads();
@@ -776,272 +865,178 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     if (n_row > 0 && nr > LOCAL_CAP)
       nr = exact_rounds<DT>(data, n_vec, n_el, lo, 1, n_row, penal, hbits, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
                             red64, cand_pen, cand_raw);
+    if (k_row == 0) np = 0;
+    if (n_row == 0) nr = 0;
 
-    // keep this chunk's best k_row / n_row and reserve their slice of the leader's lists
-    const int sent_pen = min(np, k_row), sent_raw = min(nr, n_row);
-    if (tid == 0) {
-      const uint32_t ctl_leader = dsmem_addr(smem_u32(ctl), 0);
-      ctl[CTL_BASE_P] = sent_pen > 0 ? dsmem_atomic_add(ctl_leader + 4u * CTL_RECV_NP, sent_pen) : 0u;
-      ctl[CTL_BASE_R] = sent_raw > 0 ? dsmem_atomic_add(ctl_leader + 4u * CTL_RECV_NR, sent_raw) : 0u;
-    }
-    int out_p = -1, out_r = -1;
-    uint4 ent_p = make_uint4(0, 0, 0, 0);
-    uint64_t ent_r = 0ull;
-    if (tid < np && k_row > 0) {
-      ent_p = cand_pen[tid];
-      out_p = tid;
-      if (np > k_row) {
-        const uint64_t ki = (static_cast<uint64_t>(ent_p.y) << 32) | ent_p.x;
-        const uint2* keys = reinterpret_cast<const uint2*>(cand_pen);
-        int rank = 0;
+    // keep this chunk's best k_row / n_row and store them into this CTA's slice of the leader's
+    // lists (threads 0..255: penalised list, 256..511: raw list)
+    const int sent_p = min(np, k_row), sent_r = min(nr, n_row);
+    const uint32_t leader_bar = dsmem_addr(smem_u32(&mbar[BAR_X1]), 0);
+    const int half = tid & (NT / 2 - 1);
+    if (tid < NT / 2) {
+      for (int i = half; i < np; i += NT / 2) {
+        const uint4 ent = cand_pen[i];
+        int out = i;
+        if (np > k_row) {
+          const uint64_t ki = (static_cast<uint64_t>(ent.y) << 32) | ent.x;
+          const uint2* keys = reinterpret_cast<const uint2*>(cand_pen);
+          int rank = 0;
 #pragma unroll 4
-        for (int j = 0; j < np; ++j) {
-          const uint2 o = keys[2 * j];
-          rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
+          for (int j = 0; j < np; ++j) {
+            const uint2 o = keys[2 * j];
+            rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
+          }
+          out = rank < k_row ? rank : -1;
         }
-        out_p = rank < k_row ? rank : -1;
+        if (out >= 0) {
+          uint4* slot_p = recv_pen + crank * P.kmax + out;
+          if (crank == 0) *slot_p = make_uint4(ent.x, ent.y, ent.z, 0u);
+          else st_async_v4(dsmem_addr(smem_u32(slot_p), 0), ent.x, ent.y, ent.z, 0u, leader_bar);
+        }
+      }
+    } else {
+      for (int i = half; i < nr; i += NT / 2) {
+        const uint64_t ki = cand_raw[i];
+        int out = i;
+        if (nr > n_row) {
+          int rank = 0;
+#pragma unroll 4
+          for (int j = 0; j < nr; ++j) rank += cand_raw[j] > ki;
+          out = rank < n_row ? rank : -1;
+        }
+        if (out >= 0) {
+          uint64_t* slot_r = recv_raw + crank * P.nmax + out;
+          if (crank == 0) *slot_r = ki;
+          else st_async_v2(dsmem_addr(smem_u32(slot_r), 0), static_cast<uint32_t>(ki), static_cast<uint32_t>(ki >> 32), leader_bar);
+        }
       }
     }
-    if (tid < nr && n_row > 0) {
-      ent_r = cand_raw[tid];
-      out_r = tid;
-      if (nr > n_row) {
-        int rank = 0;
-#pragma unroll 4
-        for (int j = 0; j < nr; ++j) rank += cand_raw[j] > ent_r;
-        out_r = rank < n_row ? rank : -1;
+    if (tid == 0) {
+      if (crank == 0) {
+        recv_cnt[0] = make_uint2(static_cast<uint32_t>(sent_p), static_cast<uint32_t>(sent_r));
+      } else {
+        st_async_v2(dsmem_addr(smem_u32(recv_cnt + crank), 0), static_cast<uint32_t>(sent_p),
+                    static_cast<uint32_t>(sent_r), leader_bar);
+        mbar_arrive_expect_tx_remote(leader_bar, static_cast<uint32_t>(8 + 16 * sent_p + 8 * sent_r));
+      }
+    }
+  }
+
+  // state of the tail (leader, warp 0)
+  int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0;
+  float Ca = 0.0f, Cb = 0.0f, wa = 0.0f, wb = 0.0f;  // tempered weights and their fp32 prefix sums
+  uint4 ea = make_uint4(0, 0, 0, 0), eb = make_uint4(0, 0, 0, 0);
+  float va = 0.0f, vb = 0.0f;
+
+  // ---- 4. the leader ranks the received keys exactly -------------------------------------------
+  if (kp > 0 && crank == 0) {
+    if (cs > 1) wait_bar(&mbar[BAR_X1], ctl, P.err, true);
+    __syncthreads();  // every slice (the leader's own included) is in place
+    // slice offsets (every copying warp scans the counts itself), then warp c copies slice c into
+    // the dense lists (the candidate buffers, free by now)
+    if (wid < cs) {
+      const uint2 n = lane < cs ? recv_cnt[lane] : make_uint2(0u, 0u);
+      const int pc = min(static_cast<int>(n.x), P.kmax), rc = min(static_cast<int>(n.y), P.nmax);
+      int ip = pc, ir = rc;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int yp = __shfl_up_sync(FULL_MASK, ip, off), yr = __shfl_up_sync(FULL_MASK, ir, off);
+        if (lane >= off) {
+          ip += yp;
+          ir += yr;
+        }
+      }
+      const int tp = __shfl_sync(FULL_MASK, ip, 31), tr = __shfl_sync(FULL_MASK, ir, 31);
+      const int my_p = __shfl_sync(FULL_MASK, pc, wid), my_r = __shfl_sync(FULL_MASK, rc, wid);
+      const int off_p = __shfl_sync(FULL_MASK, ip, wid) - my_p, off_r = __shfl_sync(FULL_MASK, ir, wid) - my_r;
+      if (wid == 0 && lane == 0) {
+        ctl[CTL_TOT_P] = static_cast<uint32_t>(tp);
+        ctl[CTL_TOT_R] = static_cast<uint32_t>(tr);
+      }
+      if (tp <= LOCAL_CAP)
+        for (int j = lane; j < my_p; j += 32) cand_pen[off_p + j] = recv_pen[wid * P.kmax + j];
+      for (int j = lane; j < my_r; j += 32) cand_raw[off_r + j] = recv_raw[wid * P.nmax + j];
+    }
+    __syncthreads();
+    const int tot_p = static_cast<int>(ctl[CTL_TOT_P]), tot_r = static_cast<int>(ctl[CTL_TOT_R]);
+    // exact ranks by counting larger keys (threads 0..255: penalised list, 256..511: raw list)
+    const int half = tid & (NT / 2 - 1);
+    if (tid < NT / 2) {
+      for (int f = half; f < tot_p; f += NT / 2) {
+        uint4 ent;
+        int rank;
+        if (tot_p <= LOCAL_CAP) {
+          ent = cand_pen[f];
+          rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_pen), 4, tot_p,
+                           (static_cast<uint64_t>(ent.y) << 32) | ent.x);
+        } else {  // more than the dense buffer holds (heavy ties): walk the slices
+          int c = 0, j = f;
+          for (int n = recv_count(recv_cnt, 0, 0, P.kmax); j >= n && c + 1 < cs; n = recv_count(recv_cnt, c, 0, P.kmax)) {
+            j -= n;
+            ++c;
+          }
+          ent = recv_pen[c * P.kmax + j];
+          rank = count_greater(reinterpret_cast<const uint32_t*>(recv_pen), 4, P.kmax, recv_cnt, 0, cs,
+                               (static_cast<uint64_t>(ent.y) << 32) | ent.x);
+        }
+        if (rank < k_row) sorted_pen[rank] = ent;
+      }
+    } else {
+      for (int f = half; f < tot_r; f += NT / 2) {
+        const uint64_t key = cand_raw[f];
+        const int rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_raw), 2, tot_r, key);
+        if (rank < n_row) sorted_raw[rank] = key;
       }
     }
     __syncthreads();
-    if (out_p >= 0)
-      dsmem_st_v4(dsmem_addr(smem_u32(sm + L.recv_pen) + (ctl[CTL_BASE_P] + out_p) * 16u, 0), ent_p.x, ent_p.y,
-                  ent_p.z, 0u);
-    if (out_r >= 0)
-      dsmem_st_v2(dsmem_addr(smem_u32(sm + L.recv_raw) + (ctl[CTL_BASE_R] + out_r) * 8u, 0),
-                  static_cast<uint32_t>(ent_r), static_cast<uint32_t>(ent_r >> 32));
-    cluster_arrive();
-    cluster_wait();  // B1: the leader holds every CTA's best candidates in two dense lists
+    k_eff = min(k_row, tot_p);
+    n_eff = min(n_row, tot_r);
 
-    // ---- 4. the leader ranks the received keys exactly -----------------------------------------
-    if (crank == 0) {
-      const int tot_p = static_cast<int>(ctl[CTL_RECV_NP]);
-      const int tot_r = static_cast<int>(ctl[CTL_RECV_NR]);
-      uint4* sorted_pen = cand_pen;   // the leader's own candidates were sent before B1
-      uint64_t* sorted_raw = reinterpret_cast<uint64_t*>(cand_pen + KMAX);
-      const uint2* pkeys = reinterpret_cast<const uint2*>(recv_pen);
-      if (tot_p <= 256 && tot_r <= 256) {
-        // common case: warp 0 sorts the penalised list, warp 1 the raw list, each in registers;
-        // no block barrier, each warp then reads its own sorted list back
-        if (wid < 2) {
-          const int n = wid == 0 ? tot_p : tot_r;
-          const int need = wid == 0 ? k_row : n_row;
-          if (n <= 128) {
-            uint64_t kk[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int i = lane * 4 + r;
-              kk[r] = i < n ? (wid == 0 ? ((static_cast<uint64_t>(pkeys[2 * i].y) << 32) | pkeys[2 * i].x) : recv_raw[i]) : 0ull;
-            }
-            warp_sort_desc<4>(kk, lane);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int i = lane * 4 + r;
-              if (i < need && i < n) {
-                if (wid == 0) sorted_pen[i] = make_uint4(static_cast<uint32_t>(kk[r]), static_cast<uint32_t>(kk[r] >> 32), 0u, 0u);
-                else sorted_raw[i] = kk[r];
-              }
-            }
+    // the tail's first half on <= 64 survivors (one warp): min_p and top_p cuts and the
+    // tempered cumulative weights; nothing here depends on the draw counter
+    if (P.mode == MODE_SAMPLE && wid == 0 && valid && k_eff > 0) {
+      ea = (lane < k_eff) ? sorted_pen[lane] : make_uint4(0, 0, 0, 0);
+      eb = (lane + 32 < k_eff) ? sorted_pen[lane + 32] : make_uint4(0, 0, 0, 0);
+      va = key_value(ea.y);
+      vb = key_value(eb.y);
+      m1 = m2 = 1;
+      if (sampled) {
+        const float v0 = __shfl_sync(FULL_MASK, va, 0);
+        m1 = k_eff;
+        if (sp.min_p > 0.0f) {  // min_p in logit space, float32
+          const float thr = __fadd_rn(v0, sp.logminp);
+          const uint32_t ba = __ballot_sync(FULL_MASK, lane < k_eff && va >= thr);
+          const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && vb >= thr);
+          m1 = max(1, __popc(ba) + __popc(bb));
+        }
+        // temperature-1 mass (top_p) and tempered weights (draw) over the min_p survivors.
+        // Prefix sums in fp32 decide unless a decision lies within 1e-5 of its boundary (the fp32
+        // scan is good to ~4e-7 relative); then double-word sums (TwoSum) decide.
+        const bool ina = lane < m1, inb = lane + 32 < m1;
+        const float da = __fsub_rn(va, v0), db = __fsub_rn(vb, v0);
+        const float Tm = sp.temperature;
+        const float qa = ina ? expf(da) : 0.0f, qb = inb ? expf(db) : 0.0f;
+        wa = ina ? expf(__fdiv_rn(da, Tm)) : 0.0f;
+        wb = inb ? expf(__fdiv_rn(db, Tm)) : 0.0f;
+        const float ca = warp_scan_f(qa, lane);
+        Ca = warp_scan_f(wa, lane);
+        const float cb = warp_scan_f(qb, lane) + __shfl_sync(FULL_MASK, ca, 31);
+        Cb = warp_scan_f(wb, lane) + __shfl_sync(FULL_MASK, Ca, 31);
+        m2 = m1;
+        if (!(sp.top_p >= 1.0f)) {
+          if (!(sp.top_p > 0.0f)) {
+            m2 = 1;
           } else {
-            uint64_t kk[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const int i = lane * 8 + r;
-              kk[r] = i < n ? (wid == 0 ? ((static_cast<uint64_t>(pkeys[2 * i].y) << 32) | pkeys[2 * i].x) : recv_raw[i]) : 0ull;
-            }
-            warp_sort_desc<8>(kk, lane);
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const int i = lane * 8 + r;
-              if (i < need && i < n) {
-                if (wid == 0) sorted_pen[i] = make_uint4(static_cast<uint32_t>(kk[r]), static_cast<uint32_t>(kk[r] >> 32), 0u, 0u);
-                else sorted_raw[i] = kk[r];
-              }
-            }
-          }
-          __syncwarp();
-        }
-      } else {
-      uint32_t* hist = reinterpret_cast<uint32_t*>(cand_raw);            // 2 x 256 bins
-      uint16_t* surv = reinterpret_cast<uint16_t*>(hist + 512);          // survivors of both lists
-      // A long list is first cut by a threshold on the high key word: a 256-bin histogram of
-      // (hi - T) over the list's range, scanned from the top, keeps the bin holding the
-      // need-th largest value and everything above it (all of the top `need`, plus that bin).
-      const bool cut_p = tot_p > max(2 * k_row, 32), cut_r = tot_r > max(2 * n_row, 32);
-      const uint32_t Thi = T;
-      if (cut_p || cut_r) {
-        if (tid < 512 / 2) reinterpret_cast<uint2*>(hist)[tid] = make_uint2(0u, 0u);
-        uint32_t mp = 0u, mr = 0u;
-        for (int f = tid; f < tot_p; f += NT) mp = max(mp, pkeys[2 * f].y);
-        for (int f = tid; f < tot_r; f += NT) mr = max(mr, static_cast<uint32_t>(recv_raw[f] >> 32));
-        mp = __reduce_max_sync(FULL_MASK, mp);
-        mr = __reduce_max_sync(FULL_MASK, mr);
-        if (lane == 0) {
-          atomicMax(&ctl[CTL_MAXP], mp);
-          atomicMax(&ctl[CTL_MAXR], mr);
-        }
-        __syncthreads();
-        const uint32_t span_p = ctl[CTL_MAXP] - Thi, span_r = ctl[CTL_MAXR] - Thi;
-        const int sh_p = max(0, 32 - __clz(static_cast<int>(span_p | 1u)) - 8);
-        const int sh_r = max(0, 32 - __clz(static_cast<int>(span_r | 1u)) - 8);
-        if (cut_p)
-          for (int f = tid; f < tot_p; f += NT) atomicAdd(&hist[(pkeys[2 * f].y - Thi) >> sh_p], 1u);
-        if (cut_r)
-          for (int f = tid; f < tot_r; f += NT) atomicAdd(&hist[256 + ((static_cast<uint32_t>(recv_raw[f] >> 32) - Thi) >> sh_r)], 1u);
-        __syncthreads();
-        if (wid < 2 && (wid == 0 ? cut_p : cut_r)) {  // warp 0: penalised list, warp 1: raw list
-          const uint32_t* hh = hist + 256 * wid;
-          const int need = wid == 0 ? k_row : n_row;
-          uint32_t c[8], tsum = 0u;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {  // lane l holds bins 255-8l .. 248-8l (from the top)
-            c[j] = hh[255 - (8 * lane + j)];
-            tsum += c[j];
-          }
-          uint32_t incl = tsum;  // inclusive prefix over lanes = count in bins above this lane's
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t y = __shfl_up_sync(FULL_MASK, incl, off);
-            if (lane >= off) incl += y;
-          }
-          uint32_t run = incl - tsum;
-          int bstar = -1;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            run += c[j];
-            if (bstar < 0 && run >= static_cast<uint32_t>(need)) bstar = 255 - (8 * lane + j);
-          }
-          const uint32_t has = __ballot_sync(FULL_MASK, bstar >= 0);
-          const int first = __ffs(has) - 1;  // lowest lane = highest bins
-          const int b = __shfl_sync(FULL_MASK, bstar, first < 0 ? 0 : first);
-          if (lane == 0) ctl[wid == 0 ? CTL_TP : CTL_TR] = first < 0 ? Thi : Thi + (static_cast<uint32_t>(b) << (wid == 0 ? sh_p : sh_r));
-        }
-        __syncthreads();
-      }
-      // survivors (indices into the received lists), then exact ranks among them; a cut that keeps
-      // more than the survivor buffer holds (ties) is dropped and the whole list is ranked
-      constexpr uint32_t SURV = 512;
-      const uint32_t tp = cut_p ? ctl[CTL_TP] : 0u, tr = cut_r ? ctl[CTL_TR] : 0u;
-      int n_sp = tot_p, n_sr = tot_r;
-      bool use_sp = false, use_sr = false;
-      if (cut_p || cut_r) {
-        if (tid == 0) {
-          ctl[CTL_BASE_P] = 0u;
-          ctl[CTL_BASE_R] = 0u;
-        }
-        __syncthreads();
-        for (int f0 = 0; f0 < max(tot_p, tot_r); f0 += NT) {
-          const int f = f0 + tid;
-          const bool kp_ = cut_p && f < tot_p && pkeys[2 * f].y >= tp;
-          const bool kr_ = cut_r && f < tot_r && static_cast<uint32_t>(recv_raw[f] >> 32) >= tr;
-          const uint32_t bp = __ballot_sync(FULL_MASK, kp_), br = __ballot_sync(FULL_MASK, kr_);
-          uint32_t basep = 0, baser = 0;
-          if (lane == 0) {
-            if (bp) basep = atomicAdd(&ctl[CTL_BASE_P], static_cast<uint32_t>(__popc(bp)));
-            if (br) baser = atomicAdd(&ctl[CTL_BASE_R], static_cast<uint32_t>(__popc(br)));
-          }
-          basep = __shfl_sync(FULL_MASK, basep, 0) + __popc(bp & ((1u << lane) - 1u));
-          baser = __shfl_sync(FULL_MASK, baser, 0) + __popc(br & ((1u << lane) - 1u));
-          if (kp_ && basep < SURV) surv[basep] = static_cast<uint16_t>(f);
-          if (kr_ && baser < SURV) surv[SURV + baser] = static_cast<uint16_t>(f);
-        }
-        __syncthreads();
-        use_sp = cut_p && ctl[CTL_BASE_P] <= SURV;
-        use_sr = cut_r && ctl[CTL_BASE_R] <= SURV;
-        if (use_sp) n_sp = static_cast<int>(ctl[CTL_BASE_P]);
-        if (use_sr) n_sr = static_cast<int>(ctl[CTL_BASE_R]);
-      }
-      const int tot = n_sp + n_sr;
-      int G = 1;  // threads per ranked key (a power of two)
-      while (G < 32 && 2 * G * tot <= NT) G *= 2;
-      for (int base = 0; base < tot; base += NT / G) {
-        const int g = base + tid / G, sub = tid & (G - 1);
-        int rank = 0;
-        uint64_t ki = 0ull;
-        int src = -1;
-        if (g < n_sp) {
-          src = use_sp ? surv[g] : g;
-          const uint2 k2 = pkeys[2 * src];
-          ki = (static_cast<uint64_t>(k2.y) << 32) | k2.x;
-          for (int j = sub; j < n_sp; j += G) {
-            const uint2 o = pkeys[2 * (use_sp ? surv[j] : j)];
-            rank += ((static_cast<uint64_t>(o.y) << 32) | o.x) > ki;
-          }
-        } else if (g < tot) {
-          src = use_sr ? surv[SURV + (g - n_sp)] : g - n_sp;
-          ki = recv_raw[src];
-          for (int j = sub; j < n_sr; j += G) rank += recv_raw[use_sr ? surv[SURV + j] : j] > ki;
-        }
-        for (int off = G >> 1; off > 0; off >>= 1) rank += __shfl_xor_sync(FULL_MASK, rank, off);
-        if (sub == 0) {
-          if (g < n_sp) {
-            if (rank < k_row) sorted_pen[rank] = recv_pen[src];
-          } else if (g < tot && rank < n_row) {
-            sorted_raw[rank] = ki;
-          }
-        }
-      }
-      __syncthreads();
-      }
-      n_recv_p = tot_p;
-      k_eff = min(k_row, tot_p);
-      n_eff = min(n_row, tot_r);
-
-      // the tail's first half on <= 64 survivors (one warp): min_p and top_p cuts and the
-      // tempered cumulative weights; nothing here depends on the draw counter
-      if (P.mode == MODE_SAMPLE && wid == 0 && valid && k_eff > 0) {
-        ea = (lane < k_eff) ? sorted_pen[lane] : make_uint4(0, 0, 0, 0);
-        eb = (lane + 32 < k_eff) ? sorted_pen[lane + 32] : make_uint4(0, 0, 0, 0);
-        va = key_value(ea.y);
-        vb = key_value(eb.y);
-        m1 = m2 = 1;
-        if (sampled) {
-          const float v0 = __shfl_sync(FULL_MASK, va, 0);
-          m1 = k_eff;
-          if (sp.min_p > 0.0f) {  // min_p in logit space, float32
-            const float thr = __fadd_rn(v0, sp.logminp);
-            const uint32_t ba = __ballot_sync(FULL_MASK, lane < k_eff && va >= thr);
-            const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && vb >= thr);
-            m1 = max(1, __popc(ba) + __popc(bb));
-          }
-          // temperature-1 mass (top_p) and tempered weights (draw) over the min_p survivors.
-          // Prefix sums in fp32 decide unless a decision lies within 1e-5 of its boundary (the fp32
-          // scan is good to ~4e-7 relative); then double-word sums (TwoSum) decide.
-          const bool ina = lane < m1, inb = lane + 32 < m1;
-          const float da = __fsub_rn(va, v0), db = __fsub_rn(vb, v0);
-          const float Tm = sp.temperature;
-          const float qa = ina ? expf(da) : 0.0f, qb = inb ? expf(db) : 0.0f;
-          wa = ina ? expf(__fdiv_rn(da, Tm)) : 0.0f;
-          wb = inb ? expf(__fdiv_rn(db, Tm)) : 0.0f;
-          const float ca = warp_scan_f(qa, lane);
-          Ca = warp_scan_f(wa, lane);
-          const float cb = warp_scan_f(qb, lane) + __shfl_sync(FULL_MASK, ca, 31);
-          Cb = warp_scan_f(wb, lane) + __shfl_sync(FULL_MASK, Ca, 31);
-          m2 = m1;
-          if (!(sp.top_p >= 1.0f)) {
-            if (!(sp.top_p > 0.0f)) {
-              m2 = 1;
+            const float tot_q = __shfl_sync(FULL_MASK, cb, 31);
+            const float target = sp.top_p * tot_q, margin = 1e-5f * tot_q;
+            const bool near = __any_sync(FULL_MASK, (ina && fabsf(ca - target) <= margin) ||
+                                                        (inb && fabsf(cb - target) <= margin));
+            if (!near) {
+              const uint32_t la = __ballot_sync(FULL_MASK, ina && ca < target);
+              const uint32_t lb = __ballot_sync(FULL_MASK, inb && cb < target);
+              m2 = min(m1, __popc(la) + __popc(lb) + 1);
             } else {
-              const float tot = __shfl_sync(FULL_MASK, cb, 31);
-              const float target = sp.top_p * tot, margin = 1e-5f * tot;
-              const bool near = __any_sync(FULL_MASK, (ina && fabsf(ca - target) <= margin) ||
-                                                          (inb && fabsf(cb - target) <= margin));
-              if (!near) {
-                const uint32_t la = __ballot_sync(FULL_MASK, ina && ca < target);
-                const uint32_t lb = __ballot_sync(FULL_MASK, inb && cb < target);
-                m2 = min(m1, __popc(la) + __popc(lb) + 1);
-              } else {
-                m2 = top_p_dw(qa, qb, ina, inb, sp.top_p, m1, lane);
-              }
+              m2 = top_p_dw(qa, qb, ina, inb, sp.top_p, m1, lane);
             }
           }
         }
@@ -1079,9 +1074,8 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   }
 
   if (kp > 0 && crank == 0) {
-    const uint64_t* sorted_raw = reinterpret_cast<const uint64_t*>(cand_pen + KMAX);
     // top-N raw alternatives and their log-probabilities
-    if (n_row > 0 && P.top_ids != nullptr && wid == 1) {  // warp 1 wrote the sorted raw list
+    if (n_row > 0 && P.top_ids != nullptr && wid == 1) {
       for (int i = lane; i < n_row; i += 32) {
         const long long o = static_cast<long long>(row) * P.top_n + i;
         if (i < n_eff) {
@@ -1106,6 +1100,11 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
         int j = 0;
         if (sampled) {
           uint32_t x0 = 0u;
+          int r_s = __popc(__ballot_sync(FULL_MASK, rs_pre[0] == slot)) + __popc(__ballot_sync(FULL_MASK, rs_pre[1] == slot));
+          for (int b0 = 64; b0 < P.B; b0 += 32) {
+            const int b = b0 + lane;
+            r_s += __popc(__ballot_sync(FULL_MASK, b < P.B && P.row_slot[b] == slot));
+          }
           if (ctr_thread) {
             if ((ctr_old & 0xFFFFull) + 1ull == static_cast<unsigned long long>(r_s))
               atomicAdd(&P.ctr[slot], (1ull << 16) - static_cast<unsigned long long>(r_s));
@@ -1129,19 +1128,7 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
         const uint32_t id_a = key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x);
         const uint32_t id_b = key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x);
         out = static_cast<int>(__shfl_sync(FULL_MASK, j < 32 ? id_a : id_b, j & 31));
-        if (P.chosen_lp != nullptr) {  // the raw logit travelled with the received entry
-          const uint32_t kx = __shfl_sync(FULL_MASK, j < 32 ? ea.x : eb.x, j & 31);
-          const uint32_t ky = __shfl_sync(FULL_MASK, j < 32 ? ea.y : eb.y, j & 31);
-          for (int f0 = 0; f0 < n_recv_p; f0 += 32) {
-            const int f = f0 + lane;
-            const uint4 ent = f < n_recv_p ? recv_pen[f] : make_uint4(0, 0, 0, 0);
-            const uint32_t bal = __ballot_sync(FULL_MASK, f < n_recv_p && ent.x == kx && ent.y == ky);
-            if (bal != 0u) {
-              chosen_raw = __shfl_sync(FULL_MASK, __uint_as_float(ent.z), __ffs(bal) - 1);
-              break;
-            }
-          }
-        }
+        chosen_raw = __uint_as_float(__shfl_sync(FULL_MASK, j < 32 ? ea.z : eb.z, j & 31));  // raw logit of the pick
       }
       if (lane == 0) {
         P.out_ids[row] = out;
@@ -1178,7 +1165,7 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   }
   if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
   if (ctl[CTL_TIMEOUT] != 0u) {  // a copy may still be in flight into this CTA: bounded wait again
-    for (int p = 0; p < n_pieces; ++p) wait_piece(mbar, p, ctl, P.err);
+    for (int p = 0; p < n_pieces; ++p) wait_bar(&mbar[p], ctl, P.err, false);
   }
 }
 

@@ -151,6 +151,7 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
     }
   }
   const Layout L = strata::make_layout(chunk, esz, s->hash_cap, cs, s->kmax, s->nmax);
+  if (!strata::layout_aligned(L)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
   s->smem = static_cast<int>(L.total);
   if (s->smem > c->max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit %d", s->smem, c->max_smem);
   return STRATA_OK;
@@ -680,7 +681,9 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
     sh.hash_bits = bits;
     sh.hash_cap = 1 << bits;
   }
-  sh.smem = static_cast<int>(strata::make_layout(chunk, esz, sh.hash_cap, cs, sh.kmax, sh.nmax).total);
+  const Layout L = strata::make_layout(chunk, esz, sh.hash_cap, cs, sh.kmax, sh.nmax);
+  if (!strata::layout_aligned(L)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
+  sh.smem = static_cast<int>(L.total);
   if (sh.smem > nd->max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit", sh.smem);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
