@@ -474,27 +474,20 @@ __device__ __forceinline__ int count_greater(const uint32_t* recv, int esz_words
   return rank;
 }
 
-// Rank of `key` in a dense list of `n` entries (entry size `esz_words` 32-bit words, key in words
-// 0-1): the number of larger keys, counted in four independent partial sums (every thread of a
-// warp reads the same entry, a broadcast).
-__device__ __forceinline__ int rank_desc(const uint32_t* list, int esz_words, int n, uint64_t key) {
-  int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-  int j = 0;
-  for (; j + 4 <= n; j += 4) {
-    const uint2 o0 = *reinterpret_cast<const uint2*>(list + (j + 0) * esz_words);
-    const uint2 o1 = *reinterpret_cast<const uint2*>(list + (j + 1) * esz_words);
-    const uint2 o2 = *reinterpret_cast<const uint2*>(list + (j + 2) * esz_words);
-    const uint2 o3 = *reinterpret_cast<const uint2*>(list + (j + 3) * esz_words);
-    r0 += ((static_cast<uint64_t>(o0.y) << 32) | o0.x) > key;
-    r1 += ((static_cast<uint64_t>(o1.y) << 32) | o1.x) > key;
-    r2 += ((static_cast<uint64_t>(o2.y) << 32) | o2.x) > key;
-    r3 += ((static_cast<uint64_t>(o3.y) << 32) | o3.x) > key;
+// Rank of `key` in a dense list (entry size `esz_words` 32-bit words, key in words 0-1) padded
+// with zero keys to `n8` entries, a multiple of 8: the number of larger keys, counted in four
+// independent partial sums (every thread of a warp reads the same entry, a broadcast).
+__device__ __forceinline__ int rank_desc(const uint32_t* list, int esz_words, int n8, uint64_t key) {
+  int r[4] = {0, 0, 0, 0};
+#pragma unroll 1
+  for (int j = 0; j < n8; j += 8) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint2 o = *reinterpret_cast<const uint2*>(list + (j + t) * esz_words);
+      r[t & 3] += ((static_cast<uint64_t>(o.y) << 32) | o.x) > key;
+    }
   }
-  for (; j < n; ++j) {
-    const uint2 o = *reinterpret_cast<const uint2*>(list + j * esz_words);
-    r0 += ((static_cast<uint64_t>(o.y) << 32) | o.x) > key;
-  }
-  return (r0 + r1) + (r2 + r3);
+  return (r[0] + r[1]) + (r[2] + r[3]);
 }
 
 // ------------------------------------------------------------------------------ the kernel
@@ -602,6 +595,7 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
   if (tid < NT / 32) hflag[tid] = 0u;
+  for (int i = tid; i < MAX_CS * XREC_WORDS; i += NT) xrec[i] = 0u;  // absent CTAs' records stay zero
   if (tid < CTL_WORDS) ctl[tid] = (tid == CTL_T) ? 0xFFFFFFFFu : 0u;
   __syncthreads();           // tables zeroed, barriers initialised
   cluster_arrive_relaxed();  // this CTA is running (remote stores wait for every CTA, below)
@@ -635,36 +629,27 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   // The draw counter: each sampled row adds one arrival to its slot's packed word (counter << 16 |
   // arrivals) and reads the counter from the returned value; the row that completes the slot's
   // arrivals also advances the counter and clears them, so every row of the call sees the value
-  // from before the call.
+  // from before the call.  The leader's warp 0 issues it once the candidates are in.
   const bool ctr_warp = k_row > 0 && wid == 0 && crank == 0 && sampled;
   const bool ctr_thread = ctr_warp && lane == 0;
   unsigned long long ctr_old = 0ull;
-  if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
   int rs_pre[2] = {-1, -1};  // row slots of the call, fetched ahead for the arrival count
-  if (ctr_warp) {
-    rs_pre[0] = lane < P.B ? P.row_slot[lane] : -1;
-    rs_pre[1] = lane + 32 < P.B ? P.row_slot[lane + 32] : -1;
-  }
 
   // ---- 1b. first pass as pieces land ----------------------------------------------------------
   float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
   int bmx = 0;
-  int hid[HPRE];
+  int hid[HPRE];  // third metadata level: this thread's first history ids, consumed after the pass
 #pragma unroll
-  for (int j = 0; j < HPRE; ++j) hid[j] = -1;
+  for (int j = 0; j < HPRE; ++j) {
+    const int i = tid + j * NT;
+    hid[j] = (penal && i < h_len) ? P.hist[h_start + i] : -1;
+  }
   {
     const int n_iter = (n_vec + PIECE_VECS - 1) / PIECE_VECS;
 #pragma unroll 1
     for (int p = 0; p < n_iter; ++p) {
       if (p < n_pieces) wait_bar(&mbar[p], ctl, P.err, false);
       pass1_piece<DT>(data, p, p * PIECE_VECS + tid, n_vec, ref, mx, mx2, bmx, s0, s1);
-      if (p == 0 && penal) {  // third metadata level: this thread's first history ids
-#pragma unroll
-        for (int j = 0; j < HPRE; ++j) {
-          const int i = tid + j * NT;
-          hid[j] = i < h_len ? P.hist[h_start + i] : -1;
-        }
-      }
     }
   }
   for (int p = 0; p < n_pieces; ++p) wait_bar(&mbar[p], ctl, P.err, false);  // all pieces visible
@@ -764,60 +749,60 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   // ---- the row threshold T and the log-normalisers -------------------------------------------
   // T = the kp-th largest of the cs*q published keys (zeros included, so T = 0 when fewer than
   // kp real keys exist): the smallest published key with fewer than kp keys above it.  A forced
-  // split can publish fewer than kp keys in all; then there is no bound (T = 0).  Unpublished
-  // record words are zero and never count as above.  Four lanes count for each published key; the
-  // last warp reduces the (max, sum) pairs meanwhile.
+  // split can publish fewer than kp keys in all; then there is no bound (T = 0).  Four lanes count
+  // for each key; the last warp reduces the (max, sum) pairs meanwhile.
   if (kp > 0) {
-    constexpr int TL = 4;  // lanes per published key; lane `sub` counts records sub, sub+4, ...
-    const int U = cs * q, nq4 = (q + 3) >> 2, sub = tid & (TL - 1);
-    for (int base = 0; base < U; base += NT / TL) {
-      const int i = base + tid / TL;
-      if (i < U) {  // whole groups of TL lanes take this branch together
-        const int c = i / q;
-        const uint32_t u = xrec[c * XREC_WORDS + (i - c * q)];
-        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+    // keys are addressed as (record, slot) with a power-of-two slot count QS >= q: slots beyond
+    // q and records beyond cs hold zero, which never counts as above and qualifies as T only when
+    // fewer than kp real keys exist (then T = 0, the right answer).  No runtime guard, no division.
+    constexpr int TL = 4;  // lanes per key; lane `sub` counts records sub, sub+4, sub+8, sub+12
+    const int qs_log = q <= 8 ? 3 : 4;
+    const int nq4 = 1 << (qs_log - 2), sub = tid & (TL - 1);
 #pragma unroll 1
-        for (int j4 = 0; j4 < nq4; ++j4) {
+    for (int base = 0; base < (MAX_CS << qs_log); base += NT / TL) {
+      const int i = base + tid / TL;
+      const int c = i >> qs_log;
+      const uint32_t u = xrec[c * XREC_WORDS + (i & ((1 << qs_log) - 1))];
+      int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll 1
+      for (int j4 = 0; j4 < nq4; ++j4) {
 #pragma unroll
-          for (int k = 0; k < MAX_CS / TL; ++k) {
-            const int c2 = sub + k * TL;
-            if (c2 < cs) {
-              const uint4 v = reinterpret_cast<const uint4*>(xrec + c2 * XREC_WORDS)[j4];
-              a0 += v.x > u;
-              a1 += v.y > u;
-              a2 += v.z > u;
-              a3 += v.w > u;
-            }
-          }
+        for (int k = 0; k < MAX_CS / TL; ++k) {
+          const uint4 v = reinterpret_cast<const uint4*>(xrec + (sub + k * TL) * XREC_WORDS)[j4];
+          a0 += v.x > u;
+          a1 += v.y > u;
+          a2 += v.z > u;
+          a3 += v.w > u;
         }
-        const unsigned act = __activemask();
-        int above = (a0 + a1) + (a2 + a3);
-        above += __shfl_xor_sync(act, above, 1);
-        above += __shfl_xor_sync(act, above, 2);
-        const uint32_t cand = (sub == 0 && above < kp) ? u : 0xFFFFFFFFu;
-        const uint32_t wmin = __reduce_min_sync(act, cand);
-        if ((tid & 31) == 0) atomicMin(&ctl[CTL_T], wmin);
       }
-    }
-  }
-  if (wid == NW - 1) {
-    const bool in = lane < cs;
-    MaxSum g{-INFINITY, 0.0f}, ga{-INFINITY, 0.0f};
-    if (in) {
-      const float4 t = reinterpret_cast<const float4*>(xrec + lane * XREC_WORDS)[4];
-      g = {t.x, t.y};
-      ga = {t.z, t.w};
-    }
-    g = warp_ms_fast(g);
-    ga = warp_ms_fast(ga);
-    if (lane == 0) {
-      ctl[CTL_LSE] = __float_as_uint((g.m == -INFINITY || !(g.s > 0.0f)) ? -INFINITY : g.m + logf(g.s));
-      ctl[CTL_LSE_A] = __float_as_uint((ga.m == -INFINITY || !(ga.s > 0.0f)) ? -INFINITY : ga.m + logf(ga.s));
+      int above = (a0 + a1) + (a2 + a3);
+      above += __shfl_xor_sync(FULL_MASK, above, 1);
+      above += __shfl_xor_sync(FULL_MASK, above, 2);
+      const uint32_t cand = (sub == 0 && above < kp) ? u : 0xFFFFFFFFu;
+      const uint32_t wmin = __reduce_min_sync(FULL_MASK, cand);
+      if (lane == 0) atomicMin(&ctl[CTL_T], wmin);
     }
   }
   __syncthreads();
   const uint32_t T = cs * q >= kp ? ctl[CTL_T] : 0u;  // fewer than kp published keys: no bound
-  const float lse = __uint_as_float(ctl[CTL_LSE]), lse_a = __uint_as_float(ctl[CTL_LSE_A]);
+  // the log-normalisers, by the last warp while the others look for candidates: lanes 0..15
+  // combine the row's (max, sum) pairs, lanes 16..31 the allowed subset's
+  if (wid == NW - 1) {
+    const int c = lane & 15;
+    float m = -INFINITY, sm_ = 0.0f;
+    if (c < cs) {
+      const float2 t = reinterpret_cast<const float2*>(xrec + c * XREC_WORDS)[8 + (lane >> 4)];
+      m = t.x;
+      sm_ = t.y;
+    }
+    float M = m;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, off));
+    float sc = (m == -INFINITY || !(sm_ > 0.0f)) ? 0.0f : sm_ * ex2_approx((m - M) * LOG2E);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) sc += __shfl_xor_sync(FULL_MASK, sc, off);
+    if (c == 0) ctl[CTL_LSE + (lane >> 4)] = __float_as_uint((M == -INFINITY || !(sc > 0.0f)) ? -INFINITY : M + logf(sc));
+  }
 
   // ---- 3. candidates of this chunk: every element at or above T --------------------------------
   if (kp > 0) {
@@ -922,6 +907,9 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     }
   }
 
+  if (kp == 0) __syncthreads();  // the log-normalisers are visible (the candidate phase has its own)
+  const float lse = __uint_as_float(ctl[CTL_LSE]), lse_a = __uint_as_float(ctl[CTL_LSE_A]);
+
   // state of the tail (leader, warp 0)
   int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0;
   float Ca = 0.0f, Cb = 0.0f, wa = 0.0f, wb = 0.0f;  // tempered weights and their fp32 prefix sums
@@ -931,6 +919,12 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   // ---- 4. the leader ranks the received keys exactly -------------------------------------------
   if (kp > 0 && crank == 0) {
     if (cs > 1) wait_bar(&mbar[BAR_X1], ctl, P.err, true);
+    // issued here, consumed by the draw: the merge and the tail's first half hide the latency
+    if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
+    if (ctr_warp) {
+      rs_pre[0] = lane < P.B ? P.row_slot[lane] : -1;
+      rs_pre[1] = lane + 32 < P.B ? P.row_slot[lane + 32] : -1;
+    }
     __syncthreads();  // every slice (the leader's own included) is in place
     // slice offsets (every copying warp scans the counts itself), then warp c copies slice c into
     // the dense lists (the candidate buffers, free by now)
@@ -953,9 +947,13 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
         ctl[CTL_TOT_P] = static_cast<uint32_t>(tp);
         ctl[CTL_TOT_R] = static_cast<uint32_t>(tr);
       }
-      if (tp <= LOCAL_CAP)
+      if (tp <= LOCAL_CAP - 8)
         for (int j = lane; j < my_p; j += 32) cand_pen[off_p + j] = recv_pen[wid * P.kmax + j];
       for (int j = lane; j < my_r; j += 32) cand_raw[off_r + j] = recv_raw[wid * P.nmax + j];
+      if (wid == 0 && lane < 8) {  // zero keys pad both lists to a multiple of 8
+        if (tp + lane < LOCAL_CAP) cand_pen[tp + lane] = make_uint4(0u, 0u, 0u, 0u);
+        if (tr + lane < LOCAL_CAP) cand_raw[tr + lane] = 0ull;
+      }
     }
     __syncthreads();
     const int tot_p = static_cast<int>(ctl[CTL_TOT_P]), tot_r = static_cast<int>(ctl[CTL_TOT_R]);
@@ -965,9 +963,9 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
       for (int f = half; f < tot_p; f += NT / 2) {
         uint4 ent;
         int rank;
-        if (tot_p <= LOCAL_CAP) {
+        if (tot_p <= LOCAL_CAP - 8) {
           ent = cand_pen[f];
-          rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_pen), 4, tot_p,
+          rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_pen), 4, (tot_p + 7) & ~7,
                            (static_cast<uint64_t>(ent.y) << 32) | ent.x);
         } else {  // more than the dense buffer holds (heavy ties): walk the slices
           int c = 0, j = f;
@@ -984,7 +982,7 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     } else {
       for (int f = half; f < tot_r; f += NT / 2) {
         const uint64_t key = cand_raw[f];
-        const int rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_raw), 2, tot_r, key);
+        const int rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_raw), 2, (tot_r + 7) & ~7, key);
         if (rank < n_row) sorted_raw[rank] = key;
       }
     }
