@@ -63,8 +63,8 @@ constexpr int NBAR = MAX_PIECES + 2;
 
 // Control words in shared memory.
 enum : int {
-  CTL_CAND_PEN = 0,  // candidates appended to this CTA's penalised / raw lists
-  CTL_CAND_RAW = 1,
+  CTL_CAND_PEN = 0,  // candidates appended to this CTA's penalised / raw lists (words 0 and 1 form
+  CTL_CAND_RAW = 1,  // one 64-bit counter: a single atomic reserves a slot in both lists)
   CTL_T = 2,         // the row threshold (atomicMin target, starts at all ones)
   CTL_TIMEOUT = 3,
   CTL_LSE = 4,       // log-sum-exp of the row / of the allowed subset (float bits)
@@ -330,11 +330,20 @@ __device__ __forceinline__ void pass1_piece(const unsigned char* data, int p, in
   }
 }
 
-// Every element of this thread whose key reaches T and that carries no penalty: appended to the
-// raw list (top-N alternatives) and the penalised list (the chain), with its raw logit; this
-// thread's vectors v_first, v_first + NT, ... up to v_last.  Only the few threads whose maximum
-// reaches T call it, usually on the one batch that holds their maximum.  Kept small and out of line: the kernel's code is
-// larger than the instruction cache, so code size on the serial phases costs fetch stalls.
+// Append one candidate that carries no penalty to both lists (one shared atomic for both slots).
+__device__ __forceinline__ void append_both(uint32_t* ctl, uint4* cand_pen, uint64_t* cand_raw, uint64_t key, float raw,
+                                            bool to_raw, bool to_pen) {
+  const unsigned long long inc = (to_pen ? 1ull : 0ull) | (to_raw ? (1ull << 32) : 0ull);
+  const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(ctl + CTL_CAND_PEN), inc);
+  const uint32_t ip = static_cast<uint32_t>(old), ir = static_cast<uint32_t>(old >> 32);
+  if (to_pen && ip < LOCAL_CAP)
+    cand_pen[ip] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
+  if (to_raw && ir < LOCAL_CAP) cand_raw[ir] = key;
+}
+
+// Every element at or above T that carries no penalty, among this thread's vectors v_first,
+// v_first + NT, ... up to v_last: appended to both lists with its raw logit.  Out of line: only a
+// thread whose maximum and whose best other batch both reach T takes this full rescan.
 template <int DT>
 __device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_first, int v_last, int n_vec, int n_el,
                                                int lo, uint32_t T, bool penal, const uint32_t* hbits, uint32_t* ctl,
@@ -349,21 +358,11 @@ __device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_
     for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(order_key(x[e]) >= T) << e;
 #pragma unroll 1
     for (; hit != 0u; hit &= hit - 1u) {
-      const int e = __ffs(hit) - 1;
-      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+      const uint32_t loc = static_cast<uint32_t>(v * EPV + __ffs(hit) - 1);
       const float xv = elem_at<DT>(data, loc);
       const uint32_t o = order_key(xv);
       if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && bit_at(hbits, loc))) continue;
-      const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
-      if (to_raw) {
-        const uint32_t i = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
-        if (i < LOCAL_CAP) cand_raw[i] = key;
-      }
-      if (to_pen) {
-        const uint32_t i = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
-        if (i < LOCAL_CAP)
-          cand_pen[i] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(xv), 0u);
-      }
+      append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, to_raw, to_pen);
     }
   }
 }
@@ -635,26 +634,15 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   unsigned long long ctr_old = 0ull;
   int rs_pre[2] = {-1, -1};  // row slots of the call, fetched ahead for the arrival count
 
-  // ---- 1b. first pass as pieces land ----------------------------------------------------------
-  float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
-  int bmx = 0;
-  int hid[HPRE];  // third metadata level: this thread's first history ids, consumed after the pass
+  int hid[HPRE];  // third metadata level: this thread's first history ids, for the table below
 #pragma unroll
   for (int j = 0; j < HPRE; ++j) {
     const int i = tid + j * NT;
     hid[j] = (penal && i < h_len) ? P.hist[h_start + i] : -1;
   }
-  {
-    const int n_iter = (n_vec + PIECE_VECS - 1) / PIECE_VECS;
-#pragma unroll 1
-    for (int p = 0; p < n_iter; ++p) {
-      if (p < n_pieces) wait_bar(&mbar[p], ctl, P.err, false);
-      pass1_piece<DT>(data, p, p * PIECE_VECS + tid, n_vec, ref, mx, mx2, bmx, s0, s1);
-    }
-  }
-  for (int p = 0; p < n_pieces; ++p) wait_bar(&mbar[p], ctl, P.err, false);  // all pieces visible
 
-  // ---- history table of this chunk's id range, and the owners of its ids ----------------------
+  // ---- history table of this chunk's id range, and the owners of its ids, built while the copies
+  // land (no logit is needed); complete before the first pass ----------------------------------
   if (penal) {
     auto add_hist = [&](int id) {
       if (id >= lo && id < hi) {
@@ -669,6 +657,21 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     for (int j = 0; j < HPRE; ++j) add_hist(hid[j]);
     for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(P.hist[h_start + i]);
   }
+  __syncthreads();
+
+  // ---- 1b. first pass as pieces land ----------------------------------------------------------
+  float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
+  int bmx = 0;
+  {
+    const int n_iter = (n_vec + PIECE_VECS - 1) / PIECE_VECS;
+#pragma unroll 1
+    for (int p = 0; p < n_iter; ++p) {
+      if (p < n_pieces) wait_bar(&mbar[p], ctl, P.err, false);
+      pass1_piece<DT>(data, p, p * PIECE_VECS + tid, n_vec, ref, mx, mx2, bmx, s0, s1);
+    }
+  }
+  for (int p = 0; p < n_pieces; ++p) wait_bar(&mbar[p], ctl, P.err, false);  // all pieces visible
+
   // allowed subset: this chunk's ids, each counted once, into (max, sum of exp)
   MaxSum al{-INFINITY, 0.0f};
   {
@@ -683,7 +686,6 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     add_allowed(aid[1]);
     for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) add_allowed(P.allowed[j]);
   }
-  __syncthreads();  // history table, owner flags complete
 
   // ---- 2. this CTA's record: warp maxima (ids without a penalty) and (max, sum) pairs ---------
   // The candidate test key covers every id of the thread; the threshold key must be the value of
@@ -807,13 +809,37 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   // ---- 3. candidates of this chunk: every element at or above T --------------------------------
   if (kp > 0) {
     if (kall != 0u && kall >= T) {
-      // only the batch holding the max, unless another batch also reaches T
       constexpr int RB = BATCH_VECS<DT>;
-      const bool one = order_key(mx2) < T;
-      const int v_first = one ? (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid : tid;
-      const int v_last = one ? v_first + (RB - 1) * NT : n_vec;
-      rescan_candidates<DT>(data, v_first, v_last, n_vec, n_el, lo, T, penal, hbits, ctl, cand_pen, cand_raw,
-                            n_row > 0, k_row > 0);
+      if (order_key(mx2) < T) {
+        // every element at or above T sits in the batch that holds the max: scan its 16 elements
+        // straight-line (independent loads), then append the hits
+        const int vb = (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid;
+        uint32_t hit = 0u;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          float x[EPV];
+          if (vb + r * NT < n_vec) {
+            load_vec<DT>(data, vb + r * NT, x);
+          } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) x[e] = -INFINITY;
+          }
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(order_key(x[e]) >= T) << (r * EPV + e);
+        }
+#pragma unroll 1
+        for (; hit != 0u; hit &= hit - 1u) {
+          const int b = __ffs(hit) - 1;
+          const uint32_t loc = static_cast<uint32_t>((vb + (b / EPV) * NT) * EPV + (b % EPV));
+          const float xv = elem_at<DT>(data, loc);
+          const uint32_t o = order_key(xv);
+          if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && bit_at(hbits, loc))) continue;
+          append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0, k_row > 0);
+        }
+      } else {
+        rescan_candidates<DT>(data, tid, n_vec, n_vec, n_el, lo, T, penal, hbits, ctl, cand_pen, cand_raw, n_row > 0,
+                              k_row > 0);
+      }
     }
     if (penal) {  // penalised ids: raw value for the raw list, penalised value for the other
       for (int i = tid; i < P.hash_cap; i += NT) {
@@ -825,13 +851,14 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
         const uint32_t id = static_cast<uint32_t>(lo) + loc;
         const uint32_t o = order_key(raw);
         if (o != 0u && o >= T && n_row > 0) {
-          const uint32_t s = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
+          const uint32_t s = static_cast<uint32_t>(
+              atomicAdd(reinterpret_cast<unsigned long long*>(ctl + CTL_CAND_PEN), 1ull << 32) >> 32);
           if (s < LOCAL_CAP) cand_raw[s] = sel_key(o, id);
         }
         const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
         const uint32_t op = order_key(pv);
         if (op != 0u && op >= T && k_row > 0) {
-          const uint32_t s = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+          const uint32_t s = static_cast<uint32_t>(atomicAdd(reinterpret_cast<unsigned long long*>(ctl + CTL_CAND_PEN), 1ull));
           const uint64_t key = sel_key(op, id);
           if (s < LOCAL_CAP)
             cand_pen[s] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
