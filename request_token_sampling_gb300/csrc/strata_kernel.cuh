@@ -17,7 +17,8 @@
 //      leader's receive lists (asynchronous DSMEM stores, one transaction-counted arrival per CTA);
 //   4. the leader ranks the received keys by counting (one thread per key), then one warp runs the
 //      tail of the chain on <= 64 survivors: min_p, top_p, temperature, the Philox draw.
-// Every CTA writes the allowed-subset and chosen-id log-probabilities of its own id range.
+// Only the leader writes outputs (the allowed-subset and chosen-id log-probabilities from logits
+// it reads back from global memory), so with early loads no other CTA waits for the previous call.
 // Every wait on another CTA or on a copy is an mbarrier poll with an iteration limit.
 //
 // The chain it computes is defined on the pages "#19 serve: per-request temperature/top_p/top_k/
@@ -937,6 +938,25 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   if (kp == 0) __syncthreads();  // the log-normalisers are visible (the candidate phase has its own)
   const float lse = __uint_as_float(ctl[CTL_LSE]), lse_a = __uint_as_float(ctl[CTL_LSE_A]);
 
+  // The leader alone writes the allowed-subset and chosen-id outputs (so no other CTA waits for the
+  // previous call); it fetches those logits from global memory here, ahead of use.
+  float alog[2] = {0.0f, 0.0f};
+  float chosen_x = 0.0f;
+  if (crank == 0) {
+    const char* rbase = static_cast<const char*>(P.logits) + static_cast<long long>(row) * P.ld * ESZ;
+    auto glogit = [&](int id) -> float {
+      if constexpr (DT == 0) {
+        return reinterpret_cast<const float*>(rbase)[id];
+      } else {
+        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(rbase)[id]) << 16);
+      }
+    };
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      if (aid[t] >= 0 && aid[t] < P.V) alog[t] = glogit(aid[t]);
+    if (tid == 0 && chosen_id >= 0 && chosen_id < P.V) chosen_x = glogit(chosen_id);
+  }
+
   // state of the tail (leader, warp 0)
   int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0;
   float Ca = 0.0f, Cb = 0.0f, wa = 0.0f, wb = 0.0f;  // tempered weights and their fp32 prefix sums
@@ -1069,30 +1089,40 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     }
   }
 
-  // ---- outputs: with early loads the previous kernel owns outputs and counters until it ends --
-  if (early) {
+  // ---- outputs (leader only): with early loads the previous kernel owns outputs and counters
+  // until it ends ---------------------------------------------------------------------------------
+  if (early && crank == 0) {
     grid_dep_wait();
     if (ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
   }
 
-  // allowed-subset log-probabilities and the given chosen id, for this chunk's ids
-  if (P.allowed_off != nullptr && P.allowed_lps != nullptr) {
-    auto out_allowed = [&](int j, int id) {
-      if (id >= lo && id < hi) {
-        P.allowed_lps[j] = elem_at<DT>(data, static_cast<uint32_t>(id - lo)) - lse_a;
-      } else if ((id < 0 || id >= P.V) && crank == 0) {
+  // allowed-subset log-probabilities and the given chosen id
+  if (crank == 0 && P.allowed_off != nullptr && P.allowed_lps != nullptr) {
+    const char* rbase = static_cast<const char*>(P.logits) + static_cast<long long>(row) * P.ld * ESZ;
+    auto out_allowed = [&](int j, int id, float x) {
+      if (id >= 0 && id < P.V) {
+        P.allowed_lps[j] = x - lse_a;
+      } else {
         P.allowed_lps[j] = __int_as_float(0x7FC00000);
         atomicOr(P.err, STRATA_DEVERR_ALLOWED);
       }
     };
-    if (a_beg + tid < a_end) out_allowed(a_beg + tid, aid[0]);
-    if (a_beg + tid + NT < a_end) out_allowed(a_beg + tid + NT, aid[1]);
-    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) out_allowed(j, P.allowed[j]);
+    if (a_beg + tid < a_end) out_allowed(a_beg + tid, aid[0], alog[0]);
+    if (a_beg + tid + NT < a_end) out_allowed(a_beg + tid + NT, aid[1], alog[1]);
+    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) {
+      const int id = P.allowed[j];
+      float x = 0.0f;
+      if (id >= 0 && id < P.V) {
+        if constexpr (DT == 0) x = reinterpret_cast<const float*>(rbase)[id];
+        else x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(rbase)[id]) << 16);
+      }
+      out_allowed(j, id, x);
+    }
   }
-  if (P.mode == MODE_LOGPROBS && P.chosen_lp != nullptr && P.chosen != nullptr && tid == 0) {
-    if (chosen_id >= lo && chosen_id < hi) {
-      P.chosen_lp[row] = elem_at<DT>(data, static_cast<uint32_t>(chosen_id - lo)) - lse;
-    } else if ((chosen_id < 0 || chosen_id >= P.V) && crank == 0) {
+  if (crank == 0 && P.mode == MODE_LOGPROBS && P.chosen_lp != nullptr && P.chosen != nullptr && tid == 0) {
+    if (chosen_id >= 0 && chosen_id < P.V) {
+      P.chosen_lp[row] = chosen_x - lse;
+    } else {
       P.chosen_lp[row] = __int_as_float(0x7FC00000);
       atomicOr(P.err, STRATA_DEVERR_CHOSEN);
     }
