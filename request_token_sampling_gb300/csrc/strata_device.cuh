@@ -118,6 +118,12 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr, uint32_t a, uint32_t 
                : "memory");
 }
 
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t a, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(a),
+               "r"(bar)
+               : "memory");
+}
+
 // One arrival on a cluster CTA's mbarrier that also announces `bytes` more transaction bytes.
 // The bytes may land before or after the arrival: the phase completes once every expected
 // arrival has happened and the transaction count is back to zero.

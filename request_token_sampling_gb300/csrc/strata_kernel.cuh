@@ -36,17 +36,17 @@
 
 namespace strata {
 
-constexpr int NT = 512;                      // threads per CTA
+constexpr int NT = 256;                      // threads per CTA (three CTAs fit an SM)
 constexpr int NW = NT / 32;                  // warps per CTA
-constexpr int VR = 4;                        // 16-byte vectors per thread per piece
+constexpr int VR = 8;                        // 16-byte vectors per thread per piece
 constexpr int PIECE_VECS = NT * VR;
 constexpr int PIECE_BYTES = PIECE_VECS * 16; // 32 KiB per bulk copy
 constexpr int MAX_PIECES = 6;                // chunk <= 192 KiB
 constexpr int MAX_CS = 16;                   // CTAs per row (non-portable cluster size)
 constexpr int KMAX = STRATA_MAX_TOP_K;
 constexpr int NMAX = STRATA_MAX_TOP_N;
-constexpr int QMAX = 8;                      // the host keeps cs >= ceil(K / QMAX): cs * NW >= 2K
-constexpr int LOCAL_CAP = 512;               // per-CTA candidate buffer (beyond: exact rounds)
+constexpr int QMAX = 8;                      // the host keeps cs >= ceil(K / QMAX): cs * NW >= K
+constexpr int LOCAL_CAP = 64;                // per-CTA candidate buffer (beyond: exact rounds)
 constexpr int HASH_CNT_BITS = 13;            // history table entry = (local id << 13) | count
 constexpr uint32_t HASH_EMPTY = 0xFFFFFFFFu;
 constexpr int MODE_SAMPLE = 0;
@@ -121,8 +121,8 @@ struct KParams {
 };
 
 struct Layout {
-  uint32_t data, mbar, hbits, abits, hash, hflag, wmax, red, ctl, xrec;
-  uint32_t cand_pen, cand_raw, recv_cnt, recv_pen, recv_raw, sorted_pen, sorted_raw, total;
+  uint32_t data, mbar, abits, hash, hflag, wmax, red, ctl, xrec;
+  uint32_t cand_pen, cand_raw, recv_cnt, recv_pkey, recv_praw, recv_raw, sorted_pen, sorted_raw, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -137,8 +137,6 @@ __host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, 
   L.mbar = o;
   o += NBAR * 8;
   const uint32_t bw = align_up((static_cast<uint32_t>(chunk) + 31) / 32 * 4, 16);
-  L.hbits = o;
-  o += bw;
   L.abits = o;
   o += bw;
   L.hash = o;
@@ -160,23 +158,25 @@ __host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, 
   o += LOCAL_CAP * 8;
   L.recv_cnt = o;
   o += MAX_CS * 8;
-  L.recv_pen = o;
-  o += static_cast<uint32_t>(cs * kmax) * 16;
+  L.recv_pkey = o;  // received penalised list: keys (8 B) and raw logits (4 B), kmax per CTA
+  o = align_up(o + static_cast<uint32_t>(cs * kmax) * 8, 16);
+  L.recv_praw = o;
+  o = align_up(o + static_cast<uint32_t>(cs * kmax) * 4, 16);
   L.recv_raw = o;
   o += static_cast<uint32_t>(cs * nmax) * 8;
   o = align_up(o, 16);
   L.sorted_pen = o;
-  o += KMAX * 16;
+  o += static_cast<uint32_t>(kmax) * 16;
   L.sorted_raw = o;
-  o += NMAX * 8;
+  o += static_cast<uint32_t>(nmax) * 8;
   L.total = align_up(o, 128);
   return L;
 }
 
 // Every region starts on a 16-byte boundary (vector and bulk accesses rely on it).
 __host__ __device__ inline bool layout_aligned(const Layout& L) {
-  const uint32_t r[] = {L.data, L.mbar, L.hbits, L.abits, L.hash, L.hflag, L.wmax, L.red, L.ctl, L.xrec,
-                        L.cand_pen, L.cand_raw, L.recv_cnt, L.recv_pen, L.recv_raw, L.sorted_pen, L.sorted_raw};
+  const uint32_t r[] = {L.data, L.mbar, L.abits, L.hash, L.hflag, L.wmax, L.red, L.ctl, L.xrec, L.cand_pen,
+                        L.cand_raw, L.recv_cnt, L.recv_pkey, L.recv_praw, L.recv_raw, L.sorted_pen, L.sorted_raw};
   for (uint32_t x : r)
     if (x % 16u != 0u) return false;
   return true;
@@ -347,7 +347,8 @@ __device__ __forceinline__ void append_both(uint32_t* ctl, uint4* cand_pen, uint
 // thread whose maximum and whose best other batch both reach T takes this full rescan.
 template <int DT>
 __device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_first, int v_last, int n_vec, int n_el,
-                                               int lo, uint32_t T, bool penal, const uint32_t* hbits, uint32_t* ctl,
+                                               int lo, uint32_t T, bool penal, const uint32_t* htab, int hash_bits,
+                                               uint32_t* ctl,
                                                uint4* cand_pen, uint64_t* cand_raw, bool to_raw, bool to_pen) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
 #pragma unroll 1
@@ -362,7 +363,7 @@ __device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_
       const uint32_t loc = static_cast<uint32_t>(v * EPV + __ffs(hit) - 1);
       const float xv = elem_at<DT>(data, loc);
       const uint32_t o = order_key(xv);
-      if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && bit_at(hbits, loc))) continue;
+      if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && hash_count(htab, hash_bits, loc) != 0u)) continue;
       append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, to_raw, to_pen);
     }
   }
@@ -386,7 +387,7 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int
 // common path stays small.  Every thread of the CTA calls it.  Returns the number found.
 template <int DT>
 __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, int n_el, int lo, int list, int need,
-                                         bool penal, const uint32_t* hbits, const uint32_t* htab, int hash_bits,
+                                         bool penal, const uint32_t* htab, int hash_bits,
                                          float rep, float freq, float pres, uint64_t* red64, uint4* cand_pen,
                                          uint64_t* cand_raw) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
@@ -403,7 +404,10 @@ __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, i
         const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
         if (loc >= static_cast<uint32_t>(n_el)) continue;
         float pv = x[e];
-        if (list == 0 && penal && bit_at(hbits, loc)) pv = penalize(pv, hash_count(htab, hash_bits, loc), rep, freq, pres);
+        if (list == 0 && penal) {
+          const uint32_t c = hash_count(htab, hash_bits, loc);
+          if (c != 0u) pv = penalize(pv, c, rep, freq, pres);
+        }
         const uint32_t o = order_key(pv);
         if (o == 0u) continue;
         const uint64_t key = sel_key(o, static_cast<uint32_t>(lo) + loc);
@@ -492,7 +496,7 @@ __device__ __forceinline__ int rank_desc(const uint32_t* list, int esz_words, in
 
 // ------------------------------------------------------------------------------ the kernel
 template <int DT>
-__global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
+__global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char sm[];
   constexpr int ESZ = DT == 0 ? 4 : 2;
   constexpr int EPV = 16 / ESZ;
@@ -550,7 +554,6 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   }
   grid_dep_launch();
 
-  uint32_t* hbits = reinterpret_cast<uint32_t*>(sm + L.hbits);
   uint32_t* abits = reinterpret_cast<uint32_t*>(sm + L.abits);
   uint32_t* htab = reinterpret_cast<uint32_t*>(sm + L.hash);
   uint32_t* hflag = reinterpret_cast<uint32_t*>(sm + L.hflag);
@@ -562,7 +565,8 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   uint4* cand_pen = reinterpret_cast<uint4*>(sm + L.cand_pen);
   uint64_t* cand_raw = reinterpret_cast<uint64_t*>(sm + L.cand_raw);
   uint2* recv_cnt = reinterpret_cast<uint2*>(sm + L.recv_cnt);
-  uint4* recv_pen = reinterpret_cast<uint4*>(sm + L.recv_pen);
+  uint64_t* recv_pkey = reinterpret_cast<uint64_t*>(sm + L.recv_pkey);
+  uint32_t* recv_praw = reinterpret_cast<uint32_t*>(sm + L.recv_praw);
   uint64_t* recv_raw = reinterpret_cast<uint64_t*>(sm + L.recv_raw);
   uint4* sorted_pen = reinterpret_cast<uint4*>(sm + L.sorted_pen);
   uint64_t* sorted_raw = reinterpret_cast<uint64_t*>(sm + L.sorted_raw);
@@ -590,7 +594,6 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
 
   const int bw_words = (P.chunk + 31) >> 5;
   for (int i = tid; i < bw_words; i += NT) {
-    hbits[i] = 0u;
     abits[i] = 0u;
   }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
@@ -648,7 +651,6 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     auto add_hist = [&](int id) {
       if (id >= lo && id < hi) {
         const uint32_t loc = static_cast<uint32_t>(id - lo);
-        atomicOr(&hbits[loc >> 5], 1u << (loc & 31));
         const uint32_t owner = (loc / EPV) % NT;
         atomicOr(&hflag[owner >> 5], 1u << (owner & 31));
         if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
@@ -752,13 +754,14 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
   // ---- the row threshold T and the log-normalisers -------------------------------------------
   // T = the kp-th largest of the cs*q published keys (zeros included, so T = 0 when fewer than
   // kp real keys exist): the smallest published key with fewer than kp keys above it.  A forced
-  // split can publish fewer than kp keys in all; then there is no bound (T = 0).  Four lanes count
+  // split can publish fewer than kp keys in all; then there is no bound (T = 0).  TL lanes count
   // for each key; the last warp reduces the (max, sum) pairs meanwhile.
   if (kp > 0) {
     // keys are addressed as (record, slot) with a power-of-two slot count QS >= q: slots beyond
     // q and records beyond cs hold zero, which never counts as above and qualifies as T only when
     // fewer than kp real keys exist (then T = 0, the right answer).  No runtime guard, no division.
-    constexpr int TL = 4;  // lanes per key; lane `sub` counts records sub, sub+4, sub+8, sub+12
+    constexpr int TL = NT / (MAX_CS * 8);  // lanes per key (all keys in one pass when q <= 8);
+    static_assert(TL >= 1 && (TL & (TL - 1)) == 0, "lanes per key");  // lane `sub` counts records sub, sub+TL, ...
     const int qs_log = q <= 8 ? 3 : 4;
     const int nq4 = 1 << (qs_log - 2), sub = tid & (TL - 1);
 #pragma unroll 1
@@ -779,8 +782,8 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
         }
       }
       int above = (a0 + a1) + (a2 + a3);
-      above += __shfl_xor_sync(FULL_MASK, above, 1);
-      above += __shfl_xor_sync(FULL_MASK, above, 2);
+#pragma unroll
+      for (int off = 1; off < TL; off <<= 1) above += __shfl_xor_sync(FULL_MASK, above, off);
       const uint32_t cand = (sub == 0 && above < kp) ? u : 0xFFFFFFFFu;
       const uint32_t wmin = __reduce_min_sync(FULL_MASK, cand);
       if (lane == 0) atomicMin(&ctl[CTL_T], wmin);
@@ -834,11 +837,13 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
           const uint32_t loc = static_cast<uint32_t>((vb + (b / EPV) * NT) * EPV + (b % EPV));
           const float xv = elem_at<DT>(data, loc);
           const uint32_t o = order_key(xv);
-          if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && bit_at(hbits, loc))) continue;
+          if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && hash_count(htab, P.hash_bits, loc) != 0u))
+            continue;
           append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0, k_row > 0);
         }
       } else {
-        rescan_candidates<DT>(data, tid, n_vec, n_vec, n_el, lo, T, penal, hbits, ctl, cand_pen, cand_raw, n_row > 0,
+        rescan_candidates<DT>(data, tid, n_vec, n_vec, n_el, lo, T, penal, htab, P.hash_bits, ctl, cand_pen, cand_raw,
+                              n_row > 0,
                               k_row > 0);
       }
     }
@@ -873,10 +878,10 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     // more candidates than the buffer holds (heavy ties): exact argmax rounds write the chunk's
     // best k_row / n_row in order into the candidate buffers
     if (k_row > 0 && np > LOCAL_CAP)
-      np = exact_rounds<DT>(data, n_vec, n_el, lo, 0, k_row, penal, hbits, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+      np = exact_rounds<DT>(data, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
                             red64, cand_pen, cand_raw);
     if (n_row > 0 && nr > LOCAL_CAP)
-      nr = exact_rounds<DT>(data, n_vec, n_el, lo, 1, n_row, penal, hbits, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+      nr = exact_rounds<DT>(data, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
                             red64, cand_pen, cand_raw);
     if (k_row == 0) np = 0;
     if (n_row == 0) nr = 0;
@@ -902,9 +907,15 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
           out = rank < k_row ? rank : -1;
         }
         if (out >= 0) {
-          uint4* slot_p = recv_pen + crank * P.kmax + out;
-          if (crank == 0) *slot_p = make_uint4(ent.x, ent.y, ent.z, 0u);
-          else st_async_v4(dsmem_addr(smem_u32(slot_p), 0), ent.x, ent.y, ent.z, 0u, leader_bar);
+          uint64_t* key_p = recv_pkey + crank * P.kmax + out;
+          uint32_t* raw_p = recv_praw + crank * P.kmax + out;
+          if (crank == 0) {
+            *key_p = (static_cast<uint64_t>(ent.y) << 32) | ent.x;
+            *raw_p = ent.z;
+          } else {
+            st_async_v2(dsmem_addr(smem_u32(key_p), 0), ent.x, ent.y, leader_bar);
+            st_async_b32(dsmem_addr(smem_u32(raw_p), 0), ent.z, leader_bar);
+          }
         }
       }
     } else {
@@ -930,7 +941,7 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
       } else {
         st_async_v2(dsmem_addr(smem_u32(recv_cnt + crank), 0), static_cast<uint32_t>(sent_p),
                     static_cast<uint32_t>(sent_r), leader_bar);
-        mbar_arrive_expect_tx_remote(leader_bar, static_cast<uint32_t>(8 + 16 * sent_p + 8 * sent_r));
+        mbar_arrive_expect_tx_remote(leader_bar, static_cast<uint32_t>(8 + 12 * sent_p + 8 * sent_r));
       }
     }
   }
@@ -975,7 +986,9 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     __syncthreads();  // every slice (the leader's own included) is in place
     // slice offsets (every copying warp scans the counts itself), then warp c copies slice c into
     // the dense lists (the candidate buffers, free by now)
-    if (wid < cs) {
+    {
+      // every warp scans the slice counts itself; warp w copies slices w, w + NW, ... into the dense
+      // lists (the candidate buffers, free by now) when a list fits them
       const uint2 n = lane < cs ? recv_cnt[lane] : make_uint2(0u, 0u);
       const int pc = min(static_cast<int>(n.x), P.kmax), rc = min(static_cast<int>(n.y), P.nmax);
       int ip = pc, ir = rc;
@@ -988,15 +1001,22 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
         }
       }
       const int tp = __shfl_sync(FULL_MASK, ip, 31), tr = __shfl_sync(FULL_MASK, ir, 31);
-      const int my_p = __shfl_sync(FULL_MASK, pc, wid), my_r = __shfl_sync(FULL_MASK, rc, wid);
-      const int off_p = __shfl_sync(FULL_MASK, ip, wid) - my_p, off_r = __shfl_sync(FULL_MASK, ir, wid) - my_r;
       if (wid == 0 && lane == 0) {
         ctl[CTL_TOT_P] = static_cast<uint32_t>(tp);
         ctl[CTL_TOT_R] = static_cast<uint32_t>(tr);
       }
-      if (tp <= LOCAL_CAP - 8)
-        for (int j = lane; j < my_p; j += 32) cand_pen[off_p + j] = recv_pen[wid * P.kmax + j];
-      for (int j = lane; j < my_r; j += 32) cand_raw[off_r + j] = recv_raw[wid * P.nmax + j];
+      for (int c = wid; c < cs; c += NW) {
+        const int my_p = __shfl_sync(FULL_MASK, pc, c), my_r = __shfl_sync(FULL_MASK, rc, c);
+        const int off_p = __shfl_sync(FULL_MASK, ip, c) - my_p, off_r = __shfl_sync(FULL_MASK, ir, c) - my_r;
+        if (tp <= LOCAL_CAP - 8)
+          for (int j = lane; j < my_p; j += 32) {
+            const uint64_t k = recv_pkey[c * P.kmax + j];
+            cand_pen[off_p + j] = make_uint4(static_cast<uint32_t>(k), static_cast<uint32_t>(k >> 32),
+                                             recv_praw[c * P.kmax + j], 0u);
+          }
+        if (tr <= LOCAL_CAP - 8)
+          for (int j = lane; j < my_r; j += 32) cand_raw[off_r + j] = recv_raw[c * P.nmax + j];
+      }
       if (wid == 0 && lane < 8) {  // zero keys pad both lists to a multiple of 8
         if (tp + lane < LOCAL_CAP) cand_pen[tp + lane] = make_uint4(0u, 0u, 0u, 0u);
         if (tr + lane < LOCAL_CAP) cand_raw[tr + lane] = 0ull;
@@ -1004,7 +1024,8 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
     }
     __syncthreads();
     const int tot_p = static_cast<int>(ctl[CTL_TOT_P]), tot_r = static_cast<int>(ctl[CTL_TOT_R]);
-    // exact ranks by counting larger keys (threads 0..255: penalised list, 256..511: raw list)
+    // exact ranks by counting larger keys (first half of the threads: penalised list, second half:
+    // raw list); a list longer than the dense buffer (heavy ties) is ranked over its slices
     const int half = tid & (NT / 2 - 1);
     if (tid < NT / 2) {
       for (int f = half; f < tot_p; f += NT / 2) {
@@ -1014,22 +1035,34 @@ __global__ void __launch_bounds__(NT, 2) rows_kernel(const KParams P) {
           ent = cand_pen[f];
           rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_pen), 4, (tot_p + 7) & ~7,
                            (static_cast<uint64_t>(ent.y) << 32) | ent.x);
-        } else {  // more than the dense buffer holds (heavy ties): walk the slices
+        } else {
           int c = 0, j = f;
           for (int n = recv_count(recv_cnt, 0, 0, P.kmax); j >= n && c + 1 < cs; n = recv_count(recv_cnt, c, 0, P.kmax)) {
             j -= n;
             ++c;
           }
-          ent = recv_pen[c * P.kmax + j];
-          rank = count_greater(reinterpret_cast<const uint32_t*>(recv_pen), 4, P.kmax, recv_cnt, 0, cs,
-                               (static_cast<uint64_t>(ent.y) << 32) | ent.x);
+          const uint64_t k = recv_pkey[c * P.kmax + j];
+          ent = make_uint4(static_cast<uint32_t>(k), static_cast<uint32_t>(k >> 32), recv_praw[c * P.kmax + j], 0u);
+          rank = count_greater(reinterpret_cast<const uint32_t*>(recv_pkey), 2, P.kmax, recv_cnt, 0, cs, k);
         }
         if (rank < k_row) sorted_pen[rank] = ent;
       }
     } else {
       for (int f = half; f < tot_r; f += NT / 2) {
-        const uint64_t key = cand_raw[f];
-        const int rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_raw), 2, (tot_r + 7) & ~7, key);
+        uint64_t key;
+        int rank;
+        if (tot_r <= LOCAL_CAP - 8) {
+          key = cand_raw[f];
+          rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_raw), 2, (tot_r + 7) & ~7, key);
+        } else {
+          int c = 0, j = f;
+          for (int n = recv_count(recv_cnt, 0, 1, P.nmax); j >= n && c + 1 < cs; n = recv_count(recv_cnt, c, 1, P.nmax)) {
+            j -= n;
+            ++c;
+          }
+          key = recv_raw[c * P.nmax + j];
+          rank = count_greater(reinterpret_cast<const uint32_t*>(recv_raw), 2, P.nmax, recv_cnt, 1, cs, key);
+        }
         if (rank < n_row) sorted_raw[rank] = key;
       }
     }
