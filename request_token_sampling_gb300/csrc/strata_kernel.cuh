@@ -58,14 +58,15 @@ constexpr float LAZY_SHIFT = 16.0f;          // the exp reference moves only whe
 constexpr int XREC_WORDS = 20;               // published per CTA: 16 warp-maximum keys + 2 (max, sum) pairs
 constexpr int XREC_BYTES = XREC_WORDS * 4;
 constexpr int HPRE = 2;                      // history ids per thread fetched ahead of the table build
+constexpr int APRE = 4;                      // allowed ids per thread fetched ahead
 constexpr int BAR_X0 = MAX_PIECES;           // mbarrier: every CTA's published record has landed
 constexpr int BAR_X1 = MAX_PIECES + 1;       // mbarrier (leader): every CTA's candidates have landed
 constexpr int NBAR = MAX_PIECES + 2;
 
 // Control words in shared memory.
 enum : int {
-  CTL_CAND_PEN = 0,  // candidates appended to this CTA's penalised / raw lists (words 0 and 1 form
-  CTL_CAND_RAW = 1,  // one 64-bit counter: a single atomic reserves a slot in both lists)
+  CTL_CAND_PEN = 0,  // candidates appended to this CTA's penalised / raw lists
+  CTL_CAND_RAW = 1,
   CTL_T = 2,         // the row threshold (atomicMin target, starts at all ones)
   CTL_TIMEOUT = 3,
   CTL_LSE = 4,       // log-sum-exp of the row / of the allowed subset (float bits)
@@ -331,12 +332,11 @@ __device__ __forceinline__ void pass1_piece(const unsigned char* data, int p, in
   }
 }
 
-// Append one candidate that carries no penalty to both lists (one shared atomic for both slots).
+// Append one candidate that carries no penalty to both lists (two independent shared atomics).
 __device__ __forceinline__ void append_both(uint32_t* ctl, uint4* cand_pen, uint64_t* cand_raw, uint64_t key, float raw,
                                             bool to_raw, bool to_pen) {
-  const unsigned long long inc = (to_pen ? 1ull : 0ull) | (to_raw ? (1ull << 32) : 0ull);
-  const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(ctl + CTL_CAND_PEN), inc);
-  const uint32_t ip = static_cast<uint32_t>(old), ir = static_cast<uint32_t>(old >> 32);
+  const uint32_t ip = to_pen ? atomicAdd(&ctl[CTL_CAND_PEN], 1u) : 0u;
+  const uint32_t ir = to_raw ? atomicAdd(&ctl[CTL_CAND_RAW], 1u) : 0u;
   if (to_pen && ip < LOCAL_CAP)
     cand_pen[ip] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
   if (to_raw && ir < LOCAL_CAP) cand_raw[ir] = key;
@@ -347,7 +347,7 @@ __device__ __forceinline__ void append_both(uint32_t* ctl, uint4* cand_pen, uint
 // thread whose maximum and whose best other batch both reach T takes this full rescan.
 template <int DT>
 __device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_first, int v_last, int n_vec, int n_el,
-                                               int lo, uint32_t T, bool penal, const uint32_t* htab, int hash_bits,
+                                               int lo, float Tf, bool penal, const uint32_t* htab, int hash_bits,
                                                uint32_t* ctl,
                                                uint4* cand_pen, uint64_t* cand_raw, bool to_raw, bool to_pen) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
@@ -355,9 +355,9 @@ __device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_
   for (int v = v_first; v < n_vec && v <= v_last; v += NT) {
     float x[EPV];
     load_vec<DT>(data, v, x);
-    uint32_t hit = 0u;  // elements of this vector at or above T
+    uint32_t hit = 0u;  // elements of this vector at or above T (NaN compares false)
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(order_key(x[e]) >= T) << e;
+    for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(x[e] >= Tf) << e;
 #pragma unroll 1
     for (; hit != 0u; hit &= hit - 1u) {
       const uint32_t loc = static_cast<uint32_t>(v * EPV + __ffs(hit) - 1);
@@ -520,39 +520,45 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + L.mbar);
   const char* grow = static_cast<const char*>(P.logits) + (static_cast<long long>(row) * P.ld + lo) * ESZ;
 
-  // row metadata, first level (independent loads; consumed once the copies are out)
+  // row metadata, first level: independent loads.  Thread 0 issues its own after the copies and
+  // the barrier fence (a release fence behind outstanding loads would wait for them); every other
+  // thread issues them first, so the three-level metadata chain starts at once.
   int slot = -1;
   unsigned long long pos = 0ull;
   int chosen_id = -1;
   int a_beg = 0, a_end = 0;
-  if (P.mode == MODE_SAMPLE) {
-    slot = P.row_slot[row];
-    pos = static_cast<unsigned long long>(P.row_pos[row]);
-  } else if (P.chosen != nullptr) {
-    chosen_id = P.chosen[row];
-  }
-  if (P.allowed_off != nullptr) {
-    a_beg = P.allowed_off[row];
-    a_end = P.allowed_off[row + 1];
-  }
+  auto load_meta1 = [&]() {
+    if (P.mode == MODE_SAMPLE) {
+      slot = P.row_slot[row];
+      pos = static_cast<unsigned long long>(P.row_pos[row]);
+    } else if (P.chosen != nullptr) {
+      chosen_id = P.chosen[row];
+    }
+    if (P.allowed_off != nullptr) {
+      a_beg = P.allowed_off[row];
+      a_end = P.allowed_off[row + 1];
+    }
+  };
+  if (tid != 0) load_meta1();
 
   // ---- 1. barriers and the bulk copies of this chunk ----------------------------------------
-  if (wid == 0) {
-    if (lane == 0) {
-      for (int p = 0; p < n_pieces; ++p) mbar_init(&mbar[p], 1);
-      mbar_init(&mbar[BAR_X0], 33);                  // the announced bytes + warp 0 (own record)
-      mbar_init(&mbar[BAR_X1], cs > 1 ? cs - 1 : 1); // one arrival per other CTA (leader only)
-      fence_mbar_init();
-      mbar_arrive_expect_tx(&mbar[BAR_X0], static_cast<uint32_t>((cs - 1) * XREC_BYTES));
-    }
-    __syncwarp();
-    for (int p = lane; p < n_pieces; p += 32) {
+  if (tid == 0) {  // the copies go out first; the exchange barriers are set up behind them
+    for (int p = 0; p < n_pieces; ++p) mbar_init(&mbar[p], 1);
+    fence_proxy_async_smem();
+    for (int p = 0; p < n_pieces; ++p) {
       const uint32_t nb = static_cast<uint32_t>(min(PIECE_BYTES, bytes_al - p * PIECE_BYTES));
       mbar_arrive_expect_tx(&mbar[p], nb);
       bulk_g2s(data + p * PIECE_BYTES, grow + p * PIECE_BYTES, nb, &mbar[p]);
     }
+    mbar_init(&mbar[BAR_X0], 2);                   // the announced bytes + this CTA's own record
+    mbar_init(&mbar[BAR_X1], cs > 1 ? cs - 1 : 1); // one arrival per other CTA (leader only)
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&mbar[BAR_X0], static_cast<uint32_t>((cs - 1) * XREC_BYTES));
   }
   grid_dep_launch();
+  if (tid == 0) load_meta1();
+
+
 
   uint32_t* abits = reinterpret_cast<uint32_t*>(sm + L.abits);
   uint32_t* htab = reinterpret_cast<uint32_t*>(sm + L.hash);
@@ -622,9 +628,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     h_len = min(sp.last_n, max(0, he - hb));
     h_start = he - h_len;
   }
-  int aid[2];
+  int aid[APRE];  // the first allowed ids of this thread, fetched ahead
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
+  for (int t = 0; t < APRE; ++t) {
     const int j = a_beg + tid + t * NT;
     aid[t] = j < a_end ? P.allowed[j] : -1;
   }
@@ -638,29 +644,12 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   unsigned long long ctr_old = 0ull;
   int rs_pre[2] = {-1, -1};  // row slots of the call, fetched ahead for the arrival count
 
-  int hid[HPRE];  // third metadata level: this thread's first history ids, for the table below
+  int hid[HPRE];  // third metadata level: this thread's first history ids, for the table after the pass
 #pragma unroll
   for (int j = 0; j < HPRE; ++j) {
     const int i = tid + j * NT;
     hid[j] = (penal && i < h_len) ? P.hist[h_start + i] : -1;
   }
-
-  // ---- history table of this chunk's id range, and the owners of its ids, built while the copies
-  // land (no logit is needed); complete before the first pass ----------------------------------
-  if (penal) {
-    auto add_hist = [&](int id) {
-      if (id >= lo && id < hi) {
-        const uint32_t loc = static_cast<uint32_t>(id - lo);
-        const uint32_t owner = (loc / EPV) % NT;
-        atomicOr(&hflag[owner >> 5], 1u << (owner & 31));
-        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
-      }
-    };
-#pragma unroll
-    for (int j = 0; j < HPRE; ++j) add_hist(hid[j]);
-    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(P.hist[h_start + i]);
-  }
-  __syncthreads();
 
   // ---- 1b. first pass as pieces land ----------------------------------------------------------
   float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
@@ -685,10 +674,27 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         if (!(atomicOr(&abits[loc >> 5], bit) & bit)) online_add(al, elem_at<DT>(data, loc));
       }
     };
-    add_allowed(aid[0]);
-    add_allowed(aid[1]);
-    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) add_allowed(P.allowed[j]);
+#pragma unroll
+    for (int t = 0; t < APRE; ++t) add_allowed(aid[t]);
+    for (int j = a_beg + tid + APRE * NT; j < a_end; j += NT) add_allowed(P.allowed[j]);
   }
+
+  // ---- history table of this chunk's id range, and the owners of its ids (their ids were fetched
+  // before the first pass and have landed by now) ------------------------------------------------
+  if (penal) {
+    auto add_hist = [&](int id) {
+      if (id >= lo && id < hi) {
+        const uint32_t loc = static_cast<uint32_t>(id - lo);
+        const uint32_t owner = (loc / EPV) % NT;
+        atomicOr(&hflag[owner >> 5], 1u << (owner & 31));
+        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
+      }
+    };
+#pragma unroll
+    for (int j = 0; j < HPRE; ++j) add_hist(hid[j]);
+    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(P.hist[h_start + i]);
+  }
+  __syncthreads();  // history table and owner flags complete
 
   // ---- 2. this CTA's record: warp maxima (ids without a penalty) and (max, sum) pairs ---------
   // The candidate test key covers every id of the thread; the threshold key must be the value of
@@ -705,37 +711,34 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
     }
   }
-  // q: warp maxima published per CTA (all NW when that is no more than 4K/cs)
-  const int q = kp > 0 ? min(NW, max((kp + cs - 1) / cs, (4 * kp + cs - 1) / cs)) : 0;
+  // q: warp maxima published per CTA (all of them; unused slots are zero)
+  const int q = kp > 0 ? NW : 0;
   __syncthreads();
   if (wid == 0) {
-    MaxSum r1{-INFINITY, 0.0f}, r2{-INFINITY, 0.0f};
-    uint32_t w = 0u;
-    if (lane < NW) {
-      const float4 t = red4[lane];
-      r1 = {t.x, t.y};
-      r2 = {t.z, t.w};
-      w = wmax[lane];
+    // the CTA's (max, sum) pairs: lanes 0..NW-1 combine the row's, lanes 16..16+NW-1 the allowed
+    // subset's (three shuffle steps each, side by side)
+    const int g = lane >> 4, w8 = lane & 15;
+    float m = -INFINITY, sum = 0.0f;
+    if (w8 < NW) {
+      const float4 t = red4[w8];
+      m = g ? t.z : t.x;
+      sum = g ? t.w : t.y;
     }
-    r1 = warp_ms_fast(r1);
-    r2 = warp_ms_fast(r2);
-    // the q largest warp maxima, in descending order, into words 0..q-1 of this CTA's record
-    // (words q..15 stay zero): rank of each lane's value by comparing it with every other lane's
-    int rank = 0;
+    float M = m;
 #pragma unroll
-    for (int m = 0; m < NW; ++m) {
-      const uint32_t o = __shfl_sync(FULL_MASK, w, m);
-      rank += (o > w) || (o == w && m < lane);
+    for (int off = NW / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, off));
+    float sc = (m == -INFINITY || !(sum > 0.0f)) ? 0.0f : sum * ex2_approx((m - M) * LOG2E);
+#pragma unroll
+    for (int off = NW / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(FULL_MASK, sc, off);
+    const float Ma = __shfl_sync(FULL_MASK, M, 16), Sa = __shfl_sync(FULL_MASK, sc, 16);
+    if (lane == 0) {  // this CTA's record: NW warp-maximum keys, zeros, the two pairs
+      uint4* own = reinterpret_cast<uint4*>(xrec + crank * XREC_WORDS);
+      const uint4* wk = reinterpret_cast<const uint4*>(wmax);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) own[i] = i < NW / 4 ? wk[i] : make_uint4(0u, 0u, 0u, 0u);
+      own[4] = make_uint4(__float_as_uint(M), __float_as_uint(sc), __float_as_uint(Ma), __float_as_uint(Sa));
+      mbar_arrive(&mbar[BAR_X0]);  // own record in place (release by this lane)
     }
-    uint32_t* own = xrec + crank * XREC_WORDS;
-    if (lane < 16) own[lane] = 0u;
-    if (lane == 16) own[16] = __float_as_uint(r1.m);
-    if (lane == 17) own[17] = __float_as_uint(r1.s);
-    if (lane == 18) own[18] = __float_as_uint(r2.m);
-    if (lane == 19) own[19] = __float_as_uint(r2.s);
-    __syncwarp();
-    if (lane < NW && rank < q) own[rank] = w;
-    mbar_arrive(&mbar[BAR_X0]);  // each lane releases its own word of the record
     __syncwarp();
   }
   cluster_wait();  // every CTA of the cluster is running: remote stores are safe from here on
@@ -812,6 +815,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 
   // ---- 3. candidates of this chunk: every element at or above T --------------------------------
   if (kp > 0) {
+    // T as a float threshold (x >= Tf exactly when order_key(x) >= T, NaN never); T = 0 is no bound
+    const float Tf = T == 0u ? -INFINITY : key_value(T);
+    const bool own_hist = penal && ((hflag[tid >> 5] >> (tid & 31)) & 1u);  // only then can a hit be a history id
     if (kall != 0u && kall >= T) {
       constexpr int RB = BATCH_VECS<DT>;
       if (order_key(mx2) < T) {
@@ -829,7 +835,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
             for (int e = 0; e < EPV; ++e) x[e] = -INFINITY;
           }
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(order_key(x[e]) >= T) << (r * EPV + e);
+          for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(x[e] >= Tf) << (r * EPV + e);
         }
 #pragma unroll 1
         for (; hit != 0u; hit &= hit - 1u) {
@@ -837,12 +843,12 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
           const uint32_t loc = static_cast<uint32_t>((vb + (b / EPV) * NT) * EPV + (b % EPV));
           const float xv = elem_at<DT>(data, loc);
           const uint32_t o = order_key(xv);
-          if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && hash_count(htab, P.hash_bits, loc) != 0u))
+          if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (own_hist && hash_count(htab, P.hash_bits, loc) != 0u))
             continue;
           append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0, k_row > 0);
         }
       } else {
-        rescan_candidates<DT>(data, tid, n_vec, n_vec, n_el, lo, T, penal, htab, P.hash_bits, ctl, cand_pen, cand_raw,
+        rescan_candidates<DT>(data, tid, n_vec, n_vec, n_el, lo, Tf, own_hist, htab, P.hash_bits, ctl, cand_pen, cand_raw,
                               n_row > 0,
                               k_row > 0);
       }
@@ -857,14 +863,13 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         const uint32_t id = static_cast<uint32_t>(lo) + loc;
         const uint32_t o = order_key(raw);
         if (o != 0u && o >= T && n_row > 0) {
-          const uint32_t s = static_cast<uint32_t>(
-              atomicAdd(reinterpret_cast<unsigned long long*>(ctl + CTL_CAND_PEN), 1ull << 32) >> 32);
+          const uint32_t s = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
           if (s < LOCAL_CAP) cand_raw[s] = sel_key(o, id);
         }
         const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
         const uint32_t op = order_key(pv);
         if (op != 0u && op >= T && k_row > 0) {
-          const uint32_t s = static_cast<uint32_t>(atomicAdd(reinterpret_cast<unsigned long long*>(ctl + CTL_CAND_PEN), 1ull));
+          const uint32_t s = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
           const uint64_t key = sel_key(op, id);
           if (s < LOCAL_CAP)
             cand_pen[s] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
@@ -951,7 +956,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 
   // The leader alone writes the allowed-subset and chosen-id outputs (so no other CTA waits for the
   // previous call); it fetches those logits from global memory here, ahead of use.
-  float alog[2] = {0.0f, 0.0f};
+  float alog[APRE] = {};
   float chosen_x = 0.0f;
   if (crank == 0) {
     const char* rbase = static_cast<const char*>(P.logits) + static_cast<long long>(row) * P.ld * ESZ;
@@ -963,8 +968,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       }
     };
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
-      if (aid[t] >= 0 && aid[t] < P.V) alog[t] = glogit(aid[t]);
+    for (int t = 0; t < APRE; ++t) alog[t] = (aid[t] >= 0 && aid[t] < P.V) ? glogit(aid[t]) : 0.0f;
     if (tid == 0 && chosen_id >= 0 && chosen_id < P.V) chosen_x = glogit(chosen_id);
   }
 
@@ -1140,9 +1144,10 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         atomicOr(P.err, STRATA_DEVERR_ALLOWED);
       }
     };
-    if (a_beg + tid < a_end) out_allowed(a_beg + tid, aid[0], alog[0]);
-    if (a_beg + tid + NT < a_end) out_allowed(a_beg + tid + NT, aid[1], alog[1]);
-    for (int j = a_beg + tid + 2 * NT; j < a_end; j += NT) {
+#pragma unroll
+    for (int t = 0; t < APRE; ++t)
+      if (a_beg + tid + t * NT < a_end) out_allowed(a_beg + tid + t * NT, aid[t], alog[t]);
+    for (int j = a_beg + tid + APRE * NT; j < a_end; j += NT) {
       const int id = P.allowed[j];
       float x = 0.0f;
       if (id >= 0 && id < P.V) {
