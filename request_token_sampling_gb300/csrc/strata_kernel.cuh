@@ -494,6 +494,21 @@ __device__ __forceinline__ int rank_desc(const uint32_t* list, int esz_words, in
   return (r[0] + r[1]) + (r[2] + r[3]);
 }
 
+// Sort 8 keys in descending order in registers (Batcher's odd-even merge network, 19 exchanges).
+__device__ __forceinline__ void sort8_desc(uint32_t (&v)[8]) {
+  auto cx = [&](int i, int j) {
+    const uint32_t a = v[i], b = v[j];
+    v[i] = max(a, b);
+    v[j] = min(a, b);
+  };
+  cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+  cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+  cx(1, 2); cx(5, 6);
+  cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+  cx(2, 4); cx(3, 5);
+  cx(1, 2); cx(3, 4); cx(5, 6);
+}
+
 // ------------------------------------------------------------------------------ the kernel
 template <int DT>
 __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
@@ -711,8 +726,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
     }
   }
-  // q: warp maxima published per CTA (all of them; unused slots are zero)
-  const int q = kp > 0 ? NW : 0;
+  // q: warp maxima published per CTA, the largest first: 4 when 4*cs covers 2K, else all NW
+  // (unused slots are zero)
+  const int q = kp > 0 ? (4 * cs >= 2 * kp ? 4 : NW) : 0;
   __syncthreads();
   if (wid == 0) {
     // the CTA's (max, sum) pairs: lanes 0..NW-1 combine the row's, lanes 16..16+NW-1 the allowed
@@ -731,11 +747,17 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 #pragma unroll
     for (int off = NW / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(FULL_MASK, sc, off);
     const float Ma = __shfl_sync(FULL_MASK, M, 16), Sa = __shfl_sync(FULL_MASK, sc, 16);
-    if (lane == 0) {  // this CTA's record: NW warp-maximum keys, zeros, the two pairs
+    if (lane == 0) {  // this CTA's record: the q largest warp-maximum keys, zeros, the two pairs
       uint4* own = reinterpret_cast<uint4*>(xrec + crank * XREC_WORDS);
-      const uint4* wk = reinterpret_cast<const uint4*>(wmax);
+      static_assert(NW == 8, "the record's key selection sorts the 8 warp maxima");
+      uint32_t k8[NW];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) own[i] = i < NW / 4 ? wk[i] : make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < NW; ++i) k8[i] = wmax[i];
+      sort8_desc(k8);
+      own[0] = make_uint4(k8[0], k8[1], k8[2], k8[3]);
+      own[1] = q > 4 ? make_uint4(k8[4], k8[5], k8[6], k8[7]) : make_uint4(0u, 0u, 0u, 0u);
+      own[2] = make_uint4(0u, 0u, 0u, 0u);
+      own[3] = make_uint4(0u, 0u, 0u, 0u);
       own[4] = make_uint4(__float_as_uint(M), __float_as_uint(sc), __float_as_uint(Ma), __float_as_uint(Sa));
       mbar_arrive(&mbar[BAR_X0]);  // own record in place (release by this lane)
     }
@@ -763,9 +785,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     // keys are addressed as (record, slot) with a power-of-two slot count QS >= q: slots beyond
     // q and records beyond cs hold zero, which never counts as above and qualifies as T only when
     // fewer than kp real keys exist (then T = 0, the right answer).  No runtime guard, no division.
-    constexpr int TL = NT / (MAX_CS * 8);  // lanes per key (all keys in one pass when q <= 8);
+    constexpr int TL = NT / (MAX_CS * 4);  // lanes per key (all keys in one pass when q <= 4);
     static_assert(TL >= 1 && (TL & (TL - 1)) == 0, "lanes per key");  // lane `sub` counts records sub, sub+TL, ...
-    const int qs_log = q <= 8 ? 3 : 4;
+    const int qs_log = q <= 4 ? 2 : 3;
     const int nq4 = 1 << (qs_log - 2), sub = tid & (TL - 1);
 #pragma unroll 1
     for (int base = 0; base < (MAX_CS << qs_log); base += NT / TL) {
