@@ -365,3 +365,35 @@ def logprobs_call(w, chosen=None, top_n=None):
         c = None if chosen is None else int(chosen[b])
         out.append(logprobs_row(raw, c, top_n, allowed))
     return out
+
+
+def accept_window(row_slot, row_ids, row_draft) -> dict:
+    """Rows kept per slot of one verify window (the step right after sampling).
+
+    "#19 ...", "What changed": the emitted tokens are always the target's own samples; the drafts
+    only fill the verified window.  "#559 ...", "Not done (yet)": a sampled row is accepted when
+    its pick equals the draft.  Reading: within one call, the rows of a slot are its window in row
+    order; row j's pick is compared with `row_draft[j]`, the draft that the window placed right
+    after row j's position (-1 for the window's last row, which has none).  Every row up to and
+    including the first one whose pick differs from its draft (or that has no draft) is kept, so
+    n_keep = 1 + the number of leading rows whose pick equals their draft; a row with pick -1
+    (an out-of-range slot or no candidate) never matches.  Returns {slot: n_keep}.
+    """
+    keep, open_ = {}, {}
+    for s, t, d in zip(row_slot, row_ids, row_draft):
+        s, t, d = int(s), int(t), int(d)
+        if s not in keep:
+            keep[s], open_[s] = 0, True
+        if not open_[s]:
+            continue
+        keep[s] += 1
+        if d < 0 or t < 0 or t != d:
+            open_[s] = False
+    return keep
+
+
+def verify_call(w, row_draft, counters=None, top_n=None):
+    """A sampling call whose rows are verify windows: `sample_call` plus the kept count per slot."""
+    rows, counters = sample_call(w, counters=counters, top_n=top_n, with_allowed=False)
+    keep = accept_window(w["row_slot"], [r["id"] for r in rows], row_draft)
+    return rows, counters, keep

@@ -39,6 +39,9 @@ MUTATIONS = [
     ("philox.py", "(position & MASK32, position >> 32, counter & MASK32, counter >> 32)",
      "(counter & MASK32, counter >> 32, position & MASK32, position >> 32)"),
     ("philox.py", "return (out[0] >> 8) * (2.0 ** -24)", "return (out[1] >> 8) * (2.0 ** -24)"),
+    ("sampling.py", "        if not open_[s]:\n            continue\n", ""),
+    ("sampling.py", "        keep[s] += 1\n        if d < 0 or t < 0 or t != d:\n            open_[s] = False",
+     "        if d < 0 or t < 0 or t != d:\n            open_[s] = False\n        else:\n            keep[s] += 1"),
 ]
 
 

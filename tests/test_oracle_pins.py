@@ -479,3 +479,53 @@ def test_configs_generate_and_run():
     assert w2["row_pos"].tolist() == [115, 116, 117, 118, 119]
     w5 = synth.config5.__doc__
     assert "2048" in w5
+
+
+# ---- verify-window acceptance ("#19 ...", "What changed"; "#559 ...", "Not done (yet)") --------
+def test_accept_window_hand_cases():
+    acc = oracle.accept_window
+    # every draft matches: the whole window is kept, its last row's pick is the bonus token
+    assert acc([0, 0, 0, 0, 0], [7, 8, 9, 10, 11], [7, 8, 9, 10, -1]) == {0: 5}
+    # the first mismatch is kept (the target's own sample) and ends the window
+    assert acc([0, 0, 0, 0, 0], [7, 8, 9, 10, 11], [7, 5, 9, 10, -1]) == {0: 2}
+    assert acc([0, 0, 0, 0, 0], [7, 8, 9, 10, 11], [1, 8, 9, 10, -1]) == {0: 1}
+    # a later match after a mismatch does not extend the window
+    assert acc([0, 0, 0], [4, 5, 6], [4, 0, 6]) == {0: 2}
+    # a lone row (no draft after it) keeps exactly one token
+    assert acc([3], [42], [-1]) == {3: 1}
+    # slots interleave; each slot's rows are its own window in row order
+    assert acc([0, 1, 0, 1, 0, 1], [1, 2, 3, 4, 5, 6], [1, 2, 9, 4, -1, -1]) == {0: 2, 1: 3}
+    # a pick of -1 (no candidate, out-of-range slot) never matches, even a -1 draft
+    assert acc([0, 0], [-1, 3], [-1, -1]) == {0: 1}
+    assert acc([0, 0], [-1, 3], [5, -1]) == {0: 1}
+
+
+def test_accept_window_greedy_drafts_are_accepted():
+    """Neutral greedy keys with drafts equal to each row's argmax (the textbook greedy pick): the
+    whole window is accepted; one wrong draft at row j keeps j + 1 rows."""
+    w = synth.config2_window(7)
+    for s in w["slot_params"]:
+        w["slot_params"][s] = synth.make_params(temperature=0.0, penalty_last_n=0)
+    raw = [oracle.widen(w["logits"][b, :w["V"]], "f32") for b in range(w["B"])]
+    argmax = [int(np.argmax(r)) for r in raw]
+    drafts = argmax[:-1] + [-1]
+    rows, ctr, keep = oracle.verify_call(w, drafts)
+    assert [r["id"] for r in rows] == argmax
+    assert keep == {0: w["B"]}
+    assert ctr == w["counters"]                    # greedy slots draw nothing
+    for j in range(w["B"] - 1):
+        bad = list(drafts)
+        bad[j] = (argmax[j] + 1) % w["V"]
+        assert oracle.verify_call(w, bad)[2] == {0: j + 1}
+
+
+def test_accept_window_sampled_counter_and_picks():
+    """A sampled window keeps the target's own picks (the same rows as a plain call) and advances
+    the slot's counter once."""
+    w = synth.config2_window(2)
+    rows_plain, ctr_plain = oracle.sample_call(w, with_allowed=False)
+    picks = [r["id"] for r in rows_plain]
+    rows, ctr, keep = oracle.verify_call(w, picks[:-1] + [-1])
+    assert [r["id"] for r in rows] == picks
+    assert ctr == ctr_plain == {0: w["counters"][0] + 1}
+    assert keep == {0: w["B"]}
