@@ -201,6 +201,31 @@ int strata_sample_rows(strata_ctx *ctx, const void *logits, int dtype, int B, in
                        uint32_t flags, void *stream);
 
 /*
+ * Sample verify windows and count the rows each slot keeps [P19, "What changed": the emitted
+ * tokens are always the target's own samples, the drafts only fill the verified window; P559,
+ * "Not done (yet)": a sampled row is accepted when its pick equals the draft].  Samples exactly as
+ * strata_sample_rows (same keys, history, counter rule, fused chosen/top-N logprobs; no allowed
+ * subsets or debug outputs) and, in the same launch, compares each row's pick with its draft:
+ *
+ *   row_draft  device int32[B]: the draft placed right after row b's position in its slot's
+ *              window, or -1 for the window's last row.  The rows of a slot, in row order, are
+ *              that slot's window.
+ *   slot_keep  device int32[max_slots]: for every slot named by a row, the number of its rows to
+ *              keep = 1 + the leading rows whose pick equals their draft (a pick of -1 never
+ *              matches).  The entries of slots no row names are not written.
+ *
+ * The count is taken on the device by the last row of each slot to finish (a per-slot arrival
+ * word in the context, cleared by that row), so the call can be captured in a CUDA graph.
+ * Errors as strata_sample_rows; row_draft and slot_keep are required (STRATA_EINVAL).
+ */
+int strata_sample_verify(strata_ctx *ctx, const void *logits, int dtype, int B, int V, int64_t ld,
+                         const int32_t *row_slot, const int64_t *row_pos, const int32_t *row_draft,
+                         const int32_t *hist, const int32_t *hist_off, int n_hist_slots,
+                         int32_t *out_ids, int32_t *slot_keep,
+                         int top_n, float *chosen_lp, int32_t *top_ids, float *top_lps,
+                         uint32_t flags, void *stream);
+
+/*
  * Logprobs without sampling [P3200, "Approach": the head logits before sampling, penalties and
  * temperature; P1916, "What changed"].  Same layouts as above; `chosen` (device int32[B], or
  * NULL) names the id whose log-probability goes to chosen_lp[b] (NaN and STRATA_DEVERR_CHOSEN

@@ -49,7 +49,7 @@ EXPORTED = (
     "strata_version", "strata_last_error", "strata_default_params", "strata_validate_params",
     "strata_create", "strata_destroy", "strata_set_slot_params", "strata_get_slot_state",
     "strata_set_slot_state", "strata_sample_rows", "strata_logprobs_rows", "strata_read_errors",
-    "strata_launch_shape", "strata_sample_rows_noalloc",
+    "strata_launch_shape", "strata_sample_rows_noalloc", "strata_sample_verify",
 )
 
 
@@ -99,6 +99,8 @@ def _load() -> ctypes.CDLL:
         "strata_sample_rows": ([vp, vp, i32, i32, i32, i64, vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp, vp,
                                 vp, vp, vp, u32, vp], i32),
         "strata_logprobs_rows": ([vp, vp, i32, i32, i32, i64, vp, vp, i32, vp, vp, vp, vp, vp, u32, vp], i32),
+        "strata_sample_verify": ([vp, vp, i32, i32, i32, i64, vp, vp, vp, vp, vp, i32, vp, vp, i32, vp, vp, vp, u32,
+                                  vp], i32),
         "strata_read_errors": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], i32),
         "strata_launch_shape": ([vp, i32, i32, i32, i32, i32, u32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
@@ -244,6 +246,22 @@ def strata_sample_rows(ctx, logits, row_slot, row_pos, out_ids, V=None, hist=Non
         _typed(allowed_lps, torch.float32, "allowed_lps"),
         _typed(topk_ids, torch.int32, "topk_ids"), _typed(topk_vals, torch.float32, "topk_vals"),
         _typed(kept, torch.int32, "kept"), int(flags), _stream(stream)))
+
+
+def strata_sample_verify(ctx, logits, row_slot, row_pos, row_draft, out_ids, slot_keep, V=None, hist=None,
+                         hist_off=None, top_n: int = 0, chosen_lp=None, top_ids=None, top_lps=None, flags: int = 0,
+                         stream=None) -> None:
+    import torch
+    ptr, dt, B, V, ld = _logits_args(logits, V)
+    n_hist = 0 if hist_off is None else int(hist_off.numel()) - 1
+    _check(lib.strata_sample_verify(
+        ctx, ptr, dt, B, V, ld,
+        _typed(row_slot, torch.int32, "row_slot"), _typed(row_pos, torch.int64, "row_pos"),
+        _typed(row_draft, torch.int32, "row_draft"),
+        _typed(hist, torch.int32, "hist"), _typed(hist_off, torch.int32, "hist_off"), n_hist,
+        _typed(out_ids, torch.int32, "out_ids"), _typed(slot_keep, torch.int32, "slot_keep"),
+        int(top_n), _typed(chosen_lp, torch.float32, "chosen_lp"), _typed(top_ids, torch.int32, "top_ids"),
+        _typed(top_lps, torch.float32, "top_lps"), int(flags), _stream(stream)))
 
 
 def strata_logprobs_rows(ctx, logits, V=None, chosen=None, chosen_lp=None, top_n: int = 0, top_ids=None,

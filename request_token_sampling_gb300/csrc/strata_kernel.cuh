@@ -119,6 +119,9 @@ struct KParams {
   uint32_t* err;
   int hash_cap, hash_bits;
   uint32_t flags;
+  const int32_t* row_draft;  // verify windows: the draft after each row (-1: none), or NULL
+  int32_t* slot_keep;        // verify windows: rows kept per slot
+  uint32_t* done;            // verify windows: per-slot count of rows done in the current call
 };
 
 struct Layout {
@@ -507,6 +510,45 @@ __device__ __forceinline__ void sort8_desc(uint32_t (&v)[8]) {
   cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
   cx(2, 4); cx(3, 5);
   cx(1, 2); cx(3, 4); cx(5, 6);
+}
+
+// Verify-window acceptance, run by the leader warp of every row of a slot once lane 0 has stored
+// the row's pick.  The row publishes its pick and counts itself done in the slot's arrival word;
+// the last row of the slot to finish reads every pick of the window (rows of the slot in row
+// order), keeps 1 + the leading rows whose pick equals their draft, and clears the word for the
+// next call.  Warp-wide; out of line (only verify calls take it).
+__device__ __noinline__ void accept_window_warp(const int32_t* row_slot, const int32_t* out_ids, const int32_t* row_draft,
+                                                uint32_t* done, int32_t* slot_keep, int B, int slot, int lane) {
+  int r_s = 0;  // rows of this slot in the call
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    r_s += __popc(__ballot_sync(FULL_MASK, b < B && row_slot[b] == slot));
+  }
+  uint32_t last = 0u;
+  if (lane == 0) {
+    __threadfence();  // this row's pick is visible before it counts as done
+    last = (atomicAdd(&done[slot], 1u) + 1u == static_cast<uint32_t>(r_s)) ? 1u : 0u;
+  }
+  if (__shfl_sync(FULL_MASK, last, 0) == 0u) return;
+  __threadfence();  // every other row of the slot was done (and its pick visible) before this one
+  int keep = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    const bool in = b < B && row_slot[b] == slot;
+    const int t = in ? __ldcg(out_ids + b) : -1;
+    const int d = in ? row_draft[b] : -1;
+    const uint32_t m_in = __ballot_sync(FULL_MASK, in);
+    const uint32_t m_stop = __ballot_sync(FULL_MASK, in && (d < 0 || t < 0 || t != d));
+    if (m_stop != 0u) {  // the window ends at the first row whose pick differs from its draft
+      keep += __popc(m_in & ((2u << (__ffs(m_stop) - 1)) - 1u));
+      break;
+    }
+    keep += __popc(m_in);
+  }
+  if (lane == 0) {
+    slot_keep[slot] = keep;
+    done[slot] = 0u;
+  }
 }
 
 // ------------------------------------------------------------------------------ the kernel
@@ -1253,6 +1295,8 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         }
         if (P.chosen_lp != nullptr) P.chosen_lp[row] = (out >= 0) ? chosen_raw - lse : __int_as_float(0x7FC00000);
       }
+      if (P.row_draft != nullptr && valid)
+        accept_window_warp(P.row_slot, P.out_ids, P.row_draft, P.done, P.slot_keep, P.B, slot, lane);
       if (P.topk_ids != nullptr) {
         const long long o = static_cast<long long>(row) * KMAX;
         const bool ia = valid && lane < k_eff, ib = valid && lane + 32 < k_eff;

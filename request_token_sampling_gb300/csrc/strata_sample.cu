@@ -54,6 +54,7 @@ struct strata_ctx {
   int max_smem = 0;
   SlotDev* d_slots = nullptr;
   unsigned long long* d_ctr = nullptr;
+  uint32_t* d_done = nullptr;  // per slot: rows of the current verify call done (reset by the last)
   uint32_t* d_err = nullptr;
   std::vector<strata_sampling_params> h_params;
   std::vector<SlotDev> h_slots;
@@ -323,6 +324,8 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
   if ((e = cudaMalloc(&c->d_slots, sizeof(SlotDev) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc slots: %s", cudaGetErrorString(e)));
   if ((e = cudaMalloc(&c->d_ctr, sizeof(unsigned long long) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc counters: %s", cudaGetErrorString(e)));
   if ((e = cudaMalloc(&c->d_err, sizeof(uint32_t))) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc error word: %s", cudaGetErrorString(e)));
+  if ((e = cudaMalloc(&c->d_done, sizeof(uint32_t) * max_slots)) != cudaSuccess) return cleanup(fail(STRATA_ENOMEM, "cudaMalloc window words: %s", cudaGetErrorString(e)));
+  if ((e = cudaMemset(c->d_done, 0, sizeof(uint32_t) * max_slots)) != cudaSuccess) return cleanup(cuda_fail(e, "window word reset"));
   if ((e = cudaMemcpy(c->d_slots, c->h_slots.data(), sizeof(SlotDev) * max_slots, cudaMemcpyHostToDevice)) != cudaSuccess) return cleanup(cuda_fail(e, "slot table upload"));
   if ((e = cudaMemset(c->d_ctr, 0, sizeof(unsigned long long) * max_slots)) != cudaSuccess) return cleanup(cuda_fail(e, "counter reset"));
   if ((e = cudaMemset(c->d_err, 0, sizeof(uint32_t))) != cudaSuccess) return cleanup(cuda_fail(e, "error word reset"));
@@ -336,6 +339,7 @@ void strata_destroy(strata_ctx* c) {
   cudaDeviceSynchronize();
   cudaFree(c->d_slots);
   cudaFree(c->d_ctr);
+  cudaFree(c->d_done);
   cudaFree(c->d_err);
   delete c;
 }
@@ -423,12 +427,12 @@ int strata_launch_shape(strata_ctx* c, int mode, int dtype, int B, int V, int to
   return STRATA_OK;
 }
 
-int strata_sample_rows(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
-                       const int32_t* row_slot, const int64_t* row_pos, const int32_t* hist,
-                       const int32_t* hist_off, int n_hist_slots, int32_t* out_ids, int top_n, float* chosen_lp,
-                       int32_t* top_ids, float* top_lps, const int32_t* allowed, const int32_t* allowed_off,
-                       float* allowed_lps, int32_t* topk_ids, float* topk_vals, int32_t* kept, uint32_t flags,
-                       void* stream) {
+static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
+                            const int32_t* row_slot, const int64_t* row_pos, const int32_t* row_draft,
+                            const int32_t* hist, const int32_t* hist_off, int n_hist_slots, int32_t* out_ids,
+                            int32_t* slot_keep, int top_n, float* chosen_lp, int32_t* top_ids, float* top_lps,
+                            const int32_t* allowed, const int32_t* allowed_off, float* allowed_lps, int32_t* topk_ids,
+                            float* topk_vals, int32_t* kept, uint32_t flags, void* stream) {
   int rc = check_rows_common(c, logits, dtype, B, V, ld, top_n, chosen_lp, top_ids, top_lps, allowed, allowed_off,
                              allowed_lps);
   if (rc != STRATA_OK) return rc;
@@ -477,7 +481,33 @@ int strata_sample_rows(strata_ctx* c, const void* logits, int dtype, int B, int 
   P.hash_cap = sh.hash_cap;
   P.hash_bits = sh.hash_bits;
   P.flags = flags;
+  P.row_draft = row_draft;
+  P.slot_keep = slot_keep;
+  P.done = c->d_done;
   return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream));
+}
+
+int strata_sample_rows(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
+                       const int32_t* row_slot, const int64_t* row_pos, const int32_t* hist,
+                       const int32_t* hist_off, int n_hist_slots, int32_t* out_ids, int top_n, float* chosen_lp,
+                       int32_t* top_ids, float* top_lps, const int32_t* allowed, const int32_t* allowed_off,
+                       float* allowed_lps, int32_t* topk_ids, float* topk_vals, int32_t* kept, uint32_t flags,
+                       void* stream) {
+  return sample_rows_impl(c, logits, dtype, B, V, ld, row_slot, row_pos, nullptr, hist, hist_off, n_hist_slots, out_ids,
+                          nullptr, top_n, chosen_lp, top_ids, top_lps, allowed, allowed_off, allowed_lps, topk_ids,
+                          topk_vals, kept, flags, stream);
+}
+
+int strata_sample_verify(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
+                         const int32_t* row_slot, const int64_t* row_pos, const int32_t* row_draft,
+                         const int32_t* hist, const int32_t* hist_off, int n_hist_slots, int32_t* out_ids,
+                         int32_t* slot_keep, int top_n, float* chosen_lp, int32_t* top_ids, float* top_lps,
+                         uint32_t flags, void* stream) {
+  if (B > 0 && (row_draft == nullptr || slot_keep == nullptr))
+    return fail(STRATA_EINVAL, "row_draft and slot_keep are required");
+  return sample_rows_impl(c, logits, dtype, B, V, ld, row_slot, row_pos, row_draft, hist, hist_off, n_hist_slots,
+                          out_ids, slot_keep, top_n, chosen_lp, top_ids, top_lps, nullptr, nullptr, nullptr, nullptr,
+                          nullptr, nullptr, flags, stream);
 }
 
 int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,

@@ -9,6 +9,7 @@ class Sampler:
 
     def __init__(self, device: int = 0, max_slots: int = 64, max_vocab: int = 262144, max_rows: int = 1024):
         self.device = device
+        self.max_slots = max_slots
         self.ctx = B.strata_create(device, max_slots, max_vocab, max_rows)
 
     def close(self) -> None:
@@ -63,6 +64,27 @@ class Sampler:
                              top_lps=o.get("top_lps"), allowed=allowed, allowed_off=allowed_off,
                              allowed_lps=o.get("allowed_lps"), topk_ids=o.get("topk_ids"),
                              topk_vals=o.get("topk_vals"), kept=o.get("kept"), flags=flags, stream=stream)
+        return o
+
+    def verify(self, logits, row_slot, row_pos, row_draft, V=None, hist=None, hist_off=None, top_n: int = 0,
+               chosen_lp: bool = False, flags: int = 0, stream=None, out=None) -> dict:
+        """Sample verify windows: the picks plus, per slot, the number of rows to keep."""
+        import torch
+        rows = logits.shape[0]
+        dev = logits.device
+        o = out if out is not None else {}
+        if "ids" not in o:
+            o["ids"] = torch.empty(rows, dtype=torch.int32, device=dev)
+        if "keep" not in o:
+            o["keep"] = torch.full((self.max_slots,), -1, dtype=torch.int32, device=dev)
+        if chosen_lp and "chosen_lp" not in o:
+            o["chosen_lp"] = torch.empty(rows, dtype=torch.float32, device=dev)
+        if top_n > 0 and "top_ids" not in o:
+            o["top_ids"] = torch.empty(rows, top_n, dtype=torch.int32, device=dev)
+            o["top_lps"] = torch.empty(rows, top_n, dtype=torch.float32, device=dev)
+        B.strata_sample_verify(self.ctx, logits, row_slot, row_pos, row_draft, o["ids"], o["keep"], V=V, hist=hist,
+                               hist_off=hist_off, top_n=top_n, chosen_lp=o.get("chosen_lp"),
+                               top_ids=o.get("top_ids"), top_lps=o.get("top_lps"), flags=flags, stream=stream)
         return o
 
     def logprobs(self, logits, V=None, chosen=None, top_n: int = 0, allowed=None, allowed_off=None,
