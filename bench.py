@@ -44,6 +44,9 @@ UNIT = "rows/s"
 WORKLOAD = ("logprobs workload fused with sampling: B=8 fp32 rows x V=248,320, N(0,3^2)+1..5 spikes; "
             "per-row keys top_k=20 T=0.8 top_p=0.95 min_p=0.05 repeat=1.1 freq=0.1 presence=0.1 "
             "penalty_last_n=64; top_logprobs=20, chosen-token logprob, allowed_token_ids of 5/100/1000")
+WORKLOAD_VERIFY = ("verify windows (strata_sample_verify): config 2's 5-row windows (4 drafts + head), 1 slot, "
+                   "fp32 V=248,320, N(0,3^2)+1..5 spikes; keys T=0.7 top_k=20 top_p=0.9 min_p=0.05 repeat=1.1 "
+                   "over a 64-token history; seeded draft ids; kept rows counted in the launch")
 KERNEL_SOURCES = ("request_token_sampling_gb300/csrc/strata_kernel.cuh",   # the device code the
                   "request_token_sampling_gb300/csrc/strata_device.cuh")   # ncu counters describe
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_config4_fused.json")
@@ -72,6 +75,29 @@ def algorithmic_bytes(w) -> int:
     n += len(w["slot_params"]) * (48 + 8 + 4)                                 # slot keys, counter
     n += B * (4 + 4 + w["top_n"] * 8) + 4 * n_allowed                         # outputs
     return n
+
+
+def algorithmic_bytes_verify(w) -> int:
+    """Logits once, the history window, row arrays with drafts, slot keys and counter, picks and
+    the kept count."""
+    B, V = w["B"], w["V"]
+    n = B * V * 4 + 4 * min(w["slot_params"][0]["penalty_last_n"], int(w["hist_off"][1] - w["hist_off"][0]))
+    n += 4 * 2 + B * (4 + 8 + 4) + (48 + 8 + 4) + B * 4 + 4
+    return n
+
+
+def oracle_windows_per_s(w, drafts, budget_s=15.0, max_windows=40):
+    """Time the unmodified oracle on whole verify windows (rows per second)."""
+    import oracle
+    t0 = time.perf_counter()
+    n = 0
+    counters = dict(w["counters"])
+    while True:
+        _, counters, _ = oracle.verify_call(w, drafts, counters=counters)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= max_windows:
+            return n * w["B"] / el, n, el
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -243,7 +269,8 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
-    w = synth.config4(fused=True)
+    verify = args.workload == "verify"
+    w = synth.config2_window(0) if verify else synth.config4(fused=True)
     B = w["B"]
     step_bytes = B * w["V"] * 4
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
@@ -256,10 +283,18 @@ def run_gpu(args, rank, world):
     ten = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     row_slot, row_pos = ten(w["row_slot"]), ten(w["row_pos"])
     hist, hist_off = ten(w["hist"]), ten(w["hist_off"])
-    allowed, allowed_off = ten(w["allowed"]), ten(w["allowed_off"])
+    allowed = allowed_off = None
+    if not verify:
+        allowed, allowed_off = ten(w["allowed"]), ten(w["allowed_off"])
+    drafts = np.random.default_rng(0x5EED0002).integers(0, w["V"], size=B).astype(np.int32)
+    drafts[-1] = -1
+    row_draft = ten(drafts)
     batches = make_batches(w, R, dev)
-    out = s.sample(batches[0], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
-                   chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags)
+    if verify:
+        out = s.verify(batches[0], row_slot, row_pos, row_draft, hist=hist, hist_off=hist_off, flags=flags)
+    else:
+        out = s.sample(batches[0], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
+                       chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags)
     torch.cuda.synchronize()
     if s.errors() != 0:
         raise RuntimeError("device error bits set")
@@ -269,8 +304,12 @@ def run_gpu(args, rank, world):
     stream.wait_stream(torch.cuda.current_stream())
 
     def call(i):
-        s.sample(batches[i % R], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
-                 chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags, stream=stream, out=out)
+        if verify:
+            s.verify(batches[i % R], row_slot, row_pos, row_draft, hist=hist, hist_off=hist_off, flags=flags,
+                     stream=stream, out=out)
+        else:
+            s.sample(batches[i % R], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
+                     chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags, stream=stream, out=out)
 
     # the K timed steps as one CUDA graph (the calls advance the device counters on replay)
     graph = torch.cuda.CUDAGraph()
@@ -323,23 +362,31 @@ def run_gpu(args, rank, world):
     # ---- e2e through the C ABI from pinned host buffers -------------------------------------
     K_e2e = max(3, min(args.steps, 200))
     h_logits = [torch.from_numpy(w["logits"]).pin_memory()]
-    h_small = {k: torch.from_numpy(np.ascontiguousarray(w[k])).pin_memory()
-               for k in ("row_slot", "row_pos", "hist", "hist_off", "allowed", "allowed_off")}
+    small_keys = ("row_slot", "row_pos", "hist", "hist_off") + (() if verify else ("allowed", "allowed_off"))
+    h_small = {k: torch.from_numpy(np.ascontiguousarray(w[k])).pin_memory() for k in small_keys}
+    if verify:
+        h_small["row_draft"] = torch.from_numpy(drafts).pin_memory()
     d_logits = torch.empty_like(batches[0])
     d_small = {k: torch.empty_like(v, device=dev) for k, v in h_small.items()}
     h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
     h2d = int(h_logits[0].numel() * 4 + sum(v.numel() * v.element_size() for v in h_small.values()))
-    d2h = int(sum(v.numel() * v.element_size() for v in out.values()))
+    if verify:  # the picks and the one slot's kept count come back
+        h_out = {"ids": h_out["ids"], "keep": torch.empty(1, dtype=torch.int32, pin_memory=True)}
+    d2h = int(sum(v.numel() * v.element_size() for v in h_out.values()))
 
     def e2e_step():
         d_logits.copy_(h_logits[0], non_blocking=True)
         for k, v in h_small.items():
             d_small[k].copy_(v, non_blocking=True)
-        s.sample(d_logits, d_small["row_slot"], d_small["row_pos"], hist=d_small["hist"],
-                 hist_off=d_small["hist_off"], top_n=w["top_n"], chosen_lp=True, allowed=d_small["allowed"],
-                 allowed_off=d_small["allowed_off"], flags=flags, stream=stream, out=out)
-        for k, v in out.items():
-            h_out[k].copy_(v, non_blocking=True)
+        if verify:
+            s.verify(d_logits, d_small["row_slot"], d_small["row_pos"], d_small["row_draft"], hist=d_small["hist"],
+                     hist_off=d_small["hist_off"], flags=flags, stream=stream, out=out)
+        else:
+            s.sample(d_logits, d_small["row_slot"], d_small["row_pos"], hist=d_small["hist"],
+                     hist_off=d_small["hist_off"], top_n=w["top_n"], chosen_lp=True, allowed=d_small["allowed"],
+                     allowed_off=d_small["allowed_off"], flags=flags, stream=stream, out=out)
+        for k, v in h_out.items():
+            v.copy_(out[k][:v.numel()], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -360,7 +407,7 @@ def run_gpu(args, rank, world):
     if rank != 0:
         s.close()
         return
-    alg = algorithmic_bytes(w)
+    alg = algorithmic_bytes_verify(w) if verify else algorithmic_bytes(w)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
         peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
@@ -370,19 +417,25 @@ def run_gpu(args, rank, world):
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         tj = json.load(open(TRAFFIC_FILE))
-        if tj.get("kernel_hash") == kernel_hash():
+        if tj.get("kernel_hash") == kernel_hash() and not verify:
             traffic = tj.get("dram_bytes_per_launch")
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rps, nrows, el = oracle_rows_per_s(w, budget_s=args.cpu_budget)
-        cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{nrows} rows of the same 8-row workload (fused sample + logprobs + allowed), "
-                         f"{el:.1f} s on 1 host core"}
+        if verify:
+            rps, nwin, el = oracle_windows_per_s(w, drafts.tolist(), budget_s=args.cpu_budget)
+            cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{nwin} whole 5-row windows (sample + acceptance), {el:.1f} s on 1 host core"}
+        else:
+            rps, nrows, el = oracle_rows_per_s(w, budget_s=args.cpu_budget)
+            cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{nrows} rows of the same 8-row workload (fused sample + logprobs + allowed), "
+                             f"{el:.1f} s on 1 host core"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "rows_per_step": B, "V": w["V"], "logits_dtype": "f32",
+        "config": {"workload": WORKLOAD_VERIFY if verify else WORKLOAD, "rows_per_step": B, "V": w["V"],
+                   "logits_dtype": "f32",
                    "l2_policy": f"inputs rotate over {R} distinct batches ({R * step_bytes / 1e6:.0f} MB, "
                                 f"{R * step_bytes / l2:.1f}x the {l2 / 1e6:.0f} MB L2)",
                    "launch": "one CUDA graph of the K calls" + (", programmatic dependent launch" if flags & 1 else "")
@@ -416,6 +469,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--batches", type=int, default=0,
                     help="distinct input batches to rotate over (0: enough for 4x the L2 size)")
+    ap.add_argument("--workload", choices=["fused", "verify"], default="fused",
+                    help="fused: the logprobs workload fused with sampling (the headline); verify: verify windows")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
