@@ -253,11 +253,17 @@ def allowed_renorm(raw32: np.ndarray, allowed) -> np.ndarray:
 # Whole rows
 # -------------------------------------------------------------------------------------------
 
-def sample_row(raw32, p: Params, hist_ids, position: int, counter: int):
+def sample_row(raw32, p: Params, hist_ids, position: int, counter: int, mask_ids=None):
     """One row of the sampled chain (or the greedy argmax); returns a dict of every decision.
 
     Chain order from "#19 ...": penalties over the history window -> top_k (ties to the lowest
     index) -> min_p -> top_p -> temperature -> Philox(seed, position) draw at the slot's counter.
+
+    `mask_ids` (optional): the row's allowed_token_ids used as a sampling mask ("#3200 ...",
+    "Problem and result" names constrained decoding as the client use).  Reading: the chain runs
+    over the named ids only (out-of-range ids are ignored, a repeat counts once); an empty or
+    absent list leaves the row unrestricted; with no named id inside [0, V) the row has no
+    candidate (id -1).
     """
     V = raw32.size
     if penalties_neutral(p) or p.penalty_last_n <= 0 or hist_ids is None:
@@ -265,13 +271,21 @@ def sample_row(raw32, p: Params, hist_ids, position: int, counter: int):
     else:
         counts = history_counts(hist_ids, p.penalty_last_n, V)
     pen = apply_penalties(raw32, counts, p.penalty_repeat, p.penalty_freq, p.penalty_present)
-    order = rank_order(pen)
+    if mask_ids is not None and len(mask_ids) > 0:
+        a = np.asarray(mask_ids, dtype=np.int64)
+        keep = np.unique(a[(a >= 0) & (a < V)])
+        if keep.size == 0:
+            return dict(greedy=p.greedy, flag_top_p=False, flag_draw=False, u=None, id=-1, nocand=True,
+                        topk_ids=np.zeros(0, np.int64), topk_vals=np.zeros(0, np.float32), m1=0, m2=0, j=0)
+        order = keep[rank_order(pen[keep])]
+    else:
+        order = rank_order(pen)
     res = dict(greedy=p.greedy, flag_top_p=False, flag_draw=False, u=None)
     if p.greedy:
         res.update(id=int(order[0]), topk_ids=order[:1].copy(), topk_vals=pen[order[:1]],
                    m1=1, m2=1, j=0)
         return res
-    k = min(p.k, V)
+    k = min(p.k, order.size)
     sel_ids = order[:k]
     sel = pen[sel_ids]
     m1 = min_p_cut(sel, p.min_p)
@@ -317,7 +331,7 @@ def _slot_history(w, s):
     return w["hist"][off[s]:off[s + 1]]
 
 
-def sample_call(w, counters=None, top_n=None, with_allowed=True):
+def sample_call(w, counters=None, top_n=None, with_allowed=True, mask_allowed=False):
     """One batched sampling call over workload dict `w` (see ``synth``); mirrors the library call.
 
     Every row reads its slot's draw counter as it stood before the call; afterwards each slot
@@ -336,7 +350,11 @@ def sample_call(w, counters=None, top_n=None, with_allowed=True):
             rows.append(dict(id=-1, invalid=True))
             continue
         p = Params.from_dict(w["slot_params"][s])
-        r = sample_row(raw, p, _slot_history(w, s), int(w["row_pos"][b]), counters.get(s, 0))
+        mask = None
+        if mask_allowed and w.get("allowed_off") is not None:
+            off = w["allowed_off"]
+            mask = w["allowed"][off[b]:off[b + 1]]
+        r = sample_row(raw, p, _slot_history(w, s), int(w["row_pos"][b]), counters.get(s, 0), mask)
         if not p.greedy:
             sampled_slots.add(s)
         allowed = None

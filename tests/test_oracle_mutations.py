@@ -42,6 +42,8 @@ MUTATIONS = [
     ("sampling.py", "        if not open_[s]:\n            continue\n", ""),
     ("sampling.py", "        keep[s] += 1\n        if d < 0 or t < 0 or t != d:\n            open_[s] = False",
      "        if d < 0 or t < 0 or t != d:\n            open_[s] = False\n        else:\n            keep[s] += 1"),
+    ("sampling.py", "        order = keep[rank_order(pen[keep])]", "        order = rank_order(pen)[:keep.size]"),
+    ("sampling.py", "        keep = np.unique(a[(a >= 0) & (a < V)])", "        keep = np.unique(np.clip(a, 0, V - 1))"),
 ]
 
 

@@ -529,3 +529,50 @@ def test_accept_window_sampled_counter_and_picks():
     assert [r["id"] for r in rows] == picks
     assert ctr == ctr_plain == {0: w["counters"][0] + 1}
     assert keep == {0: w["B"]}
+
+
+# ---- allowed_token_ids as a sampling mask ("#3200 ...", "Problem and result") ----------------
+def _mask_params(**kw):
+    return Params.from_dict(synth.make_params(**kw))
+
+
+def test_mask_restricts_the_chain_to_the_named_ids():
+    rng = np.random.default_rng(5)
+    raw = (rng.standard_normal(500) * 3).astype(np.float32)
+    top = int(np.argmax(raw))
+    mask = [int(i) for i in rng.choice(np.delete(np.arange(500), top), 7, replace=False)]
+    best_allowed = max(mask, key=lambda i: (raw[i], -i))
+    g = oracle.sample_row(raw, _mask_params(temperature=0.0), None, 0, 0, mask)
+    assert g["id"] == best_allowed                       # the greedy pick is the best named id
+    s = oracle.sample_row(raw, _mask_params(temperature=1.3, top_k=64, top_p=1.0), None, 3, 0, mask)
+    assert sorted(s["topk_ids"].tolist()) == sorted(mask)  # top_k larger than the mask: all of it
+    assert s["topk_ids"][0] == best_allowed
+    for c in range(200):
+        r = oracle.sample_row(raw, _mask_params(temperature=2.0, top_k=64, top_p=1.0), None, 3, c, mask)
+        assert r["id"] in mask
+    one = oracle.sample_row(raw, _mask_params(temperature=0.9), None, 0, 0, [mask[3]])
+    assert one["id"] == mask[3] and one["m1"] == one["m2"] == 1
+
+
+def test_mask_edge_readings():
+    rng = np.random.default_rng(6)
+    raw = (rng.standard_normal(300) * 2).astype(np.float32)
+    p = _mask_params(temperature=0.8, top_k=20, top_p=0.9, min_p=0.05, seed=11)
+    plain = oracle.sample_row(raw, p, None, 7, 2)
+    assert oracle.sample_row(raw, p, None, 7, 2, [])["id"] == plain["id"]          # empty: no mask
+    assert oracle.sample_row(raw, p, None, 7, 2, None)["id"] == plain["id"]
+    m = [5, 17, 17, -3, 300, 299, 5]                                               # dups, out of range
+    a = oracle.sample_row(raw, p, None, 7, 2, m)
+    b = oracle.sample_row(raw, p, None, 7, 2, [5, 17, 299])
+    assert a["id"] == b["id"] and a["topk_ids"].tolist() == b["topk_ids"].tolist()
+    none = oracle.sample_row(raw, p, None, 7, 2, [-1, 300, 1000])
+    assert none["id"] == -1 and none.get("nocand")
+
+
+def test_mask_keeps_the_penalties():
+    """A named id in the history window is penalised inside the mask exactly as without it."""
+    raw = np.array([1.0, 4.0, 3.9, -2.0, 0.5], np.float32)
+    p = _mask_params(temperature=0.0, penalty_repeat=2.0, penalty_last_n=8)
+    r = oracle.sample_row(raw, p, np.array([1], np.int32), 0, 0, [1, 2])
+    assert r["id"] == 2                                  # 4.0 / 2 = 2.0 < 3.9
+    assert oracle.sample_row(raw, p, None, 0, 0, [1, 2])["id"] == 1
