@@ -66,6 +66,13 @@ extern "C" {
  * kernel on the stream started (they are not that kernel's output).  The kernel then starts its
  * logit loads before waiting for the previous kernel; slot state is still read after the wait.  */
 #define STRATA_FLAG_EARLY_LOAD  0x2u
+/* strata_sample_rows with allowed/allowed_off: a row that names allowed ids samples only among
+ * them (allowed_token_ids as a sampling mask for constrained decoding [P3200, "Problem and result"
+ * names the client use]): penalties, top_k, min_p, top_p, temperature and the draw run over the
+ * named ids (a repeat counts once, ids outside [0, V) are ignored).  A row with an empty list is
+ * not restricted; a row whose ids are all outside [0, V) gets id -1 and STRATA_DEVERR_NOCAND.
+ * The log-probability outputs still describe the row's full raw distribution.                  */
+#define STRATA_FLAG_ALLOWED_MASK 0x4u
 /* Testing aid: force the number of thread blocks (1..16) that split each row; 0 = automatic.   */
 #define STRATA_FLAG_SPLIT(n)    (((uint32_t)(n) & 0x1Fu) << 8)
 

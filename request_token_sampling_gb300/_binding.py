@@ -31,6 +31,7 @@ STRATA_NOALLOC_MAX_ROWS = 1024
 
 STRATA_FLAG_PDL = 0x1
 STRATA_FLAG_EARLY_LOAD = 0x2
+STRATA_FLAG_ALLOWED_MASK = 0x4
 
 
 def STRATA_FLAG_SPLIT(n: int) -> int:

@@ -125,7 +125,7 @@ struct KParams {
 };
 
 struct Layout {
-  uint32_t data, mbar, abits, hash, hflag, wmax, red, ctl, xrec;
+  uint32_t data, mbar, abits, mbits, hash, hflag, wmax, red, ctl, xrec;
   uint32_t cand_pen, cand_raw, recv_cnt, recv_pkey, recv_praw, recv_raw, sorted_pen, sorted_raw, total;
 };
 
@@ -133,7 +133,7 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 
 // Shared-memory layout of one CTA; identical in every CTA of a launch.
 __host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, int cs, int kmax,
-                                              int nmax) {
+                                              int nmax, bool mask = false) {
   Layout L;
   uint32_t o = 0;
   L.data = o;
@@ -143,6 +143,8 @@ __host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, 
   const uint32_t bw = align_up((static_cast<uint32_t>(chunk) + 31) / 32 * 4, 16);
   L.abits = o;
   o += bw;
+  L.mbits = o;  // allowed ids already in a masked row's top_k list (mask launches only)
+  o += mask ? bw : 0u;
   L.hash = o;
   o += align_up(static_cast<uint32_t>(hash_cap) * 4, 16);
   L.hflag = o;
@@ -179,7 +181,7 @@ __host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, 
 
 // Every region starts on a 16-byte boundary (vector and bulk accesses rely on it).
 __host__ __device__ inline bool layout_aligned(const Layout& L) {
-  const uint32_t r[] = {L.data, L.mbar, L.abits, L.hash, L.hflag, L.wmax, L.red, L.ctl, L.xrec, L.cand_pen,
+  const uint32_t r[] = {L.data, L.mbar, L.abits, L.mbits, L.hash, L.hflag, L.wmax, L.red, L.ctl, L.xrec, L.cand_pen,
                         L.cand_raw, L.recv_cnt, L.recv_pkey, L.recv_praw, L.recv_raw, L.sorted_pen, L.sorted_raw};
   for (uint32_t x : r)
     if (x % 16u != 0u) return false;
@@ -372,6 +374,34 @@ __device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_
   }
 }
 
+// A masked row's top_k candidates: each of this thread's named ids inside the chunk, the first
+// time any thread meets it (`mbits`), with its penalised value.  Out of line (mask launches only).
+template <int DT>
+__device__ __noinline__ void masked_candidates(const unsigned char* data, int lo, int hi, int a0, int a1, int a2,
+                                               int a3, const int32_t* allowed, int j_first, int a_end,
+                                               uint32_t* mbits, bool penal, const uint32_t* htab, int hash_bits,
+                                               float rep, float freq, float pres, uint32_t* ctl, uint4* cand_pen) {
+  auto add = [&](int id) {
+    if (id < lo || id >= hi) return;
+    const uint32_t loc = static_cast<uint32_t>(id - lo);
+    const uint32_t bit = 1u << (loc & 31);
+    if (atomicOr(&mbits[loc >> 5], bit) & bit) return;
+    const float raw = elem_at<DT>(data, loc);
+    const uint32_t c = penal ? hash_count(htab, hash_bits, loc) : 0u;
+    const uint32_t op = order_key(c != 0u ? penalize(raw, c, rep, freq, pres) : raw);
+    if (op == 0u) return;
+    const uint32_t s = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
+    const uint64_t key = sel_key(op, static_cast<uint32_t>(id));
+    if (s < LOCAL_CAP)
+      cand_pen[s] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
+  };
+  add(a0);
+  add(a1);
+  add(a2);
+  add(a3);
+  for (int j = j_first; j < a_end; j += NT) add(allowed[j]);
+}
+
 // Block-wide max of a 64-bit key (all threads call; result in every thread).
 __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int lane, int wid) {
   x = warp_max_u64(x);
@@ -387,12 +417,13 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int
 // Exact argmax rounds over this CTA's chunk: the `need` largest keys in order (penalised values
 // for list 0, raw values for list 1), written to the candidate buffer.  Only taken when more
 // candidates reach the row threshold than the buffer holds (heavy ties); kept out of line so the
-// common path stays small.  Every thread of the CTA calls it.  Returns the number found.
-template <int DT>
+// common path stays small.  `member` (list 0 of a masked row) restricts the rounds to the ids whose
+// bit is set.  Every thread of the CTA calls it.  Returns the number found.
+template <int DT, bool MEMBER>
 __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, int n_el, int lo, int list, int need,
                                          bool penal, const uint32_t* htab, int hash_bits,
                                          float rep, float freq, float pres, uint64_t* red64, uint4* cand_pen,
-                                         uint64_t* cand_raw) {
+                                         uint64_t* cand_raw, const uint32_t* member) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   uint64_t prev = ~0ull;
@@ -406,6 +437,7 @@ __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, i
       for (int e = 0; e < EPV; ++e) {
         const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
         if (loc >= static_cast<uint32_t>(n_el)) continue;
+        if (MEMBER && list == 0 && member != nullptr && !bit_at(member, loc)) continue;  // masked row: named ids
         float pv = x[e];
         if (list == 0 && penal) {
           const uint32_t c = hash_count(htab, hash_bits, loc);
@@ -512,6 +544,21 @@ __device__ __forceinline__ void sort8_desc(uint32_t (&v)[8]) {
   cx(1, 2); cx(3, 4); cx(5, 6);
 }
 
+// The end of a sampled row's arrival on its slot's packed counter word (warp-wide, the leader's
+// warp 0; lane 0 holds the value its arrival atomic returned): the row that completes the call's
+// arrivals for the slot advances the counter by one and clears them.  r_s counts the call's rows of
+// the slot (the first 64 row slots were fetched ahead into rs0/rs1).
+__device__ __noinline__ void slot_arrival_done(int rs0, int rs1, const int32_t* row_slot, int B, int slot,
+                                               unsigned long long* ctr, unsigned long long ctr_old, int lane) {
+  int r_s = __popc(__ballot_sync(FULL_MASK, rs0 == slot)) + __popc(__ballot_sync(FULL_MASK, rs1 == slot));
+  for (int b0 = 64; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    r_s += __popc(__ballot_sync(FULL_MASK, b < B && row_slot[b] == slot));
+  }
+  if (lane == 0 && (ctr_old & 0xFFFFull) + 1ull == static_cast<unsigned long long>(r_s))
+    atomicAdd(&ctr[slot], (1ull << 16) - static_cast<unsigned long long>(r_s));
+}
+
 // Verify-window acceptance, run by the leader warp of every row of a slot once lane 0 has stored
 // the row's pick.  The row publishes its pick and counts itself done in the slot's arrival word;
 // the last row of the slot to finish reads every pick of the window (rows of the slot in row
@@ -552,7 +599,9 @@ __device__ __noinline__ void accept_window_warp(const int32_t* row_slot, const i
 }
 
 // ------------------------------------------------------------------------------ the kernel
-template <int DT>
+// DT: 0 fp32 rows, 1 bf16 rows.  MASK: allowed ids restrict the sampling (STRATA_FLAG_ALLOWED_MASK);
+// a separate instantiation so that plain launches carry none of its state.
+template <int DT, bool MASK>
 __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char sm[];
   constexpr int ESZ = DT == 0 ? 4 : 2;
@@ -564,7 +613,8 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const uint32_t crank = cluster_ctarank();
   const int cs = P.cs;
   const int row = blockIdx.x / cs;
-  const Layout L = make_layout(P.chunk, ESZ, P.hash_cap, cs, P.kmax, P.nmax);
+  const bool mask_launch = MASK && P.mode == MODE_SAMPLE && P.allowed_off != nullptr;
+  const Layout L = make_layout(P.chunk, ESZ, P.hash_cap, cs, P.kmax, P.nmax, mask_launch);
   const int lo = static_cast<int>(crank) * P.chunk;
   const int hi = min(P.V, lo + P.chunk);
   const int n_el = max(0, hi - lo);
@@ -618,6 +668,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 
 
   uint32_t* abits = reinterpret_cast<uint32_t*>(sm + L.abits);
+  uint32_t* mbits = reinterpret_cast<uint32_t*>(sm + L.mbits);
   uint32_t* htab = reinterpret_cast<uint32_t*>(sm + L.hash);
   uint32_t* hflag = reinterpret_cast<uint32_t*>(sm + L.hflag);
   uint32_t* wmax = reinterpret_cast<uint32_t*>(sm + L.wmax);
@@ -658,6 +709,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const int bw_words = (P.chunk + 31) >> 5;
   for (int i = tid; i < bw_words; i += NT) {
     abits[i] = 0u;
+    if (mask_launch) mbits[i] = 0u;
   }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
   if (tid < NT / 32) hflag[tid] = 0u;
@@ -882,7 +934,10 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     // T as a float threshold (x >= Tf exactly when order_key(x) >= T, NaN never); T = 0 is no bound
     const float Tf = T == 0u ? -INFINITY : key_value(T);
     const bool own_hist = penal && ((hflag[tid >> 5] >> (tid & 31)) & 1u);  // only then can a hit be a history id
-    if (kall != 0u && kall >= T) {
+    // a masked row's top_k list holds exactly its named ids (below); T still serves the raw list
+    const bool masked = mask_launch && a_end > a_beg && k_row > 0;
+    const bool pen_from_t = k_row > 0 && !masked;
+    if (kall != 0u && kall >= T && (n_row > 0 || pen_from_t)) {
       constexpr int RB = BATCH_VECS<DT>;
       if (order_key(mx2) < T) {
         // every element at or above T sits in the batch that holds the max: scan its 16 elements
@@ -909,12 +964,11 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
           const uint32_t o = order_key(xv);
           if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (own_hist && hash_count(htab, P.hash_bits, loc) != 0u))
             continue;
-          append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0, k_row > 0);
+          append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0, pen_from_t);
         }
       } else {
         rescan_candidates<DT>(data, tid, n_vec, n_vec, n_el, lo, Tf, own_hist, htab, P.hash_bits, ctl, cand_pen, cand_raw,
-                              n_row > 0,
-                              k_row > 0);
+                              n_row > 0, pen_from_t);
       }
     }
     if (penal) {  // penalised ids: raw value for the raw list, penalised value for the other
@@ -932,7 +986,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         }
         const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
         const uint32_t op = order_key(pv);
-        if (op != 0u && op >= T && k_row > 0) {
+        if (op != 0u && op >= T && pen_from_t) {
           const uint32_t s = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
           const uint64_t key = sel_key(op, id);
           if (s < LOCAL_CAP)
@@ -940,6 +994,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         }
       }
     }
+    if (masked)  // every named id of this chunk once, with its penalised value
+      masked_candidates<DT>(data, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + threadIdx.x + APRE * NT,
+                            a_end, mbits, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, ctl, cand_pen);
     __syncthreads();
 
     int np = static_cast<int>(ctl[CTL_CAND_PEN]);
@@ -947,11 +1004,11 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     // more candidates than the buffer holds (heavy ties): exact argmax rounds write the chunk's
     // best k_row / n_row in order into the candidate buffers
     if (k_row > 0 && np > LOCAL_CAP)
-      np = exact_rounds<DT>(data, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
-                            red64, cand_pen, cand_raw);
+      np = exact_rounds<DT, MASK>(data, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+                                  red64, cand_pen, cand_raw, MASK && masked ? abits : nullptr);
     if (n_row > 0 && nr > LOCAL_CAP)
-      nr = exact_rounds<DT>(data, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
-                            red64, cand_pen, cand_raw);
+      nr = exact_rounds<DT, false>(data, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq,
+                                   sp.pres, red64, cand_pen, cand_raw, nullptr);
     if (k_row == 0) np = 0;
     if (n_row == 0) nr = 0;
 
@@ -1253,20 +1310,14 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         if (lane == 0) atomicOr(P.err, STRATA_DEVERR_SLOT);
       } else if (k_eff == 0) {
         if (lane == 0) atomicOr(P.err, STRATA_DEVERR_NOCAND);
+        // a sampled row without a candidate still counted itself among its slot's arrivals
+        if (sampled) slot_arrival_done(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, P.ctr, ctr_old, lane);
       } else {
         int j = 0;
         if (sampled) {
           uint32_t x0 = 0u;
-          int r_s = __popc(__ballot_sync(FULL_MASK, rs_pre[0] == slot)) + __popc(__ballot_sync(FULL_MASK, rs_pre[1] == slot));
-          for (int b0 = 64; b0 < P.B; b0 += 32) {
-            const int b = b0 + lane;
-            r_s += __popc(__ballot_sync(FULL_MASK, b < P.B && P.row_slot[b] == slot));
-          }
-          if (ctr_thread) {
-            if ((ctr_old & 0xFFFFull) + 1ull == static_cast<unsigned long long>(r_s))
-              atomicAdd(&P.ctr[slot], (1ull << 16) - static_cast<unsigned long long>(r_s));
-            x0 = philox_word0(sp.seed, pos, ctr_old >> 16);
-          }
+          slot_arrival_done(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, P.ctr, ctr_old, lane);
+          if (ctr_thread) x0 = philox_word0(sp.seed, pos, ctr_old >> 16);
           x0 = __shfl_sync(FULL_MASK, x0, 0);
           const float u = static_cast<float>(x0 >> 8) * 0x1p-24f;
           const int last = m2 - 1;  // the draw reads prefixes below m2 only; W = C[m2 - 1]

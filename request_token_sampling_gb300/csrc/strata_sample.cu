@@ -151,7 +151,8 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
       s->hash_cap = 1 << bits;
     }
   }
-  const Layout L = strata::make_layout(chunk, esz, s->hash_cap, cs, s->kmax, s->nmax);
+  const Layout L = strata::make_layout(chunk, esz, s->hash_cap, cs, s->kmax, s->nmax,
+                                       mode == strata::MODE_SAMPLE && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u);
   if (!strata::layout_aligned(L)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
   s->smem = static_cast<int>(L.total);
   if (s->smem > c->max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit %d", s->smem, c->max_smem);
@@ -179,10 +180,11 @@ int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t
   cfg.attrs = attrs;
   cfg.numAttrs = na;
   cudaError_t e;
+  const bool mask = P.mode == strata::MODE_SAMPLE && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u && P.allowed_off != nullptr;
   if (dtype == STRATA_DTYPE_F32)
-    e = cudaLaunchKernelEx(&cfg, strata::rows_kernel<0>, P);
+    e = mask ? cudaLaunchKernelEx(&cfg, strata::rows_kernel<0, true>, P) : cudaLaunchKernelEx(&cfg, strata::rows_kernel<0, false>, P);
   else
-    e = cudaLaunchKernelEx(&cfg, strata::rows_kernel<1>, P);
+    e = mask ? cudaLaunchKernelEx(&cfg, strata::rows_kernel<1, true>, P) : cudaLaunchKernelEx(&cfg, strata::rows_kernel<1, false>, P);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   (void)c;
   return STRATA_OK;
@@ -284,8 +286,10 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
     strata_destroy(c);
     return code;
   };
-  const void* kernels[2] = {reinterpret_cast<const void*>(strata::rows_kernel<0>),
-                            reinterpret_cast<const void*>(strata::rows_kernel<1>)};
+  const void* kernels[4] = {reinterpret_cast<const void*>(strata::rows_kernel<0, false>),
+                            reinterpret_cast<const void*>(strata::rows_kernel<1, false>),
+                            reinterpret_cast<const void*>(strata::rows_kernel<0, true>),
+                            reinterpret_cast<const void*>(strata::rows_kernel<1, true>)};
   for (const void* k : kernels) {
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->max_smem)) != cudaSuccess)
       return cleanup(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
@@ -307,7 +311,7 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
     cfg.attrs = &a;
     cfg.numAttrs = 1;
     int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, strata::rows_kernel<0>, &cfg) == cudaSuccess && nclusters > 0)
+    if (cudaOccupancyMaxActiveClusters(&nclusters, strata::rows_kernel<0, false>, &cfg) == cudaSuccess && nclusters > 0)
       c->max_cluster = strata::MAX_CS;
     cudaGetLastError();
   }
@@ -599,8 +603,8 @@ int noalloc_setup(int dev, NoallocDevice** out) {
     if (prop.major < 10) return fail(STRATA_ECUDA, "device %s is not a Blackwell GPU", prop.name);
     d.num_sms = prop.multiProcessorCount;
     d.max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
-    const void* kernels[2] = {reinterpret_cast<const void*>(strata::rows_kernel<0>),
-                              reinterpret_cast<const void*>(strata::rows_kernel<1>)};
+    const void* kernels[2] = {reinterpret_cast<const void*>(strata::rows_kernel<0, false>),
+                              reinterpret_cast<const void*>(strata::rows_kernel<1, false>)};
     for (const void* k : kernels) {
       if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(smem)");
@@ -620,7 +624,7 @@ int noalloc_setup(int dev, NoallocDevice** out) {
     cfg.attrs = &a;
     cfg.numAttrs = 1;
     int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, strata::rows_kernel<0>, &cfg) == cudaSuccess && nclusters > 0)
+    if (cudaOccupancyMaxActiveClusters(&nclusters, strata::rows_kernel<0, false>, &cfg) == cudaSuccess && nclusters > 0)
       d.max_cluster = strata::MAX_CS;
     cudaGetLastError();
     static int32_t identity[NA_MAX_ROWS];

@@ -120,7 +120,9 @@ def compare_sample(w, rows, g, top_n=None, stats=None, debug=True):
         else:
             assert gid == r["id"], f"row {b}: sampled id {gid} vs oracle {r['id']}"
         lp_all = None
-        if "chosen_lp" in g:
+        if "chosen_lp" in g and gid < 0:
+            assert np.isnan(g["chosen_lp"][b]), f"row {b}: a row without a pick has a NaN chosen lp"
+        elif "chosen_lp" in g:
             lp_all = oracle.log_softmax(raw)
             d = stats.lp([g["chosen_lp"][b]], [lp_all[gid]])
             assert d.max() <= LP_TOL, f"row {b}: chosen lp off by {d.max()}"
