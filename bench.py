@@ -47,6 +47,7 @@ WORKLOAD = ("logprobs workload fused with sampling: B=8 fp32 rows x V=248,320, N
 WORKLOAD_VERIFY = ("verify windows (strata_sample_verify): config 2's 5-row windows (4 drafts + head), 1 slot, "
                    "fp32 V=248,320, N(0,3^2)+1..5 spikes; keys T=0.7 top_k=20 top_p=0.9 min_p=0.05 repeat=1.1 "
                    "over a 64-token history; seeded draft ids; kept rows counted in the launch")
+WORKLOAD_MASK = WORKLOAD + "; the allowed ids used as a sampling mask (STRATA_FLAG_ALLOWED_MASK)"
 KERNEL_SOURCES = ("request_token_sampling_gb300/csrc/strata_kernel.cuh",   # the device code the
                   "request_token_sampling_gb300/csrc/strata_device.cuh")   # ncu counters describe
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_config4_fused.json")
@@ -182,7 +183,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ CPU oracle timing
-def oracle_rows_per_s(w, budget_s=15.0, max_rows=400):
+def oracle_rows_per_s(w, budget_s=15.0, max_rows=400, mask=False):
     """Time the unmodified oracle on rows of the workload (fused sample + logprobs + allowed)."""
     import oracle
     t0 = time.perf_counter()
@@ -198,7 +199,7 @@ def oracle_rows_per_s(w, budget_s=15.0, max_rows=400):
         off = w["allowed_off"]
         wb["allowed"] = w["allowed"][off[b]:off[b + 1]]
         wb["allowed_off"] = np.array([0, off[b + 1] - off[b]], np.int32)
-        _, counters = oracle.sample_call(wb, counters=counters)
+        _, counters = oracle.sample_call(wb, counters=counters, mask_allowed=mask)
         rows += 1
         el = time.perf_counter() - t0
         if el >= budget_s or rows >= max_rows:
@@ -263,7 +264,7 @@ def make_batches(w, R, dev):
 def run_gpu(args, rank, world):
     import torch
     import torch.distributed as dist
-    from request_token_sampling_gb300 import STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL, Sampler
+    from request_token_sampling_gb300 import STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL, Sampler
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -276,6 +277,8 @@ def run_gpu(args, rank, world):
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     R = max(2, -(-4 * l2 // step_bytes)) if args.batches <= 0 else args.batches
     flags = 0 if args.no_pdl else (STRATA_FLAG_PDL | (0 if args.no_early_load else STRATA_FLAG_EARLY_LOAD))
+    if args.workload == "mask":
+        flags |= STRATA_FLAG_ALLOWED_MASK
 
     s = Sampler(device=local, max_slots=16, max_vocab=w["V"], max_rows=B)
     for slot, p in w["slot_params"].items():
@@ -417,7 +420,7 @@ def run_gpu(args, rank, world):
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         tj = json.load(open(TRAFFIC_FILE))
-        if tj.get("kernel_hash") == kernel_hash() and not verify:
+        if tj.get("kernel_hash") == kernel_hash() and args.workload == "fused":
             traffic = tj.get("dram_bytes_per_launch")
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -426,7 +429,7 @@ def run_gpu(args, rank, world):
             cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{nwin} whole 5-row windows (sample + acceptance), {el:.1f} s on 1 host core"}
         else:
-            rps, nrows, el = oracle_rows_per_s(w, budget_s=args.cpu_budget)
+            rps, nrows, el = oracle_rows_per_s(w, budget_s=args.cpu_budget, mask=args.workload == "mask")
             cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{nrows} rows of the same 8-row workload (fused sample + logprobs + allowed), "
                              f"{el:.1f} s on 1 host core"}
@@ -434,7 +437,8 @@ def run_gpu(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_VERIFY if verify else WORKLOAD, "rows_per_step": B, "V": w["V"],
+        "config": {"workload": {"verify": WORKLOAD_VERIFY, "mask": WORKLOAD_MASK}.get(args.workload, WORKLOAD),
+                   "rows_per_step": B, "V": w["V"],
                    "logits_dtype": "f32",
                    "l2_policy": f"inputs rotate over {R} distinct batches ({R * step_bytes / 1e6:.0f} MB, "
                                 f"{R * step_bytes / l2:.1f}x the {l2 / 1e6:.0f} MB L2)",
@@ -469,8 +473,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--batches", type=int, default=0,
                     help="distinct input batches to rotate over (0: enough for 4x the L2 size)")
-    ap.add_argument("--workload", choices=["fused", "verify"], default="fused",
-                    help="fused: the logprobs workload fused with sampling (the headline); verify: verify windows")
+    ap.add_argument("--workload", choices=["fused", "verify", "mask"], default="fused",
+                    help="fused: the logprobs workload fused with sampling (the headline); verify: verify "
+                         "windows; mask: the fused workload with its allowed ids as a sampling mask")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -403,6 +403,52 @@ __device__ __noinline__ void masked_candidates(const unsigned char* data, int lo
 }
 
 // Block-wide max of a 64-bit key (all threads call; result in every thread).
+__device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int lane, int wid);
+
+// A masked row's top_k list when its named ids overflow the candidate buffer: `need` argmax
+// rounds over the named ids only (each thread's own ids, as in masked_candidates), in order, into
+// the candidate buffer.  Every thread of the CTA calls it; returns the number found.
+template <int DT>
+__device__ __noinline__ int masked_rounds(const unsigned char* data, int lo, int hi, int a0, int a1, int a2, int a3,
+                                          const int32_t* allowed, int j_first, int a_end, int need, bool penal,
+                                          const uint32_t* htab, int hash_bits, float rep, float freq, float pres,
+                                          uint64_t* red64, uint4* cand_pen) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  auto key_of = [&](int id) -> uint64_t {
+    if (id < lo || id >= hi) return 0ull;
+    const uint32_t loc = static_cast<uint32_t>(id - lo);
+    const float raw = elem_at<DT>(data, loc);
+    const uint32_t c = penal ? hash_count(htab, hash_bits, loc) : 0u;
+    const uint32_t op = order_key(c != 0u ? penalize(raw, c, rep, freq, pres) : raw);
+    return op == 0u ? 0ull : sel_key(op, static_cast<uint32_t>(id));
+  };
+  uint64_t prev = ~0ull;
+  int got = 0;
+  for (int r = 0; r < need; ++r) {
+    uint64_t best = 0ull;
+    auto consider = [&](int id) {
+      const uint64_t k = key_of(id);
+      if (k < prev && k > best) best = k;  // repeats of an id give the same key: taken once
+    };
+    consider(a0);
+    consider(a1);
+    consider(a2);
+    consider(a3);
+    for (int j = j_first; j < a_end; j += NT) consider(allowed[j]);
+    best = block_max_u64(best, red64, lane, wid);
+    if (best == 0ull) break;
+    if (threadIdx.x == 0) {
+      const float raw = elem_at<DT>(data, key_id(best) - static_cast<uint32_t>(lo));
+      cand_pen[r] = make_uint4(static_cast<uint32_t>(best), static_cast<uint32_t>(best >> 32), __float_as_uint(raw), 0u);
+    }
+    prev = best;
+    got = r + 1;
+  }
+  __syncthreads();
+  return got;
+}
+
+// Block-wide max of a 64-bit key (all threads call; result in every thread).
 __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int lane, int wid) {
   x = warp_max_u64(x);
   __syncthreads();
@@ -417,13 +463,12 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int
 // Exact argmax rounds over this CTA's chunk: the `need` largest keys in order (penalised values
 // for list 0, raw values for list 1), written to the candidate buffer.  Only taken when more
 // candidates reach the row threshold than the buffer holds (heavy ties); kept out of line so the
-// common path stays small.  `member` (list 0 of a masked row) restricts the rounds to the ids whose
-// bit is set.  Every thread of the CTA calls it.  Returns the number found.
-template <int DT, bool MEMBER>
+// common path stays small.  Every thread of the CTA calls it.  Returns the number found.
+template <int DT>
 __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, int n_el, int lo, int list, int need,
                                          bool penal, const uint32_t* htab, int hash_bits,
                                          float rep, float freq, float pres, uint64_t* red64, uint4* cand_pen,
-                                         uint64_t* cand_raw, const uint32_t* member) {
+                                         uint64_t* cand_raw) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   uint64_t prev = ~0ull;
@@ -437,7 +482,6 @@ __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, i
       for (int e = 0; e < EPV; ++e) {
         const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
         if (loc >= static_cast<uint32_t>(n_el)) continue;
-        if (MEMBER && list == 0 && member != nullptr && !bit_at(member, loc)) continue;  // masked row: named ids
         float pv = x[e];
         if (list == 0 && penal) {
           const uint32_t c = hash_count(htab, hash_bits, loc);
@@ -1003,12 +1047,17 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     int nr = static_cast<int>(ctl[CTL_CAND_RAW]);
     // more candidates than the buffer holds (heavy ties): exact argmax rounds write the chunk's
     // best k_row / n_row in order into the candidate buffers
-    if (k_row > 0 && np > LOCAL_CAP)
-      np = exact_rounds<DT, MASK>(data, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
-                                  red64, cand_pen, cand_raw, MASK && masked ? abits : nullptr);
+    if (k_row > 0 && np > LOCAL_CAP) {
+      if (MASK && masked)
+        np = masked_rounds<DT>(data, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + tid + APRE * NT, a_end,
+                               k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, red64, cand_pen);
+      else
+        np = exact_rounds<DT>(data, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+                              red64, cand_pen, cand_raw);
+    }
     if (n_row > 0 && nr > LOCAL_CAP)
-      nr = exact_rounds<DT, false>(data, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq,
-                                   sp.pres, red64, cand_pen, cand_raw, nullptr);
+      nr = exact_rounds<DT>(data, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+                            red64, cand_pen, cand_raw);
     if (k_row == 0) np = 0;
     if (n_row == 0) nr = 0;
 
