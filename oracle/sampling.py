@@ -415,3 +415,65 @@ def verify_call(w, row_draft, counters=None, top_n=None):
     rows, counters = sample_call(w, counters=counters, top_n=top_n, with_allowed=False)
     keep = accept_window(w["row_slot"], [r["id"] for r in rows], row_draft)
     return rows, counters, keep
+
+
+# -------------------------------------------------------------------------------------------
+# Per-slot histories kept between calls (the history-ring variant of the calls above)
+# -------------------------------------------------------------------------------------------
+
+HISTORY_RING_CAP = 4096   # ids a slot keeps: the largest penalty window ("#19 ...": penalty_last_n)
+
+
+def _with_histories(w, state):
+    """Workload `w` with each slot's penalty window taken from `state` ({slot: list of ids})."""
+    slots = sorted(set(int(s) for s in w["row_slot"]) | set(int(s) for s in state))
+    n = (max(slots) + 1) if slots else 0
+    lists = [np.asarray(state.get(s, []), dtype=np.int32) for s in range(n)]
+    off = np.zeros(n + 1, dtype=np.int32)
+    for s, a in enumerate(lists):
+        off[s + 1] = off[s] + a.size
+    w2 = dict(w)
+    w2["hist"] = np.concatenate(lists).astype(np.int32) if n else np.zeros(0, np.int32)
+    w2["hist_off"] = off
+    w2["n_hist_slots"] = n
+    return w2
+
+
+def history_call(w, state, counters=None, top_n=None, row_draft=None, mask_allowed=False):
+    """One sampling call (a verify call when `row_draft` is given) whose penalty windows come from
+    the slots' own run histories, followed by the history update.
+
+    "#19 ...", "min_p and the penalties": before every window the serve loop hands the sampler the
+    request's last penalty_last_n tokens, the consumed tail plus the fed-back head.  Kept on the
+    device instead, each slot's history is its run so far: every row of the call counts over the
+    same window, the last min(penalty_last_n, length) ids as they stood before the call; after it
+    the slot's history grows by its rows' picks in row order (a verify call appends only the kept
+    rows, "#19 ...", "What changed": the emitted tokens are the target's own samples), and a pick of
+    -1 (no candidate, an out-of-range slot) appends nothing.  `state` is {slot: list of ids} and is
+    not modified.  Returns (rows, new_counters, new_state, keep) with keep None for a plain call.
+    """
+    w2 = _with_histories(w, state)
+    if row_draft is None:
+        rows, counters = sample_call(w2, counters=counters, top_n=top_n, mask_allowed=mask_allowed)
+        keep = None
+    else:
+        rows, counters, keep = verify_call(w2, row_draft, counters=counters, top_n=top_n)
+    new = {s: list(v) for s, v in state.items()}
+    taken = {}
+    for b, r in enumerate(rows):
+        s = int(w["row_slot"][b])
+        if r.get("invalid"):
+            continue
+        taken[s] = taken.get(s, 0) + 1
+        if keep is not None and taken[s] > keep[s]:
+            continue
+        if int(r["id"]) >= 0:
+            new.setdefault(s, []).append(int(r["id"]))
+    return rows, counters, new, keep
+
+
+def history_tail(state, slot, max_n=HISTORY_RING_CAP):
+    """What a slot's history read returns: (the last min(length, capacity, max_n) ids, length)."""
+    h = list(state.get(slot, []))
+    m = min(len(h), HISTORY_RING_CAP, max(0, int(max_n)))
+    return np.asarray(h[len(h) - m:], dtype=np.int32), len(h)

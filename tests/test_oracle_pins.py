@@ -576,3 +576,113 @@ def test_mask_keeps_the_penalties():
     r = oracle.sample_row(raw, p, np.array([1], np.int32), 0, 0, [1, 2])
     assert r["id"] == 2                                  # 4.0 / 2 = 2.0 < 3.9
     assert oracle.sample_row(raw, p, None, 0, 0, [1, 2])["id"] == 1
+
+
+# ---- per-slot histories kept between calls ("#19 ...", "min_p and the penalties") -------------
+def _hw(rows, row_slot, params, pos=None):
+    rows = np.asarray(rows, np.float32)
+    pos = list(range(len(row_slot))) if pos is None else pos
+    return synth._workload("ring_hand", "f32", rows.shape[1], rows, params, row_slot, pos, [], 0)
+
+
+def _greedy_steps(raw, p, n):
+    w = _hw([raw], [0], {0: p})
+    state, ids = {}, []
+    for _ in range(n):
+        rows, _, state, keep = oracle.history_call(w, state)
+        assert keep is None
+        ids.append(rows[0]["id"])
+    return ids, state
+
+
+def test_history_hand_sequences():
+    """Greedy decode of one fixed row, its picks fed back through the slot's history.
+
+    repeat 2, freq 1 over a window of 8 (worked by hand): step 1 takes id 1 (4.0); step 2 sees
+    id 1 at 4.0/2 - 1 = 1.0 and takes id 2 (3.9); step 3 sees 1.0 (id 1), 0.95 (id 2) and the
+    untouched 1.0 of id 0, a tie that goes to the lower index, id 0; step 4: id 0 drops to
+    1.0/2 - 1 = -0.5, id 1 is best at 1.0; step 5: id 1 counted twice, 2.0 - 2 = 0.0, id 2 at 0.95.
+    A window of one id alternates the two best ids."""
+    raw = [1.0, 4.0, 3.9, -2.0, 0.5]
+    p = synth.make_params(temperature=0.0, penalty_repeat=2.0, penalty_freq=1.0, penalty_last_n=8)
+    ids, state = _greedy_steps(raw, p, 5)
+    assert ids == [1, 2, 0, 1, 2]
+    assert state == {0: [1, 2, 0, 1, 2]}
+    p1 = synth.make_params(temperature=0.0, penalty_repeat=2.0, penalty_freq=1.0, penalty_last_n=1)
+    assert _greedy_steps(raw, p1, 6)[0] == [1, 2, 1, 2, 1, 2]
+    p0 = synth.make_params(temperature=0.0, penalty_repeat=2.0, penalty_last_n=0)   # no penalty
+    ids0, st0 = _greedy_steps(raw, p0, 3)
+    assert ids0 == [1, 1, 1] and st0 == {0: [1, 1, 1]}                               # still recorded
+
+
+def test_history_rows_of_one_call_share_the_window_and_append_in_row_order():
+    a = [1.0, 4.0, 3.9, -2.0, 0.5]
+    b = [0.0, 0.0, 0.0, 5.0, 0.0]
+    p = synth.make_params(temperature=0.0, penalty_repeat=2.0, penalty_last_n=8)
+    _, _, st, _ = oracle.history_call(_hw([a, b], [0, 0], {0: p}), {})
+    assert st == {0: [1, 3]}
+    _, _, st, _ = oracle.history_call(_hw([b, a], [0, 0], {0: p}), {})
+    assert st == {0: [3, 1]}
+    # both rows see the window from before the call: the second does not see the first's pick
+    rows, _, st, _ = oracle.history_call(_hw([a, a], [0, 0], {0: p}), {})
+    assert [r["id"] for r in rows] == [1, 1] and st == {0: [1, 1]}
+    # the history given in the state is the window: id 1 penalised from the first call on
+    rows, _, st, _ = oracle.history_call(_hw([a, a], [0, 0], {0: p}), {0: [9, 1]})
+    assert [r["id"] for r in rows] == [2, 2] and st == {0: [9, 1, 2, 2]}
+    # slots interleave; a slot without rows keeps its history untouched
+    rows, _, st, _ = oracle.history_call(_hw([a, b, b], [1, 0, 1], {0: p, 1: p}), {0: [4], 2: [7]})
+    assert st == {0: [4, 3], 1: [1, 3], 2: [7]}
+
+
+def test_history_verify_appends_the_kept_rows_only():
+    rows3 = [[0.0, 9.0, 0.0, 0.0], [0.0, 0.0, 9.0, 0.0], [0.0, 0.0, 0.0, 9.0]]   # argmax 1, 2, 3
+    p = synth.make_params(temperature=0.0, penalty_last_n=0)
+    w = _hw(rows3, [0, 0, 0], {0: p})
+    _, _, st, keep = oracle.history_call(w, {0: [5]}, row_draft=[1, 2, -1])
+    assert keep == {0: 3} and st == {0: [5, 1, 2, 3]}          # every draft matched: all + bonus
+    _, _, st, keep = oracle.history_call(w, {0: [5]}, row_draft=[1, 0, -1])
+    assert keep == {0: 2} and st == {0: [5, 1, 2]}             # the first miss is kept, then stop
+    _, _, st, keep = oracle.history_call(w, {}, row_draft=[0, 2, -1])
+    assert keep == {0: 1} and st == {0: [1]}
+
+
+def test_history_no_pick_appends_nothing():
+    raw = [1.0, 4.0, 3.9, -2.0, 0.5]
+    p = synth.make_params(temperature=0.0, penalty_last_n=8)
+    w = _hw([raw, raw], [0, 0], {0: p})
+    w["allowed"], w["allowed_off"] = synth.csr([[-1, 99], [2]])
+    rows, _, st, _ = oracle.history_call(w, {0: [3]}, mask_allowed=True)
+    assert [r["id"] for r in rows] == [-1, 2] and st == {0: [3, 2]}
+
+
+def test_history_matches_the_pages_upload_loop():
+    """The pages' serve loop hands the sampler the request's last penalty_last_n tokens before
+    every window; a kept history must give the same run (sampled rows, penalties, 40 steps)."""
+    rng = np.random.default_rng(21)
+    V = 64
+    p = synth.make_params(temperature=0.9, top_k=12, top_p=0.95, min_p=0.02, penalty_repeat=1.4,
+                          penalty_freq=0.3, penalty_present=0.2, penalty_last_n=6, seed=77)
+    prompt = [int(x) for x in rng.integers(0, V, 9)]
+    tokens = list(prompt)                 # the host's own record of the run
+    state, ctr_a, ctr_b = {0: list(prompt)}, {0: 0}, {0: 0}
+    for step in range(40):
+        raw = (rng.standard_normal((1, V)) * 1.5).astype(np.float32)
+        wa = synth._workload("loop", "f32", V, raw, {0: p}, [0], [step], [tokens[-6:]], 0)
+        rows_a, ctr_a = oracle.sample_call(wa, counters=ctr_a)
+        rows_b, ctr_b, state, _ = oracle.history_call(_hw(raw, [0], {0: p}, [step]), state, counters=ctr_b)
+        assert rows_a[0]["id"] == rows_b[0]["id"]
+        tokens.append(int(rows_a[0]["id"]))
+    assert state[0] == tokens and ctr_a == ctr_b == {0: 40}
+    assert len(set(tokens[len(prompt):])) > 5                    # the penalties moved the run around
+
+
+def test_history_tail_capacity():
+    st = {0: list(range(5000)), 1: [3, 4]}
+    t, n = oracle.history_tail(st, 0)
+    assert n == 5000 and t.tolist() == list(range(5000 - 4096, 5000))
+    assert oracle.HISTORY_RING_CAP == 4096
+    t, n = oracle.history_tail(st, 0, 10)
+    assert t.tolist() == list(range(4990, 5000))
+    assert oracle.history_tail(st, 1)[0].tolist() == [3, 4]
+    assert oracle.history_tail(st, 5)[0].size == 0 and oracle.history_tail(st, 5)[1] == 0
+    assert oracle.history_tail(st, 1, 0)[0].size == 0
