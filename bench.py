@@ -48,6 +48,8 @@ WORKLOAD_VERIFY = ("verify windows (strata_sample_verify): config 2's 5-row wind
                    "fp32 V=248,320, N(0,3^2)+1..5 spikes; keys T=0.7 top_k=20 top_p=0.9 min_p=0.05 repeat=1.1 "
                    "over a 64-token history; seeded draft ids; kept rows counted in the launch")
 WORKLOAD_MASK = WORKLOAD + "; the allowed ids used as a sampling mask (STRATA_FLAG_ALLOWED_MASK)"
+WORKLOAD_VERIFY_RING = (WORKLOAD_VERIFY + "; the 64-token window read from the slot's history kept on the device "
+                        "(STRATA_FLAG_HISTORY_RING) and the kept picks appended in the launch")
 KERNEL_SOURCES = ("request_token_sampling_gb300/csrc/strata_kernel.cuh",   # the device code the
                   "request_token_sampling_gb300/csrc/strata_device.cuh")   # ncu counters describe
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_config4_fused.json")
@@ -78,23 +80,31 @@ def algorithmic_bytes(w) -> int:
     return n
 
 
-def algorithmic_bytes_verify(w) -> int:
+def algorithmic_bytes_verify(w, ring=False) -> int:
     """Logits once, the history window, row arrays with drafts, slot keys and counter, picks and
-    the kept count."""
+    the kept count (with a kept history: its length read and written, the kept picks written;
+    counted as the whole window)."""
     B, V = w["B"], w["V"]
     n = B * V * 4 + 4 * min(w["slot_params"][0]["penalty_last_n"], int(w["hist_off"][1] - w["hist_off"][0]))
     n += 4 * 2 + B * (4 + 8 + 4) + (48 + 8 + 4) + B * 4 + 4
+    if ring:
+        n += 16 + 4 * B
     return n
 
 
-def oracle_windows_per_s(w, drafts, budget_s=15.0, max_windows=40):
-    """Time the unmodified oracle on whole verify windows (rows per second)."""
+def oracle_windows_per_s(w, drafts, budget_s=15.0, max_windows=40, ring=False):
+    """Time the unmodified oracle on whole verify windows (rows per second); with `ring`, windows
+    whose history is kept between calls."""
     import oracle
     t0 = time.perf_counter()
     n = 0
     counters = dict(w["counters"])
+    state = {0: [int(x) for x in w["hist"]]}
     while True:
-        _, counters, _ = oracle.verify_call(w, drafts, counters=counters)
+        if ring:
+            _, counters, state, _ = oracle.history_call(w, state, counters=counters, row_draft=drafts)
+        else:
+            _, counters, _ = oracle.verify_call(w, drafts, counters=counters)
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s or n >= max_windows:
@@ -264,13 +274,15 @@ def make_batches(w, R, dev):
 def run_gpu(args, rank, world):
     import torch
     import torch.distributed as dist
-    from request_token_sampling_gb300 import STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL, Sampler
+    from request_token_sampling_gb300 import (STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_HISTORY_RING,
+                                              STRATA_FLAG_PDL, Sampler)
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
-    verify = args.workload == "verify"
+    verify = args.workload in ("verify", "verify-ring")
+    ring = args.workload == "verify-ring"
     w = synth.config2_window(0) if verify else synth.config4(fused=True)
     B = w["B"]
     step_bytes = B * w["V"] * 4
@@ -279,6 +291,8 @@ def run_gpu(args, rank, world):
     flags = 0 if args.no_pdl else (STRATA_FLAG_PDL | (0 if args.no_early_load else STRATA_FLAG_EARLY_LOAD))
     if args.workload == "mask":
         flags |= STRATA_FLAG_ALLOWED_MASK
+    if ring:
+        flags |= STRATA_FLAG_HISTORY_RING
 
     s = Sampler(device=local, max_slots=16, max_vocab=w["V"], max_rows=B)
     for slot, p in w["slot_params"].items():
@@ -286,6 +300,10 @@ def run_gpu(args, rank, world):
     ten = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     row_slot, row_pos = ten(w["row_slot"]), ten(w["row_pos"])
     hist, hist_off = ten(w["hist"]), ten(w["hist_off"])
+    if ring:  # the window lives in the slot's kept history; the call uploads none
+        s.history_enable()
+        s.history_set(0, w["hist"])
+        hist = hist_off = None
     allowed = allowed_off = None
     if not verify:
         allowed, allowed_off = ten(w["allowed"]), ten(w["allowed_off"])
@@ -365,7 +383,8 @@ def run_gpu(args, rank, world):
     # ---- e2e through the C ABI from pinned host buffers -------------------------------------
     K_e2e = max(3, min(args.steps, 200))
     h_logits = [torch.from_numpy(w["logits"]).pin_memory()]
-    small_keys = ("row_slot", "row_pos", "hist", "hist_off") + (() if verify else ("allowed", "allowed_off"))
+    small_keys = ("row_slot", "row_pos") + (() if ring else ("hist", "hist_off")) + \
+        (() if verify else ("allowed", "allowed_off"))
     h_small = {k: torch.from_numpy(np.ascontiguousarray(w[k])).pin_memory() for k in small_keys}
     if verify:
         h_small["row_draft"] = torch.from_numpy(drafts).pin_memory()
@@ -382,8 +401,8 @@ def run_gpu(args, rank, world):
         for k, v in h_small.items():
             d_small[k].copy_(v, non_blocking=True)
         if verify:
-            s.verify(d_logits, d_small["row_slot"], d_small["row_pos"], d_small["row_draft"], hist=d_small["hist"],
-                     hist_off=d_small["hist_off"], flags=flags, stream=stream, out=out)
+            s.verify(d_logits, d_small["row_slot"], d_small["row_pos"], d_small["row_draft"], hist=d_small.get("hist"),
+                     hist_off=d_small.get("hist_off"), flags=flags, stream=stream, out=out)
         else:
             s.sample(d_logits, d_small["row_slot"], d_small["row_pos"], hist=d_small["hist"],
                      hist_off=d_small["hist_off"], top_n=w["top_n"], chosen_lp=True, allowed=d_small["allowed"],
@@ -410,7 +429,7 @@ def run_gpu(args, rank, world):
     if rank != 0:
         s.close()
         return
-    alg = algorithmic_bytes_verify(w) if verify else algorithmic_bytes(w)
+    alg = algorithmic_bytes_verify(w, ring) if verify else algorithmic_bytes(w)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
         peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
@@ -425,9 +444,10 @@ def run_gpu(args, rank, world):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         if verify:
-            rps, nwin, el = oracle_windows_per_s(w, drafts.tolist(), budget_s=args.cpu_budget)
+            rps, nwin, el = oracle_windows_per_s(w, drafts.tolist(), budget_s=args.cpu_budget, ring=ring)
             cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{nwin} whole 5-row windows (sample + acceptance), {el:.1f} s on 1 host core"}
+                   "sample": f"{nwin} whole 5-row windows (sample + acceptance"
+                             + (" + history update" if ring else "") + f"), {el:.1f} s on 1 host core"}
         else:
             rps, nrows, el = oracle_rows_per_s(w, budget_s=args.cpu_budget, mask=args.workload == "mask")
             cpu = {"value": rps, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -437,7 +457,8 @@ def run_gpu(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": {"verify": WORKLOAD_VERIFY, "mask": WORKLOAD_MASK}.get(args.workload, WORKLOAD),
+        "config": {"workload": {"verify": WORKLOAD_VERIFY, "mask": WORKLOAD_MASK,
+                                "verify-ring": WORKLOAD_VERIFY_RING}.get(args.workload, WORKLOAD),
                    "rows_per_step": B, "V": w["V"],
                    "logits_dtype": "f32",
                    "l2_policy": f"inputs rotate over {R} distinct batches ({R * step_bytes / 1e6:.0f} MB, "
@@ -473,9 +494,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--batches", type=int, default=0,
                     help="distinct input batches to rotate over (0: enough for 4x the L2 size)")
-    ap.add_argument("--workload", choices=["fused", "verify", "mask"], default="fused",
+    ap.add_argument("--workload", choices=["fused", "verify", "mask", "verify-ring"], default="fused",
                     help="fused: the logprobs workload fused with sampling (the headline); verify: verify "
-                         "windows; mask: the fused workload with its allowed ids as a sampling mask")
+                         "windows; mask: the fused workload with its allowed ids as a sampling mask; "
+                         "verify-ring: verify windows over histories kept on the device")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -57,14 +57,17 @@ extern "C" {
 #define STRATA_DEFAULT_LAST_N      64   /* [P19]: a penalty without a window uses 64 tokens      */
 #define STRATA_MAX_PENALTY_LAST_N  4096 /* library limit on the penalty history window           */
 #define STRATA_MAX_VOCAB           524288 /* library limit on V (per-row split over <= 16 SMs)   */
+#define STRATA_HISTORY_CAP         4096 /* ids a slot's kept history holds (its newest ids)      */
 
 /* ---- launch flags (strata_sample_rows / strata_logprobs_rows `flags`) --------------------- */
 /* Launch with programmatic dependent launch: the kernel may be scheduled while the previous
  * kernel on the stream finishes; it waits for that kernel before reading any input.            */
 #define STRATA_FLAG_PDL         0x1u
-/* With STRATA_FLAG_PDL: the caller asserts that the logit rows were complete before the previous
- * kernel on the stream started (they are not that kernel's output).  The kernel then starts its
- * logit loads before waiting for the previous kernel; slot state is still read after the wait.  */
+/* With STRATA_FLAG_PDL: the caller asserts that every input the call reads (logit rows, row
+ * slots, positions, drafts, history rows, allowed lists) was complete before the previous kernel
+ * on the stream started (none of it is that kernel's output).  The kernel then starts its loads
+ * before waiting for the previous kernel; draw counters, the slots' kept histories
+ * (STRATA_FLAG_HISTORY_RING) and every output are still read or written after the wait.        */
 #define STRATA_FLAG_EARLY_LOAD  0x2u
 /* strata_sample_rows with allowed/allowed_off: a row that names allowed ids samples only among
  * them (allowed_token_ids as a sampling mask for constrained decoding [P3200, "Problem and result"
@@ -73,6 +76,16 @@ extern "C" {
  * not restricted; a row whose ids are all outside [0, V) gets id -1 and STRATA_DEVERR_NOCAND.
  * The log-probability outputs still describe the row's full raw distribution.                  */
 #define STRATA_FLAG_ALLOWED_MASK 0x4u
+/* strata_sample_rows / strata_sample_verify: take each row's penalty window from its slot's kept
+ * history in the context (strata_history_enable) instead of hist/hist_off, which must then be
+ * NULL.  [P19, "min_p and the penalties": the serve loop uploads the request's last
+ * penalty_last_n tokens before every window.]  Every row of a slot counts over the same window,
+ * the last min(penalty_last_n, length) ids as they stood before the call; in the same launch
+ * the slot's history then grows by its rows' picks in row order (strata_sample_verify: only the
+ * rows it keeps), a pick of -1 appending nothing.  Slots that no row names are not touched.  The
+ * update happens on the device, so a captured call carries the history forward on every replay.
+ * Ignored by strata_logprobs_rows.                                                              */
+#define STRATA_FLAG_HISTORY_RING 0x8u
 /* Testing aid: force the number of thread blocks (1..16) that split each row; 0 = automatic.   */
 #define STRATA_FLAG_SPLIT(n)    (((uint32_t)(n) & 0x1Fu) << 8)
 
@@ -175,6 +188,9 @@ int strata_set_slot_state(strata_ctx *ctx, int slot, const strata_sampling_param
  *               The penalties count the last min(penalty_last_n, length) ids of the slot's run;
  *               ids outside [0, V) are ignored.  hist/hist_off NULL (or a slot >= n_hist_slots)
  *               means no history: the penalty stage is skipped and the logits are used unchanged [P19].
+ *               With STRATA_FLAG_HISTORY_RING both must be NULL (else STRATA_EINVAL) and the
+ *               window comes from the slot's kept history; without strata_history_enable first
+ *               that flag is STRATA_EINVAL.
  *   out_ids     device int32[B]: the sampled id of each row (always written; -1 for a row whose
  *               slot is out of range, with STRATA_DEVERR_SLOT).
  *   Optional fused logprobs of the raw (pre-penalty, pre-temperature) logits [P3200, P1916];
@@ -243,6 +259,32 @@ int strata_logprobs_rows(strata_ctx *ctx, const void *logits, int dtype, int B, 
                          int top_n, int32_t *top_ids, float *top_lps,
                          const int32_t *allowed, const int32_t *allowed_off, float *allowed_lps,
                          uint32_t flags, void *stream);
+
+/*
+ * Kept per-slot histories (STRATA_FLAG_HISTORY_RING).  A slot's history is the ids of its run so
+ * far; the context keeps its newest STRATA_HISTORY_CAP ids (a ring per slot, enough for every
+ * penalty window) and its total length.
+ *
+ * strata_history_enable: allocate the histories of all max_slots slots (4 * STRATA_HISTORY_CAP
+ * bytes per slot plus an 8-byte length), every one empty.  Synchronous; a second call is a no-op.
+ * STRATA_ENOMEM when the device allocation fails.
+ *
+ * strata_history_set: replace slot `slot`'s history by the n ids of host array `ids` (the
+ * prompt, or a run restored from a checkpoint); only the newest min(n, STRATA_HISTORY_CAP) are
+ * read, n becomes the length.  ids outside [0, V) are kept but never penalise.  Asynchronous on
+ * `stream` like strata_set_slot_params (the host array is read before the call returns).
+ *
+ * strata_history_get: synchronise `stream`, then write the newest min(length,
+ * STRATA_HISTORY_CAP, max_n) ids of the slot, oldest first, to host array `ids`, their count to
+ * *n_out and the total length to *length (either pointer may be NULL).
+ *
+ * All three: STRATA_EINVAL for a null context, STRATA_ERANGE for a slot outside [0, max_slots);
+ * set/get before enable, or n < 0 / max_n < 0, is STRATA_EINVAL.
+ */
+int strata_history_enable(strata_ctx *ctx);
+int strata_history_set(strata_ctx *ctx, int slot, const int32_t *ids, int64_t n, void *stream);
+int strata_history_get(strata_ctx *ctx, int slot, int32_t *ids, int max_n, int *n_out, int64_t *length,
+                       void *stream);
 
 /* Synchronise `stream`, return the accumulated STRATA_DEVERR_* bits in *bits and clear them. */
 int strata_read_errors(strata_ctx *ctx, uint32_t *bits, void *stream);

@@ -458,18 +458,24 @@ def history_call(w, state, counters=None, top_n=None, row_draft=None, mask_allow
         keep = None
     else:
         rows, counters, keep = verify_call(w2, row_draft, counters=counters, top_n=top_n)
+    new = history_append(state, w["row_slot"], [r["id"] for r in rows], keep)
+    return rows, counters, new, keep
+
+
+def history_append(state, row_slot, ids, keep=None):
+    """The history update that ends a call: each slot's picks in row order, only its first
+    keep[slot] rows when `keep` is given (a verify call), picks of -1 skipped.  Returns a new
+    {slot: list of ids}; `state` is not modified."""
     new = {s: list(v) for s, v in state.items()}
     taken = {}
-    for b, r in enumerate(rows):
-        s = int(w["row_slot"][b])
-        if r.get("invalid"):
-            continue
+    for s, t in zip(row_slot, ids):
+        s, t = int(s), int(t)
         taken[s] = taken.get(s, 0) + 1
-        if keep is not None and taken[s] > keep[s]:
+        if keep is not None and taken[s] > keep.get(s, 0):
             continue
-        if int(r["id"]) >= 0:
-            new.setdefault(s, []).append(int(r["id"]))
-    return rows, counters, new, keep
+        if t >= 0:
+            new.setdefault(s, []).append(t)
+    return new
 
 
 def history_tail(state, slot, max_n=HISTORY_RING_CAP):

@@ -28,10 +28,12 @@ STRATA_DEFAULT_TOP_K = 20
 STRATA_MAX_TOP_N = 20
 STRATA_MAX_PENALTY_LAST_N = 4096
 STRATA_NOALLOC_MAX_ROWS = 1024
+STRATA_HISTORY_CAP = 4096
 
 STRATA_FLAG_PDL = 0x1
 STRATA_FLAG_EARLY_LOAD = 0x2
 STRATA_FLAG_ALLOWED_MASK = 0x4
+STRATA_FLAG_HISTORY_RING = 0x8
 
 
 def STRATA_FLAG_SPLIT(n: int) -> int:
@@ -50,7 +52,8 @@ EXPORTED = (
     "strata_version", "strata_last_error", "strata_default_params", "strata_validate_params",
     "strata_create", "strata_destroy", "strata_set_slot_params", "strata_get_slot_state",
     "strata_set_slot_state", "strata_sample_rows", "strata_logprobs_rows", "strata_read_errors",
-    "strata_launch_shape", "strata_sample_rows_noalloc", "strata_sample_verify",
+    "strata_launch_shape", "strata_sample_rows_noalloc", "strata_sample_verify", "strata_history_enable",
+    "strata_history_set", "strata_history_get",
 )
 
 
@@ -107,6 +110,9 @@ def _load() -> ctypes.CDLL:
                                  ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "strata_sample_rows_noalloc": ([vp, i32, i32, i32, i64, P, ctypes.POINTER(ctypes.c_uint64), vp, vp, vp, vp,
                                         i32, vp, vp, vp, vp], i32),
+        "strata_history_enable": ([vp], i32),
+        "strata_history_set": ([vp, i32, vp, i64, vp], i32),
+        "strata_history_get": ([vp, i32, vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i64), vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -309,3 +315,24 @@ def strata_sample_rows_noalloc(logits, row_params, row_counters, row_pos, out_id
         _typed(hist_off, torch.int32, "hist_off"), _typed(out_ids, torch.int32, "out_ids"), int(top_n),
         _typed(chosen_lp, torch.float32, "chosen_lp"), _typed(top_ids, torch.int32, "top_ids"),
         _typed(top_lps, torch.float32, "top_lps"), _stream(stream)))
+
+
+def strata_history_enable(ctx) -> None:
+    _check(lib.strata_history_enable(ctx))
+
+
+def strata_history_set(ctx, slot: int, ids, stream=None) -> None:
+    """Replace a slot's kept history by `ids` (any integer sequence, host side)."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).reshape(-1))
+    _check(lib.strata_history_set(ctx, slot, a.ctypes.data if a.size else None, int(a.size), _stream(stream)))
+
+
+def strata_history_get(ctx, slot: int, max_n: int = STRATA_HISTORY_CAP, stream=None):
+    """(newest min(length, capacity, max_n) ids of the slot, oldest first, as int32 numpy; length)."""
+    import numpy as np
+    out = np.zeros(max(int(max_n), 1), dtype=np.int32)
+    n, length = ctypes.c_int(), ctypes.c_int64()
+    _check(lib.strata_history_get(ctx, slot, out.ctypes.data, int(max_n), ctypes.byref(n), ctypes.byref(length),
+                                  _stream(stream)))
+    return out[:n.value].copy(), int(length.value)

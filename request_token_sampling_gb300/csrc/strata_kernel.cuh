@@ -121,7 +121,9 @@ struct KParams {
   uint32_t flags;
   const int32_t* row_draft;  // verify windows: the draft after each row (-1: none), or NULL
   int32_t* slot_keep;        // verify windows: rows kept per slot
-  uint32_t* done;            // verify windows: per-slot count of rows done in the current call
+  uint32_t* done;            // verify windows / kept histories: per-slot rows done in the current call
+  int32_t* ring;             // kept histories: STRATA_HISTORY_CAP ids per slot, or NULL
+  unsigned long long* hlen;  // kept histories: per-slot total length
 };
 
 struct Layout {
@@ -603,13 +605,17 @@ __device__ __noinline__ void slot_arrival_done(int rs0, int rs1, const int32_t* 
     atomicAdd(&ctr[slot], (1ull << 16) - static_cast<unsigned long long>(r_s));
 }
 
-// Verify-window acceptance, run by the leader warp of every row of a slot once lane 0 has stored
-// the row's pick.  The row publishes its pick and counts itself done in the slot's arrival word;
-// the last row of the slot to finish reads every pick of the window (rows of the slot in row
-// order), keeps 1 + the leading rows whose pick equals their draft, and clears the word for the
-// next call.  Warp-wide; out of line (only verify calls take it).
-__device__ __noinline__ void accept_window_warp(const int32_t* row_slot, const int32_t* out_ids, const int32_t* row_draft,
-                                                uint32_t* done, int32_t* slot_keep, int B, int slot, int lane) {
+// The end of a slot's rows in a verify call or a call that keeps histories, run by the leader warp
+// of every row of the slot once lane 0 has stored the row's pick.  The row publishes its pick and
+// counts itself done in the slot's arrival word; the last row of the slot to finish reads every
+// pick of the call (rows of the slot in row order), keeps 1 + the leading rows whose pick equals
+// their draft (verify; a plain call keeps every row), appends the kept picks other than -1 to the
+// slot's history ring and length (when kept), and clears the word for the next call.  Every row
+// of the slot read its window before its candidates reached its leader, so no reader is left when
+// the ring is written.  Warp-wide; out of line (plain calls without histories never take it).
+__device__ __noinline__ void slot_window_done(const int32_t* row_slot, const int32_t* out_ids, const int32_t* row_draft,
+                                              uint32_t* done, int32_t* slot_keep, int32_t* ring,
+                                              unsigned long long* hlen, int B, int slot, int lane) {
   int r_s = 0;  // rows of this slot in the call
   for (int b0 = 0; b0 < B; b0 += 32) {
     const int b = b0 + lane;
@@ -622,22 +628,46 @@ __device__ __noinline__ void accept_window_warp(const int32_t* row_slot, const i
   }
   if (__shfl_sync(FULL_MASK, last, 0) == 0u) return;
   __threadfence();  // every other row of the slot was done (and its pick visible) before this one
-  int keep = 0;
-  for (int b0 = 0; b0 < B; b0 += 32) {
-    const int b = b0 + lane;
-    const bool in = b < B && row_slot[b] == slot;
-    const int t = in ? __ldcg(out_ids + b) : -1;
-    const int d = in ? row_draft[b] : -1;
-    const uint32_t m_in = __ballot_sync(FULL_MASK, in);
-    const uint32_t m_stop = __ballot_sync(FULL_MASK, in && (d < 0 || t < 0 || t != d));
-    if (m_stop != 0u) {  // the window ends at the first row whose pick differs from its draft
-      keep += __popc(m_in & ((2u << (__ffs(m_stop) - 1)) - 1u));
-      break;
+  int keep = r_s;
+  if (row_draft != nullptr) {
+    keep = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      const bool in = b < B && row_slot[b] == slot;
+      const int t = in ? __ldcg(out_ids + b) : -1;
+      const int d = in ? row_draft[b] : -1;
+      const uint32_t m_in = __ballot_sync(FULL_MASK, in);
+      const uint32_t m_stop = __ballot_sync(FULL_MASK, in && (d < 0 || t < 0 || t != d));
+      if (m_stop != 0u) {  // the window ends at the first row whose pick differs from its draft
+        keep += __popc(m_in & ((2u << (__ffs(m_stop) - 1)) - 1u));
+        break;
+      }
+      keep += __popc(m_in);
     }
-    keep += __popc(m_in);
+  }
+  if (ring != nullptr) {
+    const unsigned long long len = hlen[slot];
+    int32_t* rs = ring + static_cast<size_t>(slot) * STRATA_HISTORY_CAP;
+    const uint32_t lt = (1u << lane) - 1u;
+    int seen = 0, app = 0;  // rows of the slot so far, picks appended so far
+    for (int b0 = 0; b0 < B && seen < keep; b0 += 32) {
+      const int b = b0 + lane;
+      const bool in = b < B && row_slot[b] == slot;
+      const int t = in ? __ldcg(out_ids + b) : -1;
+      const uint32_t m_in = __ballot_sync(FULL_MASK, in);
+      const bool kept = in && seen + __popc(m_in & lt) < keep;
+      const uint32_t m_app = __ballot_sync(FULL_MASK, kept && t >= 0);
+      if (kept && t >= 0) {
+        const unsigned long long at = len + static_cast<unsigned long long>(app + __popc(m_app & lt));
+        rs[at & static_cast<unsigned long long>(STRATA_HISTORY_CAP - 1)] = t;
+      }
+      seen += __popc(m_in);
+      app += __popc(m_app);
+    }
+    if (lane == 0) hlen[slot] = len + static_cast<unsigned long long>(app);
   }
   if (lane == 0) {
-    slot_keep[slot] = keep;
+    if (slot_keep != nullptr) slot_keep[slot] = keep;
     done[slot] = 0u;
   }
 }
@@ -773,13 +803,27 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const int k_row = (P.mode == MODE_SAMPLE && valid) ? min(max(sp.k, 1), P.kmax) : 0;
   const int n_row = P.nmax;
   const int kp = max(k_row, n_row);
-  const bool penal = (P.mode == MODE_SAMPLE) && valid && (sp.flags & SLOT_PENAL) && P.hist_off != nullptr &&
-                     slot < P.n_hist_slots && P.hash_cap > 0;
-  int h_len = 0, h_start = 0;
+  const bool kept_hist = P.ring != nullptr;
+  const bool penal = (P.mode == MODE_SAMPLE) && valid && (sp.flags & SLOT_PENAL) && P.hash_cap > 0 &&
+                     (kept_hist || (P.hist_off != nullptr && slot < P.n_hist_slots));
+  // the window: ids hb[(h_start + i) & h_mask] for i < h_len (a caller's CSR row, or the slot's ring)
+  int h_len = 0;
+  uint32_t h_start = 0u, h_mask = 0xFFFFFFFFu;
+  const int32_t* hb = P.hist;
   if (penal) {
-    const int hb = P.hist_off[slot], he = P.hist_off[slot + 1];
-    h_len = min(sp.last_n, max(0, he - hb));
-    h_start = he - h_len;
+    if (kept_hist) {
+      // the previous call appends to the ring: with early loads this is where the row waits for it
+      if (early) grid_dep_wait();
+      const unsigned long long n = P.hlen[slot];
+      h_len = static_cast<int>(min(static_cast<unsigned long long>(sp.last_n), n));
+      hb = P.ring + static_cast<size_t>(slot) * STRATA_HISTORY_CAP;
+      h_mask = STRATA_HISTORY_CAP - 1;
+      h_start = static_cast<uint32_t>(n - static_cast<unsigned long long>(h_len)) & h_mask;
+    } else {
+      const int hs = P.hist_off[slot], he = P.hist_off[slot + 1];
+      h_len = min(sp.last_n, max(0, he - hs));
+      h_start = static_cast<uint32_t>(he - h_len);
+    }
   }
   int aid[APRE];  // the first allowed ids of this thread, fetched ahead
 #pragma unroll
@@ -801,7 +845,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 #pragma unroll
   for (int j = 0; j < HPRE; ++j) {
     const int i = tid + j * NT;
-    hid[j] = (penal && i < h_len) ? P.hist[h_start + i] : -1;
+    hid[j] = (penal && i < h_len) ? hb[(h_start + static_cast<uint32_t>(i)) & h_mask] : -1;
   }
 
   // ---- 1b. first pass as pieces land ----------------------------------------------------------
@@ -845,7 +889,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     };
 #pragma unroll
     for (int j = 0; j < HPRE; ++j) add_hist(hid[j]);
-    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(P.hist[h_start + i]);
+    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(hb[(h_start + static_cast<uint32_t>(i)) & h_mask]);
   }
   __syncthreads();  // history table and owner flags complete
 
@@ -1395,8 +1439,8 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         }
         if (P.chosen_lp != nullptr) P.chosen_lp[row] = (out >= 0) ? chosen_raw - lse : __int_as_float(0x7FC00000);
       }
-      if (P.row_draft != nullptr && valid)
-        accept_window_warp(P.row_slot, P.out_ids, P.row_draft, P.done, P.slot_keep, P.B, slot, lane);
+      if ((P.row_draft != nullptr || P.ring != nullptr) && valid)
+        slot_window_done(P.row_slot, P.out_ids, P.row_draft, P.done, P.slot_keep, P.ring, P.hlen, P.B, slot, lane);
       if (P.topk_ids != nullptr) {
         const long long o = static_cast<long long>(row) * KMAX;
         const bool ia = valid && lane < k_eff, ib = valid && lane + 32 < k_eff;

@@ -4,7 +4,9 @@
 // word per slot holding its 48-bit draw counter and the 16-bit arrival count the kernel uses to
 // advance it, and a device error word.  Keys are validated and prepared here (top_k 0 -> 20, logf(min_p) once on the host,
 // penalty activity), mirrored on the host, and copied to the device on the caller's stream.
-// Every sampling or logprobs call is one launch of the fused row kernel.
+// On request (strata_history_enable) it also keeps each slot's run history on the device: a ring
+// of the newest STRATA_HISTORY_CAP ids and a 64-bit length per slot, read and extended by the
+// kernel itself.  Every sampling or logprobs call is one launch of the fused row kernel.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -56,6 +58,8 @@ struct strata_ctx {
   unsigned long long* d_ctr = nullptr;
   uint32_t* d_done = nullptr;  // per slot: rows of the current verify call done (reset by the last)
   uint32_t* d_err = nullptr;
+  int32_t* d_ring = nullptr;              // kept histories: STRATA_HISTORY_CAP ids per slot
+  unsigned long long* d_hlen = nullptr;   // kept histories: per-slot total length
   std::vector<strata_sampling_params> h_params;
   std::vector<SlotDev> h_slots;
   // histograms over slots, for the launch shape: top_k of sampled slots, window of penal slots
@@ -345,7 +349,98 @@ void strata_destroy(strata_ctx* c) {
   cudaFree(c->d_ctr);
   cudaFree(c->d_done);
   cudaFree(c->d_err);
+  cudaFree(c->d_ring);
+  cudaFree(c->d_hlen);
   delete c;
+}
+
+// ---- kept per-slot histories: slot s's id number i (0-based over its run) lives at
+// d_ring[s * STRATA_HISTORY_CAP + i % STRATA_HISTORY_CAP] while it is among the newest CAP ids.
+int strata_history_enable(strata_ctx* c) {
+  if (c == nullptr) return fail(STRATA_EINVAL, "null context");
+  int rc = check_device(c);
+  if (rc != STRATA_OK) return rc;
+  if (c->d_ring != nullptr) return STRATA_OK;
+  const size_t ring_bytes = sizeof(int32_t) * STRATA_HISTORY_CAP * static_cast<size_t>(c->max_slots);
+  cudaError_t e;
+  if ((e = cudaMalloc(&c->d_ring, ring_bytes)) != cudaSuccess) {
+    c->d_ring = nullptr;
+    return fail(STRATA_ENOMEM, "cudaMalloc histories (%zu bytes): %s", ring_bytes, cudaGetErrorString(e));
+  }
+  if ((e = cudaMalloc(&c->d_hlen, sizeof(unsigned long long) * c->max_slots)) != cudaSuccess) {
+    cudaFree(c->d_ring);
+    c->d_ring = nullptr;
+    c->d_hlen = nullptr;
+    return fail(STRATA_ENOMEM, "cudaMalloc history lengths: %s", cudaGetErrorString(e));
+  }
+  if ((e = cudaMemset(c->d_hlen, 0, sizeof(unsigned long long) * c->max_slots)) != cudaSuccess ||
+      (e = cudaDeviceSynchronize()) != cudaSuccess) {
+    cudaFree(c->d_ring);
+    cudaFree(c->d_hlen);
+    c->d_ring = nullptr;
+    c->d_hlen = nullptr;
+    return cuda_fail(e, "history reset");
+  }
+  return STRATA_OK;
+}
+
+static int history_check(strata_ctx* c, int slot) {
+  if (c == nullptr) return fail(STRATA_EINVAL, "null context");
+  if (slot < 0 || slot >= c->max_slots) return fail(STRATA_ERANGE, "slot %d outside 0..%d", slot, c->max_slots - 1);
+  if (c->d_ring == nullptr) return fail(STRATA_EINVAL, "histories not enabled (strata_history_enable)");
+  return check_device(c);
+}
+
+int strata_history_set(strata_ctx* c, int slot, const int32_t* ids, int64_t n, void* stream) {
+  int rc = history_check(c, slot);
+  if (rc != STRATA_OK) return rc;
+  if (n < 0) return fail(STRATA_EINVAL, "n=%lld", static_cast<long long>(n));
+  if (n > 0 && ids == nullptr) return fail(STRATA_EINVAL, "null ids");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t cap = STRATA_HISTORY_CAP;
+  const int64_t m = std::min(n, cap);
+  int32_t* ring = c->d_ring + static_cast<size_t>(slot) * STRATA_HISTORY_CAP;
+  // ids n-m .. n-1 go to ring positions (n-m) % cap onward, wrapping once at most
+  const int64_t first = (n - m) % cap;
+  const int64_t run1 = std::min(m, cap - first);
+  // staged in pageable memory, so that the caller's array is free again when the call returns
+  // (a page-locked source would be read later, by the copy engine)
+  std::vector<int32_t> stage(ids + (n - m), ids + n);
+  cudaError_t e;
+  if (run1 > 0 && (e = cudaMemcpyAsync(ring + first, stage.data(), sizeof(int32_t) * run1, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "history upload");
+  if (m > run1 && (e = cudaMemcpyAsync(ring, stage.data() + run1, sizeof(int32_t) * (m - run1), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "history upload");
+  const unsigned long long len = static_cast<unsigned long long>(n);
+  if ((e = cudaMemcpyAsync(c->d_hlen + slot, &len, sizeof(len), cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "history length upload");
+  return STRATA_OK;
+}
+
+int strata_history_get(strata_ctx* c, int slot, int32_t* ids, int max_n, int* n_out, int64_t* length, void* stream) {
+  int rc = history_check(c, slot);
+  if (rc != STRATA_OK) return rc;
+  if (max_n < 0) return fail(STRATA_EINVAL, "max_n=%d", max_n);
+  if (max_n > 0 && ids == nullptr) return fail(STRATA_EINVAL, "null ids");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long len = 0;
+  cudaError_t e = cudaMemcpyAsync(&len, c->d_hlen + slot, sizeof(len), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "history length read");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "history length sync");
+  const int64_t cap = STRATA_HISTORY_CAP;
+  const int64_t n = static_cast<int64_t>(len);
+  const int64_t m = std::min({n, cap, static_cast<int64_t>(max_n)});
+  const int32_t* ring = c->d_ring + static_cast<size_t>(slot) * STRATA_HISTORY_CAP;
+  const int64_t first = (n - m) % cap;
+  const int64_t run1 = std::min(m, cap - first);
+  if (run1 > 0 && (e = cudaMemcpyAsync(ids, ring + first, sizeof(int32_t) * run1, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "history read");
+  if (m > run1 && (e = cudaMemcpyAsync(ids + run1, ring, sizeof(int32_t) * (m - run1), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "history read");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "history read sync");
+  if (n_out != nullptr) *n_out = static_cast<int>(m);
+  if (length != nullptr) *length = n;
+  return STRATA_OK;
 }
 
 static int set_slot(strata_ctx* c, int slot, const strata_sampling_params* p, bool set_ctr, uint64_t ctr,
@@ -442,6 +537,12 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   if (rc != STRATA_OK) return rc;
   if (B > 0 && (row_slot == nullptr || row_pos == nullptr || out_ids == nullptr))
     return fail(STRATA_EINVAL, "row_slot, row_pos and out_ids are required");
+  const bool kept_hist = (flags & STRATA_FLAG_HISTORY_RING) != 0u;
+  if (kept_hist) {
+    if (hist != nullptr || hist_off != nullptr)
+      return fail(STRATA_EINVAL, "STRATA_FLAG_HISTORY_RING takes the windows from the kept histories: hist and hist_off must be NULL");
+    if (c->d_ring == nullptr) return fail(STRATA_EINVAL, "STRATA_FLAG_HISTORY_RING before strata_history_enable");
+  }
   if (hist_off != nullptr && (hist == nullptr || n_hist_slots < 1))
     return fail(STRATA_EINVAL, "hist_off needs hist and n_hist_slots >= 1");
   if (hist_off == nullptr) n_hist_slots = 0;
@@ -449,7 +550,8 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   if (B == 0) return STRATA_OK;
   const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
   Shape sh;
-  if ((rc = compute_shape(c, strata::MODE_SAMPLE, dtype, B, V, top_n_eff, hist_off != nullptr, flags, &sh)) != STRATA_OK)
+  if ((rc = compute_shape(c, strata::MODE_SAMPLE, dtype, B, V, top_n_eff, hist_off != nullptr || kept_hist, flags, &sh)) !=
+      STRATA_OK)
     return rc;
   KParams P{};
   P.logits = logits;
@@ -488,6 +590,8 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   P.row_draft = row_draft;
   P.slot_keep = slot_keep;
   P.done = c->d_done;
+  P.ring = kept_hist ? c->d_ring : nullptr;
+  P.hlen = kept_hist ? c->d_hlen : nullptr;
   return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream));
 }
 

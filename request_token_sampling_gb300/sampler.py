@@ -32,6 +32,15 @@ class Sampler:
     def restore_slot(self, slot: int, params, counter: int, stream=None) -> None:
         B.strata_set_slot_state(self.ctx, slot, params, counter, stream)
 
+    def history_enable(self) -> None:
+        B.strata_history_enable(self.ctx)
+
+    def history_set(self, slot: int, ids, stream=None) -> None:
+        B.strata_history_set(self.ctx, slot, ids, stream)
+
+    def history_get(self, slot: int, max_n: int = B.STRATA_HISTORY_CAP, stream=None):
+        return B.strata_history_get(self.ctx, slot, max_n, stream)
+
     def errors(self, stream=None) -> int:
         return B.strata_read_errors(self.ctx, stream)
 

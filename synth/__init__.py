@@ -257,3 +257,55 @@ def random_case(seed, B, V, dtype="f32", ld=None, n_slots=None, sampled_frac=0.5
             allowed.append(a)
     return _workload(f"random_case_{seed}", dtype, V, logits, prm, row_slot, row_pos, hists, top_n,
                      allowed_lists=allowed)
+
+
+# ---------------------------------------------------------------------------------------------
+# Decode runs: the same slots sampled step after step (for kept per-slot histories)
+# ---------------------------------------------------------------------------------------------
+
+class DecodeRun:
+    """A seeded run of `steps` calls over `S` slots with penalties on, for histories kept between
+    calls.  Each slot has its own keys, a prompt (its history before the first call) and a fixed
+    set of `hot` ids that carry +5..+8 spikes in every row of the slot (redrawn each step), so the
+    penalties over the history decide between them.  ``step(t)`` returns call t's workload:
+    `rows_per_slot` rows per slot in a seeded interleaved order, positions advancing with t, and no
+    history of its own (the kept histories supply the windows)."""
+
+    def __init__(self, seed, S, V, dtype="f32", rows_per_slot=1, hot=24, prompt_len=(0, 40),
+                 last_ns=(1, 8, 64, 300, 4096), greedy_frac=0.3):
+        self.seed, self.S, self.V, self.dtype = seed, S, V, dtype
+        self.rows_per_slot = rows_per_slot
+        rng = _rng(0xD0C0DE, seed)
+        self.slot_params, self.prompts, self.hot = {}, {}, {}
+        for s in range(S):
+            greedy = rng.random() < greedy_frac
+            self.slot_params[s] = make_params(
+                temperature=0.0 if greedy else float(rng.uniform(0.5, 1.5)),
+                top_k=int(rng.integers(0, 65)), top_p=float(rng.choice([1.0, rng.uniform(0.6, 1.0)])),
+                min_p=float(rng.choice([0.0, rng.uniform(0.0, 0.1)])),
+                penalty_repeat=float(rng.uniform(1.2, 2.0)), penalty_freq=float(rng.uniform(0.2, 1.0)),
+                penalty_present=float(rng.choice([0.0, rng.uniform(0.0, 0.5)])),
+                penalty_last_n=int(rng.choice(last_ns)), seed=int(rng.integers(0, 2**63)))
+            self.hot[s] = rng.choice(V, size=hot, replace=False).astype(np.int32)
+            n = int(rng.integers(prompt_len[0], prompt_len[1] + 1))
+            pick_hot = rng.random(n) < 0.5
+            self.prompts[s] = np.where(pick_hot, rng.choice(self.hot[s], size=n),
+                                       rng.integers(0, V, size=n)).astype(np.int32)
+
+    def step(self, t, top_n=0, allowed_lists=None):
+        rng = _rng(0xD0C0DE, self.seed, t)
+        order = np.repeat(np.arange(self.S), self.rows_per_slot)
+        order = order[rng.permutation(order.size)]                # slots interleave
+        B = order.size
+        x = (rng.standard_normal((B, self.V)) * 1.5).astype(np.float32)
+        for b, s in enumerate(order):
+            x[b, self.hot[s]] = rng.uniform(5.0, 8.0, size=self.hot[s].size).astype(np.float32)
+        logits = to_bf16_bits(x) if self.dtype == "bf16" else x
+        seen = {}
+        pos = []
+        for s in order:
+            j = seen.get(int(s), 0)
+            seen[int(s)] = j + 1
+            pos.append(10_000 * int(s) + t * self.rows_per_slot + j)
+        return _workload(f"decode_{self.seed}_t{t}", self.dtype, self.V, logits, dict(self.slot_params),
+                         order.astype(np.int32), pos, [], top_n, allowed_lists=allowed_lists)

@@ -93,4 +93,16 @@ def test_null_arguments_rejected_without_cuda(S):
     assert S.lib.strata_sample_rows(None, None, 0, 1, 10, 10, None, None, None, None, 0, None, 0, None, None, None,
                                     None, None, None, None, None, None, 0, None) == S.STRATA_EINVAL
     assert S.lib.strata_read_errors(None, None, None) == S.STRATA_EINVAL
+    assert S.lib.strata_history_enable(None) == S.STRATA_EINVAL
+    assert S.lib.strata_history_set(None, 0, None, 0, None) == S.STRATA_EINVAL
+    assert S.lib.strata_history_get(None, 0, None, 0, None, None, None) == S.STRATA_EINVAL
     S.lib.strata_destroy(None)
+
+
+def test_history_capacity_constants(S):
+    import oracle
+    text = open(HEADER).read()
+    cap = int(re.search(r"#define STRATA_HISTORY_CAP\s+(\d+)", text).group(1))
+    assert cap == S.STRATA_HISTORY_CAP == oracle.HISTORY_RING_CAP
+    assert cap & (cap - 1) == 0                         # a power of two: ring positions are masked
+    assert cap >= S.STRATA_MAX_PENALTY_LAST_N           # every penalty window fits

@@ -44,12 +44,10 @@ MUTATIONS = [
      "        if d < 0 or t < 0 or t != d:\n            open_[s] = False\n        else:\n            keep[s] += 1"),
     ("sampling.py", "        order = keep[rank_order(pen[keep])]", "        order = rank_order(pen)[:keep.size]"),
     ("sampling.py", "        keep = np.unique(a[(a >= 0) & (a < V)])", "        keep = np.unique(np.clip(a, 0, V - 1))"),
-    ("sampling.py", "        if keep is not None and taken[s] > keep[s]:\n            continue\n", ""),
-    ("sampling.py", "if keep is not None and taken[s] > keep[s]:", "if keep is not None and taken[s] >= keep[s]:"),
-    ("sampling.py", "        if int(r[\"id\"]) >= 0:\n            new.setdefault(s, []).append(int(r[\"id\"]))",
-     "        new.setdefault(s, []).append(int(r[\"id\"]))"),
-    ("sampling.py", "new.setdefault(s, []).append(int(r[\"id\"]))",
-     "new.setdefault(s, []).insert(len(state.get(s, [])), int(r[\"id\"]))"),
+    ("sampling.py", "        if keep is not None and taken[s] > keep.get(s, 0):\n            continue\n", ""),
+    ("sampling.py", "if keep is not None and taken[s] > keep.get(s, 0):", "if keep is not None and taken[s] >= keep.get(s, 0):"),
+    ("sampling.py", "        if t >= 0:\n            new.setdefault(s, []).append(t)", "        new.setdefault(s, []).append(t)"),
+    ("sampling.py", "new.setdefault(s, []).append(t)", "new.setdefault(s, []).insert(len(state.get(s, [])), t)"),
     ("sampling.py", "np.asarray(h[len(h) - m:], dtype=np.int32)", "np.asarray(h[:m], dtype=np.int32)"),
 ]
 
