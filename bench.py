@@ -275,7 +275,7 @@ def run_gpu(args, rank, world):
     import torch
     import torch.distributed as dist
     from request_token_sampling_gb300 import (STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_HISTORY_RING,
-                                              STRATA_FLAG_PDL, Sampler)
+                                              STRATA_FLAG_PDL, STRATA_FLAG_SPLIT, Sampler)
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -293,6 +293,8 @@ def run_gpu(args, rank, world):
         flags |= STRATA_FLAG_ALLOWED_MASK
     if ring:
         flags |= STRATA_FLAG_HISTORY_RING
+    if args.split > 0:
+        flags |= STRATA_FLAG_SPLIT(args.split)
 
     s = Sampler(device=local, max_slots=16, max_vocab=w["V"], max_rows=B)
     for slot, p in w["slot_params"].items():
@@ -492,6 +494,8 @@ def main():
                     help="with PDL, wait for the previous kernel before loading logits (inputs produced by it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--split", type=int, default=0,
+                    help="blocks per row (1..16; 0: the library's choice), for launch-shape sweeps")
     ap.add_argument("--batches", type=int, default=0,
                     help="distinct input batches to rotate over (0: enough for 4x the L2 size)")
     ap.add_argument("--workload", choices=["fused", "verify", "mask", "verify-ring"], default="fused",

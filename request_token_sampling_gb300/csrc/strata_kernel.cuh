@@ -1,20 +1,25 @@
 // strata_kernel.cuh -- the fused row kernel: one HBM pass per logit row.
 //
-// Each logit row is split over a thread-block cluster of `cs` CTAs (one chunk per CTA).  A CTA
-//   1. bulk-copies its chunk into shared memory (32 KiB pieces, one mbarrier each) and, as each
-//      piece lands, runs the first pass: per thread the running maximum and the sum of exp
-//      against a lazily moved reference (log-sum-exp of the raw logits); meanwhile the row's
-//      metadata loads are in flight, and the history table of the chunk's id range (bitmap +
-//      open-addressing counts) and the allowed-subset partial sums follow the last piece;
+// Each logit row is split over a thread-block cluster of `cs` CTAs (one chunk per CTA; few large
+// chunks for pipelined calls, more smaller ones when a single call's latency matters).  A CTA
+//   1. streams its chunk through a ring of shared-memory slots (16 KiB bulk copies, one mbarrier
+//      per slot; the last warp done with a slot refills it) and, as each piece lands, runs the
+//      first pass: per thread the running maximum and the sum of exp against a lazily moved
+//      reference (log-sum-exp of the raw logits); meanwhile the row's metadata loads are in
+//      flight, and the logits of its allowed and history ids are fetched behind the first piece;
+//      the history table of the chunk's id range (bitmap + open-addressing counts + raw logits)
+//      and the allowed-subset partial sums follow the last piece;
 //   2. publishes to every CTA of the cluster, with asynchronous DSMEM stores completed on one
-//      mbarrier per CTA, its largest q per-warp maxima of the logits that carry no penalty and its
-//      two (max, sum) pairs (row and allowed subset).  Every CTA then takes T = the K-th largest of
-//      the cs*q published values (K = max(top_k, top_n)): they are K distinct elements of the row,
-//      so the row's K-th largest value (raw, and penalised, since those ids carry no penalty) is
-//      at least T;
-//   3. rescans only the threads whose maximum reaches T, adds the penalised ids of the history
-//      table, keeps its best <= K candidates and stores them into its own slice of the cluster
-//      leader's receive lists (asynchronous DSMEM stores, one transaction-counted arrival per CTA);
+//      mbarrier per CTA, the qw largest thread maxima of each warp (logits that carry no
+//      penalty) and its two (max, sum) pairs (row and allowed subset).  Every CTA then takes
+//      T = the K-th largest of the published values (K = max(top_k, top_n)): they are values of
+//      distinct ids, so the row's K-th largest value (raw, and penalised, since those ids carry no
+//      penalty) is at least T;
+//   3. rescans (from L2: the chunk passed through it moments ago) only the threads whose maximum
+//      reaches T, adds the penalised ids of the history table, keeps its best <= K candidates (the
+//      candidate lists live in the ring, free by then) and stores them into its own slice of the
+//      cluster leader's receive lists (asynchronous DSMEM stores, one transaction-counted arrival
+//      per CTA);
 //   4. the leader ranks the received keys by counting (one thread per key), then one warp runs the
 //      tail of the chain on <= 64 survivors: min_p, top_p, temperature, the Philox draw.
 // Only the leader writes outputs (the allowed-subset and chosen-id log-probabilities from logits
@@ -38,15 +43,15 @@ namespace strata {
 
 constexpr int NT = 256;                      // threads per CTA (three CTAs fit an SM)
 constexpr int NW = NT / 32;                  // warps per CTA
-constexpr int VR = 8;                        // 16-byte vectors per thread per piece
+constexpr int VR = 4;                        // 16-byte vectors per thread per piece
 constexpr int PIECE_VECS = NT * VR;
-constexpr int PIECE_BYTES = PIECE_VECS * 16; // 32 KiB per bulk copy
-constexpr int MAX_PIECES = 6;                // chunk <= 192 KiB
+constexpr int PIECE_BYTES = PIECE_VECS * 16; // 16 KiB per bulk copy
+constexpr int MAX_SLOTS = 8;                 // ring slots: pieces in flight per CTA
 constexpr int MAX_CS = 16;                   // CTAs per row (non-portable cluster size)
 constexpr int KMAX = STRATA_MAX_TOP_K;
 constexpr int NMAX = STRATA_MAX_TOP_N;
-constexpr int QMAX = 8;                      // the host keeps cs >= ceil(K / QMAX): cs * NW >= K
-constexpr int LOCAL_CAP = 64;                // per-CTA candidate buffer (beyond: exact rounds)
+constexpr int QW_MAX = 8;                    // thread maxima a warp publishes, at most
+constexpr int RANK_LIMIT = 256;              // candidates ranked by counting; beyond: argmax rounds
 constexpr int HASH_CNT_BITS = 13;            // history table entry = (local id << 13) | count
 constexpr uint32_t HASH_EMPTY = 0xFFFFFFFFu;
 constexpr int MODE_SAMPLE = 0;
@@ -55,13 +60,13 @@ constexpr uint32_t SLOT_SAMPLED = 1u;
 constexpr uint32_t SLOT_PENAL = 2u;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // bounded waits: ~2 s at GB300 clocks
 constexpr float LAZY_SHIFT = 16.0f;          // the exp reference moves only when the max passes it by this
-constexpr int XREC_WORDS = 20;               // published per CTA: 16 warp-maximum keys + 2 (max, sum) pairs
-constexpr int XREC_BYTES = XREC_WORDS * 4;
+constexpr int XKEYS = NW * QW_MAX;           // published keys per CTA, at most
+constexpr int XREC_WORDS = XKEYS + 4;        // record stride: the keys, then 2 (max, sum) pairs
 constexpr int HPRE = 2;                      // history ids per thread fetched ahead of the table build
 constexpr int APRE = 4;                      // allowed ids per thread fetched ahead
-constexpr int BAR_X0 = MAX_PIECES;           // mbarrier: every CTA's published record has landed
-constexpr int BAR_X1 = MAX_PIECES + 1;       // mbarrier (leader): every CTA's candidates have landed
-constexpr int NBAR = MAX_PIECES + 2;
+constexpr int BAR_X0 = MAX_SLOTS;            // mbarrier: every CTA's published record has landed
+constexpr int BAR_X1 = MAX_SLOTS + 1;        // mbarrier (leader): every CTA's candidates have landed
+constexpr int NBAR = MAX_SLOTS + 2;
 
 // Control words in shared memory.
 enum : int {
@@ -73,7 +78,9 @@ enum : int {
   CTL_LSE_A = 5,
   CTL_TOT_P = 6,     // leader: received entries per list
   CTL_TOT_R = 7,
-  CTL_WORDS = 8
+  CTL_SLOT0 = 8,     // per ring slot: warps done with the piece it holds (the last one refills it)
+  CTL_LAST0 = CTL_SLOT0 + MAX_SLOTS,  // per ring slot: the last piece issued into it
+  CTL_WORDS = CTL_LAST0 + MAX_SLOTS
 };
 
 // A slot's keys as the kernel reads them (prepared and validated by the host).
@@ -118,6 +125,8 @@ struct KParams {
   int max_slots;
   uint32_t* err;
   int hash_cap, hash_bits;
+  int nslot;          // ring slots (pieces in flight) per CTA, 2..MAX_SLOTS
+  int qw;             // thread maxima each warp publishes: 1, 2, 4 or 8
   uint32_t flags;
   const int32_t* row_draft;  // verify windows: the draft after each row (-1: none), or NULL
   int32_t* slot_keep;        // verify windows: rows kept per slot
@@ -127,43 +136,47 @@ struct KParams {
 };
 
 struct Layout {
-  uint32_t data, mbar, abits, mbits, hash, hflag, wmax, red, ctl, xrec;
+  uint32_t data, mbar, abits, mbits, hash, hraw, hflag, wkey, red, ctl, xrec;
   uint32_t cand_pen, cand_raw, recv_cnt, recv_pkey, recv_praw, recv_raw, sorted_pen, sorted_raw, total;
+  int cand_cap;  // entries of each candidate list (they live in the ring once the first pass is done)
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Shared-memory layout of one CTA; identical in every CTA of a launch.
-__host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, int cs, int kmax,
-                                              int nmax, bool mask = false) {
+// Shared-memory layout of one CTA; identical in every CTA of a launch.  `data` is the ring of
+// `nslot` pieces; once the first pass is done it holds the candidate lists.
+__host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, int kmax, int nmax, int nslot,
+                                              bool allowed, bool mask) {
   Layout L;
   uint32_t o = 0;
   L.data = o;
-  o += align_up(static_cast<uint32_t>(chunk) * esz, 128);
+  const uint32_t ring = static_cast<uint32_t>(nslot) * PIECE_BYTES;
+  o += ring;
+  L.cand_cap = static_cast<int>(ring / 24u) & ~7;
+  L.cand_pen = L.data;
+  L.cand_raw = L.data + static_cast<uint32_t>(L.cand_cap) * 16u;
   L.mbar = o;
   o += NBAR * 8;
   const uint32_t bw = align_up((static_cast<uint32_t>(chunk) + 31) / 32 * 4, 16);
-  L.abits = o;
-  o += bw;
+  L.abits = o;  // allowed ids met in this chunk (calls with allowed lists only)
+  o += allowed ? bw : 0u;
   L.mbits = o;  // allowed ids already in a masked row's top_k list (mask launches only)
   o += mask ? bw : 0u;
   L.hash = o;
   o += align_up(static_cast<uint32_t>(hash_cap) * 4, 16);
+  L.hraw = o;   // raw logit of each history table entry
+  o += align_up(static_cast<uint32_t>(hash_cap) * 4, 16);
   L.hflag = o;
   o += NT / 8;
-  L.wmax = o;
-  o += NW * 4;
+  L.wkey = o;
+  o += NW * QW_MAX * 4;
   L.red = o;
   o += NW * 16;
   L.ctl = o;
   o += CTL_WORDS * 4;
   o = align_up(o, 16);
   L.xrec = o;
-  o += MAX_CS * XREC_BYTES;
-  L.cand_pen = o;
-  o += LOCAL_CAP * 16;
-  L.cand_raw = o;
-  o += LOCAL_CAP * 8;
+  o += static_cast<uint32_t>(cs) * XREC_WORDS * 4;
   L.recv_cnt = o;
   o += MAX_CS * 8;
   L.recv_pkey = o;  // received penalised list: keys (8 B) and raw logits (4 B), kmax per CTA
@@ -183,8 +196,9 @@ __host__ __device__ inline Layout make_layout(int chunk, int esz, int hash_cap, 
 
 // Every region starts on a 16-byte boundary (vector and bulk accesses rely on it).
 __host__ __device__ inline bool layout_aligned(const Layout& L) {
-  const uint32_t r[] = {L.data, L.mbar, L.abits, L.mbits, L.hash, L.hflag, L.wmax, L.red, L.ctl, L.xrec, L.cand_pen,
-                        L.cand_raw, L.recv_cnt, L.recv_pkey, L.recv_praw, L.recv_raw, L.sorted_pen, L.sorted_raw};
+  const uint32_t r[] = {L.data, L.mbar, L.abits, L.mbits, L.hash, L.hraw, L.hflag, L.wkey, L.red, L.ctl, L.xrec,
+                        L.cand_pen, L.cand_raw, L.recv_cnt, L.recv_pkey, L.recv_praw, L.recv_raw, L.sorted_pen,
+                        L.sorted_raw};
   for (uint32_t x : r)
     if (x % 16u != 0u) return false;
   return true;
@@ -219,6 +233,50 @@ __device__ __forceinline__ float elem_at(const unsigned char* data, uint32_t loc
   }
 }
 
+// Vector v of a chunk in global memory (the row is in L2 by the time anything reads it again);
+// elements at or beyond n_el read as -inf, so the ragged last vector never reads past the row.
+template <int DT>
+__device__ __forceinline__ void load_vec_g(const unsigned char* g, int v, int n_el, float (&x)[16 / (DT == 0 ? 4 : 2)]) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+  if ((v + 1) * EPV <= n_el) {
+    if constexpr (DT == 0) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(g) + v);
+      x[0] = f.x;
+      x[1] = f.y;
+      x[2] = f.z;
+      x[3] = f.w;
+    } else {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(g) + v);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const int idx = v * EPV + e;
+      if (idx < n_el) {
+        if constexpr (DT == 0) x[e] = __ldg(reinterpret_cast<const float*>(g) + idx);
+        else x[e] = __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(g) + idx)) << 16);
+      } else {
+        x[e] = -INFINITY;
+      }
+    }
+  }
+}
+
+// Element e (< N) of a small register array, by a chain of selects (no local-memory indexing).
+template <int N>
+__device__ __forceinline__ float pick(const float (&x)[N], int e) {
+  float r = x[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) r = (e == k) ? x[k] : r;
+  return r;
+}
+
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, uint32_t loc) {
   return (bits[loc >> 5] >> (loc & 31)) & 1u;
 }
@@ -227,24 +285,25 @@ __device__ __forceinline__ uint32_t hash_slot(uint32_t loc, int bits) {
   return (loc * 0x9E3779B1u) >> (32 - bits);
 }
 
-// Count one occurrence of chunk-local id `loc`; false if the table is full.
-__device__ bool hash_add(uint32_t* tab, int bits, uint32_t loc) {
+// Count one occurrence of chunk-local id `loc`: returns the entry's index when this call created it,
+// -1 when the id was already there, -2 when the table is full.
+__device__ int hash_add(uint32_t* tab, int bits, uint32_t loc) {
   const uint32_t mask = (1u << bits) - 1u;
   uint32_t h = hash_slot(loc, bits);
   for (uint32_t n = 0; n <= mask; ++n) {
     uint32_t cur = *reinterpret_cast<volatile uint32_t*>(&tab[h]);
     if (cur == HASH_EMPTY) {
       const uint32_t prev = atomicCAS(&tab[h], HASH_EMPTY, (loc << HASH_CNT_BITS) | 1u);
-      if (prev == HASH_EMPTY) return true;
+      if (prev == HASH_EMPTY) return static_cast<int>(h);
       cur = prev;
     }
     if ((cur >> HASH_CNT_BITS) == loc) {
       atomicAdd(&tab[h], 1u);
-      return true;
+      return -1;
     }
     h = (h + 1u) & mask;
   }
-  return false;
+  return -2;
 }
 
 __device__ uint32_t hash_count(const uint32_t* tab, int bits, uint32_t loc) {
@@ -259,12 +318,13 @@ __device__ uint32_t hash_count(const uint32_t* tab, int bits, uint32_t loc) {
   return 0u;
 }
 
-// Bounded poll of an mbarrier phase (parity 0).  On timeout the error word and a shared flag are
+// Bounded poll of an mbarrier phase (the one with the given parity).  On timeout the error word and a shared flag are
 // set and the caller carries on with whatever has landed.
-__device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t* ctl, uint32_t* err, bool cluster_scope) {
-  if (cluster_scope ? mbar_try_wait_cluster(bar, 0) : mbar_try_wait(bar, 0)) return;
+__device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t* ctl, uint32_t* err, bool cluster_scope,
+                                         uint32_t parity = 0u) {
+  if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return;
   const long long t0 = clock64();
-  while (!(cluster_scope ? mbar_try_wait_cluster(bar, 0) : mbar_try_wait(bar, 0))) {
+  while (!(cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))) {
     if (clock64() - t0 > WAIT_CYCLES) {
       atomicOr(err, STRATA_DEVERR_TIMEOUT);
       ctl[CTL_TIMEOUT] = 1u;
@@ -290,9 +350,12 @@ constexpr int BATCH_VECS = DT == 0 ? 4 : 2;  // 16 elements
 // running max `mx`, the batch `bmx` that holds it and the largest max `mx2` of the thread's other
 // batches, and the sum of exp(x - ref) in two partial sums.  The reference `ref` moves to the piece's max only when that
 // exceeds it by LAZY_SHIFT (or on the first finite piece), so the common piece costs one compare.
+// `slot` holds piece p (vectors p * PIECE_VECS ...) for the vectors below n_full; the ragged last
+// vector (n_full, when the chunk's bytes are not a multiple of 16) comes from global memory.
 template <int DT>
-__device__ __forceinline__ void pass1_piece(const unsigned char* data, int p, int v0, int n_vec, float& ref,
-                                            float& mx, float& mx2, int& bmx, float& s0, float& s1) {
+__device__ __forceinline__ void pass1_piece(const unsigned char* slot, const unsigned char* gchunk, int p, int n_full,
+                                            int n_vec, int n_el, float& ref, float& mx, float& mx2, int& bmx, float& s0,
+                                            float& s1) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
   constexpr int RB = BATCH_VECS<DT>;  // vectors held at once: one batch of 16 elements
 #pragma unroll
@@ -300,9 +363,12 @@ __device__ __forceinline__ void pass1_piece(const unsigned char* data, int p, in
     float x[RB][EPV];
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
-      const int v = v0 + (r0 + r) * NT;
-      if (v < n_vec) {
-        load_vec<DT>(data, v, x[r]);
+      const int vl = static_cast<int>(threadIdx.x) + (r0 + r) * NT;
+      const int v = p * PIECE_VECS + vl;
+      if (v < n_full) {
+        load_vec<DT>(slot, vl, x[r]);
+      } else if (v < n_vec) {
+        load_vec_g<DT>(gchunk, v, n_el, x[r]);
       } else {
 #pragma unroll
         for (int e = 0; e < EPV; ++e) x[r][e] = -INFINITY;
@@ -340,38 +406,40 @@ __device__ __forceinline__ void pass1_piece(const unsigned char* data, int p, in
 }
 
 // Append one candidate that carries no penalty to both lists (two independent shared atomics).
-__device__ __forceinline__ void append_both(uint32_t* ctl, uint4* cand_pen, uint64_t* cand_raw, uint64_t key, float raw,
-                                            bool to_raw, bool to_pen) {
+__device__ __forceinline__ void append_both(uint32_t* ctl, uint4* cand_pen, uint64_t* cand_raw, int cap, uint64_t key,
+                                            float raw, bool to_raw, bool to_pen) {
   const uint32_t ip = to_pen ? atomicAdd(&ctl[CTL_CAND_PEN], 1u) : 0u;
   const uint32_t ir = to_raw ? atomicAdd(&ctl[CTL_CAND_RAW], 1u) : 0u;
-  if (to_pen && ip < LOCAL_CAP)
+  if (to_pen && ip < static_cast<uint32_t>(cap))
     cand_pen[ip] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
-  if (to_raw && ir < LOCAL_CAP) cand_raw[ir] = key;
+  if (to_raw && ir < static_cast<uint32_t>(cap)) cand_raw[ir] = key;
 }
 
 // Every element at or above T that carries no penalty, among this thread's vectors v_first,
 // v_first + NT, ... up to v_last: appended to both lists with its raw logit.  Out of line: only a
 // thread whose maximum and whose best other batch both reach T takes this full rescan.
 template <int DT>
-__device__ __noinline__ void rescan_candidates(const unsigned char* data, int v_first, int v_last, int n_vec, int n_el,
+__device__ __noinline__ void rescan_candidates(const unsigned char* g, int v_first, int v_last, int n_vec, int n_el,
                                                int lo, float Tf, bool penal, const uint32_t* htab, int hash_bits,
-                                               uint32_t* ctl,
-                                               uint4* cand_pen, uint64_t* cand_raw, bool to_raw, bool to_pen) {
+                                               uint32_t* ctl, uint4* cand_pen, uint64_t* cand_raw, int cap, bool to_raw,
+                                               bool to_pen) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
 #pragma unroll 1
   for (int v = v_first; v < n_vec && v <= v_last; v += NT) {
     float x[EPV];
-    load_vec<DT>(data, v, x);
+    load_vec_g<DT>(g, v, n_el, x);
     uint32_t hit = 0u;  // elements of this vector at or above T (NaN compares false)
 #pragma unroll
     for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(x[e] >= Tf) << e;
 #pragma unroll 1
     for (; hit != 0u; hit &= hit - 1u) {
-      const uint32_t loc = static_cast<uint32_t>(v * EPV + __ffs(hit) - 1);
-      const float xv = elem_at<DT>(data, loc);
+      const int e = __ffs(hit) - 1;
+      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+      if (loc >= static_cast<uint32_t>(n_el)) continue;
+      const float xv = pick(x, e);
       const uint32_t o = order_key(xv);
-      if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (penal && hash_count(htab, hash_bits, loc) != 0u)) continue;
-      append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, to_raw, to_pen);
+      if (o == 0u || (penal && hash_count(htab, hash_bits, loc) != 0u)) continue;
+      append_both(ctl, cand_pen, cand_raw, cap, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, to_raw, to_pen);
     }
   }
 }
@@ -382,7 +450,8 @@ template <int DT>
 __device__ __noinline__ void masked_candidates(const unsigned char* data, int lo, int hi, int a0, int a1, int a2,
                                                int a3, const int32_t* allowed, int j_first, int a_end,
                                                uint32_t* mbits, bool penal, const uint32_t* htab, int hash_bits,
-                                               float rep, float freq, float pres, uint32_t* ctl, uint4* cand_pen) {
+                                               float rep, float freq, float pres, uint32_t* ctl, uint4* cand_pen,
+                                               int cap) {
   auto add = [&](int id) {
     if (id < lo || id >= hi) return;
     const uint32_t loc = static_cast<uint32_t>(id - lo);
@@ -394,7 +463,7 @@ __device__ __noinline__ void masked_candidates(const unsigned char* data, int lo
     if (op == 0u) return;
     const uint32_t s = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
     const uint64_t key = sel_key(op, static_cast<uint32_t>(id));
-    if (s < LOCAL_CAP)
+    if (s < static_cast<uint32_t>(cap))
       cand_pen[s] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
   };
   add(a0);
@@ -479,7 +548,7 @@ __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, i
     uint64_t best = 0ull;
     for (int v = tid; v < n_vec; v += NT) {
       float x[EPV];
-      load_vec<DT>(data, v, x);
+      load_vec_g<DT>(data, v, n_el, x);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
         const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
@@ -508,6 +577,37 @@ __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, i
     prev = best;
     got = r + 1;
   }
+  __syncthreads();
+  return got;
+}
+
+// The best `need` entries of a candidate list longer than RANK_LIMIT (heavy ties), in order, by
+// argmax rounds over the list itself; they end up at the head of the list.  Entries are `words`
+// 32-bit words with the 64-bit key first; keys are distinct.  `tmp` holds need * words words.
+// Every thread of the CTA calls it; returns the number kept.
+__device__ __noinline__ int buffer_rounds(uint32_t* list, int words, int n, int need, uint32_t* tmp, uint64_t* red64) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  uint64_t prev = ~0ull;
+  int got = 0;
+  for (int r = 0; r < need; ++r) {
+    uint64_t best = 0ull;
+    for (int i = tid; i < n; i += NT) {
+      const uint2 o = *reinterpret_cast<const uint2*>(list + i * words);
+      const uint64_t k = (static_cast<uint64_t>(o.y) << 32) | o.x;
+      if (k < prev && k > best) best = k;
+    }
+    best = block_max_u64(best, red64, lane, wid);
+    if (best == 0ull) break;
+    for (int i = tid; i < n; i += NT) {
+      const uint2 o = *reinterpret_cast<const uint2*>(list + i * words);
+      if (((static_cast<uint64_t>(o.y) << 32) | o.x) == best)
+        for (int w = 0; w < words; ++w) tmp[r * words + w] = list[i * words + w];
+    }
+    prev = best;
+    got = r + 1;
+  }
+  __syncthreads();
+  for (int i = tid; i < got * words; i += NT) list[i] = tmp[i];
   __syncthreads();
   return got;
 }
@@ -590,18 +690,24 @@ __device__ __forceinline__ void sort8_desc(uint32_t (&v)[8]) {
   cx(1, 2); cx(3, 4); cx(5, 6);
 }
 
-// The end of a sampled row's arrival on its slot's packed counter word (warp-wide, the leader's
-// warp 0; lane 0 holds the value its arrival atomic returned): the row that completes the call's
-// arrivals for the slot advances the counter by one and clears them.  r_s counts the call's rows of
-// the slot (the first 64 row slots were fetched ahead into rs0/rs1).
-__device__ __noinline__ void slot_arrival_done(int rs0, int rs1, const int32_t* row_slot, int B, int slot,
-                                               unsigned long long* ctr, unsigned long long ctr_old, int lane) {
+// Rows of the call whose slot is `slot` (warp-wide; the first 64 row slots were fetched ahead into
+// rs0/rs1).
+__device__ __forceinline__ int slot_rows(int rs0, int rs1, const int32_t* row_slot, int B, int slot, int lane) {
   int r_s = __popc(__ballot_sync(FULL_MASK, rs0 == slot)) + __popc(__ballot_sync(FULL_MASK, rs1 == slot));
   for (int b0 = 64; b0 < B; b0 += 32) {
     const int b = b0 + lane;
     r_s += __popc(__ballot_sync(FULL_MASK, b < B && row_slot[b] == slot));
   }
-  if (lane == 0 && (ctr_old & 0xFFFFull) + 1ull == static_cast<unsigned long long>(r_s))
+  return r_s;
+}
+
+// The end of a sampled row's arrival on its slot's packed counter word (lane 0 holds the value its
+// atomic returned).  A slot with one row in the call advanced its counter in that same atomic; with
+// r_s > 1 rows, each added one arrival, and the row that completes them advances the counter by one
+// and clears them.
+__device__ __forceinline__ void slot_arrival_done(int r_s, int slot, unsigned long long* ctr,
+                                                  unsigned long long ctr_old, int lane) {
+  if (r_s > 1 && lane == 0 && (ctr_old & 0xFFFFull) + 1ull == static_cast<unsigned long long>(r_s))
     atomicAdd(&ctr[slot], (1ull << 16) - static_cast<unsigned long long>(r_s));
 }
 
@@ -688,18 +794,24 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const int cs = P.cs;
   const int row = blockIdx.x / cs;
   const bool mask_launch = MASK && P.mode == MODE_SAMPLE && P.allowed_off != nullptr;
-  const Layout L = make_layout(P.chunk, ESZ, P.hash_cap, cs, P.kmax, P.nmax, mask_launch);
+  const Layout L = make_layout(P.chunk, P.hash_cap, cs, P.kmax, P.nmax, P.nslot, P.allowed_off != nullptr, mask_launch);
   const int lo = static_cast<int>(crank) * P.chunk;
   const int hi = min(P.V, lo + P.chunk);
   const int n_el = max(0, hi - lo);
   const int bytes = n_el * ESZ;
   const int bytes_al = bytes & ~15;
   const int n_vec = (bytes + 15) >> 4;
+  const int n_full = bytes_al >> 4;  // vectors the bulk copies bring; a ragged last one is read directly
   const int n_pieces = (bytes_al + PIECE_BYTES - 1) / PIECE_BYTES;
+  const int nslot = P.nslot;
+  const int cap = L.cand_cap;
+  const int Q = NW * P.qw;                                  // keys this CTA publishes
+  const uint32_t rec_bytes = static_cast<uint32_t>(Q + 4) * 4u;
 
-  unsigned char* data = sm + L.data;
+  unsigned char* data = sm + L.data;  // the ring of pieces in flight
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + L.mbar);
   const char* grow = static_cast<const char*>(P.logits) + (static_cast<long long>(row) * P.ld + lo) * ESZ;
+  const unsigned char* gchunk = reinterpret_cast<const unsigned char*>(grow);
 
   // row metadata, first level: independent loads.  Thread 0 issues its own after the copies and
   // the barrier fence (a release fence behind outstanding loads would wait for them); every other
@@ -723,10 +835,11 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   if (tid != 0) load_meta1();
 
   // ---- 1. barriers and the bulk copies of this chunk ----------------------------------------
-  if (tid == 0) {  // the copies go out first; the exchange barriers are set up behind them
-    for (int p = 0; p < n_pieces; ++p) mbar_init(&mbar[p], 1);
+  if (tid == 0) {  // the first pieces go out first; the exchange barriers are set up behind them
+    const int n0 = min(nslot, n_pieces);
+    for (int p = 0; p < n0; ++p) mbar_init(&mbar[p], 1);
     fence_proxy_async_smem();
-    for (int p = 0; p < n_pieces; ++p) {
+    for (int p = 0; p < n0; ++p) {
       const uint32_t nb = static_cast<uint32_t>(min(PIECE_BYTES, bytes_al - p * PIECE_BYTES));
       mbar_arrive_expect_tx(&mbar[p], nb);
       bulk_g2s(data + p * PIECE_BYTES, grow + p * PIECE_BYTES, nb, &mbar[p]);
@@ -734,7 +847,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     mbar_init(&mbar[BAR_X0], 2);                   // the announced bytes + this CTA's own record
     mbar_init(&mbar[BAR_X1], cs > 1 ? cs - 1 : 1); // one arrival per other CTA (leader only)
     fence_mbar_init();
-    mbar_arrive_expect_tx(&mbar[BAR_X0], static_cast<uint32_t>((cs - 1) * XREC_BYTES));
+    mbar_arrive_expect_tx(&mbar[BAR_X0], static_cast<uint32_t>(cs - 1) * rec_bytes);
   }
   grid_dep_launch();
   if (tid == 0) load_meta1();
@@ -744,8 +857,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   uint32_t* abits = reinterpret_cast<uint32_t*>(sm + L.abits);
   uint32_t* mbits = reinterpret_cast<uint32_t*>(sm + L.mbits);
   uint32_t* htab = reinterpret_cast<uint32_t*>(sm + L.hash);
+  uint32_t* hraw = reinterpret_cast<uint32_t*>(sm + L.hraw);
   uint32_t* hflag = reinterpret_cast<uint32_t*>(sm + L.hflag);
-  uint32_t* wmax = reinterpret_cast<uint32_t*>(sm + L.wmax);
+  uint32_t* wkey = reinterpret_cast<uint32_t*>(sm + L.wkey);
   uint64_t* red64 = reinterpret_cast<uint64_t*>(sm + L.red);
   float4* red4 = reinterpret_cast<float4*>(sm + L.red);
   uint32_t* ctl = reinterpret_cast<uint32_t*>(sm + L.ctl);
@@ -759,36 +873,15 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   uint4* sorted_pen = reinterpret_cast<uint4*>(sm + L.sorted_pen);
   uint64_t* sorted_raw = reinterpret_cast<uint64_t*>(sm + L.sorted_raw);
 
-  // The ragged last vector (chunk bytes not a multiple of 16) is read with plain loads by the
-  // thread that owns it in every pass, padded with -inf.
-  if (bytes > bytes_al && tid == (n_vec - 1) % NT) {
-    const int tv = n_vec - 1;
-    if constexpr (DT == 0) {
-      const float* g = reinterpret_cast<const float*>(grow);
-      float* d = reinterpret_cast<float*>(data);
-      for (int e = 0; e < EPV; ++e) {
-        const int idx = tv * EPV + e;
-        d[idx] = idx < n_el ? g[idx] : -INFINITY;
-      }
-    } else {
-      const uint16_t* g = reinterpret_cast<const uint16_t*>(grow);
-      uint16_t* d = reinterpret_cast<uint16_t*>(data);
-      for (int e = 0; e < EPV; ++e) {
-        const int idx = tv * EPV + e;
-        d[idx] = idx < n_el ? g[idx] : static_cast<uint16_t>(0xFF80u);
-      }
-    }
-  }
-
   const int bw_words = (P.chunk + 31) >> 5;
-  for (int i = tid; i < bw_words; i += NT) {
-    abits[i] = 0u;
-    if (mask_launch) mbits[i] = 0u;
-  }
+  if (P.allowed_off != nullptr)
+    for (int i = tid; i < bw_words; i += NT) {
+      abits[i] = 0u;
+      if (mask_launch) mbits[i] = 0u;
+    }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
   if (tid < NT / 32) hflag[tid] = 0u;
-  for (int i = tid; i < MAX_CS * XREC_WORDS; i += NT) xrec[i] = 0u;  // absent CTAs' records stay zero
-  if (tid < CTL_WORDS) ctl[tid] = (tid == CTL_T) ? 0xFFFFFFFFu : 0u;
+  if (tid < CTL_WORDS) ctl[tid] = (tid == CTL_T) ? 0xFFFFFFFFu : (tid >= CTL_LAST0 ? static_cast<uint32_t>(tid - CTL_LAST0) : 0u);
   __syncthreads();           // tables zeroed, barriers initialised
   cluster_arrive_relaxed();  // this CTA is running (remote stores wait for every CTA, below)
 
@@ -832,14 +925,20 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     aid[t] = j < a_end ? P.allowed[j] : -1;
   }
 
-  // The draw counter: each sampled row adds one arrival to its slot's packed word (counter << 16 |
-  // arrivals) and reads the counter from the returned value; the row that completes the slot's
-  // arrivals also advances the counter and clears them, so every row of the call sees the value
+  // The draw counter: a sampled row whose slot has no other row in the call reads and advances
+  // its slot's packed word (counter << 16 | arrivals) in one atomic; otherwise each row adds one
+  // arrival and reads the counter from the returned value, and the row that completes the slot's
+  // arrivals also advances the counter and clears them.  Every row of the call sees the value
   // from before the call.  The leader's warp 0 issues it once the candidates are in.
   const bool ctr_warp = k_row > 0 && wid == 0 && crank == 0 && sampled;
   const bool ctr_thread = ctr_warp && lane == 0;
   unsigned long long ctr_old = 0ull;
-  int rs_pre[2] = {-1, -1};  // row slots of the call, fetched ahead for the arrival count
+  int rs_pre[2] = {-1, -1};  // row slots of the call, fetched ahead for the count of the slot's rows
+  if (crank == 0 && wid == 0 && P.mode == MODE_SAMPLE) {
+    rs_pre[0] = lane < P.B ? P.row_slot[lane] : -1;
+    rs_pre[1] = lane + 32 < P.B ? P.row_slot[lane + 32] : -1;
+  }
+  int r_slot = 0;  // rows of this row's slot in the call (leader's warp 0)
 
   int hid[HPRE];  // third metadata level: this thread's first history ids, for the table after the pass
 #pragma unroll
@@ -851,66 +950,111 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   // ---- 1b. first pass as pieces land ----------------------------------------------------------
   float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
   int bmx = 0;
+  // logits of this thread's first allowed and history ids, fetched once their ids have landed
+  // (after the first piece) and used after the pass
+  float aval[APRE], hval[HPRE];
+#pragma unroll
+  for (int t = 0; t < APRE; ++t) aval[t] = 0.0f;
+#pragma unroll
+  for (int j = 0; j < HPRE; ++j) hval[j] = 0.0f;
+  auto prefetch = [&]() {
+#pragma unroll
+    for (int t = 0; t < APRE; ++t)
+      if (aid[t] >= lo && aid[t] < hi) aval[t] = elem_at<DT>(gchunk, static_cast<uint32_t>(aid[t] - lo));
+#pragma unroll
+    for (int j = 0; j < HPRE; ++j)
+      if (hid[j] >= lo && hid[j] < hi) hval[j] = elem_at<DT>(gchunk, static_cast<uint32_t>(hid[j] - lo));
+  };
   {
+    // pieces stream through the ring: the last warp done with a slot refills it with the piece
+    // nslot further on
     const int n_iter = (n_vec + PIECE_VECS - 1) / PIECE_VECS;
+    if (n_iter == 0) prefetch();
+    int si = 0;
+    uint32_t ph = 0u;
 #pragma unroll 1
     for (int p = 0; p < n_iter; ++p) {
-      if (p < n_pieces) wait_bar(&mbar[p], ctl, P.err, false);
-      pass1_piece<DT>(data, p, p * PIECE_VECS + tid, n_vec, ref, mx, mx2, bmx, s0, s1);
+      if (p < n_pieces) wait_bar(&mbar[si], ctl, P.err, false, ph);
+      pass1_piece<DT>(data + si * PIECE_BYTES, gchunk, p, n_full, n_vec, n_el, ref, mx, mx2, bmx, s0, s1);
+      if (p + nslot < n_pieces) {
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();  // this warp's reads of the slot are done before it counts
+          if (atomicAdd(&ctl[CTL_SLOT0 + si], 1u) == NW - 1 && ctl[CTL_TIMEOUT] == 0u) {
+            ctl[CTL_SLOT0 + si] = 0u;
+            const int pn = p + nslot;
+            ctl[CTL_LAST0 + si] = static_cast<uint32_t>(pn);
+            fence_proxy_async_smem();
+            const uint32_t nb = static_cast<uint32_t>(min(PIECE_BYTES, bytes_al - pn * PIECE_BYTES));
+            mbar_arrive_expect_tx(&mbar[si], nb);
+            bulk_g2s(data + si * PIECE_BYTES, grow + pn * PIECE_BYTES, nb, &mbar[si]);
+          }
+        }
+      }
+      if (p == 0) prefetch();
+      if (++si == nslot) {
+        si = 0;
+        ph ^= 1u;
+      }
     }
   }
-  for (int p = 0; p < n_pieces; ++p) wait_bar(&mbar[p], ctl, P.err, false);  // all pieces visible
 
   // allowed subset: this chunk's ids, each counted once, into (max, sum of exp)
   MaxSum al{-INFINITY, 0.0f};
   {
-    auto add_allowed = [&](int id) {
+    auto add_allowed = [&](int id, float x) {
       if (id >= lo && id < hi) {
         const uint32_t loc = static_cast<uint32_t>(id - lo);
         const uint32_t bit = 1u << (loc & 31);
-        if (!(atomicOr(&abits[loc >> 5], bit) & bit)) online_add(al, elem_at<DT>(data, loc));
+        if (!(atomicOr(&abits[loc >> 5], bit) & bit)) online_add(al, x);
       }
     };
 #pragma unroll
-    for (int t = 0; t < APRE; ++t) add_allowed(aid[t]);
-    for (int j = a_beg + tid + APRE * NT; j < a_end; j += NT) add_allowed(P.allowed[j]);
+    for (int t = 0; t < APRE; ++t) add_allowed(aid[t], aval[t]);
+    for (int j = a_beg + tid + APRE * NT; j < a_end; j += NT) {
+      const int id = P.allowed[j];
+      if (id >= lo && id < hi) add_allowed(id, elem_at<DT>(gchunk, static_cast<uint32_t>(id - lo)));
+    }
   }
 
   // ---- history table of this chunk's id range, and the owners of its ids (their ids were fetched
   // before the first pass and have landed by now) ------------------------------------------------
   if (penal) {
-    auto add_hist = [&](int id) {
+    auto add_hist = [&](int id, bool have, float x) {
       if (id >= lo && id < hi) {
         const uint32_t loc = static_cast<uint32_t>(id - lo);
         const uint32_t owner = (loc / EPV) % NT;
         atomicOr(&hflag[owner >> 5], 1u << (owner & 31));
-        if (!hash_add(htab, P.hash_bits, loc)) atomicOr(P.err, STRATA_DEVERR_HISTORY);
+        const int h = hash_add(htab, P.hash_bits, loc);
+        if (h == -2) atomicOr(P.err, STRATA_DEVERR_HISTORY);
+        if (h >= 0) hraw[h] = __float_as_uint(have ? x : elem_at<DT>(gchunk, loc));  // the entry's creator
       }
     };
 #pragma unroll
-    for (int j = 0; j < HPRE; ++j) add_hist(hid[j]);
-    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(hb[(h_start + static_cast<uint32_t>(i)) & h_mask]);
+    for (int j = 0; j < HPRE; ++j) add_hist(hid[j], true, hval[j]);
+    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(hb[(h_start + static_cast<uint32_t>(i)) & h_mask], false, 0.0f);
   }
   __syncthreads();  // history table and owner flags complete
 
-  // ---- 2. this CTA's record: warp maxima (ids without a penalty) and (max, sum) pairs ---------
-  // The candidate test key covers every id of the thread; the threshold key must be the value of
-  // an id without a penalty, so a thread that owns a history id publishes nothing (a valid, very
-  // slightly weaker bound).
+  // ---- 2. this CTA's record: the qw largest thread maxima of each warp (ids without a penalty)
+  // and the (max, sum) pairs.  The candidate test key covers every id of the thread; a threshold
+  // key must be the value of an id without a penalty, so a thread that owns a history id
+  // publishes nothing (a valid, very slightly weaker bound).
   const uint32_t kall = tid < n_vec ? order_key(mx) : 0u;
   const uint32_t kthr = (penal && ((hflag[tid >> 5] >> (tid & 31)) & 1u)) ? 0u : kall;
   {
-    const uint32_t wm = __reduce_max_sync(FULL_MASK, kthr);
+    uint32_t kk = kthr;
+#pragma unroll 1
+    for (int r = 0; r < P.qw; ++r) {  // the warp's r-th largest thread maximum, then drop it
+      const uint32_t m = __reduce_max_sync(FULL_MASK, kk);
+      if (lane == 0) wkey[wid * QW_MAX + r] = m;
+      const uint32_t b = __ballot_sync(FULL_MASK, kk == m);
+      if (lane == __ffs(b) - 1) kk = 0u;
+    }
     const MaxSum wrow = warp_ms_fast(MaxSum{ref, s0 + s1});
     const MaxSum wal = warp_ms_fast(al);
-    if (lane == 0) {
-      wmax[wid] = wm;
-      red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
-    }
+    if (lane == 0) red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
   }
-  // q: warp maxima published per CTA, the largest first: 4 when 4*cs covers 2K, else all NW
-  // (unused slots are zero)
-  const int q = kp > 0 ? (4 * cs >= 2 * kp ? 4 : NW) : 0;
   __syncthreads();
   if (wid == 0) {
     // the CTA's (max, sum) pairs: lanes 0..NW-1 combine the row's, lanes 16..16+NW-1 the allowed
@@ -929,20 +1073,15 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 #pragma unroll
     for (int off = NW / 2; off > 0; off >>= 1) sc += __shfl_xor_sync(FULL_MASK, sc, off);
     const float Ma = __shfl_sync(FULL_MASK, M, 16), Sa = __shfl_sync(FULL_MASK, sc, 16);
-    if (lane == 0) {  // this CTA's record: the q largest warp-maximum keys, zeros, the two pairs
-      uint4* own = reinterpret_cast<uint4*>(xrec + crank * XREC_WORDS);
-      static_assert(NW == 8, "the record's key selection sorts the 8 warp maxima");
-      uint32_t k8[NW];
-#pragma unroll
-      for (int i = 0; i < NW; ++i) k8[i] = wmax[i];
-      sort8_desc(k8);
-      own[0] = make_uint4(k8[0], k8[1], k8[2], k8[3]);
-      own[1] = q > 4 ? make_uint4(k8[4], k8[5], k8[6], k8[7]) : make_uint4(0u, 0u, 0u, 0u);
-      own[2] = make_uint4(0u, 0u, 0u, 0u);
-      own[3] = make_uint4(0u, 0u, 0u, 0u);
-      own[4] = make_uint4(__float_as_uint(M), __float_as_uint(sc), __float_as_uint(Ma), __float_as_uint(Sa));
-      mbar_arrive(&mbar[BAR_X0]);  // own record in place (release by this lane)
-    }
+    // this CTA's record: key i = the (i / NW)-th largest of warp i % NW, then the two pairs
+    static_assert(NW == 8, "record key i belongs to warp i % 8");
+    uint32_t* own = xrec + crank * XREC_WORDS;
+    for (int i = lane; i < Q; i += 32) own[i] = wkey[(i & (NW - 1)) * QW_MAX + (i >> 3)];
+    if (lane == 0)
+      *reinterpret_cast<uint4*>(own + Q) =
+          make_uint4(__float_as_uint(M), __float_as_uint(sc), __float_as_uint(Ma), __float_as_uint(Sa));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&mbar[BAR_X0]);  // own record in place (release by this lane)
     __syncwarp();
   }
   cluster_wait();  // every CTA of the cluster is running: remote stores are safe from here on
@@ -950,8 +1089,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     const uint4* own = reinterpret_cast<const uint4*>(xrec + crank * XREC_WORDS);
     const uint32_t dst = dsmem_addr(smem_u32(xrec + crank * XREC_WORDS), static_cast<uint32_t>(lane));
     const uint32_t bar = dsmem_addr(smem_u32(&mbar[BAR_X0]), static_cast<uint32_t>(lane));
-#pragma unroll
-    for (int i = 0; i < XREC_WORDS / 4; ++i) {
+    const int n4 = (Q + 4) >> 2;
+#pragma unroll 1
+    for (int i = 0; i < n4; ++i) {
       const uint4 v = own[i];
       st_async_v4(dst + 16u * i, v.x, v.y, v.z, v.w, bar);
     }
@@ -959,52 +1099,47 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   wait_bar(&mbar[BAR_X0], ctl, P.err, true);  // every CTA's record is here
 
   // ---- the row threshold T and the log-normalisers -------------------------------------------
-  // T = the kp-th largest of the cs*q published keys (zeros included, so T = 0 when fewer than
-  // kp real keys exist): the smallest published key with fewer than kp keys above it.  A forced
-  // split can publish fewer than kp keys in all; then there is no bound (T = 0).  TL lanes count
-  // for each key; the last warp reduces the (max, sum) pairs meanwhile.
+  // T = the kp-th largest of the cs*Q published keys (zeros included, so T = 0 when fewer than
+  // kp real keys exist): the smallest published key with fewer than kp keys above it.  The keys
+  // are values of distinct ids, so at least kp ids reach T.  One thread per key counts; the last
+  // warp reduces the (max, sum) pairs meanwhile.
   if (kp > 0) {
-    // keys are addressed as (record, slot) with a power-of-two slot count QS >= q: slots beyond
-    // q and records beyond cs hold zero, which never counts as above and qualifies as T only when
-    // fewer than kp real keys exist (then T = 0, the right answer).  No runtime guard, no division.
-    constexpr int TL = NT / (MAX_CS * 4);  // lanes per key (all keys in one pass when q <= 4);
-    static_assert(TL >= 1 && (TL & (TL - 1)) == 0, "lanes per key");  // lane `sub` counts records sub, sub+TL, ...
-    const int qs_log = q <= 4 ? 2 : 3;
-    const int nq4 = 1 << (qs_log - 2), sub = tid & (TL - 1);
+    const int nk = cs * Q;
+    const int qlog = 31 - __clz(Q);  // Q is a power of two
 #pragma unroll 1
-    for (int base = 0; base < (MAX_CS << qs_log); base += NT / TL) {
-      const int i = base + tid / TL;
-      const int c = i >> qs_log;
-      const uint32_t u = xrec[c * XREC_WORDS + (i & ((1 << qs_log) - 1))];
-      int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+    for (int base = 0; base < nk; base += NT) {
+      const int i = base + tid;
+      uint32_t cand = 0xFFFFFFFFu;
+      if (i < nk) {
+        const uint32_t u = xrec[(i >> qlog) * XREC_WORDS + (i & (Q - 1))];
+        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll 1
-      for (int j4 = 0; j4 < nq4; ++j4) {
-#pragma unroll
-        for (int k = 0; k < MAX_CS / TL; ++k) {
-          const uint4 v = reinterpret_cast<const uint4*>(xrec + (sub + k * TL) * XREC_WORDS)[j4];
-          a0 += v.x > u;
-          a1 += v.y > u;
-          a2 += v.z > u;
-          a3 += v.w > u;
+        for (int c = 0; c < cs; ++c) {
+          const uint4* rk = reinterpret_cast<const uint4*>(xrec + c * XREC_WORDS);
+#pragma unroll 2
+          for (int j = 0; j < (Q >> 2); ++j) {
+            const uint4 v = rk[j];
+            a0 += v.x > u;
+            a1 += v.y > u;
+            a2 += v.z > u;
+            a3 += v.w > u;
+          }
         }
+        if ((a0 + a1) + (a2 + a3) < kp) cand = u;
       }
-      int above = (a0 + a1) + (a2 + a3);
-#pragma unroll
-      for (int off = 1; off < TL; off <<= 1) above += __shfl_xor_sync(FULL_MASK, above, off);
-      const uint32_t cand = (sub == 0 && above < kp) ? u : 0xFFFFFFFFu;
       const uint32_t wmin = __reduce_min_sync(FULL_MASK, cand);
-      if (lane == 0) atomicMin(&ctl[CTL_T], wmin);
+      if (lane == 0 && wmin != 0xFFFFFFFFu) atomicMin(&ctl[CTL_T], wmin);
     }
   }
   __syncthreads();
-  const uint32_t T = cs * q >= kp ? ctl[CTL_T] : 0u;  // fewer than kp published keys: no bound
+  const uint32_t T = cs * Q >= kp ? ctl[CTL_T] : 0u;  // fewer than kp published keys: no bound
   // the log-normalisers, by the last warp while the others look for candidates: lanes 0..15
   // combine the row's (max, sum) pairs, lanes 16..31 the allowed subset's
   if (wid == NW - 1) {
     const int c = lane & 15;
     float m = -INFINITY, sm_ = 0.0f;
     if (c < cs) {
-      const float2 t = reinterpret_cast<const float2*>(xrec + c * XREC_WORDS)[8 + (lane >> 4)];
+      const float2 t = reinterpret_cast<const float2*>(xrec + c * XREC_WORDS + Q)[lane >> 4];
       m = t.x;
       sm_ = t.y;
     }
@@ -1032,31 +1167,36 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         // straight-line (independent loads), then append the hits
         const int vb = (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid;
         uint32_t hit = 0u;
+        float xf[RB * EPV];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
           float x[EPV];
           if (vb + r * NT < n_vec) {
-            load_vec<DT>(data, vb + r * NT, x);
+            load_vec_g<DT>(gchunk, vb + r * NT, n_el, x);
           } else {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) x[e] = -INFINITY;
           }
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(x[e] >= Tf) << (r * EPV + e);
+          for (int e = 0; e < EPV; ++e) {
+            xf[r * EPV + e] = x[e];
+            hit |= static_cast<uint32_t>(x[e] >= Tf) << (r * EPV + e);
+          }
         }
 #pragma unroll 1
         for (; hit != 0u; hit &= hit - 1u) {
           const int b = __ffs(hit) - 1;
           const uint32_t loc = static_cast<uint32_t>((vb + (b / EPV) * NT) * EPV + (b % EPV));
-          const float xv = elem_at<DT>(data, loc);
+          if (loc >= static_cast<uint32_t>(n_el)) continue;
+          const float xv = pick(xf, b);
           const uint32_t o = order_key(xv);
-          if (o == 0u || loc >= static_cast<uint32_t>(n_el) || (own_hist && hash_count(htab, P.hash_bits, loc) != 0u))
-            continue;
-          append_both(ctl, cand_pen, cand_raw, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0, pen_from_t);
+          if (o == 0u || (own_hist && hash_count(htab, P.hash_bits, loc) != 0u)) continue;
+          append_both(ctl, cand_pen, cand_raw, cap, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0,
+                      pen_from_t);
         }
       } else {
-        rescan_candidates<DT>(data, tid, n_vec, n_vec, n_el, lo, Tf, own_hist, htab, P.hash_bits, ctl, cand_pen, cand_raw,
-                              n_row > 0, pen_from_t);
+        rescan_candidates<DT>(gchunk, tid, n_vec, n_vec, n_el, lo, Tf, own_hist, htab, P.hash_bits, ctl, cand_pen,
+                              cand_raw, cap, n_row > 0, pen_from_t);
       }
     }
     if (penal) {  // penalised ids: raw value for the raw list, penalised value for the other
@@ -1065,43 +1205,50 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         if (ent == HASH_EMPTY) continue;
         const uint32_t loc = ent >> HASH_CNT_BITS;
         const uint32_t c = ent & ((1u << HASH_CNT_BITS) - 1u);
-        const float raw = elem_at<DT>(data, loc);
+        const float raw = __uint_as_float(hraw[i]);
         const uint32_t id = static_cast<uint32_t>(lo) + loc;
         const uint32_t o = order_key(raw);
         if (o != 0u && o >= T && n_row > 0) {
           const uint32_t s = atomicAdd(&ctl[CTL_CAND_RAW], 1u);
-          if (s < LOCAL_CAP) cand_raw[s] = sel_key(o, id);
+          if (s < static_cast<uint32_t>(cap)) cand_raw[s] = sel_key(o, id);
         }
         const float pv = penalize(raw, c, sp.rep, sp.freq, sp.pres);
         const uint32_t op = order_key(pv);
         if (op != 0u && op >= T && pen_from_t) {
           const uint32_t s = atomicAdd(&ctl[CTL_CAND_PEN], 1u);
           const uint64_t key = sel_key(op, id);
-          if (s < LOCAL_CAP)
+          if (s < static_cast<uint32_t>(cap))
             cand_pen[s] = make_uint4(static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32), __float_as_uint(raw), 0u);
         }
       }
     }
     if (masked)  // every named id of this chunk once, with its penalised value
-      masked_candidates<DT>(data, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + threadIdx.x + APRE * NT,
-                            a_end, mbits, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, ctl, cand_pen);
+      masked_candidates<DT>(gchunk, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + threadIdx.x + APRE * NT,
+                            a_end, mbits, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, ctl, cand_pen, cap);
     __syncthreads();
 
     int np = static_cast<int>(ctl[CTL_CAND_PEN]);
     int nr = static_cast<int>(ctl[CTL_CAND_RAW]);
-    // more candidates than the buffer holds (heavy ties): exact argmax rounds write the chunk's
-    // best k_row / n_row in order into the candidate buffers
-    if (k_row > 0 && np > LOCAL_CAP) {
+    // more candidates than the buffer holds (extreme ties): exact argmax rounds over the chunk
+    // write its best k_row / n_row in order into the candidate buffers; more than RANK_LIMIT in
+    // the buffer: argmax rounds over the buffer keep the best ones at its head
+    if (k_row > 0 && np > cap) {
       if (MASK && masked)
-        np = masked_rounds<DT>(data, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + tid + APRE * NT, a_end,
-                               k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, red64, cand_pen);
+        np = masked_rounds<DT>(gchunk, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + tid + APRE * NT,
+                               a_end, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, red64, cand_pen);
       else
-        np = exact_rounds<DT>(data, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+        np = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
                               red64, cand_pen, cand_raw);
+    } else if (k_row > 0 && np > RANK_LIMIT) {
+      np = buffer_rounds(reinterpret_cast<uint32_t*>(cand_pen), 4, np, k_row, reinterpret_cast<uint32_t*>(sorted_pen),
+                         red64);
     }
-    if (n_row > 0 && nr > LOCAL_CAP)
-      nr = exact_rounds<DT>(data, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
+    if (n_row > 0 && nr > cap)
+      nr = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
                             red64, cand_pen, cand_raw);
+    else if (n_row > 0 && nr > RANK_LIMIT)
+      nr = buffer_rounds(reinterpret_cast<uint32_t*>(cand_raw), 2, nr, n_row, reinterpret_cast<uint32_t*>(sorted_raw),
+                         red64);
     if (k_row == 0) np = 0;
     if (n_row == 0) nr = 0;
 
@@ -1195,12 +1342,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   // ---- 4. the leader ranks the received keys exactly -------------------------------------------
   if (kp > 0 && crank == 0) {
     if (cs > 1) wait_bar(&mbar[BAR_X1], ctl, P.err, true);
+    if (ctr_warp) r_slot = slot_rows(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, lane);
     // issued here, consumed by the draw: the merge and the tail's first half hide the latency
-    if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
-    if (ctr_warp) {
-      rs_pre[0] = lane < P.B ? P.row_slot[lane] : -1;
-      rs_pre[1] = lane + 32 < P.B ? P.row_slot[lane + 32] : -1;
-    }
+    if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], r_slot == 1 ? (1ull << 16) : 1ull);
     __syncthreads();  // every slice (the leader's own included) is in place
     // slice offsets (every copying warp scans the counts itself), then warp c copies slice c into
     // the dense lists (the candidate buffers, free by now)
@@ -1226,18 +1370,18 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       for (int c = wid; c < cs; c += NW) {
         const int my_p = __shfl_sync(FULL_MASK, pc, c), my_r = __shfl_sync(FULL_MASK, rc, c);
         const int off_p = __shfl_sync(FULL_MASK, ip, c) - my_p, off_r = __shfl_sync(FULL_MASK, ir, c) - my_r;
-        if (tp <= LOCAL_CAP - 8)
+        if (tp <= cap - 8)
           for (int j = lane; j < my_p; j += 32) {
             const uint64_t k = recv_pkey[c * P.kmax + j];
             cand_pen[off_p + j] = make_uint4(static_cast<uint32_t>(k), static_cast<uint32_t>(k >> 32),
                                              recv_praw[c * P.kmax + j], 0u);
           }
-        if (tr <= LOCAL_CAP - 8)
+        if (tr <= cap - 8)
           for (int j = lane; j < my_r; j += 32) cand_raw[off_r + j] = recv_raw[c * P.nmax + j];
       }
       if (wid == 0 && lane < 8) {  // zero keys pad both lists to a multiple of 8
-        if (tp + lane < LOCAL_CAP) cand_pen[tp + lane] = make_uint4(0u, 0u, 0u, 0u);
-        if (tr + lane < LOCAL_CAP) cand_raw[tr + lane] = 0ull;
+        if (tp + lane < cap) cand_pen[tp + lane] = make_uint4(0u, 0u, 0u, 0u);
+        if (tr + lane < cap) cand_raw[tr + lane] = 0ull;
       }
     }
     __syncthreads();
@@ -1249,7 +1393,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       for (int f = half; f < tot_p; f += NT / 2) {
         uint4 ent;
         int rank;
-        if (tot_p <= LOCAL_CAP - 8) {
+        if (tot_p <= cap - 8) {
           ent = cand_pen[f];
           rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_pen), 4, (tot_p + 7) & ~7,
                            (static_cast<uint64_t>(ent.y) << 32) | ent.x);
@@ -1269,7 +1413,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       for (int f = half; f < tot_r; f += NT / 2) {
         uint64_t key;
         int rank;
-        if (tot_r <= LOCAL_CAP - 8) {
+        if (tot_r <= cap - 8) {
           key = cand_raw[f];
           rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_raw), 2, (tot_r + 7) & ~7, key);
         } else {
@@ -1344,7 +1488,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   // until it ends ---------------------------------------------------------------------------------
   if (early && crank == 0) {
     grid_dep_wait();
-    if (ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], 1ull);
+    if (ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], r_slot == 1 ? (1ull << 16) : 1ull);
   }
 
   // allowed-subset log-probabilities and the given chosen id
@@ -1404,13 +1548,13 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       } else if (k_eff == 0) {
         if (lane == 0) atomicOr(P.err, STRATA_DEVERR_NOCAND);
         // a sampled row without a candidate still counted itself among its slot's arrivals
-        if (sampled) slot_arrival_done(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, P.ctr, ctr_old, lane);
+        if (sampled) slot_arrival_done(r_slot, slot, P.ctr, ctr_old, lane);
       } else {
         int j = 0;
         if (sampled) {
           uint32_t x0 = 0u;
-          slot_arrival_done(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, P.ctr, ctr_old, lane);
           if (ctr_thread) x0 = philox_word0(sp.seed, pos, ctr_old >> 16);
+          slot_arrival_done(r_slot, slot, P.ctr, ctr_old, lane);
           x0 = __shfl_sync(FULL_MASK, x0, 0);
           const float u = static_cast<float>(x0 >> 8) * 0x1p-24f;
           const int last = m2 - 1;  // the draw reads prefixes below m2 only; W = C[m2 - 1]
@@ -1468,7 +1612,10 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   }
   if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
   if (ctl[CTL_TIMEOUT] != 0u) {  // a copy may still be in flight into this CTA: bounded wait again
-    for (int p = 0; p < n_pieces; ++p) wait_bar(&mbar[p], ctl, P.err, false);
+    for (int si = 0; si < min(nslot, n_pieces); ++si) {
+      const int pl = static_cast<int>(ctl[CTL_LAST0 + si]);
+      wait_bar(&mbar[si], ctl, P.err, false, static_cast<uint32_t>(pl / nslot) & 1u);
+    }
   }
 }
 

@@ -41,8 +41,15 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(STRATA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-constexpr int CHUNK_TARGET_BYTES = 64 * 1024;  // preferred bytes of logits per CTA
-constexpr int MIN_CHUNK_ELEMS = 2048;          // do not split a row finer than this
+// Blocks per row.  Pipelined calls (early loads: the next call's loads overlap this one) are
+// throughput-bound, so a row goes to few blocks that each stream up to PIPELINED_BYTES of logits;
+// otherwise a call is latency-bound, so rows split into blocks of about LATENCY_BYTES, enough of
+// them to fill the GPU (but no block below MIN_CHUNK_ELEMS ids).
+constexpr int PIPELINED_BYTES = 128 * 1024;
+constexpr int LATENCY_BYTES = 64 * 1024;
+constexpr int MIN_CHUNK_ELEMS = 2048;
+constexpr int RING_SLOTS = 4;                 // pieces in flight per CTA when shared memory allows
+constexpr int SMEM_THREE_PER_SM = 74 * 1024;  // a CTA at or below this leaves room for three per SM
 constexpr int KEY_BINS = STRATA_MAX_TOP_K + 1;
 constexpr int LASTN_BINS = STRATA_MAX_PENALTY_LAST_N + 1;
 
@@ -114,53 +121,74 @@ int check_device(const strata_ctx* c) {
 }
 
 struct Shape {
-  int cs, chunk, smem, kmax, nmax, hash_cap, hash_bits;
+  int cs, chunk, smem, kmax, nmax, hash_cap, hash_bits, nslot, qw;
 };
 
-int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int top_n_eff, bool with_hist,
-                  uint32_t flags, Shape* s) {
-  const int esz = dtype == STRATA_DTYPE_F32 ? 4 : 2;
+// The launch shape of a call: blocks per row (one cluster), the chunk each streams, ring slots,
+// keys each warp publishes for the row threshold, history table size and shared memory.  Shared
+// by the context calls and the allocation-free call.
+int shape_for(int max_cluster, int max_smem, int num_sms, int mode, int esz, int B, int V, int kmax, int nmax,
+              int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined, int forced, Shape* s) {
   const long long row_bytes = static_cast<long long>(V) * esz;
-  s->nmax = top_n_eff;
-  s->kmax = mode == strata::MODE_SAMPLE ? std::max(1, max_k_sampled(c)) : 0;
-  const int kp_max = std::max(s->kmax, s->nmax);
-  const int forced = static_cast<int>((flags >> 8) & 0x1Fu);
+  s->nmax = nmax;
+  s->kmax = kmax;
+  const int kp_max = std::max(kmax, nmax);
   int cs;
   if (forced > 0) {
-    if (forced > c->max_cluster) return fail(STRATA_ERANGE, "forced split %d above the cluster limit %d", forced, c->max_cluster);
+    if (forced > max_cluster) return fail(STRATA_ERANGE, "forced split %d above the cluster limit %d", forced, max_cluster);
     cs = forced;
+  } else if (pipelined) {
+    cs = static_cast<int>((row_bytes + PIPELINED_BYTES - 1) / PIPELINED_BYTES);
+    cs = std::min(std::max(cs, 1), max_cluster);
   } else {
-    const int cs_bytes = static_cast<int>((row_bytes + CHUNK_TARGET_BYTES - 1) / CHUNK_TARGET_BYTES);
-    const int cs_q = (kp_max + strata::QMAX - 1) / strata::QMAX;
-    const int cs_fill = (c->num_sms + B - 1) / std::max(1, B);
+    const int cs_bytes = static_cast<int>((row_bytes + LATENCY_BYTES - 1) / LATENCY_BYTES);
+    const int cs_fill = (num_sms + B - 1) / std::max(1, B);
     const int cs_small = std::max(1, (V + MIN_CHUNK_ELEMS - 1) / MIN_CHUNK_ELEMS);
-    cs = std::max({cs_bytes, cs_q, std::min(cs_fill, cs_small), 1});
-    cs = std::min(cs, c->max_cluster);
+    cs = std::max({cs_bytes, std::min(cs_fill, cs_small), 1});
+    cs = std::min(cs, max_cluster);
   }
   int chunk = (V + cs - 1) / cs;
   chunk = (chunk + 15) / 16 * 16;
-  if (static_cast<long long>(chunk) * esz > static_cast<long long>(strata::MAX_PIECES) * strata::PIECE_BYTES)
-    return fail(STRATA_ERANGE, "V=%d needs %d bytes per block (limit %d)", V, chunk * esz,
-                strata::MAX_PIECES * strata::PIECE_BYTES);
   s->cs = cs;
   s->chunk = chunk;
+  // keys per warp: enough that the row publishes about 2 * kp of them (a tight threshold)
+  const int per_warp = (2 * kp_max + cs * strata::NW - 1) / (cs * strata::NW);
+  int qw = 1;
+  while (qw < per_warp && qw < strata::QW_MAX) qw *= 2;
+  s->qw = qw;
   s->hash_cap = 0;
   s->hash_bits = 0;
-  if (mode == strata::MODE_SAMPLE && with_hist) {
-    const int ln = max_lastn_penal(c);
-    if (ln > 0) {
-      int bits = 6;
-      while ((1 << bits) < 2 * ln) ++bits;
-      s->hash_bits = bits;
-      s->hash_cap = 1 << bits;
-    }
+  if (mode == strata::MODE_SAMPLE && with_hist && lastn_max > 0) {
+    int bits = 6;
+    while ((1 << bits) < 2 * lastn_max) ++bits;
+    s->hash_bits = bits;
+    s->hash_cap = 1 << bits;
   }
-  const Layout L = strata::make_layout(chunk, esz, s->hash_cap, cs, s->kmax, s->nmax,
-                                       mode == strata::MODE_SAMPLE && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u);
+  // the most ring slots that still leave room for three CTAs on the SM (at least 2)
+  Layout L{};
+  for (int ns = RING_SLOTS; ns >= 2; --ns) {
+    L = strata::make_layout(chunk, s->hash_cap, cs, kmax, nmax, ns, with_allowed, mask);
+    s->nslot = ns;
+    if (static_cast<int>(L.total) <= SMEM_THREE_PER_SM) break;
+  }
   if (!strata::layout_aligned(L)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
+  if (L.cand_cap < cs * std::max(kmax, nmax) + 8) return fail(STRATA_EINVAL, "internal: candidate lists too small");
   s->smem = static_cast<int>(L.total);
-  if (s->smem > c->max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit %d", s->smem, c->max_smem);
+  if (s->smem > max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit %d", s->smem, max_smem);
   return STRATA_OK;
+}
+
+int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int top_n_eff, bool with_hist,
+                  bool with_allowed, uint32_t flags, Shape* s) {
+  const int esz = dtype == STRATA_DTYPE_F32 ? 4 : 2;
+  const int kmax = mode == strata::MODE_SAMPLE ? std::max(1, max_k_sampled(c)) : 0;
+  const bool mask = mode == strata::MODE_SAMPLE && with_allowed && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u;
+  // calls that read kept histories wait for the previous call before their penalties: they do
+  // not overlap, so they take the latency split
+  const bool pipelined = (flags & STRATA_FLAG_PDL) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u &&
+                         (flags & STRATA_FLAG_HISTORY_RING) == 0u;
+  return shape_for(c->max_cluster, c->max_smem, c->num_sms, mode, esz, B, V, kmax, top_n_eff, max_lastn_penal(c),
+                   with_hist, with_allowed, mask, pipelined, static_cast<int>((flags >> 8) & 0x1Fu), s);
 }
 
 int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t flags, cudaStream_t stream) {
@@ -517,7 +545,7 @@ int strata_launch_shape(strata_ctx* c, int mode, int dtype, int B, int V, int to
   if (dtype != STRATA_DTYPE_F32 && dtype != STRATA_DTYPE_BF16) return fail(STRATA_EINVAL, "dtype %d", dtype);
   if (B < 1 || V < 1 || V > c->max_vocab || top_n < 0 || top_n > STRATA_MAX_TOP_N) return fail(STRATA_EINVAL, "shape");
   Shape sh;
-  const int rc = compute_shape(c, mode, dtype, B, V, top_n, true, flags, &sh);
+  const int rc = compute_shape(c, mode, dtype, B, V, top_n, true, false, flags, &sh);
   if (rc != STRATA_OK) return rc;
   if (split) *split = sh.cs;
   if (chunk_elems) *chunk_elems = sh.chunk;
@@ -550,8 +578,8 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   if (B == 0) return STRATA_OK;
   const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
   Shape sh;
-  if ((rc = compute_shape(c, strata::MODE_SAMPLE, dtype, B, V, top_n_eff, hist_off != nullptr || kept_hist, flags, &sh)) !=
-      STRATA_OK)
+  if ((rc = compute_shape(c, strata::MODE_SAMPLE, dtype, B, V, top_n_eff, hist_off != nullptr || kept_hist,
+                          allowed_off != nullptr, flags, &sh)) != STRATA_OK)
     return rc;
   KParams P{};
   P.logits = logits;
@@ -586,6 +614,8 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   P.err = c->d_err;
   P.hash_cap = sh.hash_cap;
   P.hash_bits = sh.hash_bits;
+  P.nslot = sh.nslot;
+  P.qw = sh.qw;
   P.flags = flags;
   P.row_draft = row_draft;
   P.slot_keep = slot_keep;
@@ -630,7 +660,9 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
   if (B == 0) return STRATA_OK;
   const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
   Shape sh;
-  if ((rc = compute_shape(c, strata::MODE_LOGPROBS, dtype, B, V, top_n_eff, false, flags, &sh)) != STRATA_OK) return rc;
+  if ((rc = compute_shape(c, strata::MODE_LOGPROBS, dtype, B, V, top_n_eff, false, allowed_off != nullptr, flags, &sh)) !=
+      STRATA_OK)
+    return rc;
   KParams P{};
   P.logits = logits;
   P.ld = ld;
@@ -653,6 +685,8 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
   P.ctr = c->d_ctr;
   P.max_slots = c->max_slots;
   P.err = c->d_err;
+  P.nslot = sh.nslot;
+  P.qw = sh.qw;
   P.flags = flags;
   return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream));
 }
@@ -798,31 +832,9 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
   // launch shape (same rules as a context's)
   const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
   Shape sh;
-  sh.nmax = top_n_eff;
-  sh.kmax = std::max(1, kmax_sampled);
-  const int kp_max = std::max(sh.kmax, sh.nmax);
-  const long long row_bytes = static_cast<long long>(V) * esz;
-  int cs = std::max({static_cast<int>((row_bytes + CHUNK_TARGET_BYTES - 1) / CHUNK_TARGET_BYTES),
-                     (kp_max + strata::QMAX - 1) / strata::QMAX,
-                     std::min((nd->num_sms + B - 1) / B, std::max(1, (V + MIN_CHUNK_ELEMS - 1) / MIN_CHUNK_ELEMS)), 1});
-  cs = std::min(cs, nd->max_cluster);
-  int chunk = ((V + cs - 1) / cs + 15) / 16 * 16;
-  if (static_cast<long long>(chunk) * esz > static_cast<long long>(strata::MAX_PIECES) * strata::PIECE_BYTES)
-    return fail(STRATA_ERANGE, "V=%d needs %d bytes per block", V, chunk * esz);
-  sh.cs = cs;
-  sh.chunk = chunk;
-  sh.hash_cap = 0;
-  sh.hash_bits = 0;
-  if (hist_off != nullptr && max_lastn > 0) {
-    int bits = 6;
-    while ((1 << bits) < 2 * max_lastn) ++bits;
-    sh.hash_bits = bits;
-    sh.hash_cap = 1 << bits;
-  }
-  const Layout L = strata::make_layout(chunk, esz, sh.hash_cap, cs, sh.kmax, sh.nmax);
-  if (!strata::layout_aligned(L)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
-  sh.smem = static_cast<int>(L.total);
-  if (sh.smem > nd->max_smem) return fail(STRATA_ERANGE, "shared memory %d above the device limit", sh.smem);
+  if ((rc = shape_for(nd->max_cluster, nd->max_smem, nd->num_sms, strata::MODE_SAMPLE, esz, B, V, std::max(1, kmax_sampled),
+                      top_n_eff, max_lastn, hist_off != nullptr, false, false, false, 0, &sh)) != STRATA_OK)
+    return rc;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((e = cudaMemcpyAsync(nd->scratch, st.head, NA_CTR + sizeof(unsigned long long) * B, cudaMemcpyHostToDevice, s)) != cudaSuccess)
@@ -856,6 +868,8 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
   P.err = reinterpret_cast<uint32_t*>(nd->scratch);
   P.hash_cap = sh.hash_cap;
   P.hash_bits = sh.hash_bits;
+  P.nslot = sh.nslot;
+  P.qw = sh.qw;
   P.flags = 0;
   return launch(nullptr, P, dtype, sh, 0u, s);
 }
