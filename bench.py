@@ -321,7 +321,9 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     if s.errors() != 0:
         raise RuntimeError("device error bits set")
-    shape = s.shape(0, 0, B, w["V"], w["top_n"], flags)
+    # the launch shape of a plain call with these flags; verify windows and kept-history calls are
+    # steps of one request's decode and take the latency split (as a call without early loads)
+    shape = s.shape(0, 0, B, w["V"], w["top_n"], flags & ~STRATA_FLAG_EARLY_LOAD if verify else flags)
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
@@ -398,17 +400,20 @@ def run_gpu(args, rank, world):
         h_out = {"ids": h_out["ids"], "keep": torch.empty(1, dtype=torch.int32, pin_memory=True)}
     d2h = int(sum(v.numel() * v.element_size() for v in h_out.values()))
 
+    # the e2e inputs are copied in right before each call, so those calls do not claim early loads
+    flags_e2e = flags & ~STRATA_FLAG_EARLY_LOAD
+
     def e2e_step():
         d_logits.copy_(h_logits[0], non_blocking=True)
         for k, v in h_small.items():
             d_small[k].copy_(v, non_blocking=True)
         if verify:
             s.verify(d_logits, d_small["row_slot"], d_small["row_pos"], d_small["row_draft"], hist=d_small.get("hist"),
-                     hist_off=d_small.get("hist_off"), flags=flags, stream=stream, out=out)
+                     hist_off=d_small.get("hist_off"), flags=flags_e2e, stream=stream, out=out)
         else:
             s.sample(d_logits, d_small["row_slot"], d_small["row_pos"], hist=d_small["hist"],
                      hist_off=d_small["hist_off"], top_n=w["top_n"], chosen_lp=True, allowed=d_small["allowed"],
-                     allowed_off=d_small["allowed_off"], flags=flags, stream=stream, out=out)
+                     allowed_off=d_small["allowed_off"], flags=flags_e2e, stream=stream, out=out)
         for k, v in h_out.items():
             v.copy_(out[k][:v.numel()], non_blocking=True)
 

@@ -179,14 +179,14 @@ int shape_for(int max_cluster, int max_smem, int num_sms, int mode, int esz, int
 }
 
 int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int top_n_eff, bool with_hist,
-                  bool with_allowed, uint32_t flags, Shape* s) {
+                  bool with_allowed, uint32_t flags, Shape* s, bool verify = false) {
   const int esz = dtype == STRATA_DTYPE_F32 ? 4 : 2;
   const int kmax = mode == strata::MODE_SAMPLE ? std::max(1, max_k_sampled(c)) : 0;
   const bool mask = mode == strata::MODE_SAMPLE && with_allowed && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u;
-  // calls that read kept histories wait for the previous call before their penalties: they do
-  // not overlap, so they take the latency split
+  // verify windows and calls that read kept histories are steps of one request's decode (the
+  // latter wait for the previous call before their penalties): they take the latency split
   const bool pipelined = (flags & STRATA_FLAG_PDL) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u &&
-                         (flags & STRATA_FLAG_HISTORY_RING) == 0u;
+                         (flags & STRATA_FLAG_HISTORY_RING) == 0u && !verify;
   return shape_for(c->max_cluster, c->max_smem, c->num_sms, mode, esz, B, V, kmax, top_n_eff, max_lastn_penal(c),
                    with_hist, with_allowed, mask, pipelined, static_cast<int>((flags >> 8) & 0x1Fu), s);
 }
@@ -579,7 +579,7 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
   Shape sh;
   if ((rc = compute_shape(c, strata::MODE_SAMPLE, dtype, B, V, top_n_eff, hist_off != nullptr || kept_hist,
-                          allowed_off != nullptr, flags, &sh)) != STRATA_OK)
+                          allowed_off != nullptr, flags, &sh, row_draft != nullptr)) != STRATA_OK)
     return rc;
   KParams P{};
   P.logits = logits;
