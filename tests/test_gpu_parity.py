@@ -120,9 +120,6 @@ def test_random_edge_cases(sampler, seed):
     set_slots(sampler, w)
     from request_token_sampling_gb300 import STRATA_FLAG_SPLIT
     split = int(rng.choice([0, 0, 1, 2, 3, 16]))
-    esz = 2 if dtype == "bf16" else 4
-    if split and -(-V // split) * esz > 190_000:
-        split = 0
     g = gpu_sample(sampler, w, flags=STRATA_FLAG_SPLIT(split))
     rows, ctr = oracle.sample_call(w)
     compare_sample(w, rows, g)
@@ -133,7 +130,40 @@ def test_random_edge_cases(sampler, seed):
         assert sampler.slot_state(s)[1] == ctr[s]
 
 
-@pytest.mark.parametrize("split", [6, 8, 13, 16])
+def test_config4_pipelined_calls(sampler):
+    """The launch bench.py times: back-to-back calls with programmatic dependent launch and early
+    loads (few, large chunks per row), no host synchronisation in between; every call's picks,
+    alternatives and log-probabilities against the oracle, the counters advancing call by call."""
+    from request_token_sampling_gb300 import STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL
+    base = synth.config4(fused=True)
+    set_slots(sampler, base)
+    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD
+    assert sampler.shape(0, 0, base["B"], base["V"], base["top_n"], fl)["split"] < \
+        sampler.shape(0, 0, base["B"], base["V"], base["top_n"], 0)["split"]
+    ws, ds, outs = [], [], []
+    for c in range(5):
+        w = dict(base)
+        w["logits"] = np.roll(base["logits"], 977 * c, axis=1) if c else base["logits"]
+        ws.append(w)
+        ds.append(upload(w))
+    torch.cuda.synchronize()
+    for w, d in zip(ws, ds):
+        outs.append(sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=d["hist"],
+                                   hist_off=d["hist_off"], top_n=w["top_n"], chosen_lp=True, allowed=d["allowed"],
+                                   allowed_off=d["allowed_off"], flags=fl))
+    torch.cuda.synchronize()
+    counters = dict(base["counters"])
+    st = Stats()
+    for w, o in zip(ws, outs):
+        rows, counters = oracle.sample_call(w, counters=counters)
+        compare_sample(w, rows, {k: v.cpu().numpy() for k, v in o.items()}, stats=st, debug=False)
+    for s in base["slot_params"]:
+        assert sampler.slot_state(s)[1] == counters[s]
+    _check_no_errors(sampler)
+    print("config4 pipelined", st)
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 6, 8, 13, 16])
 def test_full_vocab_every_split(sampler, split):
     """The 248,320-id rows give the same answer whatever the number of CTAs per row."""
     from request_token_sampling_gb300 import STRATA_FLAG_SPLIT

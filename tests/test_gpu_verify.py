@@ -130,6 +130,33 @@ def test_verify_graph_replay_resets_the_window_words(sampler):
     assert sampler.slot_state(0)[1] == 4
 
 
+def test_verify_pipelined_windows(sampler):
+    """Six windows of config 2 enqueued back to back with programmatic dependent launch and early
+    loads: the five rows of a window share one slot (every row counts itself in, the last one
+    advances the counter), and each window must see the counter the previous one left."""
+    from request_token_sampling_gb300 import STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL
+    w0 = synth.config2_window(60)
+    set_slots(sampler, w0, {0: 0})
+    rng = np.random.default_rng(3)
+    ws, drafts, outs = [], [], []
+    for k in range(6):
+        w = synth.config2_window(60 + k, counter=k)
+        ws.append(w)
+        drafts.append([int(x) for x in rng.integers(0, w["V"], 4)] + [-1])
+    ds = [upload(w) for w in ws]
+    drs = [torch.from_numpy(np.asarray(d, np.int32)).to("cuda:0") for d in drafts]
+    torch.cuda.synchronize()
+    for w, d, dr in zip(ws, ds, drs):
+        outs.append(sampler.verify(d["logits"], d["row_slot"], d["row_pos"], dr, V=w["V"], hist=d["hist"],
+                                   hist_off=d["hist_off"], chosen_lp=True,
+                                   flags=STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD))
+    torch.cuda.synchronize()
+    for k, (w, o) in enumerate(zip(ws, outs)):
+        rows, _, _ = oracle.verify_call(w, drafts[k], counters={0: k})
+        _check(w, rows, {key: v.cpu().numpy() for key, v in o.items()}, drafts[k])
+    assert sampler.slot_state(0)[1] == 6
+
+
 def test_verify_needs_drafts_and_keep(sampler):
     import request_token_sampling_gb300 as S
     w = synth.config1()
