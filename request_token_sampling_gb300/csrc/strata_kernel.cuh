@@ -61,7 +61,9 @@ constexpr uint32_t SLOT_PENAL = 2u;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // bounded waits: ~2 s at GB300 clocks
 constexpr float LAZY_SHIFT = 16.0f;          // the exp reference moves only when the max passes it by this
 constexpr int XKEYS = NW * QW_MAX;           // published keys per CTA, at most
-constexpr int XREC_WORDS = XKEYS + 4;        // record stride: the keys, then 2 (max, sum) pairs
+// A CTA's record: its NW * qw keys, then 2 (max, sum) pairs; records sit NW * qw + 4 words apart
+// (a multiple of 16 bytes, since NW * qw is a multiple of 8).
+__host__ __device__ inline int xrec_words(int qw) { return NW * qw + 4; }
 constexpr int HPRE = 2;                      // history ids per thread fetched ahead of the table build
 constexpr int APRE = 4;                      // allowed ids per thread fetched ahead
 constexpr int BAR_X0 = MAX_SLOTS;            // mbarrier: every CTA's published record has landed
@@ -145,7 +147,7 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 
 // Shared-memory layout of one CTA; identical in every CTA of a launch.  `data` is the ring of
 // `nslot` pieces; once the first pass is done it holds the candidate lists.
-__host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, int kmax, int nmax, int nslot,
+__host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, int kmax, int nmax, int nslot, int qw,
                                               bool allowed, bool mask) {
   Layout L;
   uint32_t o = 0;
@@ -176,7 +178,7 @@ __host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, i
   o += CTL_WORDS * 4;
   o = align_up(o, 16);
   L.xrec = o;
-  o += static_cast<uint32_t>(cs) * XREC_WORDS * 4;
+  o += static_cast<uint32_t>(cs * xrec_words(qw)) * 4;
   L.recv_cnt = o;
   o += MAX_CS * 8;
   L.recv_pkey = o;  // received penalised list: keys (8 B) and raw logits (4 B), kmax per CTA
@@ -794,7 +796,8 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const int cs = P.cs;
   const int row = blockIdx.x / cs;
   const bool mask_launch = MASK && P.mode == MODE_SAMPLE && P.allowed_off != nullptr;
-  const Layout L = make_layout(P.chunk, P.hash_cap, cs, P.kmax, P.nmax, P.nslot, P.allowed_off != nullptr, mask_launch);
+  const Layout L = make_layout(P.chunk, P.hash_cap, cs, P.kmax, P.nmax, P.nslot, P.qw, P.allowed_off != nullptr,
+                               mask_launch);
   const int lo = static_cast<int>(crank) * P.chunk;
   const int hi = min(P.V, lo + P.chunk);
   const int n_el = max(0, hi - lo);
@@ -806,6 +809,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const int nslot = P.nslot;
   const int cap = L.cand_cap;
   const int Q = NW * P.qw;                                  // keys this CTA publishes
+  const int XW = Q + 4;                                     // record stride in words
   const uint32_t rec_bytes = static_cast<uint32_t>(Q + 4) * 4u;
 
   unsigned char* data = sm + L.data;  // the ring of pieces in flight
@@ -1075,7 +1079,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     const float Ma = __shfl_sync(FULL_MASK, M, 16), Sa = __shfl_sync(FULL_MASK, sc, 16);
     // this CTA's record: key i = the (i / NW)-th largest of warp i % NW, then the two pairs
     static_assert(NW == 8, "record key i belongs to warp i % 8");
-    uint32_t* own = xrec + crank * XREC_WORDS;
+    uint32_t* own = xrec + crank * XW;
     for (int i = lane; i < Q; i += 32) own[i] = wkey[(i & (NW - 1)) * QW_MAX + (i >> 3)];
     if (lane == 0)
       *reinterpret_cast<uint4*>(own + Q) =
@@ -1086,8 +1090,8 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   }
   cluster_wait();  // every CTA of the cluster is running: remote stores are safe from here on
   if (wid == 0 && lane < cs && static_cast<uint32_t>(lane) != crank) {
-    const uint4* own = reinterpret_cast<const uint4*>(xrec + crank * XREC_WORDS);
-    const uint32_t dst = dsmem_addr(smem_u32(xrec + crank * XREC_WORDS), static_cast<uint32_t>(lane));
+    const uint4* own = reinterpret_cast<const uint4*>(xrec + crank * XW);
+    const uint32_t dst = dsmem_addr(smem_u32(xrec + crank * XW), static_cast<uint32_t>(lane));
     const uint32_t bar = dsmem_addr(smem_u32(&mbar[BAR_X0]), static_cast<uint32_t>(lane));
     const int n4 = (Q + 4) >> 2;
 #pragma unroll 1
@@ -1111,11 +1115,11 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       const int i = base + tid;
       uint32_t cand = 0xFFFFFFFFu;
       if (i < nk) {
-        const uint32_t u = xrec[(i >> qlog) * XREC_WORDS + (i & (Q - 1))];
+        const uint32_t u = xrec[(i >> qlog) * XW + (i & (Q - 1))];
         int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll 1
         for (int c = 0; c < cs; ++c) {
-          const uint4* rk = reinterpret_cast<const uint4*>(xrec + c * XREC_WORDS);
+          const uint4* rk = reinterpret_cast<const uint4*>(xrec + c * XW);
 #pragma unroll 2
           for (int j = 0; j < (Q >> 2); ++j) {
             const uint4 v = rk[j];
@@ -1139,7 +1143,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     const int c = lane & 15;
     float m = -INFINITY, sm_ = 0.0f;
     if (c < cs) {
-      const float2 t = reinterpret_cast<const float2*>(xrec + c * XREC_WORDS + Q)[lane >> 4];
+      const float2 t = reinterpret_cast<const float2*>(xrec + c * XW + Q)[lane >> 4];
       m = t.x;
       sm_ = t.y;
     }

@@ -49,7 +49,6 @@ constexpr int PIPELINED_BYTES = 128 * 1024;
 constexpr int LATENCY_BYTES = 64 * 1024;
 constexpr int MIN_CHUNK_ELEMS = 2048;
 constexpr int RING_SLOTS = 4;                 // pieces in flight per CTA when shared memory allows
-constexpr int SMEM_THREE_PER_SM = 74 * 1024;  // a CTA at or below this leaves room for three per SM
 constexpr int KEY_BINS = STRATA_MAX_TOP_K + 1;
 constexpr int LASTN_BINS = STRATA_MAX_PENALTY_LAST_N + 1;
 
@@ -61,6 +60,7 @@ struct strata_ctx {
   int max_slots = 0, max_vocab = 0, max_rows = 0;
   int max_cluster = 8;
   int max_smem = 0;
+  int smem_three = 0;  // the most dynamic shared memory per CTA that still fits three CTAs per SM
   SlotDev* d_slots = nullptr;
   unsigned long long* d_ctr = nullptr;
   uint32_t* d_done = nullptr;  // per slot: rows of the current verify call done (reset by the last)
@@ -120,6 +120,16 @@ int check_device(const strata_ctx* c) {
   return STRATA_OK;
 }
 
+// Dynamic shared memory per CTA for three CTAs per SM, kept ~12 KB per SM below the largest
+// shared-memory carveout: measured on GB300, a fourth 16 KiB ring slot that takes the carveout to
+// its limit (and the L1 data cache down with it) costs more than the slot brings.
+constexpr int SMEM_L1_MARGIN = 4 * 1024;
+int smem_for_three(const cudaDeviceProp& prop) {
+  const int per_sm = static_cast<int>(prop.sharedMemPerMultiprocessor);
+  const int reserved = static_cast<int>(prop.reservedSharedMemPerBlock);
+  return std::min(static_cast<int>(prop.sharedMemPerBlockOptin), per_sm / 3 - reserved - SMEM_L1_MARGIN) & ~127;
+}
+
 struct Shape {
   int cs, chunk, smem, kmax, nmax, hash_cap, hash_bits, nslot, qw;
 };
@@ -127,8 +137,9 @@ struct Shape {
 // The launch shape of a call: blocks per row (one cluster), the chunk each streams, ring slots,
 // keys each warp publishes for the row threshold, history table size and shared memory.  Shared
 // by the context calls and the allocation-free call.
-int shape_for(int max_cluster, int max_smem, int num_sms, int mode, int esz, int B, int V, int kmax, int nmax,
-              int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined, int forced, Shape* s) {
+int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mode, int esz, int B, int V, int kmax,
+              int nmax, int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined, int forced,
+              Shape* s) {
   const long long row_bytes = static_cast<long long>(V) * esz;
   s->nmax = nmax;
   s->kmax = kmax;
@@ -167,9 +178,9 @@ int shape_for(int max_cluster, int max_smem, int num_sms, int mode, int esz, int
   // the most ring slots that still leave room for three CTAs on the SM (at least 2)
   Layout L{};
   for (int ns = RING_SLOTS; ns >= 2; --ns) {
-    L = strata::make_layout(chunk, s->hash_cap, cs, kmax, nmax, ns, with_allowed, mask);
+    L = strata::make_layout(chunk, s->hash_cap, cs, kmax, nmax, ns, s->qw, with_allowed, mask);
     s->nslot = ns;
-    if (static_cast<int>(L.total) <= SMEM_THREE_PER_SM) break;
+    if (static_cast<int>(L.total) <= smem_three) break;
   }
   if (!strata::layout_aligned(L)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
   if (L.cand_cap < cs * std::max(kmax, nmax) + 8) return fail(STRATA_EINVAL, "internal: candidate lists too small");
@@ -187,7 +198,8 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
   // latter wait for the previous call before their penalties): they take the latency split
   const bool pipelined = (flags & STRATA_FLAG_PDL) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u &&
                          (flags & STRATA_FLAG_HISTORY_RING) == 0u && !verify;
-  return shape_for(c->max_cluster, c->max_smem, c->num_sms, mode, esz, B, V, kmax, top_n_eff, max_lastn_penal(c),
+  return shape_for(c->max_cluster, c->max_smem, c->smem_three, c->num_sms, mode, esz, B, V, kmax, top_n_eff,
+                   max_lastn_penal(c),
                    with_hist, with_allowed, mask, pipelined, static_cast<int>((flags >> 8) & 0x1Fu), s);
 }
 
@@ -311,6 +323,7 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
   c->max_vocab = max_vocab;
   c->max_rows = max_rows;
   c->max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
+  c->smem_three = smem_for_three(prop);
   c->k_bins.assign(KEY_BINS, 0);
   c->lastn_bins.assign(LASTN_BINS, 0);
 
@@ -722,7 +735,7 @@ namespace {
 struct NoallocDevice {
   bool ready = false;
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-  int num_sms = 0, max_cluster = 8, max_smem = 0;
+  int num_sms = 0, max_cluster = 8, max_smem = 0, smem_three = 0;
 };
 constexpr int NA_MAX_DEVICES = 64;
 NoallocDevice g_na[NA_MAX_DEVICES];
@@ -741,6 +754,7 @@ int noalloc_setup(int dev, NoallocDevice** out) {
     if (prop.major < 10) return fail(STRATA_ECUDA, "device %s is not a Blackwell GPU", prop.name);
     d.num_sms = prop.multiProcessorCount;
     d.max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
+    d.smem_three = smem_for_three(prop);
     const void* kernels[2] = {reinterpret_cast<const void*>(strata::rows_kernel<0, false>),
                               reinterpret_cast<const void*>(strata::rows_kernel<1, false>)};
     for (const void* k : kernels) {
@@ -832,7 +846,8 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
   // launch shape (same rules as a context's)
   const int top_n_eff = (top_n > 0 && top_ids != nullptr) ? top_n : 0;
   Shape sh;
-  if ((rc = shape_for(nd->max_cluster, nd->max_smem, nd->num_sms, strata::MODE_SAMPLE, esz, B, V, std::max(1, kmax_sampled),
+  if ((rc = shape_for(nd->max_cluster, nd->max_smem, nd->smem_three, nd->num_sms, strata::MODE_SAMPLE, esz, B, V,
+                      std::max(1, kmax_sampled),
                       top_n_eff, max_lastn, hist_off != nullptr, false, false, false, 0, &sh)) != STRATA_OK)
     return rc;
 
