@@ -292,7 +292,10 @@ int strata_read_errors(strata_ctx *ctx, uint32_t *bits, void *stream);
 /*
  * The launch shape a call with these arguments would use (host only, nothing enqueued):
  * blocks per row (the thread-block cluster size), elements per block, dynamic shared memory
- * bytes and the total grid size.  mode 0 = strata_sample_rows, 1 = strata_logprobs_rows.
+ * bytes and the total grid size.  mode 0 = strata_sample_rows, 1 = strata_logprobs_rows.  The
+ * shape is that of a call without allowed lists and, for mode 0, of strata_sample_rows (allowed
+ * lists add a bitmap of the block's ids to its shared memory, which can leave one ring slot fewer;
+ * strata_sample_verify splits rows as a call without STRATA_FLAG_EARLY_LOAD does).
  */
 int strata_launch_shape(strata_ctx *ctx, int mode, int dtype, int B, int V, int top_n,
                         uint32_t flags, int *split, int *chunk_elems, int *smem_bytes, int *grid);
