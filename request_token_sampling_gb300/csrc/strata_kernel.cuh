@@ -1055,6 +1055,15 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       const uint32_t b = __ballot_sync(FULL_MASK, kk == m);
       if (lane == __ffs(b) - 1) kk = 0u;
     }
+    // a thread whose maximum was published is the likeliest to reach T: bring the batch that holds
+    // its maximum back into L1 now, so that the candidate scan after the exchange finds it there
+    if (kk == 0u && kthr != 0u) {
+      constexpr int RB = BATCH_VECS<DT>;
+      const int vb = (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid;
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+        if (vb + r * NT < n_full) prefetch_l1(gchunk + static_cast<size_t>(vb + r * NT) * 16);
+    }
     const MaxSum wrow = warp_ms_fast(MaxSum{ref, s0 + s1});
     const MaxSum wal = warp_ms_fast(al);
     if (lane == 0) red4[wid] = make_float4(wrow.m, wrow.s, wal.m, wal.s);
@@ -1110,17 +1119,21 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   if (kp > 0) {
     const int nk = cs * Q;
     const int qlog = 31 - __clz(Q);  // Q is a power of two
+    // lpk consecutive lanes count for one key, lane `sub` over records sub, sub + lpk, ...
+    int lpk = 1;
+    while (lpk < 16 && nk * lpk * 2 <= NT) lpk *= 2;
+    const int llog = 31 - __clz(lpk), sub = tid & (lpk - 1);
 #pragma unroll 1
-    for (int base = 0; base < nk; base += NT) {
-      const int i = base + tid;
-      uint32_t cand = 0xFFFFFFFFu;
+    for (int base = 0; base < nk * lpk; base += NT) {
+      const int i = (base + tid) >> llog;
+      uint32_t u = 0xFFFFFFFFu;
+      int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
       if (i < nk) {
-        const uint32_t u = xrec[(i >> qlog) * XW + (i & (Q - 1))];
-        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+        u = xrec[(i >> qlog) * XW + (i & (Q - 1))];
 #pragma unroll 1
-        for (int c = 0; c < cs; ++c) {
+        for (int c = sub; c < cs; c += lpk) {
           const uint4* rk = reinterpret_cast<const uint4*>(xrec + c * XW);
-#pragma unroll 2
+#pragma unroll 4
           for (int j = 0; j < (Q >> 2); ++j) {
             const uint4 v = rk[j];
             a0 += v.x > u;
@@ -1129,8 +1142,10 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
             a3 += v.w > u;
           }
         }
-        if ((a0 + a1) + (a2 + a3) < kp) cand = u;
       }
+      int above = (a0 + a1) + (a2 + a3);
+      for (int off = 1; off < lpk; off <<= 1) above += __shfl_xor_sync(FULL_MASK, above, off);
+      const uint32_t cand = (i < nk && sub == 0 && above < kp) ? u : 0xFFFFFFFFu;
       const uint32_t wmin = __reduce_min_sync(FULL_MASK, cand);
       if (lane == 0 && wmin != 0xFFFFFFFFu) atomicMin(&ctl[CTL_T], wmin);
     }
