@@ -909,13 +909,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const int32_t* hb = P.hist;
   if (penal) {
     if (kept_hist) {
-      // the previous call appends to the ring: with early loads this is where the row waits for it
-      if (early) grid_dep_wait();
-      const unsigned long long n = P.hlen[slot];
-      h_len = static_cast<int>(min(static_cast<unsigned long long>(sp.last_n), n));
+      // the previous call appends to the ring, so its window is read after the first pass (below)
       hb = P.ring + static_cast<size_t>(slot) * STRATA_HISTORY_CAP;
       h_mask = STRATA_HISTORY_CAP - 1;
-      h_start = static_cast<uint32_t>(n - static_cast<unsigned long long>(h_len)) & h_mask;
     } else {
       const int hs = P.hist_off[slot], he = P.hist_off[slot + 1];
       h_len = min(sp.last_n, max(0, he - hs));
@@ -1021,8 +1017,15 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     }
   }
 
-  // ---- history table of this chunk's id range, and the owners of its ids (their ids were fetched
-  // before the first pass and have landed by now) ------------------------------------------------
+  // ---- history table of this chunk's id range, and the owners of its ids (a caller's window was
+  // fetched before the first pass and has landed by now; a kept history is read now, after the
+  // previous call: with early loads the first pass ran while that call finished) ---------------
+  if (penal && kept_hist) {
+    if (early) grid_dep_wait();
+    const unsigned long long n = P.hlen[slot];
+    h_len = static_cast<int>(min(static_cast<unsigned long long>(sp.last_n), n));
+    h_start = static_cast<uint32_t>(n - static_cast<unsigned long long>(h_len)) & h_mask;
+  }
   if (penal) {
     auto add_hist = [&](int id, bool have, float x) {
       if (id >= lo && id < hi) {
@@ -1036,7 +1039,8 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     };
 #pragma unroll
     for (int j = 0; j < HPRE; ++j) add_hist(hid[j], true, hval[j]);
-    for (int i = tid + HPRE * NT; i < h_len; i += NT) add_hist(hb[(h_start + static_cast<uint32_t>(i)) & h_mask], false, 0.0f);
+    for (int i = tid + (kept_hist ? 0 : HPRE * NT); i < h_len; i += NT)
+      add_hist(hb[(h_start + static_cast<uint32_t>(i)) & h_mask], false, 0.0f);
   }
   __syncthreads();  // history table and owner flags complete
 
