@@ -86,6 +86,10 @@ extern "C" {
  * update happens on the device, so a captured call carries the history forward on every replay.
  * Ignored by strata_logprobs_rows.                                                              */
 #define STRATA_FLAG_HISTORY_RING 0x8u
+/* Testing aid: the row leaders also wait for one arrival that nothing sends, so that their bounded
+ * device wait (about two seconds) runs out: the call sets STRATA_DEVERR_TIMEOUT, its outputs are
+ * undefined, and the context stays usable.  It exercises the failure path without a GPU fault.  */
+#define STRATA_FLAG_TEST_STALL  0x10000u
 /* Testing aid: force the number of thread blocks (1..16) that split each row; 0 = automatic.   */
 #define STRATA_FLAG_SPLIT(n)    (((uint32_t)(n) & 0x1Fu) << 8)
 

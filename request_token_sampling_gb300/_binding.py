@@ -34,6 +34,7 @@ STRATA_FLAG_PDL = 0x1
 STRATA_FLAG_EARLY_LOAD = 0x2
 STRATA_FLAG_ALLOWED_MASK = 0x4
 STRATA_FLAG_HISTORY_RING = 0x8
+STRATA_FLAG_TEST_STALL = 0x10000
 
 
 def STRATA_FLAG_SPLIT(n: int) -> int:

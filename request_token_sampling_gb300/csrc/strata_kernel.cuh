@@ -68,7 +68,8 @@ constexpr int HPRE = 2;                      // history ids per thread fetched a
 constexpr int APRE = 4;                      // allowed ids per thread fetched ahead
 constexpr int BAR_X0 = MAX_SLOTS;            // mbarrier: every CTA's published record has landed
 constexpr int BAR_X1 = MAX_SLOTS + 1;        // mbarrier (leader): every CTA's candidates have landed
-constexpr int NBAR = MAX_SLOTS + 2;
+constexpr int BAR_STALL = MAX_SLOTS + 2;     // mbarrier nothing arrives at (STRATA_FLAG_TEST_STALL)
+constexpr int NBAR = MAX_SLOTS + 3;
 
 // Control words in shared memory.
 enum : int {
@@ -158,7 +159,7 @@ __host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, i
   L.cand_pen = L.data;
   L.cand_raw = L.data + static_cast<uint32_t>(L.cand_cap) * 16u;
   L.mbar = o;
-  o += NBAR * 8;
+  o = align_up(o + NBAR * 8, 16);
   const uint32_t bw = align_up((static_cast<uint32_t>(chunk) + 31) / 32 * 4, 16);
   L.abits = o;  // allowed ids met in this chunk (calls with allowed lists only)
   o += allowed ? bw : 0u;
@@ -334,6 +335,10 @@ __device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t* ctl, uint32_t*
     }
   }
 }
+
+// STRATA_FLAG_TEST_STALL: a bounded wait on an mbarrier nothing arrives at (it runs out).  Out of
+// line, so that the common path carries none of it.
+__device__ __noinline__ void test_stall(uint64_t* bar, uint32_t* ctl, uint32_t* err) { wait_bar(bar, ctl, err, false); }
 
 __device__ __forceinline__ void online_add(MaxSum& a, float v) {
   if (v == -INFINITY || v != v) return;
@@ -850,6 +855,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     }
     mbar_init(&mbar[BAR_X0], 2);                   // the announced bytes + this CTA's own record
     mbar_init(&mbar[BAR_X1], cs > 1 ? cs - 1 : 1); // one arrival per other CTA (leader only)
+    mbar_init(&mbar[BAR_STALL], 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&mbar[BAR_X0], static_cast<uint32_t>(cs - 1) * rec_bytes);
   }
@@ -1363,6 +1369,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   float va = 0.0f, vb = 0.0f;
 
   // ---- 4. the leader ranks the received keys exactly -------------------------------------------
+  if (crank == 0 && (P.flags & STRATA_FLAG_TEST_STALL)) test_stall(&mbar[BAR_STALL], ctl, P.err);
   if (kp > 0 && crank == 0) {
     if (cs > 1) wait_bar(&mbar[BAR_X1], ctl, P.err, true);
     if (ctr_warp) r_slot = slot_rows(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, lane);

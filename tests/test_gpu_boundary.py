@@ -196,3 +196,21 @@ def test_graph_capture_replays_draw_fresh_numbers(sampler):
         seen.append(ids.tolist())
     assert seen[0] != seen[1] or seen[1] != seen[2]
     assert sampler.slot_state(0)[1] == 4
+
+
+@pytest.mark.parametrize("split", [0, 1])
+def test_bounded_wait_runs_out_and_the_context_recovers(sampler, split):
+    """Failure detection without a GPU fault: the leaders wait on an mbarrier nothing arrives at;
+    the bounded wait runs out (about two seconds), the call reports STRATA_DEVERR_TIMEOUT, and the
+    next call on the same context is exact again."""
+    import request_token_sampling_gb300 as S
+    w = synth.config1()
+    set_slots(sampler, w)
+    sampler.errors()
+    gpu_sample(sampler, w, flags=S.STRATA_FLAG_TEST_STALL | S.STRATA_FLAG_SPLIT(split))
+    assert sampler.errors() & S.STRATA_DEVERR_TIMEOUT
+    set_slots(sampler, w)
+    g = gpu_sample(sampler, w)
+    rows, _ = oracle.sample_call(w)
+    compare_sample(w, rows, g)
+    assert sampler.errors() == 0
