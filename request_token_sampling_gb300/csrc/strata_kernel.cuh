@@ -1641,10 +1641,16 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     if (P.topk_vals != nullptr) P.topk_vals[static_cast<long long>(row) * KMAX + tid] = __int_as_float(0x7FC00000);
   }
   if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
-  if (ctl[CTL_TIMEOUT] != 0u) {  // a copy may still be in flight into this CTA: bounded wait again
+  if (ctl[CTL_TIMEOUT] != 0u) {
+    // a wait ran out: a copy, or another CTA's stores into this one, may still be on the way, so
+    // wait for each once more (bounded) before the CTA leaves
     for (int si = 0; si < min(nslot, n_pieces); ++si) {
       const int pl = static_cast<int>(ctl[CTL_LAST0 + si]);
       wait_bar(&mbar[si], ctl, P.err, false, static_cast<uint32_t>(pl / nslot) & 1u);
+    }
+    if (cs > 1) {
+      wait_bar(&mbar[BAR_X0], ctl, P.err, true);
+      if (crank == 0) wait_bar(&mbar[BAR_X1], ctl, P.err, true);
     }
   }
 }
