@@ -15,6 +15,10 @@ with top_logprobs=20, the sampled token's log-probability and allowed_token_ids 
              the kernel source still matches it.
   cpu_baseline  the CPU oracle (plain numpy) on a bounded sample of the same workload, 1 core.
 
+Other workloads (`--workload`): `verify` (config 2's five-row verify windows, strata_sample_verify),
+`verify-ring` (the same windows over histories kept on the device), `mask` (the default step with its
+allowed ids as a sampling mask).  `--split N` forces N blocks per row (launch-shape sweeps).
+
 `--impl reference` times the CPU oracle alone on the same workload (one row per step).
 Multi-GPU (torchrun): every rank runs its own batch stream (weak scaling, no collective on the data
 path); time is the max over ranks.
