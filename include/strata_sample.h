@@ -28,6 +28,11 @@
  *   - A context serves one stream at a time: calls on one context must be ordered (one stream,
  *     or synchronised streams).  Calls on different contexts are independent.
  *   - The calling thread's current CUDA device must be the context's device.
+ *   - With STRATA_SAMPLE_DEBUG set to a value other than "0" in the environment (read once per
+ *     process), every sampling or logprobs call that passes its argument checks prints one line
+ *     to stderr before it launches: the entry point, B, V, the logit type, the flags and the
+ *     launch shape chosen (split, chunk, ring slots, warp-maxima per warp, hash capacity, dynamic
+ *     shared memory, grid).  Unset, the library prints nothing.
  */
 #ifndef STRATA_SAMPLE_H
 #define STRATA_SAMPLE_H

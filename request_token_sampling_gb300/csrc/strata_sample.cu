@@ -13,6 +13,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -203,7 +204,24 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
                    with_hist, with_allowed, mask, pipelined, static_cast<int>((flags >> 8) & 0x1Fu), s);
 }
 
-int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t flags, cudaStream_t stream) {
+// STRATA_SAMPLE_DEBUG=1 in the environment: one line per call on stderr (entry point, rows,
+// vocabulary, flags and the launch shape chosen).  Read once per process.
+bool trace_on() {
+  static const bool on = [] {
+    const char* v = std::getenv("STRATA_SAMPLE_DEBUG");
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+  }();
+  return on;
+}
+
+int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t flags, cudaStream_t stream,
+           const char* entry) {
+  if (trace_on())
+    std::fprintf(stderr,
+                 "strata: %s B=%d V=%d dtype=%s flags=0x%x split=%d chunk=%d ring_slots=%d qw=%d hash=%d smem=%d "
+                 "grid=%d\n",
+                 entry, P.B, P.V, dtype == STRATA_DTYPE_F32 ? "f32" : "bf16", flags, sh.cs, sh.chunk, sh.nslot, sh.qw,
+                 sh.hash_cap, sh.smem, P.B * sh.cs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(P.B * sh.cs), 1, 1);
   cfg.blockDim = dim3(strata::NT, 1, 1);
@@ -635,7 +653,8 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   P.done = c->d_done;
   P.ring = kept_hist ? c->d_ring : nullptr;
   P.hlen = kept_hist ? c->d_hlen : nullptr;
-  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream));
+  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream),
+                row_draft != nullptr ? "sample_verify" : "sample_rows");
 }
 
 int strata_sample_rows(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
@@ -701,7 +720,7 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
   P.nslot = sh.nslot;
   P.qw = sh.qw;
   P.flags = flags;
-  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream));
+  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream), "logprobs_rows");
 }
 
 }  // extern "C"
@@ -886,5 +905,5 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
   P.nslot = sh.nslot;
   P.qw = sh.qw;
   P.flags = 0;
-  return launch(nullptr, P, dtype, sh, 0u, s);
+  return launch(nullptr, P, dtype, sh, 0u, s, "sample_rows_noalloc");
 }

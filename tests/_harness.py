@@ -80,7 +80,8 @@ class Stats:
         both_nan = np.isnan(a) & np.isnan(b)
         both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
         ok = both_nan | both_inf
-        d = np.where(ok, 0.0, np.abs(a - b))
+        with np.errstate(invalid="ignore"):     # inf - inf and NaN operands are settled by `ok`
+            d = np.where(ok, 0.0, np.abs(a - b))
         d = np.nan_to_num(d, nan=np.inf)
         if d.size:
             self.max_dlp = max(self.max_dlp, float(d.max()))

@@ -214,3 +214,21 @@ def test_bounded_wait_runs_out_and_the_context_recovers(sampler, split):
     rows, _ = oracle.sample_call(w)
     compare_sample(w, rows, g)
     assert sampler.errors() == 0
+
+
+def test_trace_lines_on_stderr():
+    """STRATA_SAMPLE_DEBUG=1: the library prints one line per call with the launch shape it chose."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys; sys.path.insert(0, %r); import torch, synth; from _harness import gpu_sample, set_slots; "
+            "from request_token_sampling_gb300 import Sampler; w = synth.config1(); s = Sampler(0, 4, w['V'], 4); "
+            "set_slots(s, w); gpu_sample(s, w); s.close()") % os.path.join(root, "tests")
+    env = dict(os.environ, STRATA_SAMPLE_DEBUG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stderr.splitlines() if l.startswith("strata: sample_rows")]
+    assert len(lines) == 1 and "V=32000" in lines[0] and "split=" in lines[0] and "smem=" in lines[0], r.stderr[-2000:]
