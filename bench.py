@@ -8,6 +8,11 @@ with top_logprobs=20, the sampled token's log-probability and allowed_token_ids 
 
   value      rows/s over exactly K timed steps: one CUDA graph holding the K calls, replayed once;
              inputs rotate over enough distinct batches to exceed 4x the L2 size (HBM serves reads).
+             The steps alternate over S independent request groups (`--streams`, default 8): each
+             group is its own context (own slots, counters, outputs) with its own stream, its calls
+             chained in order, the groups' calls overlapping, with the concurrency launch hint.
+  single_group  the same K steps as one group alone (one stream, the library's pipelined launch
+             shape): each call then waits for the previous call's counters before its draw.
   e2e        the same metric through the C ABI from pinned host buffers: every step copies its
              inputs host->device (the logits, and the small arrays packed into one copy), runs the
              call and copies every output back (one packed copy); copies run on their own streams
@@ -281,8 +286,8 @@ def make_batches(w, R, dev):
 def run_gpu(args, rank, world):
     import torch
     import torch.distributed as dist
-    from request_token_sampling_gb300 import (STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_HISTORY_RING,
-                                              STRATA_FLAG_PDL, STRATA_FLAG_SPLIT, Sampler)
+    from request_token_sampling_gb300 import (STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD,
+                                              STRATA_FLAG_HISTORY_RING, STRATA_FLAG_PDL, STRATA_FLAG_SPLIT, Sampler)
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -302,16 +307,26 @@ def run_gpu(args, rank, world):
         flags |= STRATA_FLAG_HISTORY_RING
     if args.split > 0:
         flags |= STRATA_FLAG_SPLIT(args.split)
+    elif args.streams > 1:  # other groups' calls run alongside: the launch shape for throughput
+        flags |= STRATA_FLAG_CONCURRENT
 
-    s = Sampler(device=local, max_slots=16, max_vocab=w["V"], max_rows=B)
-    for slot, p in w["slot_params"].items():
-        s.restore_slot(slot, p, 0)
+    # S independent request groups: a context each (its own slots, counters and outputs), a stream
+    # each; one group's calls are ordered, the groups' calls overlap
+    S = max(1, args.streams)
+    samplers = []
+    for _ in range(S):
+        sg = Sampler(device=local, max_slots=16, max_vocab=w["V"], max_rows=B)
+        for slot, p in w["slot_params"].items():
+            sg.restore_slot(slot, p, 0)
+        samplers.append(sg)
+    s = samplers[0]
     ten = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     row_slot, row_pos = ten(w["row_slot"]), ten(w["row_pos"])
     hist, hist_off = ten(w["hist"]), ten(w["hist_off"])
     if ring:  # the window lives in the slot's kept history; the call uploads none
-        s.history_enable()
-        s.history_set(0, w["hist"])
+        for sg in samplers:
+            sg.history_enable()
+            sg.history_set(0, w["hist"])
         hist = hist_off = None
     allowed = allowed_off = None
     if not verify:
@@ -320,13 +335,16 @@ def run_gpu(args, rank, world):
     drafts[-1] = -1
     row_draft = ten(drafts)
     batches = make_batches(w, R, dev)
-    if verify:
-        out = s.verify(batches[0], row_slot, row_pos, row_draft, hist=hist, hist_off=hist_off, flags=flags)
-    else:
-        out = s.sample(batches[0], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
-                       chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags)
+    outs = []
+    for sg in samplers:
+        if verify:
+            outs.append(sg.verify(batches[0], row_slot, row_pos, row_draft, hist=hist, hist_off=hist_off, flags=flags))
+        else:
+            outs.append(sg.sample(batches[0], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
+                                  chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags))
+    out = outs[0]
     torch.cuda.synchronize()
-    if s.errors() != 0:
+    if any(sg.errors() != 0 for sg in samplers):
         raise RuntimeError("device error bits set")
     # the launch shape of a plain call with these flags; verify windows and kept-history calls are
     # steps of one request's decode and take the latency split (as a call without early loads)
@@ -334,28 +352,38 @@ def run_gpu(args, rank, world):
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
+    gstreams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(S - 1)]
+
+    def call_on(sg, st, o, fl, i):
+        if verify:
+            sg.verify(batches[i % R], row_slot, row_pos, row_draft, hist=hist, hist_off=hist_off, flags=fl,
+                      stream=st, out=o)
+        else:
+            sg.sample(batches[i % R], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
+                      chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=fl, stream=st, out=o)
 
     def call(i):
-        if verify:
-            s.verify(batches[i % R], row_slot, row_pos, row_draft, hist=hist, hist_off=hist_off, flags=flags,
-                     stream=stream, out=out)
-        else:
-            s.sample(batches[i % R], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
-                     chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags, stream=stream, out=out)
+        g = i % S
+        call_on(samplers[g], gstreams[g], outs[g], flags, i)
+
+    def calls(n):  # n steps spread over the groups' streams, forked from and joined back to `stream`
+        for st in gstreams[1:]:
+            st.wait_stream(stream)
+        for i in range(n):
+            call(i)
+        for st in gstreams[1:]:
+            stream.wait_stream(st)
 
     # the K timed steps as one CUDA graph (the calls advance the device counters on replay)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        for i in range(3):
-            call(i)
-        stream.synchronize()
+        calls(3 * S)
+        torch.cuda.synchronize()
         with torch.cuda.graph(graph, stream=stream):
-            for i in range(args.steps):
-                call(i)
+            calls(args.steps)
         warm = torch.cuda.CUDAGraph()
         with torch.cuda.graph(warm, stream=stream):
-            for i in range(max(args.warmup, 1)):
-                call(i)
+            calls(max(args.warmup, 1))
     torch.cuda.synchronize()
     # untimed: bring clocks up, then exactly W warm-up steps
     with torch.cuda.stream(stream):
@@ -386,10 +414,39 @@ def run_gpu(args, rank, world):
     ms = max_over_ranks(e0.elapsed_time(e1), dev)
     if world > 1:
         dist.barrier()
-    if s.errors() != 0:
+    if any(sg.errors() != 0 for sg in samplers):
         raise RuntimeError("device error bits set after the timed region")
     per_launch_s = ms / 1e3 / args.steps
     value = job_rows_per_s(B * args.steps, world, ms / 1e3)
+
+    # ---- one request group alone: its K calls chained on one stream with the library's launch
+    # shape for that case (no concurrency hint), timed the same way and reported beside the value
+    single = None
+    if S > 1:
+        flags1 = flags & ~STRATA_FLAG_CONCURRENT
+        shape1 = s.shape(0, 0, B, w["V"], w["top_n"], flags1 & ~STRATA_FLAG_EARLY_LOAD if verify else flags1)
+        g1, warm1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                call_on(s, stream, outs[0], flags1, i)
+            stream.synchronize()
+            with torch.cuda.graph(g1, stream=stream):
+                for i in range(args.steps):
+                    call_on(s, stream, outs[0], flags1, i)
+            with torch.cuda.graph(warm1, stream=stream):
+                for i in range(max(args.warmup, 1)):
+                    call_on(s, stream, outs[0], flags1, i)
+            warm1.replay()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            g1.replay()
+            f1.record(stream)
+        stream.synchronize()
+        ms1 = max_over_ranks(f0.elapsed_time(f1), dev)
+        if s.errors() != 0:
+            raise RuntimeError("device error bits set in the single-group leg")
+        single = {"value": job_rows_per_s(B * args.steps, world, ms1 / 1e3), "ms_per_step": ms1 / args.steps,
+                  "split": shape1["split"], "smem_bytes": shape1["smem"], "grid": shape1["grid"]}
 
     # ---- e2e through the C ABI from pinned host buffers -------------------------------------
     # Every step copies its inputs in (the logits, plus the small arrays packed into one copy) and
@@ -434,7 +491,7 @@ def run_gpu(args, rank, world):
     copy_out = torch.cuda.Stream(device=dev)
 
     # the e2e inputs are copied in right before each call, so those calls do not claim early loads
-    flags_e2e = flags & ~STRATA_FLAG_EARLY_LOAD
+    flags_e2e = flags & ~(STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_CONCURRENT)
 
     def e2e_step(k):
         st_ = sets[k % 2]
@@ -489,7 +546,8 @@ def run_gpu(args, rank, world):
     e2e_value = job_rows_per_s(B * K_e2e, world, e2e_ms / 1e3)
 
     if rank != 0:
-        s.close()
+        for sg in samplers:
+            sg.close()
         return
     alg = algorithmic_bytes_verify(w, ring) if verify else algorithmic_bytes(w)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -498,6 +556,8 @@ def run_gpu(args, rank, world):
     else:
         peak, peak_src = 6800.0, "fallback"
     achieved = alg / per_launch_s / 1e9
+    if single is not None:
+        single["roofline_frac"] = alg / (single["ms_per_step"] / 1e3) / 1e9 / peak
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         tj = json.load(open(TRAFFIC_FILE))
@@ -529,18 +589,21 @@ def run_gpu(args, rank, world):
                              + (", logit loads start before the previous call ends (inputs resident)"
                                 if flags & 2 else ""),
                    "split": shape["split"], "chunk_elems": shape["chunk"], "smem_bytes": shape["smem"],
-                   "grid": shape["grid"], "parallelism": f"replicas x{world}"},
+                   "grid": shape["grid"], "parallelism": f"replicas x{world}",
+                   "streams": S},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg, "launch_us": per_launch_s * 1e6},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": K_e2e},
+        "single_group": single,
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
-    s.close()
+    for sg in samplers:
+        sg.close()
 
 
 def main():
@@ -556,6 +619,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--split", type=int, default=0,
                     help="blocks per row (1..16; 0: the library's choice), for launch-shape sweeps")
+    ap.add_argument("--streams", type=int, default=8,
+                    help="independent request groups, each its own context, slots and stream; the steps "
+                         "alternate over them and the groups' calls overlap")
     ap.add_argument("--batches", type=int, default=0,
                     help="distinct input batches to rotate over (0: enough for 4x the L2 size)")
     ap.add_argument("--workload", choices=["fused", "verify", "mask", "verify-ring"], default="fused",

@@ -25,8 +25,10 @@ STRATA_DTYPE_BF16 = 1
 
 STRATA_MAX_TOP_K = 64
 STRATA_DEFAULT_TOP_K = 20
+STRATA_DEFAULT_LAST_N = 64
 STRATA_MAX_TOP_N = 20
 STRATA_MAX_PENALTY_LAST_N = 4096
+STRATA_MAX_VOCAB = 524288
 STRATA_NOALLOC_MAX_ROWS = 1024
 STRATA_HISTORY_CAP = 4096
 
@@ -34,6 +36,8 @@ STRATA_FLAG_PDL = 0x1
 STRATA_FLAG_EARLY_LOAD = 0x2
 STRATA_FLAG_ALLOWED_MASK = 0x4
 STRATA_FLAG_HISTORY_RING = 0x8
+STRATA_FLAG_CONCURRENT = 0x10
+STRATA_CONCURRENT_ROW_BYTES = 1 << 20
 STRATA_FLAG_TEST_STALL = 0x10000
 
 

@@ -161,8 +161,10 @@ __host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, i
   L.mbar = o;
   o = align_up(o + NBAR * 8, 16);
   const uint32_t bw = align_up((static_cast<uint32_t>(chunk) + 31) / 32 * 4, 16);
-  L.abits = o;  // allowed ids met in this chunk (calls with allowed lists only)
-  o += allowed ? bw : 0u;
+  // allowed ids met in this chunk (calls with allowed lists only): in the ring, which is free from
+  // the end of the first pass until the candidate lists move in, whenever the ring can hold it
+  L.abits = bw <= ring ? L.data : o;
+  o += (allowed && bw > ring) ? bw : 0u;
   L.mbits = o;  // allowed ids already in a masked row's top_k list (mask launches only)
   o += mask ? bw : 0u;
   L.hash = o;
@@ -422,31 +424,54 @@ __device__ __forceinline__ void append_both(uint32_t* ctl, uint4* cand_pen, uint
   if (to_raw && ir < static_cast<uint32_t>(cap)) cand_raw[ir] = key;
 }
 
-// Every element at or above T that carries no penalty, among this thread's vectors v_first,
-// v_first + NT, ... up to v_last: appended to both lists with its raw logit.  Out of line: only a
-// thread whose maximum and whose best other batch both reach T takes this full rescan.
+// Every element at or above T that carries no penalty, among the vectors of each thread named in
+// `need` (one bit per lane of this warp; thread t owns vectors t, t + NT, ...): appended to both
+// lists with its raw logit.  The warp scans one such thread's vectors at a time, each lane loading
+// up to U of them at once, so a scan of a long chunk costs a round trip or two rather than one per
+// vector.  `hist` marks the threads that own a history id (only their hits need the table lookup).
+// Called by whole warps; a thread is named only when its maximum and its best other batch both reach T.
 template <int DT>
-__device__ __noinline__ void rescan_candidates(const unsigned char* g, int v_first, int v_last, int n_vec, int n_el,
-                                               int lo, float Tf, bool penal, const uint32_t* htab, int hash_bits,
-                                               uint32_t* ctl, uint4* cand_pen, uint64_t* cand_raw, int cap, bool to_raw,
-                                               bool to_pen) {
+__device__ __forceinline__ void warp_rescan(const unsigned char* g, uint32_t need, uint32_t hist, int wid, int lane,
+                                         int n_vec, int n_el, int lo, float Tf, const uint32_t* htab, int hash_bits,
+                                         uint32_t* ctl, uint4* cand_pen, uint64_t* cand_raw, int cap, bool to_raw,
+                                         bool to_pen) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+  constexpr int U = 32 / EPV;  // vectors in flight per lane (32 registers of elements)
 #pragma unroll 1
-  for (int v = v_first; v < n_vec && v <= v_last; v += NT) {
-    float x[EPV];
-    load_vec_g<DT>(g, v, n_el, x);
-    uint32_t hit = 0u;  // elements of this vector at or above T (NaN compares false)
+  for (; need != 0u; need &= need - 1u) {
+    const int src = __ffs(need) - 1;
+    const int t = wid * 32 + src;
+    const bool penal = (hist >> src) & 1u;
+    const int nt = n_vec > t ? (n_vec - t + NT - 1) / NT : 0;  // vectors of thread t
+#pragma unroll 1
+    for (int j0 = 0; j0 < nt; j0 += 32 * U) {
+      float x[U][EPV];
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(x[e] >= Tf) << e;
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + lane + 32 * u;
+        if (j < nt) {
+          load_vec_g<DT>(g, t + j * NT, n_el, x[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) x[u][e] = -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        uint32_t hit = 0u;  // elements of this vector at or above T (NaN compares false)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) hit |= static_cast<uint32_t>(x[u][e] >= Tf) << e;
 #pragma unroll 1
-    for (; hit != 0u; hit &= hit - 1u) {
-      const int e = __ffs(hit) - 1;
-      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
-      if (loc >= static_cast<uint32_t>(n_el)) continue;
-      const float xv = pick(x, e);
-      const uint32_t o = order_key(xv);
-      if (o == 0u || (penal && hash_count(htab, hash_bits, loc) != 0u)) continue;
-      append_both(ctl, cand_pen, cand_raw, cap, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, to_raw, to_pen);
+        for (; hit != 0u; hit &= hit - 1u) {
+          const int e = __ffs(hit) - 1;
+          const uint32_t loc = static_cast<uint32_t>((t + (j0 + lane + 32 * u) * NT) * EPV + e);
+          if (loc >= static_cast<uint32_t>(n_el)) continue;
+          const float xv = pick(x[u], e);
+          const uint32_t o = order_key(xv);
+          if (o == 0u || (penal && hash_count(htab, hash_bits, loc) != 0u)) continue;
+          append_both(ctl, cand_pen, cand_raw, cap, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, to_raw, to_pen);
+        }
+      }
     }
   }
 }
@@ -796,6 +821,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool early = (P.flags & STRATA_FLAG_EARLY_LOAD) != 0u;
   if (!early) grid_dep_wait();  // inputs may be the previous kernel's outputs
+  // the next call may start its own loads now: launching it is what bounds a stream of calls
+  // whose CTAs each take microseconds to reach their first copy (its outputs still wait for ours)
+  grid_dep_launch();
 
   const uint32_t crank = cluster_ctarank();
   const int cs = P.cs;
@@ -859,7 +887,6 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     fence_mbar_init();
     mbar_arrive_expect_tx(&mbar[BAR_X0], static_cast<uint32_t>(cs - 1) * rec_bytes);
   }
-  grid_dep_launch();
   if (tid == 0) load_meta1();
 
 
@@ -884,9 +911,10 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   uint64_t* sorted_raw = reinterpret_cast<uint64_t*>(sm + L.sorted_raw);
 
   const int bw_words = (P.chunk + 31) >> 5;
-  if (P.allowed_off != nullptr)
+  const bool abits_in_ring = L.abits == L.data;  // then zeroed once the first pass is done
+  if (P.allowed_off != nullptr && (mask_launch || !abits_in_ring))
     for (int i = tid; i < bw_words; i += NT) {
-      abits[i] = 0u;
+      if (!abits_in_ring) abits[i] = 0u;
       if (mask_launch) mbits[i] = 0u;
     }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
@@ -1007,6 +1035,11 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 
   // allowed subset: this chunk's ids, each counted once, into (max, sum of exp)
   MaxSum al{-INFINITY, 0.0f};
+  if (abits_in_ring && a_end > a_beg) {  // the ring's last piece is read by every warp, then cleared
+    __syncthreads();
+    for (int i = tid; i < bw_words; i += NT) abits[i] = 0u;
+    __syncthreads();
+  }
   {
     auto add_allowed = [&](int id, float x) {
       if (id >= lo && id < hi) {
@@ -1189,45 +1222,46 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     // a masked row's top_k list holds exactly its named ids (below); T still serves the raw list
     const bool masked = mask_launch && a_end > a_beg && k_row > 0;
     const bool pen_from_t = k_row > 0 && !masked;
-    if (kall != 0u && kall >= T && (n_row > 0 || pen_from_t)) {
+    const bool want = kall != 0u && kall >= T && (n_row > 0 || pen_from_t);
+    const bool whole = want && order_key(mx2) >= T;  // another batch also reaches T: a full rescan
+    if (want && !whole) {
       constexpr int RB = BATCH_VECS<DT>;
-      if (order_key(mx2) < T) {
-        // every element at or above T sits in the batch that holds the max: scan its 16 elements
-        // straight-line (independent loads), then append the hits
-        const int vb = (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid;
-        uint32_t hit = 0u;
-        float xf[RB * EPV];
+      // every element at or above T sits in the batch that holds the max: scan its 16 elements
+      // straight-line (independent loads), then append the hits
+      const int vb = (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid;
+      uint32_t hit = 0u;
+      float xf[RB * EPV];
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          float x[EPV];
-          if (vb + r * NT < n_vec) {
-            load_vec_g<DT>(gchunk, vb + r * NT, n_el, x);
-          } else {
+      for (int r = 0; r < RB; ++r) {
+        float x[EPV];
+        if (vb + r * NT < n_vec) {
+          load_vec_g<DT>(gchunk, vb + r * NT, n_el, x);
+        } else {
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) x[e] = -INFINITY;
-          }
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            xf[r * EPV + e] = x[e];
-            hit |= static_cast<uint32_t>(x[e] >= Tf) << (r * EPV + e);
-          }
+          for (int e = 0; e < EPV; ++e) x[e] = -INFINITY;
         }
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          xf[r * EPV + e] = x[e];
+          hit |= static_cast<uint32_t>(x[e] >= Tf) << (r * EPV + e);
+        }
+      }
 #pragma unroll 1
-        for (; hit != 0u; hit &= hit - 1u) {
-          const int b = __ffs(hit) - 1;
-          const uint32_t loc = static_cast<uint32_t>((vb + (b / EPV) * NT) * EPV + (b % EPV));
-          if (loc >= static_cast<uint32_t>(n_el)) continue;
-          const float xv = pick(xf, b);
-          const uint32_t o = order_key(xv);
-          if (o == 0u || (own_hist && hash_count(htab, P.hash_bits, loc) != 0u)) continue;
-          append_both(ctl, cand_pen, cand_raw, cap, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0,
-                      pen_from_t);
-        }
-      } else {
-        rescan_candidates<DT>(gchunk, tid, n_vec, n_vec, n_el, lo, Tf, own_hist, htab, P.hash_bits, ctl, cand_pen,
-                              cand_raw, cap, n_row > 0, pen_from_t);
+      for (; hit != 0u; hit &= hit - 1u) {
+        const int b = __ffs(hit) - 1;
+        const uint32_t loc = static_cast<uint32_t>((vb + (b / EPV) * NT) * EPV + (b % EPV));
+        if (loc >= static_cast<uint32_t>(n_el)) continue;
+        const float xv = pick(xf, b);
+        const uint32_t o = order_key(xv);
+        if (o == 0u || (own_hist && hash_count(htab, P.hash_bits, loc) != 0u)) continue;
+        append_both(ctl, cand_pen, cand_raw, cap, sel_key(o, static_cast<uint32_t>(lo) + loc), xv, n_row > 0,
+                    pen_from_t);
       }
     }
+    const uint32_t need = __ballot_sync(FULL_MASK, whole);
+    if (need != 0u)
+      warp_rescan<DT>(gchunk, need, __ballot_sync(FULL_MASK, own_hist), wid, lane, n_vec, n_el, lo, Tf, htab,
+                      P.hash_bits, ctl, cand_pen, cand_raw, cap, n_row > 0, pen_from_t);
     if (penal) {  // penalised ids: raw value for the raw list, penalised value for the other
       for (int i = tid; i < P.hash_cap; i += NT) {
         const uint32_t ent = htab[i];

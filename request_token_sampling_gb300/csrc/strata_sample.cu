@@ -45,11 +45,16 @@ int cuda_fail(cudaError_t e, const char* what) {
 // Blocks per row.  Pipelined calls (early loads: the next call's loads overlap this one) are
 // throughput-bound, so a row goes to few blocks that each stream up to PIPELINED_BYTES of logits;
 // otherwise a call is latency-bound, so rows split into blocks of about LATENCY_BYTES, enough of
-// them to fill the GPU (but no block below MIN_CHUNK_ELEMS ids).
+// them to fill the GPU (but no block below MIN_CHUNK_ELEMS ids).  With STRATA_FLAG_CONCURRENT a
+// block streams up to STRATA_CONCURRENT_ROW_BYTES.
 constexpr int PIPELINED_BYTES = 128 * 1024;
 constexpr int LATENCY_BYTES = 64 * 1024;
 constexpr int MIN_CHUNK_ELEMS = 2048;
 constexpr int RING_SLOTS = 4;                 // pieces in flight per CTA when shared memory allows
+// A pipelined call's blocks rescan their candidates through L1, and a fourth slot at three blocks
+// per SM takes the shared-memory carveout to its maximum, which leaves L1 a fraction of its size:
+// measured slower than three slots.  Blocks that stream whole rows want the deeper ring.
+constexpr int RING_SLOTS_PIPELINED = 3;
 constexpr int KEY_BINS = STRATA_MAX_TOP_K + 1;
 constexpr int LASTN_BINS = STRATA_MAX_PENALTY_LAST_N + 1;
 
@@ -139,8 +144,8 @@ struct Shape {
 // keys each warp publishes for the row threshold, history table size and shared memory.  Shared
 // by the context calls and the allocation-free call.
 int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mode, int esz, int B, int V, int kmax,
-              int nmax, int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined, int forced,
-              Shape* s) {
+              int nmax, int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined, bool concurrent,
+              int forced, Shape* s) {
   const long long row_bytes = static_cast<long long>(V) * esz;
   s->nmax = nmax;
   s->kmax = kmax;
@@ -149,6 +154,9 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
   if (forced > 0) {
     if (forced > max_cluster) return fail(STRATA_ERANGE, "forced split %d above the cluster limit %d", forced, max_cluster);
     cs = forced;
+  } else if (concurrent) {
+    cs = static_cast<int>((row_bytes + STRATA_CONCURRENT_ROW_BYTES - 1) / STRATA_CONCURRENT_ROW_BYTES);
+    cs = std::min(std::max(cs, 1), max_cluster);
   } else if (pipelined) {
     cs = static_cast<int>((row_bytes + PIPELINED_BYTES - 1) / PIPELINED_BYTES);
     cs = std::min(std::max(cs, 1), max_cluster);
@@ -178,7 +186,7 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
   }
   // the most ring slots that still leave room for three CTAs on the SM (at least 2)
   Layout L{};
-  for (int ns = RING_SLOTS; ns >= 2; --ns) {
+  for (int ns = (pipelined && !concurrent) ? RING_SLOTS_PIPELINED : RING_SLOTS; ns >= 2; --ns) {
     L = strata::make_layout(chunk, s->hash_cap, cs, kmax, nmax, ns, s->qw, with_allowed, mask);
     s->nslot = ns;
     if (static_cast<int>(L.total) <= smem_three) break;
@@ -201,7 +209,8 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
                          (flags & STRATA_FLAG_HISTORY_RING) == 0u && !verify;
   return shape_for(c->max_cluster, c->max_smem, c->smem_three, c->num_sms, mode, esz, B, V, kmax, top_n_eff,
                    max_lastn_penal(c),
-                   with_hist, with_allowed, mask, pipelined, static_cast<int>((flags >> 8) & 0x1Fu), s);
+                   with_hist, with_allowed, mask, pipelined, (flags & STRATA_FLAG_CONCURRENT) != 0u,
+                   static_cast<int>((flags >> 8) & 0x1Fu), s);
 }
 
 // STRATA_SAMPLE_DEBUG=1 in the environment: one line per call on stderr (entry point, rows,
@@ -867,7 +876,7 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
   Shape sh;
   if ((rc = shape_for(nd->max_cluster, nd->max_smem, nd->smem_three, nd->num_sms, strata::MODE_SAMPLE, esz, B, V,
                       std::max(1, kmax_sampled),
-                      top_n_eff, max_lastn, hist_off != nullptr, false, false, false, 0, &sh)) != STRATA_OK)
+                      top_n_eff, max_lastn, hist_off != nullptr, false, false, false, false, 0, &sh)) != STRATA_OK)
     return rc;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -106,3 +106,18 @@ def test_history_capacity_constants(S):
     assert cap == S.STRATA_HISTORY_CAP == oracle.HISTORY_RING_CAP
     assert cap & (cap - 1) == 0                         # a power of two: ring positions are masked
     assert cap >= S.STRATA_MAX_PENALTY_LAST_N           # every penalty window fits
+
+
+def test_header_constants_match_the_binding(S):
+    """Every integer constant the header defines has the same value under the same name in Python."""
+    text = open(HEADER).read()
+    found = 0
+    for name, expr in re.findall(r"^#define (STRATA_[A-Z0-9_]+)[ \t]+([^/\n]+)", text, flags=re.M):
+        expr = expr.strip()
+        if name == "STRATA_SAMPLE_H" or "(n)" in name or not expr:
+            continue
+        value = eval(re.sub(r"(0x[0-9A-Fa-f]+|\d+)u\b", r"\1", expr))  # integer literals and shifts only
+        assert getattr(S, name) == value, name
+        found += 1
+    assert found >= 30
+    assert S.STRATA_FLAG_SPLIT(5) == 5 << 8

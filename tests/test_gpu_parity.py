@@ -163,6 +163,50 @@ def test_config4_pipelined_calls(sampler):
     print("config4 pipelined", st)
 
 
+def test_config4_concurrent_groups():
+    """Two request groups, each its own context and stream, their pipelined calls interleaved with
+    the concurrency hint (one block per full row): every call of each group matches the oracle,
+    and each group's counters advance by its own calls only."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from request_token_sampling_gb300 import (STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL,
+                                              Sampler)
+    base = synth.config4(fused=True)
+    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_CONCURRENT
+    groups = [Sampler(device=0, max_slots=16, max_vocab=synth.V_FULL, max_rows=64) for _ in range(2)]
+    try:
+        for g in groups:
+            set_slots(g, base)
+        assert groups[0].shape(0, 0, base["B"], base["V"], base["top_n"], fl)["split"] == 1
+        streams = [torch.cuda.Stream() for _ in groups]
+        ws, outs = [], []
+        for c in range(6):
+            w = dict(base)
+            w["logits"] = np.roll(base["logits"], 1231 * c, axis=1) if c else base["logits"]
+            ws.append((w, upload(w)))
+        torch.cuda.synchronize()
+        for c, (w, d) in enumerate(ws):
+            g = c % 2
+            outs.append(groups[g].sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=d["hist"],
+                                         hist_off=d["hist_off"], top_n=w["top_n"], chosen_lp=True,
+                                         allowed=d["allowed"], allowed_off=d["allowed_off"], flags=fl,
+                                         stream=streams[g]))
+        torch.cuda.synchronize()
+        counters = [dict(base["counters"]), dict(base["counters"])]
+        st = Stats()
+        for c, ((w, _), o) in enumerate(zip(ws, outs)):
+            rows, counters[c % 2] = oracle.sample_call(w, counters=counters[c % 2])
+            compare_sample(w, rows, {k: v.cpu().numpy() for k, v in o.items()}, stats=st, debug=False)
+        for g, ctr in zip(groups, counters):
+            for s in base["slot_params"]:
+                assert g.slot_state(s)[1] == ctr[s]
+            _check_no_errors(g)
+        print("config4 concurrent groups", st)
+    finally:
+        for g in groups:
+            g.close()
+
+
 @pytest.mark.parametrize("split", [1, 2, 4, 6, 8, 13, 16])
 def test_full_vocab_every_split(sampler, split):
     """The 248,320-id rows give the same answer whatever the number of CTAs per row."""
