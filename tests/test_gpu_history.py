@@ -242,9 +242,12 @@ def test_history_graph_replay(sampler, S):
         assert sampler.slot_state(s)[1] == counters[s]
 
 
-def test_history_verify_windows_full_vocab(sampler, S):
+@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+def test_history_verify_windows_full_vocab(sampler, S, concurrent):
     """The verify-window shape at V=248,320 fp32 (5 rows: 4 drafts + head, one request, repeat 1.1
-    over 64 ids) for ten consecutive windows, history kept on the device."""
+    over 64 ids) for ten consecutive windows, history kept on the device; also with the
+    concurrency hint (one CTA streams each whole row)."""
+    fl = S.STRATA_FLAG_CONCURRENT if concurrent else 0
     run = synth.DecodeRun(51, 1, synth.V_FULL, rows_per_slot=5, last_ns=(64,), prompt_len=(64, 64),
                           greedy_frac=0.0)
     state, counters = _start(sampler, run)
@@ -257,6 +260,6 @@ def test_history_verify_windows_full_vocab(sampler, S):
         drafts = [picks[j] if j < good else (picks[j] + 5) % w["V"] for j in range(4)] + [-1]
         d = upload(w)
         d["draft"] = torch.from_numpy(np.asarray(drafts, np.int32)).to("cuda:0")
-        g = _host(_call(sampler, S, w, d, drafts=drafts))
+        g = _host(_call(sampler, S, w, d, drafts=drafts, flags=fl))
         state, counters = _advance(w, state, counters, g, drafts=drafts, debug=False)
     _check_rings(sampler, state)

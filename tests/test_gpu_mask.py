@@ -29,11 +29,14 @@ def _mask_flag():
     return STRATA_FLAG_ALLOWED_MASK
 
 
-def test_mask_config4_fused(sampler):
-    """Config 4's rows with their 5/100/1000-id lists used as masks."""
+@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+def test_mask_config4_fused(sampler, concurrent):
+    """Config 4's rows with their 5/100/1000-id lists used as masks (also with the concurrency hint:
+    one CTA per row, both id bitmaps as long as the row)."""
+    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT
     w = synth.config4(fused=True)
     set_slots(sampler, w)
-    g = gpu_sample(sampler, w, flags=_mask_flag())
+    g = gpu_sample(sampler, w, flags=_mask_flag() | (STRATA_FLAG_CONCURRENT if concurrent else 0))
     rows, ctr = oracle.sample_call(w, mask_allowed=True)
     compare_sample(w, rows, g)
     off = w["allowed_off"]

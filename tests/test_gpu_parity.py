@@ -60,10 +60,12 @@ def test_config2_verify_windows_counter_persists(sampler):
     print("config2", st)
 
 
-def test_config3_batch_slots_bf16(sampler):
+@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+def test_config3_batch_slots_bf16(sampler, concurrent):
+    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT
     w = synth.config3()
     set_slots(sampler, w)
-    g = gpu_sample(sampler, w, top_n=0, chosen_lp=True)
+    g = gpu_sample(sampler, w, top_n=0, chosen_lp=True, flags=STRATA_FLAG_CONCURRENT if concurrent else 0)
     rows, ctr = oracle.sample_call(w)
     st = compare_sample(w, rows, g, top_n=0)
     _check_no_errors(sampler)
@@ -91,10 +93,14 @@ def test_config4_fused_sample_and_logprobs(sampler):
     print("config4 fused", st)
 
 
-def test_config5_stress_bf16_ties(sampler):
+@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+def test_config5_stress_bf16_ties(sampler, concurrent):
+    """Heavy ties: with one CTA per row a thread's tied ids at the threshold take the warp-wide
+    rescan and the exact rounds over the whole row."""
+    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT
     w = synth.config5()
     set_slots(sampler, w)
-    g = gpu_sample(sampler, w)
+    g = gpu_sample(sampler, w, flags=STRATA_FLAG_CONCURRENT if concurrent else 0)
     rows, ctr = oracle.sample_call(w)
     st = compare_sample(w, rows, g)
     _check_no_errors(sampler)

@@ -65,6 +65,26 @@ def test_verify_window_every_prefix(sampler, accepted):
     assert sampler.slot_state(0)[1] == ctr[0]
 
 
+@pytest.mark.parametrize("accepted", [0, 2, 4])
+def test_verify_window_one_cta_per_row(sampler, accepted):
+    """The same windows with the concurrency hint (one CTA streams each whole row, no exchange
+    between CTAs) and pipelined flags, as independent request groups run them."""
+    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL
+    w = synth.config2_window(31 + accepted)
+    set_slots(sampler, w)
+    rows, _ = oracle.sample_call(w, with_allowed=False)
+    picks = [r["id"] for r in rows]
+    drafts = picks[:-1] + [-1]
+    if accepted < w["B"] - 1:
+        drafts[accepted] = (picks[accepted] + 29) % w["V"]
+    set_slots(sampler, w)
+    g = _verify(sampler, w, drafts, flags=STRATA_FLAG_CONCURRENT | STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD)
+    rows2, ctr, keep = oracle.verify_call(w, drafts)
+    assert keep == {0: accepted + 1}
+    _check(w, rows2, g, drafts)
+    assert sampler.slot_state(0)[1] == ctr[0]
+
+
 def test_verify_batch_of_slots_mixed(sampler):
     """Eight slots of config 3 (greedy and sampled), each a window of three rows, drafts mixing the
     slot's own picks and seeded ids."""
