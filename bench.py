@@ -287,7 +287,8 @@ def run_gpu(args, rank, world):
     import torch
     import torch.distributed as dist
     from request_token_sampling_gb300 import (STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD,
-                                              STRATA_FLAG_HISTORY_RING, STRATA_FLAG_PDL, STRATA_FLAG_SPLIT, Sampler)
+                                              STRATA_FLAG_HISTORY_RING, STRATA_FLAG_OWN_OUTPUTS, STRATA_FLAG_PDL,
+                                              STRATA_FLAG_SPLIT, Sampler)
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -309,6 +310,11 @@ def run_gpu(args, rank, world):
         flags |= STRATA_FLAG_SPLIT(args.split)
     elif args.streams > 1:  # other groups' calls run alongside: the launch shape for throughput
         flags |= STRATA_FLAG_CONCURRENT
+    # every call writes its own output buffers (they rotate like the inputs), so no call waits for
+    # the one before it; verify windows and kept histories depend on the previous call by nature
+    own = (not args.no_own_outputs and (flags & STRATA_FLAG_EARLY_LOAD) != 0 and not verify)
+    if own:
+        flags |= STRATA_FLAG_OWN_OUTPUTS
 
     # S independent request groups: a context each (its own slots, counters and outputs), a stream
     # each; one group's calls are ordered, the groups' calls overlap
@@ -343,6 +349,8 @@ def run_gpu(args, rank, world):
             outs.append(sg.sample(batches[0], row_slot, row_pos, hist=hist, hist_off=hist_off, top_n=w["top_n"],
                                   chosen_lp=True, allowed=allowed, allowed_off=allowed_off, flags=flags))
     out = outs[0]
+    # with own outputs, call i writes output set i % R: more sets than calls can be resident at once
+    out_sets = [{k: torch.empty_like(v) for k, v in out.items()} for _ in range(R)] if own else None
     torch.cuda.synchronize()
     if any(sg.errors() != 0 for sg in samplers):
         raise RuntimeError("device error bits set")
@@ -364,7 +372,7 @@ def run_gpu(args, rank, world):
 
     def call(i):
         g = i % S
-        call_on(samplers[g], gstreams[g], outs[g], flags, i)
+        call_on(samplers[g], gstreams[g], out_sets[i % R] if own else outs[g], flags, i)
 
     def calls(n):  # n steps spread over the groups' streams, forked from and joined back to `stream`
         for st in gstreams[1:]:
@@ -423,7 +431,7 @@ def run_gpu(args, rank, world):
     # shape for that case (no concurrency hint), timed the same way and reported beside the value
     single = None
     if S > 1:
-        flags1 = flags & ~STRATA_FLAG_CONCURRENT
+        flags1 = flags & ~(STRATA_FLAG_CONCURRENT | STRATA_FLAG_OWN_OUTPUTS)
         shape1 = s.shape(0, 0, B, w["V"], w["top_n"], flags1 & ~STRATA_FLAG_EARLY_LOAD if verify else flags1)
         g1, warm1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
@@ -491,7 +499,7 @@ def run_gpu(args, rank, world):
     copy_out = torch.cuda.Stream(device=dev)
 
     # the e2e inputs are copied in right before each call, so those calls do not claim early loads
-    flags_e2e = flags & ~(STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_CONCURRENT)
+    flags_e2e = flags & ~(STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_CONCURRENT | STRATA_FLAG_OWN_OUTPUTS)
 
     def e2e_step(k):
         st_ = sets[k % 2]
@@ -587,7 +595,9 @@ def run_gpu(args, rank, world):
                                 f"{R * step_bytes / l2:.1f}x the {l2 / 1e6:.0f} MB L2)",
                    "launch": "one CUDA graph of the K calls" + (", programmatic dependent launch" if flags & 1 else "")
                              + (", logit loads start before the previous call ends (inputs resident)"
-                                if flags & 2 else ""),
+                                if flags & 2 else "")
+                             + (", each call writes its own output set (no wait for the previous call)"
+                                if flags & STRATA_FLAG_OWN_OUTPUTS else ""),
                    "split": shape["split"], "chunk_elems": shape["chunk"], "smem_bytes": shape["smem"],
                    "grid": shape["grid"], "parallelism": f"replicas x{world}",
                    "streams": S},
@@ -619,6 +629,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--split", type=int, default=0,
                     help="blocks per row (1..16; 0: the library's choice), for launch-shape sweeps")
+    ap.add_argument("--no-own-outputs", action="store_true",
+                    help="every call of a group writes the same output buffers, so each call waits for the "
+                         "previous one before its counters and writes")
     ap.add_argument("--streams", type=int, default=8,
                     help="independent request groups, each its own context, slots and stream; the steps "
                          "alternate over them and the groups' calls overlap")

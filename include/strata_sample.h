@@ -91,6 +91,18 @@ extern "C" {
  * update happens on the device, so a captured call carries the history forward on every replay.
  * Ignored by strata_logprobs_rows.                                                              */
 #define STRATA_FLAG_HISTORY_RING 0x8u
+/* With STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD, for strata_sample_rows and strata_logprobs_rows
+ * (not verify windows, not kept histories: STRATA_EINVAL): the caller asserts that no call that
+ * may still be running when this one starts (the previous calls on the stream) writes or reads
+ * this call's output buffers, for instance because consecutive calls write different buffers.
+ * The call then never waits for the previous one: it takes its draw counters at its start, before
+ * the next call on the stream may launch, so counters still advance in call order (each sampled
+ * slot by one per call, every row of a slot seeing the value from before the call), and it writes
+ * its outputs when they are ready.  Results are the same as without the flag.  The next call's
+ * launch then waits for this call's counter atomics (a few memory round trips at its start), so
+ * one stream of calls alone can run slower with the flag; it pays when independent request groups
+ * (other contexts, other streams) keep the GPU busy meanwhile (see STRATA_FLAG_CONCURRENT).     */
+#define STRATA_FLAG_OWN_OUTPUTS 0x20u
 /* A launch-shape hint: calls on other streams (of other contexts) run on the GPU at the same time
  * as this one, so whole-GPU throughput matters more than this call's latency.  The call then gives
  * each row one block per STRATA_CONCURRENT_ROW_BYTES of logits (one block for a full fp32 or bf16

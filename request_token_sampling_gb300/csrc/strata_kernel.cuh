@@ -83,7 +83,8 @@ enum : int {
   CTL_TOT_R = 7,
   CTL_SLOT0 = 8,     // per ring slot: warps done with the piece it holds (the last one refills it)
   CTL_LAST0 = CTL_SLOT0 + MAX_SLOTS,  // per ring slot: the last piece issued into it
-  CTL_WORDS = CTL_LAST0 + MAX_SLOTS
+  CTL_CTR = CTL_LAST0 + MAX_SLOTS,    // leader, own outputs: the counter word (2) and a use of the
+  CTL_WORDS = CTL_CTR + 3             // advancing atomic's value (1)
 };
 
 // A slot's keys as the kernel reads them (prepared and validated by the host).
@@ -743,6 +744,26 @@ __device__ __forceinline__ void slot_arrival_done(int r_s, int slot, unsigned lo
     atomicAdd(&ctr[slot], (1ull << 16) - static_cast<unsigned long long>(r_s));
 }
 
+// A call with own outputs takes its slot's counter at its start (warp-wide, the leader's warp 0 of a
+// sampled row), the same way the draw takes it otherwise: one atomic for a slot with one row in
+// the call; with several, one arrival each and the row completing them advances the counter.  The
+// value waits in shared memory until the draw (no register held through the first pass); the
+// stores need both atomics' returned values, so both have been performed when they are done.
+// Out of line: plain calls never take it.
+__device__ __noinline__ void take_counter_early(int rs0, int rs1, const int32_t* row_slot, int B, int slot,
+                                                unsigned long long* ctr, uint32_t* ctl, int lane) {
+  const int rs = slot_rows(rs0, rs1, row_slot, B, slot, lane);
+  if (lane == 0) {
+    const unsigned long long v = atomicAdd(&ctr[slot], rs == 1 ? (1ull << 16) : 1ull);
+    uint32_t adv = 0u;
+    if (rs > 1 && (v & 0xFFFFull) + 1ull == static_cast<unsigned long long>(rs))
+      adv = static_cast<uint32_t>(atomicAdd(&ctr[slot], (1ull << 16) - static_cast<unsigned long long>(rs)));
+    ctl[CTL_CTR] = static_cast<uint32_t>(v);
+    ctl[CTL_CTR + 1] = static_cast<uint32_t>(v >> 32);
+    ctl[CTL_CTR + 2] = adv;
+  }
+}
+
 // The end of a slot's rows in a verify call or a call that keeps histories, run by the leader warp
 // of every row of the slot once lane 0 has stored the row's pick.  The row publishes its pick and
 // counts itself done in the slot's arrival word; the last row of the slot to finish reads every
@@ -812,18 +833,22 @@ __device__ __noinline__ void slot_window_done(const int32_t* row_slot, const int
 
 // ------------------------------------------------------------------------------ the kernel
 // DT: 0 fp32 rows, 1 bf16 rows.  MASK: allowed ids restrict the sampling (STRATA_FLAG_ALLOWED_MASK);
-// a separate instantiation so that plain launches carry none of its state.
-template <int DT, bool MASK>
+// OWN: a call with own outputs and early loads (STRATA_FLAG_OWN_OUTPUTS).  Separate instantiations
+// so that plain launches carry none of their state or code.
+template <int DT, bool MASK, bool OWN = false>
 __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char sm[];
   constexpr int ESZ = DT == 0 ? 4 : 2;
   constexpr int EPV = 16 / ESZ;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool early = (P.flags & STRATA_FLAG_EARLY_LOAD) != 0u;
+  // own outputs (early loads only): nothing of this call waits for the previous call; the draw
+  // counters are taken before the next call may launch, which keeps them in call order
+  const bool own_out = OWN && early;
   if (!early) grid_dep_wait();  // inputs may be the previous kernel's outputs
   // the next call may start its own loads now: launching it is what bounds a stream of calls
   // whose CTAs each take microseconds to reach their first copy (its outputs still wait for ours)
-  grid_dep_launch();
+  if (!own_out) grid_dep_launch();
 
   const uint32_t crank = cluster_ctarank();
   const int cs = P.cs;
@@ -919,7 +944,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     }
   for (int i = tid; i < P.hash_cap; i += NT) htab[i] = HASH_EMPTY;
   if (tid < NT / 32) hflag[tid] = 0u;
-  if (tid < CTL_WORDS) ctl[tid] = (tid == CTL_T) ? 0xFFFFFFFFu : (tid >= CTL_LAST0 ? static_cast<uint32_t>(tid - CTL_LAST0) : 0u);
+  if (tid < CTL_WORDS)
+    ctl[tid] = (tid == CTL_T) ? 0xFFFFFFFFu
+                              : (tid >= CTL_LAST0 && tid < CTL_CTR ? static_cast<uint32_t>(tid - CTL_LAST0) : 0u);
   __syncthreads();           // tables zeroed, barriers initialised
   cluster_arrive_relaxed();  // this CTA is running (remote stores wait for every CTA, below)
 
@@ -973,6 +1000,13 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     rs_pre[1] = lane + 32 < P.B ? P.row_slot[lane + 32] : -1;
   }
   int r_slot = 0;  // rows of this row's slot in the call (leader's warp 0)
+  if (own_out) {
+    // The counters now, before any CTA lets the next call launch: that call's atomics on these
+    // words are issued after its launch, so after these have returned.
+    if (ctr_warp) take_counter_early(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, P.ctr, ctl, lane);
+    __syncthreads();
+    grid_dep_launch();
+  }
 
   int hid[HPRE];  // third metadata level: this thread's first history ids, for the table after the pass
 #pragma unroll
@@ -1406,7 +1440,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   if (crank == 0 && (P.flags & STRATA_FLAG_TEST_STALL)) test_stall(&mbar[BAR_STALL], ctl, P.err);
   if (kp > 0 && crank == 0) {
     if (cs > 1) wait_bar(&mbar[BAR_X1], ctl, P.err, true);
-    if (ctr_warp) r_slot = slot_rows(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, lane);
+    if (ctr_warp && !own_out) r_slot = slot_rows(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, lane);
     // issued here, consumed by the draw: the merge and the tail's first half hide the latency
     if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], r_slot == 1 ? (1ull << 16) : 1ull);
     __syncthreads();  // every slice (the leader's own included) is in place
@@ -1550,10 +1584,12 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 
   // ---- outputs (leader only): with early loads the previous kernel owns outputs and counters
   // until it ends ---------------------------------------------------------------------------------
-  if (early && crank == 0) {
+  if (early && !own_out && crank == 0) {
     grid_dep_wait();
     if (ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], r_slot == 1 ? (1ull << 16) : 1ull);
   }
+  if (own_out && ctr_thread)  // taken at the start
+    ctr_old = (static_cast<unsigned long long>(ctl[CTL_CTR + 1]) << 32) | ctl[CTL_CTR];
 
   // allowed-subset log-probabilities and the given chosen id
   if (crank == 0 && P.allowed_off != nullptr && P.allowed_lps != nullptr) {
@@ -1612,13 +1648,13 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       } else if (k_eff == 0) {
         if (lane == 0) atomicOr(P.err, STRATA_DEVERR_NOCAND);
         // a sampled row without a candidate still counted itself among its slot's arrivals
-        if (sampled) slot_arrival_done(r_slot, slot, P.ctr, ctr_old, lane);
+        if (sampled && !own_out) slot_arrival_done(r_slot, slot, P.ctr, ctr_old, lane);
       } else {
         int j = 0;
         if (sampled) {
           uint32_t x0 = 0u;
           if (ctr_thread) x0 = philox_word0(sp.seed, pos, ctr_old >> 16);
-          slot_arrival_done(r_slot, slot, P.ctr, ctr_old, lane);
+          if (!own_out) slot_arrival_done(r_slot, slot, P.ctr, ctr_old, lane);
           x0 = __shfl_sync(FULL_MASK, x0, 0);
           const float u = static_cast<float>(x0 >> 8) * 0x1p-24f;
           const int last = m2 - 1;  // the draw reads prefixes below m2 only; W = C[m2 - 1]

@@ -38,6 +38,17 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+// The kernel instance for a launch: logit type x allowed-id mask x own outputs.
+using KernelFn = void (*)(strata::KParams);
+KernelFn kernel_for(int dtype, bool mask, bool own) {
+  static const KernelFn table[2][2][2] = {
+      {{strata::rows_kernel<0, false, false>, strata::rows_kernel<0, false, true>},
+       {strata::rows_kernel<0, true, false>, strata::rows_kernel<0, true, true>}},
+      {{strata::rows_kernel<1, false, false>, strata::rows_kernel<1, false, true>},
+       {strata::rows_kernel<1, true, false>, strata::rows_kernel<1, true, true>}}};
+  return table[dtype == STRATA_DTYPE_F32 ? 0 : 1][mask ? 1 : 0][own ? 1 : 0];
+}
+
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(STRATA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -252,10 +263,8 @@ int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t
   cfg.numAttrs = na;
   cudaError_t e;
   const bool mask = P.mode == strata::MODE_SAMPLE && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u && P.allowed_off != nullptr;
-  if (dtype == STRATA_DTYPE_F32)
-    e = mask ? cudaLaunchKernelEx(&cfg, strata::rows_kernel<0, true>, P) : cudaLaunchKernelEx(&cfg, strata::rows_kernel<0, false>, P);
-  else
-    e = mask ? cudaLaunchKernelEx(&cfg, strata::rows_kernel<1, true>, P) : cudaLaunchKernelEx(&cfg, strata::rows_kernel<1, false>, P);
+  const bool own = (flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u;
+  e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, mask, own), P);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   (void)c;
   return STRATA_OK;
@@ -358,11 +367,9 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
     strata_destroy(c);
     return code;
   };
-  const void* kernels[4] = {reinterpret_cast<const void*>(strata::rows_kernel<0, false>),
-                            reinterpret_cast<const void*>(strata::rows_kernel<1, false>),
-                            reinterpret_cast<const void*>(strata::rows_kernel<0, true>),
-                            reinterpret_cast<const void*>(strata::rows_kernel<1, true>)};
-  for (const void* k : kernels) {
+  for (int i = 0; i < 8; ++i) {
+    const void* k = reinterpret_cast<const void*>(kernel_for(i & 1 ? STRATA_DTYPE_BF16 : STRATA_DTYPE_F32, (i >> 1) & 1,
+                                                             (i >> 2) & 1));
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->max_smem)) != cudaSuccess)
       return cleanup(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
@@ -613,6 +620,8 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   }
   if (hist_off != nullptr && (hist == nullptr || n_hist_slots < 1))
     return fail(STRATA_EINVAL, "hist_off needs hist and n_hist_slots >= 1");
+  if ((flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && (kept_hist || row_draft != nullptr))
+    return fail(STRATA_EINVAL, "STRATA_FLAG_OWN_OUTPUTS is for plain sampling calls (no verify windows, no kept histories)");
   if (hist_off == nullptr) n_hist_slots = 0;
   if ((rc = check_device(c)) != STRATA_OK) return rc;
   if (B == 0) return STRATA_OK;

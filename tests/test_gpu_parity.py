@@ -169,6 +169,66 @@ def test_config4_pipelined_calls(sampler):
     print("config4 pipelined", st)
 
 
+@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+def test_config4_pipelined_own_outputs(sampler, concurrent):
+    """Back-to-back calls on one stream that each write their own outputs: no call waits for the
+    one before it, each takes its counters at its start, and the draws still follow call order."""
+    from request_token_sampling_gb300 import (STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_OWN_OUTPUTS,
+                                              STRATA_FLAG_PDL)
+    base = synth.config4(fused=True)
+    set_slots(sampler, base)
+    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS
+    if concurrent:
+        fl |= STRATA_FLAG_CONCURRENT
+    ws = []
+    for c in range(8):
+        w = dict(base)
+        w["logits"] = np.roll(base["logits"], 613 * c, axis=1) if c else base["logits"]
+        ws.append((w, upload(w)))
+    torch.cuda.synchronize()
+    outs = [sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=d["hist"], hist_off=d["hist_off"],
+                           top_n=w["top_n"], chosen_lp=True, allowed=d["allowed"], allowed_off=d["allowed_off"],
+                           flags=fl) for w, d in ws]
+    torch.cuda.synchronize()
+    counters = dict(base["counters"])
+    st = Stats()
+    for (w, _), o in zip(ws, outs):
+        rows, counters = oracle.sample_call(w, counters=counters)
+        compare_sample(w, rows, {k: v.cpu().numpy() for k, v in o.items()}, stats=st, debug=False)
+    for s in base["slot_params"]:
+        assert sampler.slot_state(s)[1] == counters[s]
+    _check_no_errors(sampler)
+    print("config4 own outputs", st)
+
+
+def test_config5_pipelined_own_outputs_rows_share_slots(sampler):
+    """Config 5's 64 rows (8 per slot) in three back-to-back calls with own outputs: every row of a
+    slot draws at the slot's counter from before its call, and each call advances it by one."""
+    from request_token_sampling_gb300 import (STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_OWN_OUTPUTS,
+                                              STRATA_FLAG_PDL)
+    base = synth.config5()
+    set_slots(sampler, base)
+    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS | STRATA_FLAG_CONCURRENT
+    ws = []
+    for c in range(3):
+        w = dict(base)
+        w["logits"] = np.roll(base["logits"], 4099 * c, axis=1) if c else base["logits"]
+        ws.append((w, upload(w)))
+    torch.cuda.synchronize()
+    outs = [sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=d["hist"], hist_off=d["hist_off"],
+                           top_n=w["top_n"], chosen_lp=True, flags=fl) for w, d in ws]
+    torch.cuda.synchronize()
+    counters = dict(base["counters"])
+    st = Stats()
+    for (w, _), o in zip(ws, outs):
+        rows, counters = oracle.sample_call(w, counters=counters, with_allowed=False)
+        compare_sample(w, rows, {k: v.cpu().numpy() for k, v in o.items()}, stats=st, debug=False)
+    for s in range(8):
+        assert sampler.slot_state(s)[1] == counters[s] == 3
+    _check_no_errors(sampler)
+    print("config5 own outputs", st)
+
+
 def test_config4_concurrent_groups():
     """Two request groups, each its own context and stream, their pipelined calls interleaved with
     the concurrency hint (one block per full row): every call of each group matches the oracle,

@@ -177,6 +177,22 @@ def test_verify_pipelined_windows(sampler):
     assert sampler.slot_state(0)[1] == 6
 
 
+def test_verify_refuses_own_outputs(sampler):
+    """Verify windows depend on the previous call (its kept counts): the own-outputs flag is an
+    argument error there, and nothing is launched."""
+    import request_token_sampling_gb300 as S
+    w = synth.config2_window(3)
+    set_slots(sampler, w)
+    d = upload(w)
+    dr = torch.full((w["B"],), -1, dtype=torch.int32, device="cuda:0")
+    before = sampler.slot_state(0)[1]
+    with pytest.raises(S.StrataError) as ei:
+        sampler.verify(d["logits"], d["row_slot"], d["row_pos"], dr, V=w["V"], hist=d["hist"], hist_off=d["hist_off"],
+                       flags=S.STRATA_FLAG_PDL | S.STRATA_FLAG_EARLY_LOAD | S.STRATA_FLAG_OWN_OUTPUTS)
+    assert ei.value.code == S.STRATA_EINVAL
+    assert sampler.slot_state(0)[1] == before
+
+
 def test_verify_needs_drafts_and_keep(sampler):
     import request_token_sampling_gb300 as S
     w = synth.config1()
