@@ -1583,7 +1583,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   }
 
   // ---- outputs (leader only): with early loads the previous kernel owns outputs and counters
-  // until it ends ---------------------------------------------------------------------------------
+  // until it ends, unless this call has its own outputs (its counter was taken at the start) -----
   if (early && !own_out && crank == 0) {
     grid_dep_wait();
     if (ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], r_slot == 1 ? (1ull << 16) : 1ull);
