@@ -116,6 +116,9 @@ def test_history_errors(sampler, S):
         sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=w["V"], hist=h, hist_off=ho,
                        flags=S.STRATA_FLAG_HISTORY_RING)
     assert ei.value.code == S.STRATA_EINVAL           # the flag replaces hist/hist_off
+    with pytest.raises(S.StrataError) as ei:
+        _call(sampler, S, w, d, flags=S.STRATA_FLAG_PDL | S.STRATA_FLAG_EARLY_LOAD | S.STRATA_FLAG_OWN_OUTPUTS)
+    assert ei.value.code == S.STRATA_EINVAL           # kept histories depend on the previous call
 
 
 @pytest.mark.parametrize("dtype,V,flags", [("f32", synth.V_SMALL, 0), ("bf16", 50_000, 0),

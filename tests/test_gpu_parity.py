@@ -83,6 +83,30 @@ def test_config4_logprobs_entry(sampler):
     print("config4 logprobs", st)
 
 
+@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+def test_config4_logprobs_entry_pipelined_own_outputs(sampler, concurrent):
+    """strata_logprobs_rows back to back with early loads and own outputs: no call waits for the
+    one before it; each call's log-probabilities against the oracle."""
+    from request_token_sampling_gb300 import (STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_OWN_OUTPUTS,
+                                              STRATA_FLAG_PDL)
+    base = synth.config4(fused=False)
+    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS
+    if concurrent:
+        fl |= STRATA_FLAG_CONCURRENT
+    ws = []
+    for c in range(5):
+        w = dict(base)
+        w["logits"] = np.roll(base["logits"], 2311 * c, axis=1) if c else base["logits"]
+        ws.append((w, upload(w)))
+    torch.cuda.synchronize()
+    outs = [sampler.logprobs(d["logits"], V=w["V"], chosen=d.get("chosen"), top_n=w["top_n"], allowed=d["allowed"],
+                             allowed_off=d["allowed_off"], flags=fl) for w, d in ws]
+    torch.cuda.synchronize()
+    for (w, _), o in zip(ws, outs):
+        compare_logprobs(w, oracle.logprobs_call(w), {k: v.cpu().numpy() for k, v in o.items()})
+    _check_no_errors(sampler)
+
+
 def test_config4_fused_sample_and_logprobs(sampler):
     w = synth.config4(fused=True)
     set_slots(sampler, w)
