@@ -9,10 +9,13 @@ with top_logprobs=20, the sampled token's log-probability and allowed_token_ids 
   value      rows/s over exactly K timed steps: one CUDA graph holding the K calls, replayed once;
              inputs rotate over enough distinct batches to exceed 4x the L2 size (HBM serves reads).
              The steps alternate over S independent request groups (`--streams`, default 8): each
-             group is its own context (own slots, counters, outputs) with its own stream, its calls
+             group is its own context (own slots and counters) with its own stream, its calls
              chained in order, the groups' calls overlapping, with the concurrency launch hint.
-  single_group  the same K steps as one group alone (one stream, the library's pipelined launch
-             shape): each call then waits for the previous call's counters before its draw.
+             Call i writes output set i % R (`STRATA_FLAG_OWN_OUTPUTS`; `--no-own-outputs` gives
+             each group one set), so no call waits for the previous one.
+  single_group  the same K steps as one group alone into one set of buffers (one stream, the
+             library's pipelined launch shape): each call waits for the previous call before its
+             counters and writes.
   e2e        the same metric through the C ABI from pinned host buffers: every step copies its
              inputs host->device (the logits, and the small arrays packed into one copy), runs the
              call and copies every output back (one packed copy); copies run on their own streams
