@@ -357,9 +357,8 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     if any(sg.errors() != 0 for sg in samplers):
         raise RuntimeError("device error bits set")
-    # the launch shape of a plain call with these flags; verify windows and kept-history calls are
-    # steps of one request's decode and take the latency split (as a call without early loads)
-    shape = s.shape(0, 0, B, w["V"], w["top_n"], flags & ~STRATA_FLAG_EARLY_LOAD if verify else flags)
+    # the launch shape of a call with these flags (mode 2: verify windows)
+    shape = s.shape(2 if verify else 0, 0, B, w["V"], w["top_n"], flags)
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
@@ -435,7 +434,7 @@ def run_gpu(args, rank, world):
     single = None
     if S > 1:
         flags1 = flags & ~(STRATA_FLAG_CONCURRENT | STRATA_FLAG_OWN_OUTPUTS)
-        shape1 = s.shape(0, 0, B, w["V"], w["top_n"], flags1 & ~STRATA_FLAG_EARLY_LOAD if verify else flags1)
+        shape1 = s.shape(2 if verify else 0, 0, B, w["V"], w["top_n"], flags1)
         g1, warm1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             for i in range(3):

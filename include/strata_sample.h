@@ -107,8 +107,10 @@ extern "C" {
  * as this one, so whole-GPU throughput matters more than this call's latency.  The call then gives
  * each row one block per STRATA_CONCURRENT_ROW_BYTES of logits (one block for a full fp32 or bf16
  * row of 248,320 ids): fewer blocks per byte, no exchange between blocks, at the price of a longer
- * call (each block streams its row alone).  Results are the same as without the flag.  A forced
- * split (STRATA_FLAG_SPLIT) takes precedence.                                                     */
+ * call (each block streams its row alone).  strata_sample_verify, whose windows wait for the
+ * previous window, uses half that, and calls with STRATA_FLAG_HISTORY_RING (which wait for the
+ * previous call before their penalties) one block per 128 KiB.  Results are the same as without
+ * the flag.  A forced split (STRATA_FLAG_SPLIT) takes precedence.                                */
 #define STRATA_FLAG_CONCURRENT  0x10u
 #define STRATA_CONCURRENT_ROW_BYTES (1u << 20)
 /* Testing aid: the row leaders also wait for one arrival that nothing sends, so that their bounded
@@ -321,11 +323,10 @@ int strata_read_errors(strata_ctx *ctx, uint32_t *bits, void *stream);
 /*
  * The launch shape a call with these arguments would use (host only, nothing enqueued):
  * blocks per row (the thread-block cluster size), elements per block, dynamic shared memory
- * bytes and the total grid size.  mode 0 = strata_sample_rows, 1 = strata_logprobs_rows.  The
- * shape is that of a call without allowed lists and, for mode 0, of strata_sample_rows.  Allowed
+ * bytes and the total grid size.  mode 0 = strata_sample_rows, 1 = strata_logprobs_rows,
+ * 2 = strata_sample_verify.  The shape is that of a call without allowed lists.  Allowed
  * lists need a bitmap of the block's ids, which shares the block's copy ring and changes nothing
  * unless it is larger than the ring; STRATA_FLAG_ALLOWED_MASK adds a second bitmap of that size.
- * strata_sample_verify splits rows as a call without STRATA_FLAG_EARLY_LOAD does.
  */
 int strata_launch_shape(strata_ctx *ctx, int mode, int dtype, int B, int V, int top_n,
                         uint32_t flags, int *split, int *chunk_elems, int *smem_bytes, int *grid);

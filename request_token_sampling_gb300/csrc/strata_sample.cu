@@ -155,8 +155,9 @@ struct Shape {
 // keys each warp publishes for the row threshold, history table size and shared memory.  Shared
 // by the context calls and the allocation-free call.
 int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mode, int esz, int B, int V, int kmax,
-              int nmax, int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined, bool concurrent,
-              int forced, Shape* s) {
+              int nmax, int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined,
+              int concurrent_bytes, int forced, Shape* s) {
+  const bool concurrent = concurrent_bytes > 0;
   const long long row_bytes = static_cast<long long>(V) * esz;
   s->nmax = nmax;
   s->kmax = kmax;
@@ -166,7 +167,7 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
     if (forced > max_cluster) return fail(STRATA_ERANGE, "forced split %d above the cluster limit %d", forced, max_cluster);
     cs = forced;
   } else if (concurrent) {
-    cs = static_cast<int>((row_bytes + STRATA_CONCURRENT_ROW_BYTES - 1) / STRATA_CONCURRENT_ROW_BYTES);
+    cs = static_cast<int>((row_bytes + concurrent_bytes - 1) / concurrent_bytes);
     cs = std::min(std::max(cs, 1), max_cluster);
   } else if (pipelined) {
     cs = static_cast<int>((row_bytes + PIPELINED_BYTES - 1) / PIPELINED_BYTES);
@@ -218,9 +219,18 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
   // latter wait for the previous call before their penalties): they take the latency split
   const bool pipelined = (flags & STRATA_FLAG_PDL) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u &&
                          (flags & STRATA_FLAG_HISTORY_RING) == 0u && !verify;
+  // the concurrency hint: a plain call's block streams up to STRATA_CONCURRENT_ROW_BYTES; a verify
+  // window waits for the previous window, so its latency stays on its group's chain and it takes
+  // half that; a call that keeps histories waits for the previous call before its penalties and
+  // takes PIPELINED_BYTES (measured at 8 groups: these were the fastest of the splits tried)
+  int concurrent_bytes = 0;
+  if ((flags & STRATA_FLAG_CONCURRENT) != 0u)
+    concurrent_bytes = (flags & STRATA_FLAG_HISTORY_RING) != 0u ? PIPELINED_BYTES
+                       : verify ? static_cast<int>(STRATA_CONCURRENT_ROW_BYTES / 2)
+                                : static_cast<int>(STRATA_CONCURRENT_ROW_BYTES);
   return shape_for(c->max_cluster, c->max_smem, c->smem_three, c->num_sms, mode, esz, B, V, kmax, top_n_eff,
                    max_lastn_penal(c),
-                   with_hist, with_allowed, mask, pipelined, (flags & STRATA_FLAG_CONCURRENT) != 0u,
+                   with_hist, with_allowed, mask, pipelined, concurrent_bytes,
                    static_cast<int>((flags >> 8) & 0x1Fu), s);
 }
 
@@ -588,11 +598,13 @@ int strata_read_errors(strata_ctx* c, uint32_t* bits, void* stream) {
 int strata_launch_shape(strata_ctx* c, int mode, int dtype, int B, int V, int top_n, uint32_t flags, int* split,
                         int* chunk_elems, int* smem_bytes, int* grid) {
   if (c == nullptr) return fail(STRATA_EINVAL, "null context");
-  if (mode != strata::MODE_SAMPLE && mode != strata::MODE_LOGPROBS) return fail(STRATA_EINVAL, "mode %d", mode);
+  const bool verify = mode == 2;  // strata_sample_verify
+  if (mode != strata::MODE_SAMPLE && mode != strata::MODE_LOGPROBS && !verify) return fail(STRATA_EINVAL, "mode %d", mode);
   if (dtype != STRATA_DTYPE_F32 && dtype != STRATA_DTYPE_BF16) return fail(STRATA_EINVAL, "dtype %d", dtype);
   if (B < 1 || V < 1 || V > c->max_vocab || top_n < 0 || top_n > STRATA_MAX_TOP_N) return fail(STRATA_EINVAL, "shape");
   Shape sh;
-  const int rc = compute_shape(c, mode, dtype, B, V, top_n, true, false, flags, &sh);
+  const int rc = compute_shape(c, verify ? strata::MODE_SAMPLE : mode, dtype, B, V, top_n, true, false, flags, &sh,
+                               verify);
   if (rc != STRATA_OK) return rc;
   if (split) *split = sh.cs;
   if (chunk_elems) *chunk_elems = sh.chunk;
@@ -885,7 +897,7 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
   Shape sh;
   if ((rc = shape_for(nd->max_cluster, nd->max_smem, nd->smem_three, nd->num_sms, strata::MODE_SAMPLE, esz, B, V,
                       std::max(1, kmax_sampled),
-                      top_n_eff, max_lastn, hist_off != nullptr, false, false, false, false, 0, &sh)) != STRATA_OK)
+                      top_n_eff, max_lastn, hist_off != nullptr, false, false, false, 0, 0, &sh)) != STRATA_OK)
     return rc;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -66,9 +66,9 @@ def test_verify_window_every_prefix(sampler, accepted):
 
 
 @pytest.mark.parametrize("accepted", [0, 2, 4])
-def test_verify_window_one_cta_per_row(sampler, accepted):
-    """The same windows with the concurrency hint (one CTA streams each whole row, no exchange
-    between CTAs) and pipelined flags, as independent request groups run them."""
+def test_verify_window_concurrency_hint(sampler, accepted):
+    """The same windows with the concurrency hint (two CTAs per full row) and pipelined flags, as
+    independent request groups run them; also one CTA per row, forced."""
     from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL
     w = synth.config2_window(31 + accepted)
     set_slots(sampler, w)
@@ -78,11 +78,16 @@ def test_verify_window_one_cta_per_row(sampler, accepted):
     if accepted < w["B"] - 1:
         drafts[accepted] = (picks[accepted] + 29) % w["V"]
     set_slots(sampler, w)
-    g = _verify(sampler, w, drafts, flags=STRATA_FLAG_CONCURRENT | STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD)
+    from request_token_sampling_gb300 import STRATA_FLAG_SPLIT
+    fl = STRATA_FLAG_CONCURRENT | STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD
+    assert sampler.shape(2, 0, w["B"], w["V"], w["top_n"], fl)["split"] == 2
     rows2, ctr, keep = oracle.verify_call(w, drafts)
     assert keep == {0: accepted + 1}
-    _check(w, rows2, g, drafts)
-    assert sampler.slot_state(0)[1] == ctr[0]
+    for extra in (0, STRATA_FLAG_SPLIT(1)):
+        set_slots(sampler, w)
+        g = _verify(sampler, w, drafts, flags=fl | extra)
+        _check(w, rows2, g, drafts)
+        assert sampler.slot_state(0)[1] == ctr[0]
 
 
 def test_verify_batch_of_slots_mixed(sampler):
