@@ -72,7 +72,8 @@ extern "C" {
  * slots, positions, drafts, history rows, allowed lists) was complete before the previous kernel
  * on the stream started (none of it is that kernel's output).  The kernel then starts its loads
  * before waiting for the previous kernel; draw counters, the slots' kept histories
- * (STRATA_FLAG_HISTORY_RING) and every output are still read or written after the wait.        */
+ * (STRATA_FLAG_HISTORY_RING) and every output are still read or written after the wait (draw
+ * counters and outputs without any wait under STRATA_FLAG_OWN_OUTPUTS, below).                  */
 #define STRATA_FLAG_EARLY_LOAD  0x2u
 /* strata_sample_rows with allowed/allowed_off: a row that names allowed ids samples only among
  * them (allowed_token_ids as a sampling mask for constrained decoding [P3200, "Problem and result"
