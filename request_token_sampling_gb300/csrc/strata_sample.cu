@@ -86,6 +86,10 @@ struct strata_ctx {
   unsigned long long* d_hlen = nullptr;   // kept histories: per-slot total length
   std::vector<strata_sampling_params> h_params;
   std::vector<SlotDev> h_slots;
+  // a sampling call that takes its draw counters after waiting for its predecessor was launched
+  // with programmatic dependent launch, and may still be running: until a launch without PDL,
+  // calls with own outputs take their counters that way too (so counters keep call order)
+  bool late_counters_pending = false;
   // histograms over slots, for the launch shape: top_k of sampled slots, window of penal slots
   std::vector<int> k_bins, lastn_bins;
 };
@@ -592,6 +596,7 @@ int strata_read_errors(strata_ctx* c, uint32_t* bits, void* stream) {
   if ((e = cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), s)) != cudaSuccess) return cuda_fail(e, "error word clear");
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "error word sync");
   *bits = v;
+  c->late_counters_pending = false;  // the stream has drained
   return STRATA_OK;
 }
 
@@ -677,14 +682,21 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   P.hash_bits = sh.hash_bits;
   P.nslot = sh.nslot;
   P.qw = sh.qw;
+  if ((flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && c->late_counters_pending) flags &= ~STRATA_FLAG_OWN_OUTPUTS;
   P.flags = flags;
   P.row_draft = row_draft;
   P.slot_keep = slot_keep;
   P.done = c->d_done;
   P.ring = kept_hist ? c->d_ring : nullptr;
   P.hlen = kept_hist ? c->d_hlen : nullptr;
-  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream),
-                row_draft != nullptr ? "sample_verify" : "sample_rows");
+  rc = launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream),
+              row_draft != nullptr ? "sample_verify" : "sample_rows");
+  if (rc == STRATA_OK) {
+    const bool pdl = (flags & STRATA_FLAG_PDL) != 0u;
+    const bool early_counters = (flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u;
+    c->late_counters_pending = pdl && (c->late_counters_pending || !early_counters);
+  }
+  return rc;
 }
 
 int strata_sample_rows(strata_ctx* c, const void* logits, int dtype, int B, int V, int64_t ld,
@@ -750,7 +762,9 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
   P.nslot = sh.nslot;
   P.qw = sh.qw;
   P.flags = flags;
-  return launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream), "logprobs_rows");
+  rc = launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream), "logprobs_rows");
+  if (rc == STRATA_OK && (flags & STRATA_FLAG_PDL) == 0u) c->late_counters_pending = false;  // all earlier work done
+  return rc;
 }
 
 }  // extern "C"

@@ -232,3 +232,36 @@ def test_trace_lines_on_stderr():
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stderr.splitlines() if l.startswith("strata: sample_rows")]
     assert len(lines) == 1 and "V=32000" in lines[0] and "split=" in lines[0] and "smem=" in lines[0], r.stderr[-2000:]
+
+
+def test_own_outputs_after_a_waiting_call_take_counters_late():
+    """A flagged call that follows an unflagged pipelined call on the same context takes its
+    counters after its wait (the launch it gets carries no own-outputs bit) until the stream has
+    drained; the trace shows the flags each launch got."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = """
+import sys; sys.path.insert(0, %r)
+import torch, synth
+from _harness import set_slots, upload
+import request_token_sampling_gb300 as S
+w = synth.config1(); s = S.Sampler(0, 4, w['V'], 4); set_slots(s, w); d = upload(w)
+own = S.STRATA_FLAG_PDL | S.STRATA_FLAG_EARLY_LOAD | S.STRATA_FLAG_OWN_OUTPUTS
+def call(fl): s.sample(d['logits'], d['row_slot'], d['row_pos'], V=w['V'], hist=d['hist'], hist_off=d['hist_off'], flags=fl)
+call(own); call(S.STRATA_FLAG_PDL | S.STRATA_FLAG_EARLY_LOAD); call(own); call(own)
+assert s.errors() == 0
+call(own)
+torch.cuda.synchronize(); print('counter', s.slot_state(0)[1]); s.close()
+""" % os.path.join(root, "tests")
+    env = dict(os.environ, STRATA_SAMPLE_DEBUG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    flags = [int(l.split("flags=")[1].split()[0], 16) for l in r.stderr.splitlines() if l.startswith("strata: sample_rows")]
+    assert len(flags) == 5, r.stderr[-2000:]
+    own_bits = [bool(f & 0x20) for f in flags]
+    assert own_bits == [True, False, False, False, True], flags
+    assert "counter 5" in r.stdout

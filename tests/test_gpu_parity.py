@@ -201,6 +201,7 @@ def test_config4_pipelined_own_outputs(sampler, concurrent):
                                               STRATA_FLAG_PDL)
     base = synth.config4(fused=True)
     set_slots(sampler, base)
+    sampler.errors()  # drained: an earlier waiting call would make these take their counters late
     fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS
     if concurrent:
         fl |= STRATA_FLAG_CONCURRENT
@@ -232,6 +233,7 @@ def test_config5_pipelined_own_outputs_rows_share_slots(sampler):
                                               STRATA_FLAG_PDL)
     base = synth.config5()
     set_slots(sampler, base)
+    sampler.errors()  # drained: an earlier waiting call would make these take their counters late
     fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS | STRATA_FLAG_CONCURRENT
     ws = []
     for c in range(3):
