@@ -265,3 +265,20 @@ torch.cuda.synchronize(); print('counter', s.slot_state(0)[1]); s.close()
     own_bits = [bool(f & 0x20) for f in flags]
     assert own_bits == [True, False, False, False, True], flags
     assert "counter 5" in r.stdout
+
+
+def test_launch_shape_modes(sampler):
+    """The shape query covers the three entry points (0 sampling, 1 logprobs, 2 verify windows) and
+    refuses any other mode; the concurrency hint gives sampling rows one CTA and verify rows two."""
+    import request_token_sampling_gb300 as S
+    fl = S.STRATA_FLAG_PDL | S.STRATA_FLAG_EARLY_LOAD | S.STRATA_FLAG_CONCURRENT
+    assert sampler.shape(0, 0, 8, synth.V_FULL, 20, fl)["split"] == 1
+    assert sampler.shape(1, 0, 8, synth.V_FULL, 20, fl)["split"] == 1
+    assert sampler.shape(2, 0, 5, synth.V_FULL, 0, fl)["split"] == 2
+    assert sampler.shape(2, 0, 5, synth.V_FULL, 0, fl | S.STRATA_FLAG_HISTORY_RING)["split"] == 8
+    for m in (0, 1, 2):
+        sh = sampler.shape(m, 1, 3, synth.V_FULL, 5, 0)
+        assert sh["grid"] == 3 * sh["split"] and sh["smem"] > 0
+    with pytest.raises(S.StrataError) as ei:
+        sampler.shape(3, 0, 8, synth.V_FULL, 20, 0)
+    assert ei.value.code == S.STRATA_EINVAL
