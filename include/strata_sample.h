@@ -122,7 +122,8 @@ extern "C" {
  * device wait (about two seconds) runs out: the call sets STRATA_DEVERR_TIMEOUT, its outputs are
  * undefined, and the context stays usable.  It exercises the failure path without a GPU fault.  */
 #define STRATA_FLAG_TEST_STALL  0x10000u
-/* Testing aid: force the number of thread blocks (1..16) that split each row; 0 = automatic.   */
+/* Testing aid: force the number of thread blocks (1..16) that split each row; 0 = automatic.  A
+ * forced split whose blocks would not fit their shared memory is STRATA_ERANGE.                */
 #define STRATA_FLAG_SPLIT(n)    (((uint32_t)(n) & 0x1Fu) << 8)
 
 /* ---- device error bits (strata_read_errors) ---------------------------------------------- */

@@ -183,15 +183,6 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
     cs = std::max({cs_bytes, std::min(cs_fill, cs_small), 1});
     cs = std::min(cs, max_cluster);
   }
-  int chunk = (V + cs - 1) / cs;
-  chunk = (chunk + 15) / 16 * 16;
-  s->cs = cs;
-  s->chunk = chunk;
-  // keys per warp: enough that the row publishes about 2 * kp of them (a tight threshold)
-  const int per_warp = (2 * kp_max + cs * strata::NW - 1) / (cs * strata::NW);
-  int qw = 1;
-  while (qw < per_warp && qw < strata::QW_MAX) qw *= 2;
-  s->qw = qw;
   s->hash_cap = 0;
   s->hash_bits = 0;
   if (mode == strata::MODE_SAMPLE && with_hist && lastn_max > 0) {
@@ -200,12 +191,26 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
     s->hash_bits = bits;
     s->hash_cap = 1 << bits;
   }
-  // the most ring slots that still leave room for three CTAs on the SM (at least 2)
   Layout L{};
-  for (int ns = (pipelined && !concurrent) ? RING_SLOTS_PIPELINED : RING_SLOTS; ns >= 2; --ns) {
-    L = strata::make_layout(chunk, s->hash_cap, cs, kmax, nmax, ns, s->qw, with_allowed, mask);
-    s->nslot = ns;
-    if (static_cast<int>(L.total) <= smem_three) break;
+  for (;;) {
+    int chunk = (V + cs - 1) / cs;
+    chunk = (chunk + 15) / 16 * 16;
+    s->cs = cs;
+    s->chunk = chunk;
+    // keys per warp: enough that the row publishes about 2 * kp of them (a tight threshold)
+    const int per_warp = (2 * kp_max + cs * strata::NW - 1) / (cs * strata::NW);
+    int qw = 1;
+    while (qw < per_warp && qw < strata::QW_MAX) qw *= 2;
+    s->qw = qw;
+    // the most ring slots that still leave room for three CTAs on the SM (at least 2)
+    for (int ns = (pipelined && !concurrent) ? RING_SLOTS_PIPELINED : RING_SLOTS; ns >= 2; --ns) {
+      L = strata::make_layout(chunk, s->hash_cap, cs, kmax, nmax, ns, s->qw, with_allowed, mask);
+      s->nslot = ns;
+      if (static_cast<int>(L.total) <= smem_three) break;
+    }
+    // a chunk whose id bitmaps do not fit the block's shared memory: split the row further
+    if (static_cast<int>(L.total) <= max_smem || forced > 0 || cs >= max_cluster) break;
+    ++cs;
   }
   if (!strata::layout_aligned(L)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
   if (L.cand_cap < cs * std::max(kmax, nmax) + 8) return fail(STRATA_EINVAL, "internal: candidate lists too small");

@@ -1,5 +1,5 @@
-"""The kernel's shared-memory layout over every launch shape (host code, CPU only): compiled from
-the kernel header with nvcc and run on the host."""
+"""The kernel's shared-memory layout over every launch shape, and the launcher's shape rule over the
+calls a GB300 context accepts (host code, CPU only): compiled with nvcc and run on the host."""
 import os
 import shutil
 import subprocess
@@ -9,15 +9,28 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_every_layout_is_aligned_and_fits(tmp_path):
+def _build_and_run(tmp_path, name):
     nvcc = shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else None)
     if nvcc is None:
         pytest.skip("nvcc not available")
-    exe = str(tmp_path / "layout_check")
-    r = subprocess.run([nvcc, "-O2", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a",
-                        "-I", os.path.join(ROOT, "include"), "-o", exe, os.path.join(ROOT, "tests", "layout_check.cu")],
-                       capture_output=True, text=True, timeout=600)
+    exe = str(tmp_path / name)
+    r = subprocess.run([nvcc, "-O1", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a",
+                        "-I", os.path.join(ROOT, "include"), "-o", exe, os.path.join(ROOT, "tests", name + ".cu")],
+                       capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-2000:]
     r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:]
     assert " 0 bad" in r.stdout
+    return r.stdout
+
+
+def test_every_layout_is_aligned_and_fits(tmp_path):
+    _build_and_run(tmp_path, "layout_check")
+
+
+def test_every_accepted_call_gets_a_shape_that_fits(tmp_path):
+    """Every automatic shape fits; a forced split that cannot fit is refused with STRATA_ERANGE.
+    (A bf16 row of 524,288 ids with a mask and a 4,096-id window under the concurrency hint is a
+    shape whose one-block split does not fit: the rule splits such a row further.)"""
+    out = _build_and_run(tmp_path, "shape_check")
+    assert "shapes" in out
