@@ -100,10 +100,12 @@ extern "C" {
  * the next call on the stream may launch, so counters still advance in call order (each sampled
  * slot by one per call, every row of a slot seeing the value from before the call), and it writes
  * its outputs when they are ready.  Results are the same as without the flag.  A sampling call
- * without the flag takes its counters only after it has waited for its predecessor, so once the
- * context has launched such a call with STRATA_FLAG_PDL, its flagged calls take their counters
- * that way too (and wait like unflagged calls) until it launches a call without STRATA_FLAG_PDL
- * or strata_read_errors drains the stream.  The next call's
+ * without the flag takes its counters late (after waiting for its predecessor, or during its
+ * run), so once the context has launched such a call, its later calls (sampling or logprobs)
+ * ignore this flag and wait as usual, until a call without STRATA_FLAG_PDL that takes no late
+ * counters, or strata_read_errors, has drained the stream.  Keep a stream that carries flagged
+ * calls to one context: another context's flagged call would break the chain of waits that this
+ * context's waiting calls rely on.  The next call's
  * launch then waits for this call's counter atomics (a few memory round trips at its start), so
  * one stream of calls alone can run slower with the flag; it pays when independent request groups
  * (other contexts, other streams) keep the GPU busy meanwhile (see STRATA_FLAG_CONCURRENT).     */

@@ -151,6 +151,22 @@ int smem_for_three(const cudaDeviceProp& prop) {
   return std::min(static_cast<int>(prop.sharedMemPerBlockOptin), per_sm / 3 - reserved - SMEM_L1_MARGIN) & ~127;
 }
 
+// Counter order under STRATA_FLAG_OWN_OUTPUTS.  A call that takes its counters after waiting for
+// its predecessor relies on the chain of waits before it: the predecessor ended, and it had waited
+// for its own predecessor, and so on.  A launch with own outputs waits for nothing and breaks that
+// chain, so while a launch that takes its counters late may still be running (`pending`), every
+// launch of the context (sampling or logprobs) drops the own-outputs bit and waits as usual.
+uint32_t launch_flags(uint32_t flags, bool pending) { return pending ? flags & ~STRATA_FLAG_OWN_OUTPUTS : flags; }
+// The pending state after a launch with `flags` (as launched; `sampling`: it takes counters).  A
+// sampling launch that takes its counters late leaves them pending, PDL or not: the kernel lets
+// the next launch start at its entry.  Otherwise a launch without PDL started after all earlier
+// work had ended, and one with PDL leaves the state as it was.
+bool pending_after(bool pending, uint32_t flags, bool sampling) {
+  const bool early_counters = (flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u;
+  if (sampling && !early_counters) return true;
+  return (flags & STRATA_FLAG_PDL) != 0u && pending;
+}
+
 struct Shape {
   int cs, chunk, smem, kmax, nmax, hash_cap, hash_bits, nslot, qw;
 };
@@ -687,7 +703,7 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   P.hash_bits = sh.hash_bits;
   P.nslot = sh.nslot;
   P.qw = sh.qw;
-  if ((flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && c->late_counters_pending) flags &= ~STRATA_FLAG_OWN_OUTPUTS;
+  flags = launch_flags(flags, c->late_counters_pending);
   P.flags = flags;
   P.row_draft = row_draft;
   P.slot_keep = slot_keep;
@@ -696,11 +712,7 @@ static int sample_rows_impl(strata_ctx* c, const void* logits, int dtype, int B,
   P.hlen = kept_hist ? c->d_hlen : nullptr;
   rc = launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream),
               row_draft != nullptr ? "sample_verify" : "sample_rows");
-  if (rc == STRATA_OK) {
-    const bool pdl = (flags & STRATA_FLAG_PDL) != 0u;
-    const bool early_counters = (flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u;
-    c->late_counters_pending = pdl && (c->late_counters_pending || !early_counters);
-  }
+  if (rc == STRATA_OK) c->late_counters_pending = pending_after(c->late_counters_pending, flags, true);
   return rc;
 }
 
@@ -766,9 +778,10 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
   P.err = c->d_err;
   P.nslot = sh.nslot;
   P.qw = sh.qw;
+  flags = launch_flags(flags, c->late_counters_pending);
   P.flags = flags;
   rc = launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream), "logprobs_rows");
-  if (rc == STRATA_OK && (flags & STRATA_FLAG_PDL) == 0u) c->late_counters_pending = false;  // all earlier work done
+  if (rc == STRATA_OK) c->late_counters_pending = pending_after(c->late_counters_pending, flags, false);
   return rc;
 }
 

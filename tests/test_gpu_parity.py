@@ -90,6 +90,7 @@ def test_config4_logprobs_entry_pipelined_own_outputs(sampler, concurrent):
     from request_token_sampling_gb300 import (STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_OWN_OUTPUTS,
                                               STRATA_FLAG_PDL)
     base = synth.config4(fused=False)
+    sampler.errors()  # drained: an earlier late-counter call would make these wait as usual
     fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS
     if concurrent:
         fl |= STRATA_FLAG_CONCURRENT

@@ -1,5 +1,7 @@
-"""The kernel's shared-memory layout over every launch shape, and the launcher's shape rule over the
-calls a GB300 context accepts (host code, CPU only): compiled with nvcc and run on the host."""
+"""Host rules checked on the CPU (compiled with nvcc, run on the host, no GPU): the kernel's
+shared-memory layout over every launch shape, the launcher's shape rule over the calls a GB300
+context accepts, and the rule that keeps draw counters in call order across calls with and
+without own outputs."""
 import os
 import shutil
 import subprocess
@@ -34,3 +36,12 @@ def test_every_accepted_call_gets_a_shape_that_fits(tmp_path):
     shape whose one-block split does not fit: the rule splits such a row further.)"""
     out = _build_and_run(tmp_path, "shape_check")
     assert "shapes" in out
+
+
+def test_counters_stay_in_call_order_across_launch_kinds(tmp_path):
+    """Random streams of sampling and logprobs launches (PDL or not, early loads or not, own outputs
+    or not) through the library's flag rule and an event model of programmatic dependent launch:
+    every sampling call takes its counters after the one before it, and calls with own outputs
+    still take theirs early when nothing before them takes counters late."""
+    out = _build_and_run(tmp_path, "order_check")
+    assert "took counters early" in out
