@@ -49,6 +49,12 @@ MUTATIONS = [
     ("sampling.py", "        if t >= 0:\n            new.setdefault(s, []).append(t)", "        new.setdefault(s, []).append(t)"),
     ("sampling.py", "new.setdefault(s, []).append(t)", "new.setdefault(s, []).insert(len(state.get(s, [])), t)"),
     ("sampling.py", "np.asarray(h[len(h) - m:], dtype=np.int32)", "np.asarray(h[:m], dtype=np.int32)"),
+    ("sampling.py", "astype(np.uint32) << 16).view(np.float32)", "astype(np.uint32) << 15).view(np.float32)"),
+    ("sampling.py", "(np.asarray(row, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)",
+     "np.asarray(row, dtype=np.uint16).view(np.float16).astype(np.float32)"),
+    ("sampling.py", "if not (0 <= p.top_k <= MAX_TOP_K):", "if not (1 <= p.top_k <= MAX_TOP_K):"),
+    ("sampling.py", "if not (np.float32(p.penalty_repeat) > 0):", "if not (np.float32(p.penalty_repeat) >= 0):"),
+    ("sampling.py", "    if np.float32(p.min_p) < 0:\n        return False\n", ""),
 ]
 
 

@@ -169,6 +169,48 @@ def test_rank_order_vs_argmax_rounds(seed):
     assert oracle.rank_order(vals)[:k].tolist() == _argmax_rounds([float(v) for v in vals], k)
 
 
+# ----------------------------------------------------------------------------- widening
+def test_widen_bf16_bit_patterns():
+    """bf16 is the high half of an IEEE binary32: fixed bit patterns widen to known values."""
+    bits = np.array([0x3F80, 0xC000, 0x8000, 0x0000, 0x7F80, 0xFF80, 0x0001, 0x4049, 0x3E80, 0xBF00,
+                     0x0080, 0x7F7F], dtype=np.uint16)
+    got = oracle.widen(bits, "bf16")
+    assert got.dtype == np.float32
+    want = [1.0, -2.0, -0.0, 0.0, math.inf, -math.inf, 2.0 ** -133, 3.140625, 0.25, -0.5, 2.0 ** -126,
+            (2.0 - 2.0 ** -7) * 2.0 ** 127]
+    assert [float(x) for x in got] == want
+    assert math.copysign(1.0, float(got[2])) == -1.0 and math.copysign(1.0, float(got[3])) == 1.0
+    # every pattern's low 16 fp32 bits are zero and the high 16 are the pattern itself
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    u = oracle.widen(allb, "bf16").view(np.uint32)
+    assert np.array_equal(u >> 16, allb.astype(np.uint32)) and not np.any(u & 0xFFFF)
+
+
+def test_widen_f32_is_the_row_itself():
+    x = np.array([1.5, -0.0, np.inf, -3.25e-39], dtype=np.float32)
+    assert oracle.widen(x, "f32").view(np.uint32).tolist() == x.view(np.uint32).tolist()
+
+
+# ----------------------------------------------------------------------------- key validity
+@pytest.mark.filterwarnings("ignore:overflow encountered in cast")
+def test_params_valid_rules():
+    """Keys the engine refuses rather than adjusts ("#19 ...", "server.py forwards the block"):
+    top_k outside 0..64 (0 means 20; the sampled path needs 1..64), a repeat penalty that is not
+    positive (the positive branch divides by it), a negative min_p, a negative window, any
+    non-finite float.  Everything else is honoured (min_p above 1 keeps the head, top_p <= 0 keeps
+    the head, top_p >= 1 disables the cut)."""
+    ok = oracle.params_valid
+    assert ok(Params())
+    assert ok(Params(temperature=0.7, top_k=64, top_p=0.0, min_p=3.0, penalty_repeat=0.5,
+                     penalty_freq=-1.0, penalty_present=-2.0, penalty_last_n=0))
+    assert ok(Params(top_k=0)) and ok(Params(top_k=1)) and ok(Params(top_p=-1.0)) and ok(Params(temperature=-1.0))
+    for bad in (dict(top_k=65), dict(top_k=-1), dict(penalty_repeat=0.0), dict(penalty_repeat=-1.0),
+                dict(min_p=-0.01), dict(penalty_last_n=-1), dict(temperature=math.nan), dict(top_p=math.inf),
+                dict(min_p=math.nan), dict(penalty_freq=-math.inf), dict(penalty_present=math.nan),
+                dict(penalty_repeat=math.inf), dict(temperature=1e39)):
+        assert not ok(Params(**bad)), bad
+
+
 def test_rank_order_special_values():
     v = np.array([np.nan, -np.inf, 1.0, -0.0, 0.0, np.inf, 1.0], dtype=f32)
     assert oracle.rank_order(v).tolist() == [5, 2, 6, 3, 4, 1, 0]
