@@ -67,6 +67,16 @@ def gpu_logprobs(sampler, w, d=None, top_n=None, flags=0):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
+# Parity counts per workload, gathered by the GPU tests and printed in pytest's terminal summary
+# (and written as JSON to the file named by STRATA_PARITY_REPORT, when set).
+REPORT = {}
+
+
+def report(name, stats):
+    """Record one workload's parity counts for the end-of-session summary."""
+    REPORT[name] = stats.as_dict()
+
+
 class Stats:
     def __init__(self):
         self.rows = 0
@@ -87,9 +97,44 @@ class Stats:
             self.max_dlp = max(self.max_dlp, float(d.max()))
         return d
 
+    def as_dict(self):
+        return {"rows": self.rows, "flagged": self.flagged, "flagged_and_different": self.flag_differs,
+                "max_dlp": self.max_dlp}
+
     def __repr__(self):
         return (f"rows={self.rows} flagged={self.flagged} flagged_and_different={self.flag_differs} "
                 f"max|dlp|={self.max_dlp:.3g}")
+
+
+def check_flagged_pick(w, b, r, gid, m2g=None):
+    """A row the oracle flags may differ from it only across the flagged boundary.
+
+    Its top_k sequence and min_p count match exactly (checked by the caller).  The GPU's top_p
+    count m2g must be one the cut gives for some top_p within 1e-6 of the key (the oracle's own
+    count when the cut is not flagged).  Given that count, the pick must be one the oracle's draw
+    (in double) makes for some uniform within 1e-6 of the row's: the oracle's own pick, or the
+    survivor on the other side of the flagged boundary.  Without the debug outputs every count the
+    cut allows is tried."""
+    eps = oracle.BOUNDARY_EPS
+    ids = r["topk_ids"].tolist()
+    assert gid in ids, f"row {b}: flagged pick {gid} is not among the top_k survivors"
+    jg = ids.index(gid)
+    p = w["slot_params"][int(w["row_slot"][b])]
+    sel, m1 = r["topk_vals"], r["m1"]
+    if r["flag_top_p"]:
+        lo = oracle.top_p_cut(sel, m1, p["top_p"] - eps)[0]
+        hi = oracle.top_p_cut(sel, m1, p["top_p"] + eps)[0]
+    else:
+        lo = hi = r["m2"]
+    if m2g is not None:
+        assert lo <= m2g <= hi, f"row {b}: top_p survivors {m2g}, the cut allows {lo}..{hi}"
+        lo = hi = m2g
+    ok = False
+    for m2 in range(lo, hi + 1):
+        j_lo = oracle.draw_index(sel, m2, p["temperature"], max(0.0, r["u"] - eps))[0]
+        j_hi = oracle.draw_index(sel, m2, p["temperature"], min(1.0 - 2.0 ** -24, r["u"] + eps))[0]
+        ok = ok or j_lo <= jg <= j_hi
+    assert ok, f"row {b}: flagged pick index {jg} is not the draw's decision (oracle {r['j']}, m2 {lo}..{hi})"
 
 
 def compare_sample(w, rows, g, top_n=None, stats=None, debug=True):
@@ -115,7 +160,8 @@ def compare_sample(w, rows, g, top_n=None, stats=None, debug=True):
         flagged = r["flag_top_p"] or r["flag_draw"]
         if flagged:
             stats.flagged += 1
-            assert gid in r["topk_ids"].tolist()
+            m2g = int(g["kept"][b, 1]) if debug else None
+            check_flagged_pick(w, b, r, gid, m2g)
             if gid != r["id"]:
                 stats.flag_differs += 1
         else:

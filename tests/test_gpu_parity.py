@@ -11,7 +11,7 @@ import pytest
 import oracle
 import synth
 
-from _harness import Stats, compare_logprobs, compare_sample, gpu_logprobs, gpu_sample, set_slots, upload
+from _harness import Stats, compare_logprobs, compare_sample, gpu_logprobs, gpu_sample, report, set_slots, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,7 @@ def test_config1_single_row(sampler):
     st = compare_sample(w, rows, g)
     _check_no_errors(sampler)
     assert sampler.slot_state(0)[1] == ctr[0] == 1
-    print("config1", st)
+    report("config1", st)
 
 
 def test_config2_verify_windows_counter_persists(sampler):
@@ -57,7 +57,7 @@ def test_config2_verify_windows_counter_persists(sampler):
         compare_sample(w, rows, g, top_n=0, stats=st)
     _check_no_errors(sampler)
     assert sampler.slot_state(0)[1] == counters[0] == synth.CONFIG2_WINDOWS
-    print("config2", st)
+    report("config2", st)
 
 
 @pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
@@ -71,7 +71,7 @@ def test_config3_batch_slots_bf16(sampler, concurrent):
     _check_no_errors(sampler)
     for s in range(8):
         assert sampler.slot_state(s)[1] == ctr[s]
-    print("config3", st)
+    report("config3", st)
 
 
 def test_config4_logprobs_entry(sampler):
@@ -80,7 +80,7 @@ def test_config4_logprobs_entry(sampler):
     ref = oracle.logprobs_call(w)
     st = compare_logprobs(w, ref, g)
     _check_no_errors(sampler)
-    print("config4 logprobs", st)
+    report("config4 logprobs", st)
 
 
 @pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
@@ -115,7 +115,7 @@ def test_config4_fused_sample_and_logprobs(sampler):
     rows, _ = oracle.sample_call(w)
     st = compare_sample(w, rows, g)
     _check_no_errors(sampler)
-    print("config4 fused", st)
+    report("config4 fused", st)
 
 
 @pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
@@ -131,7 +131,7 @@ def test_config5_stress_bf16_ties(sampler, concurrent):
     _check_no_errors(sampler)
     for s in range(8):
         assert sampler.slot_state(s)[1] == ctr[s] == 1
-    print("config5", st)
+    report("config5", st)
 
 
 @pytest.mark.parametrize("seed", range(24))
@@ -191,7 +191,7 @@ def test_config4_pipelined_calls(sampler):
     for s in base["slot_params"]:
         assert sampler.slot_state(s)[1] == counters[s]
     _check_no_errors(sampler)
-    print("config4 pipelined", st)
+    report("config4 pipelined", st)
 
 
 @pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
@@ -224,7 +224,7 @@ def test_config4_pipelined_own_outputs(sampler, concurrent):
     for s in base["slot_params"]:
         assert sampler.slot_state(s)[1] == counters[s]
     _check_no_errors(sampler)
-    print("config4 own outputs", st)
+    report("config4 own outputs", st)
 
 
 def test_config5_pipelined_own_outputs_rows_share_slots(sampler):
@@ -253,7 +253,7 @@ def test_config5_pipelined_own_outputs_rows_share_slots(sampler):
     for s in range(8):
         assert sampler.slot_state(s)[1] == counters[s] == 3
     _check_no_errors(sampler)
-    print("config5 own outputs", st)
+    report("config5 own outputs", st)
 
 
 def test_config4_concurrent_groups():
@@ -294,7 +294,7 @@ def test_config4_concurrent_groups():
             for s in base["slot_params"]:
                 assert g.slot_state(s)[1] == ctr[s]
             _check_no_errors(g)
-        print("config4 concurrent groups", st)
+        report("config4 concurrent groups", st)
     finally:
         for g in groups:
             g.close()
