@@ -10,5 +10,5 @@ from .sampling import (  # noqa: F401
     Params, params_valid, widen, history_counts, apply_penalties, rank_order, min_p_cut, top_p_cut,
     draw_index, log_softmax, allowed_renorm, sample_row, logprobs_row, sample_call, logprobs_call,
     c_logf, BOUNDARY_EPS, accept_window, verify_call, history_call, history_append, history_tail,
-    HISTORY_RING_CAP,
+    HISTORY_RING_CAP, shard_record, merge_records,
 )

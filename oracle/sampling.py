@@ -483,3 +483,71 @@ def history_tail(state, slot, max_n=HISTORY_RING_CAP):
     h = list(state.get(slot, []))
     m = min(len(h), HISTORY_RING_CAP, max(0, int(max_n)))
     return np.asarray(h[len(h) - m:], dtype=np.int32), len(h)
+
+
+# -------------------------------------------------------------------------------------------
+# Vocabulary shards: a row's vocabulary split into slices (devices or buffers), each reporting a
+# record, the records merged into the row's result
+# -------------------------------------------------------------------------------------------
+
+def shard_record(raw32_shard, v0: int, p: Params, hist_ids, k: int, top_n: int) -> dict:
+    """What one slice of a row (ids v0 .. v0 + len - 1) reports for the merge.
+
+    The row's top_k list and top_n raw alternatives are each among the union of its slices' own
+    lists, so a slice reports its k best penalised entries (value, id, raw logit), its top_n raw
+    entries (value, id) and the log-sum-exp of its raw logits ("#19 ...": penalties over the
+    history window, then top_k; "#3200 ...", "Approach": log-probabilities of the raw logits).
+    History ids are the row's own (global) ids; a slice counts those that fall inside it.
+    """
+    raw = np.asarray(raw32_shard, dtype=np.float32)
+    n = raw.size
+    counts = {}
+    if not (penalties_neutral(p) or p.penalty_last_n <= 0 or hist_ids is None):
+        for t, c in history_counts(hist_ids, p.penalty_last_n, v0 + n).items():
+            if t >= v0:
+                counts[t - v0] = c
+    pen = apply_penalties(raw, counts, p.penalty_repeat, p.penalty_freq, p.penalty_present)
+    op = rank_order(pen)[:k]
+    orr = rank_order(raw)[:top_n]
+    l = raw.astype(np.float64)
+    m = np.max(l) if n else -np.inf
+    lse = float(m + np.log(np.sum(np.exp(l - m)))) if n and np.isfinite(m) else float("-inf")
+    return dict(pen=[(float(pen[i]), v0 + int(i), float(raw[i])) for i in op],
+                raw=[(float(raw[i]), v0 + int(i)) for i in orr], lse=lse)
+
+
+def merge_records(records, p: Params, position: int, counter: int, top_n: int) -> dict:
+    """A row's result from its slices' records: the same chain as sample_row and logprobs_row.
+
+    The penalised entries of all slices, ordered by value descending with ties to the lowest id,
+    give the top_k list; min_p, top_p, temperature and the Philox draw follow on it; the row's
+    log-sum-exp is the log of the summed exponentials of the slices' log-sum-exps.
+    """
+    pen = sorted((e for r in records for e in r["pen"]), key=lambda e: (-e[0], e[1]))
+    raw = sorted((e for r in records for e in r["raw"]), key=lambda e: (-e[0], e[1]))
+    lses = np.array([r["lse"] for r in records], dtype=np.float64)
+    mx = np.max(lses)
+    lse = float(mx + np.log(np.sum(np.exp(lses - mx)))) if np.isfinite(mx) else float("-inf")
+    res = dict(greedy=p.greedy, flag_top_p=False, flag_draw=False, u=None)
+    k = 1 if p.greedy else min(p.k, len(pen))
+    sel = pen[:k]
+    sel_vals = np.array([e[0] for e in sel], dtype=np.float32)
+    sel_ids = np.array([e[1] for e in sel], dtype=np.int64)
+    if p.greedy:
+        j, m1, m2 = 0, 1, 1
+    else:
+        m1 = min_p_cut(sel_vals, p.min_p)
+        m2, f_tp = top_p_cut(sel_vals, m1, p.top_p)
+        u = row_uniform(p.seed, position, counter)
+        j, f_dr = draw_index(sel_vals, m2, p.temperature, u)
+        res.update(u=u, flag_top_p=f_tp, flag_draw=f_dr)
+    res.update(id=int(sel_ids[j]), topk_ids=sel_ids, topk_vals=sel_vals, m1=m1, m2=m2, j=j,
+               chosen_lp=float(np.float64(sel[j][2]) - lse))
+    top = raw[:top_n]
+    ids = np.full(top_n, -1, dtype=np.int64)
+    lps = np.full(top_n, -np.inf)
+    for i, (v, t) in enumerate(top):
+        ids[i] = t
+        lps[i] = float(np.float64(v) - lse)
+    res.update(top_ids=ids, top_lps=lps, lse=lse)
+    return res

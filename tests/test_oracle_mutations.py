@@ -55,6 +55,10 @@ MUTATIONS = [
     ("sampling.py", "if not (0 <= p.top_k <= MAX_TOP_K):", "if not (1 <= p.top_k <= MAX_TOP_K):"),
     ("sampling.py", "if not (np.float32(p.penalty_repeat) > 0):", "if not (np.float32(p.penalty_repeat) >= 0):"),
     ("sampling.py", "    if np.float32(p.min_p) < 0:\n        return False\n", ""),
+    ("sampling.py", "lse = float(mx + np.log(np.sum(np.exp(lses - mx))))", "lse = float(mx)"),
+    ("sampling.py", "pen = sorted((e for r in records for e in r[\"pen\"]), key=lambda e: (-e[0], e[1]))",
+     "pen = sorted((e for r in records for e in r[\"pen\"]), key=lambda e: (-e[0], -e[1]))"),
+    ("sampling.py", "            if t >= v0:\n                counts[t - v0] = c", "            if t >= v0:\n                counts[t - v0] = 1"),
 ]
 
 

@@ -728,3 +728,46 @@ def test_history_tail_capacity():
     assert oracle.history_tail(st, 1)[0].tolist() == [3, 4]
     assert oracle.history_tail(st, 5)[0].size == 0 and oracle.history_tail(st, 5)[1] == 0
     assert oracle.history_tail(st, 1, 0)[0].size == 0
+
+
+# ----------------------------------------------------------------------------- vocabulary shards
+@pytest.mark.parametrize("seed", range(12))
+def test_shard_records_merge_to_the_full_row(seed):
+    """Splitting a row's vocabulary into slices, reporting each slice's record and merging them
+    gives the full row's chain exactly: the same top_k list, cuts and pick, the same top_n
+    alternatives and log-probabilities (to rounding of the log-sum-exp).  Ties straddle the cuts
+    (values on a coarse grid) and history ids fall in every slice."""
+    rng = np.random.default_rng(900 + seed)
+    V = int(rng.integers(40, 400))
+    raw = (np.round(rng.standard_normal(V) * 4) / 2).astype(f32)
+    G = int(rng.integers(1, 5))
+    cuts = np.sort(rng.choice(np.arange(1, V), size=G - 1, replace=False)).tolist()
+    bounds = [0] + cuts + [V]
+    hot = rng.integers(0, V, size=8)  # a few ids repeated, so counts above one matter
+    hist = np.concatenate([rng.integers(0, V, size=int(rng.integers(0, 20))), rng.choice(hot, size=20)])
+    p = Params(temperature=float(rng.choice([0.0, 0.7, 1.3])), top_k=int(rng.integers(0, 65)),
+               top_p=float(rng.choice([1.0, 0.8])), min_p=float(rng.choice([0.0, 0.1])), penalty_repeat=1.5,
+               penalty_freq=0.3, penalty_present=0.2, penalty_last_n=32, seed=int(rng.integers(0, 2**40)))
+    k = 1 if p.greedy else p.k
+    recs = [oracle.shard_record(raw[bounds[i]:bounds[i + 1]], bounds[i], p, hist, k, 7) for i in range(G)]
+    m = oracle.merge_records(recs, p, 77, 5, 7)
+    r = oracle.sample_row(raw, p, hist, 77, 5)
+    lr = oracle.logprobs_row(raw, r["id"], 7)
+    assert m["topk_ids"].tolist() == r["topk_ids"].tolist()
+    assert m["m1"] == r["m1"] and m["m2"] == r["m2"] and m["id"] == r["id"]
+    assert m["top_ids"].tolist() == lr["top_ids"].tolist()
+    fin = np.isfinite(lr["top_lps"])
+    assert np.max(np.abs(m["top_lps"][fin] - lr["top_lps"][fin]), initial=0.0) < 1e-12
+    assert abs(m["chosen_lp"] - lr["chosen_lp"]) < 1e-12
+
+
+def test_shard_record_hand_case():
+    """Two slices of [3, 1, 4, 1 | 5, 9, 2, 6]: the second slice's best raw entries are 9 (id 5)
+    and 6 (id 7); with repeat 2 over a history naming id 5 twice, its penalised 9 becomes 4.5, so
+    the slice's best penalised entries are 6 (id 7) and 5 (id 4)."""
+    raw = np.array([3, 1, 4, 1, 5, 9, 2, 6], dtype=f32)
+    p = Params(temperature=1.0, top_k=2, penalty_repeat=2.0, penalty_last_n=8)
+    r1 = oracle.shard_record(raw[4:], 4, p, [5, 5, 1], 2, 2)
+    assert [(v, t) for v, t, _ in r1["pen"]] == [(6.0, 7), (5.0, 4)]
+    assert r1["raw"] == [(9.0, 5), (6.0, 7)]
+    assert abs(r1["lse"] - math.log(math.exp(5) + math.exp(9) + math.exp(2) + math.exp(6))) < 1e-12
