@@ -120,6 +120,13 @@ extern "C" {
  * the flag.  A forced split (STRATA_FLAG_SPLIT) takes precedence.                                */
 #define STRATA_FLAG_CONCURRENT  0x10u
 #define STRATA_CONCURRENT_ROW_BYTES (1u << 20)
+/* A launch-shape choice: hold each block's chunk whole in shared memory (at most 64 KiB of logits:
+ * up to 16 blocks per row) instead of streaming it through a ring of shared-memory slots, with a
+ * row threshold exchanged across the row's blocks and candidates read from shared memory.  A row
+ * too large for 16 such blocks streams as usual.  Results are the same either way.  Measured on
+ * GB300 slower than streaming for every workload (the post-pass dominates a block's life), so it
+ * is off by default.                                                                           */
+#define STRATA_FLAG_RESIDENT    0x40u
 /* Testing aid: the row leaders also wait for one arrival that nothing sends, so that their bounded
  * device wait (about two seconds) runs out: the call sets STRATA_DEVERR_TIMEOUT, its outputs are
  * undefined, and the context stays usable.  It exercises the failure path without a GPU fault.  */
@@ -352,14 +359,18 @@ int strata_launch_shape(strata_ctx *ctx, int mode, int dtype, int B, int V, int 
  * ([B+1] offsets; NULL = no history).  Outputs as in strata_sample_rows (no allowed subsets, no
  * debug outputs).  B is at most STRATA_NOALLOC_MAX_ROWS; more rows is STRATA_ERANGE.
  *
- * Memory: nothing is allocated, on the device or the host heap.  The per-row key records, counter
- * words, the row-to-slot table and the device error word live in one static device array of about
- * 60 KiB that every GPU loading this library holds until the process exits.  Every call shares
- * that array and it keeps the last call's contents; each call rewrites (and zeroes) what it reads,
- * but calls that overlap on the GPU race, so issue them on one stream.  Device error bits of these
- * calls are not reported.  The first call on each device sets that device up synchronously (finds
- * the array's device address, sets kernel attributes, uploads the row table); make that first call
- * before capturing any stream.
+ * Memory: nothing is allocated on the device.  The per-row key records, counter words, the
+ * row-to-slot table and the device error word live in one static device array of about 60 KiB
+ * that every GPU loading this library holds until the process exits.  Every call shares that
+ * array and it keeps the last call's contents; each call rewrites (and zeroes) what it reads, but
+ * calls that overlap on the GPU race, so issue them on one stream.  Device error bits of these
+ * calls are not reported.  On the host, each call prepares the keys and counters in one static
+ * buffer of the library and copies them to the device array with cudaMemcpyAsync on `stream`;
+ * host threads take turns on that buffer (a lock), and a copy from such pageable memory returns
+ * once the CUDA runtime holds the bytes, which can mean waiting for work already queued on the
+ * stream.  The first call on each device sets that device up synchronously (finds the array's
+ * device address, sets kernel attributes, uploads the row table); make that first call before
+ * capturing any stream.
  */
 #define STRATA_NOALLOC_MAX_ROWS 1024
 int strata_sample_rows_noalloc(const void *logits, int dtype, int B, int V, int64_t ld,

@@ -38,6 +38,7 @@ STRATA_FLAG_ALLOWED_MASK = 0x4
 STRATA_FLAG_HISTORY_RING = 0x8
 STRATA_FLAG_CONCURRENT = 0x10
 STRATA_FLAG_OWN_OUTPUTS = 0x20
+STRATA_FLAG_RESIDENT = 0x40
 STRATA_CONCURRENT_ROW_BYTES = 1 << 20
 STRATA_FLAG_TEST_STALL = 0x10000
 

@@ -256,40 +256,6 @@ __device__ __forceinline__ MaxSum warp_ms_fast(MaxSum x) {
   return {M, s};
 }
 
-// Bitonic sort, descending, of 32*PER 64-bit keys held by one warp: element i = lane*PER + r.
-// Partners closer than PER sit in the same lane; farther ones are exchanged with xor shuffles.
-template <int PER>
-__device__ __forceinline__ void warp_sort_desc(uint64_t (&k)[PER], int lane) {
-#pragma unroll
-  for (int size = 2; size <= 32 * PER; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride < PER) {
-#pragma unroll
-        for (int r = 0; r < PER; ++r) {
-          const int r2 = r ^ stride;
-          if (r2 > r) {
-            const bool desc = ((lane * PER + r) & size) == 0;
-            const uint64_t a = k[r], b = k[r2];
-            const bool sw = desc ? (a < b) : (a > b);
-            k[r] = sw ? b : a;
-            k[r2] = sw ? a : b;
-          }
-        }
-      } else {
-        const int lm = stride / PER;
-#pragma unroll
-        for (int r = 0; r < PER; ++r) {
-          const uint64_t o = __shfl_xor_sync(FULL_MASK, k[r], lm);
-          const int i = lane * PER + r;
-          const bool keep_max = (((i & size) == 0) == ((i & stride) == 0));
-          k[r] = keep_max ? (o > k[r] ? o : k[r]) : (o < k[r] ? o : k[r]);
-        }
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------------------------------ double-word fp32
 // A value carried as an unevaluated sum hi + lo of two floats, added with Knuth's TwoSum (an
 // error-free transformation), so a prefix sum of <= 64 terms keeps ~44 significant bits without

@@ -50,7 +50,7 @@ constexpr int MAX_SLOTS = 8;                 // ring slots: pieces in flight per
 constexpr int MAX_CS = 16;                   // CTAs per row (non-portable cluster size)
 constexpr int KMAX = STRATA_MAX_TOP_K;
 constexpr int NMAX = STRATA_MAX_TOP_N;
-constexpr int QW_MAX = 8;                    // thread maxima a warp publishes, at most
+constexpr int QW_MAX = 16;                   // thread maxima a warp publishes, at most
 constexpr int RANK_LIMIT = 256;              // candidates ranked by counting; beyond: argmax rounds
 constexpr int HASH_CNT_BITS = 13;            // history table entry = (local id << 13) | count
 constexpr uint32_t HASH_EMPTY = 0xFFFFFFFFu;
@@ -60,7 +60,6 @@ constexpr uint32_t SLOT_SAMPLED = 1u;
 constexpr uint32_t SLOT_PENAL = 2u;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // bounded waits: ~2 s at GB300 clocks
 constexpr float LAZY_SHIFT = 16.0f;          // the exp reference moves only when the max passes it by this
-constexpr int XKEYS = NW * QW_MAX;           // published keys per CTA, at most
 // A CTA's record: its NW * qw keys, then 2 (max, sum) pairs; records sit NW * qw + 4 words apart
 // (a multiple of 16 bytes, since NW * qw is a multiple of 8).
 __host__ __device__ inline int xrec_words(int qw) { return NW * qw + 4; }
@@ -1551,7 +1550,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         // Prefix sums in fp32 decide unless a decision lies within 1e-5 of its boundary (the fp32
         // scan is good to ~4e-7 relative); then double-word sums (TwoSum) decide.
         const bool ina = lane < m1, inb = lane + 32 < m1;
-        const float da = __fsub_rn(va, v0), db = __fsub_rn(vb, v0);
+        // lanes outside the survivors divide a plain zero (a NaN or an infinity would take the
+        // division's slow path)
+        const float da = ina ? __fsub_rn(va, v0) : 0.0f, db = inb ? __fsub_rn(vb, v0) : 0.0f;
         const float Tm = sp.temperature;
         const float qa = ina ? expf(da) : 0.0f, qb = inb ? expf(db) : 0.0f;
         wa = ina ? expf(__fdiv_rn(da, Tm)) : 0.0f;

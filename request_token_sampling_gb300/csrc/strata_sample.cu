@@ -21,6 +21,7 @@
 
 #include "../../include/strata_sample.h"
 #include "strata_kernel.cuh"
+#include "strata_resident.cuh"
 
 using strata::KParams;
 using strata::Layout;
@@ -38,15 +39,33 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
-// The kernel instance for a launch: logit type x allowed-id mask x own outputs.
+// The kernel instance for a launch: streaming or resident chunk x logit type x allowed-id mask x
+// own outputs.
 using KernelFn = void (*)(strata::KParams);
-KernelFn kernel_for(int dtype, bool mask, bool own) {
-  static const KernelFn table[2][2][2] = {
-      {{strata::rows_kernel<0, false, false>, strata::rows_kernel<0, false, true>},
-       {strata::rows_kernel<0, true, false>, strata::rows_kernel<0, true, true>}},
-      {{strata::rows_kernel<1, false, false>, strata::rows_kernel<1, false, true>},
-       {strata::rows_kernel<1, true, false>, strata::rows_kernel<1, true, true>}}};
-  return table[dtype == STRATA_DTYPE_F32 ? 0 : 1][mask ? 1 : 0][own ? 1 : 0];
+KernelFn kernel_for(int dtype, bool mask, bool own, bool resident = false) {
+  static const KernelFn table[2][2][2][2] = {
+      {{{strata::rows_kernel<0, false, false>, strata::rows_kernel<0, false, true>},
+        {strata::rows_kernel<0, true, false>, strata::rows_kernel<0, true, true>}},
+       {{strata::rows_kernel<1, false, false>, strata::rows_kernel<1, false, true>},
+        {strata::rows_kernel<1, true, false>, strata::rows_kernel<1, true, true>}}},
+      {{{strata::res_kernel<0, false, false>, strata::res_kernel<0, false, true>},
+        {strata::res_kernel<0, true, false>, strata::res_kernel<0, true, true>}},
+       {{strata::res_kernel<1, false, false>, strata::res_kernel<1, false, true>},
+        {strata::res_kernel<1, true, false>, strata::res_kernel<1, true, true>}}}};
+  return table[resident ? 1 : 0][dtype == STRATA_DTYPE_F32 ? 0 : 1][mask ? 1 : 0][own ? 1 : 0];
+}
+
+// Both kernels' instances may use up to `max_smem` of dynamic shared memory and non-portable
+// cluster sizes (up to 16 blocks per row).
+cudaError_t set_kernel_attributes(int max_smem) {
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 16 && e == cudaSuccess; ++i) {
+    const void* k = reinterpret_cast<const void*>(
+        kernel_for(i & 1 ? STRATA_DTYPE_BF16 : STRATA_DTYPE_F32, (i >> 1) & 1, (i >> 2) & 1, (i >> 3) & 1));
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem)) == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
+  return e;
 }
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -169,14 +188,23 @@ bool pending_after(bool pending, uint32_t flags, bool sampling) {
 
 struct Shape {
   int cs, chunk, smem, kmax, nmax, hash_cap, hash_bits, nslot, qw;
+  bool resident;  // the chunk is held whole in shared memory (res_kernel); else it streams
 };
+
+// Keys each warp of a resident block publishes for the row's threshold: enough that the row's
+// blocks together publish about 2 * kp of them (a power of two, at most RES_QW_MAX per warp).
+int res_qw(int kp, int cs) {
+  int qw = 1;
+  while (qw < strata::RES_QW_MAX && cs * strata::NW * qw < 2 * kp) qw *= 2;
+  return qw;
+}
 
 // The launch shape of a call: blocks per row (one cluster), the chunk each streams, ring slots,
 // keys each warp publishes for the row threshold, history table size and shared memory.  Shared
 // by the context calls and the allocation-free call.
 int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mode, int esz, int B, int V, int kmax,
               int nmax, int lastn_max, bool with_hist, bool with_allowed, bool mask, bool pipelined,
-              int concurrent_bytes, int forced, Shape* s) {
+              int concurrent_bytes, int forced, Shape* s, bool streaming = true) {
   const bool concurrent = concurrent_bytes > 0;
   const long long row_bytes = static_cast<long long>(V) * esz;
   s->nmax = nmax;
@@ -201,11 +229,46 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
   }
   s->hash_cap = 0;
   s->hash_bits = 0;
+  s->resident = false;
   if (mode == strata::MODE_SAMPLE && with_hist && lastn_max > 0) {
     int bits = 6;
     while ((1 << bits) < 2 * lastn_max) ++bits;
     s->hash_bits = bits;
     s->hash_cap = 1 << bits;
+  }
+  // The resident shape: every block holds its chunk whole (at most RES_MAX_CHUNK_BYTES).  Latency-
+  // bound calls spread a row over enough blocks to fill the GPU; with the concurrency hint a row
+  // takes the fewest blocks that hold it.  A forced split is resident when its chunks fit.
+  if (!streaming) {
+    const int cs_min = static_cast<int>((row_bytes + strata::RES_MAX_CHUNK_BYTES - 1) / strata::RES_MAX_CHUNK_BYTES);
+    int rcs = 0;
+    if (forced > 0) {
+      if (forced >= cs_min && forced <= max_cluster) rcs = forced;
+    } else if (cs_min <= max_cluster) {
+      if (concurrent) {
+        rcs = std::max(cs_min, 1);
+      } else {
+        const int cs_fill = (num_sms + B - 1) / std::max(1, B);
+        const int cs_small = std::max(1, (V + MIN_CHUNK_ELEMS - 1) / MIN_CHUNK_ELEMS);
+        rcs = std::min(std::max({cs_min, std::min(cs_fill, cs_small), 1}), max_cluster);
+      }
+    }
+    if (rcs > 0) {
+      int chunk = (V + rcs - 1) / rcs;
+      chunk = (chunk + 15) / 16 * 16;
+      const int rqw = res_qw(kp_max, rcs);
+      const strata::RLayout RL = strata::make_res_layout(chunk, esz, s->hash_cap, rcs, kmax, nmax, rqw, with_allowed, mask);
+      if (static_cast<long long>(chunk) * esz <= strata::RES_MAX_CHUNK_BYTES && static_cast<int>(RL.total) <= max_smem) {
+        if (!strata::res_layout_aligned(RL)) return fail(STRATA_EINVAL, "internal: shared-memory layout not 16-byte aligned");
+        s->resident = true;
+        s->cs = rcs;
+        s->chunk = chunk;
+        s->qw = rqw;
+        s->nslot = (chunk * esz + strata::PIECE_BYTES - 1) / strata::PIECE_BYTES;
+        s->smem = static_cast<int>(RL.total);
+        return STRATA_OK;
+      }
+    }
   }
   Layout L{};
   for (;;) {
@@ -256,7 +319,7 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
   return shape_for(c->max_cluster, c->max_smem, c->smem_three, c->num_sms, mode, esz, B, V, kmax, top_n_eff,
                    max_lastn_penal(c),
                    with_hist, with_allowed, mask, pipelined, concurrent_bytes,
-                   static_cast<int>((flags >> 8) & 0x1Fu), s);
+                   static_cast<int>((flags >> 8) & 0x1Fu), s, (flags & STRATA_FLAG_RESIDENT) == 0u);
 }
 
 // STRATA_SAMPLE_DEBUG=1 in the environment: one line per call on stderr (entry point, rows,
@@ -273,10 +336,11 @@ int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t
            const char* entry) {
   if (trace_on())
     std::fprintf(stderr,
-                 "strata: %s B=%d V=%d dtype=%s flags=0x%x split=%d chunk=%d ring_slots=%d qw=%d hash=%d smem=%d "
-                 "grid=%d\n",
-                 entry, P.B, P.V, dtype == STRATA_DTYPE_F32 ? "f32" : "bf16", flags, sh.cs, sh.chunk, sh.nslot, sh.qw,
-                 sh.hash_cap, sh.smem, P.B * sh.cs);
+                 "strata: %s B=%d V=%d dtype=%s flags=0x%x kernel=%s split=%d chunk=%d ring_slots=%d qw=%d hash=%d "
+                 "smem=%d grid=%d\n",
+                 entry, P.B, P.V, dtype == STRATA_DTYPE_F32 ? "f32" : "bf16", flags,
+                 sh.resident ? "resident" : "streaming", sh.cs, sh.chunk, sh.nslot, sh.qw, sh.hash_cap, sh.smem,
+                 P.B * sh.cs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(P.B * sh.cs), 1, 1);
   cfg.blockDim = dim3(strata::NT, 1, 1);
@@ -299,7 +363,7 @@ int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t
   cudaError_t e;
   const bool mask = P.mode == strata::MODE_SAMPLE && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u && P.allowed_off != nullptr;
   const bool own = (flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u;
-  e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, mask, own), P);
+  e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, mask, own, sh.resident), P);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   (void)c;
   return STRATA_OK;
@@ -402,14 +466,7 @@ int strata_create(strata_ctx** out, int device, int max_slots, int max_vocab, in
     strata_destroy(c);
     return code;
   };
-  for (int i = 0; i < 8; ++i) {
-    const void* k = reinterpret_cast<const void*>(kernel_for(i & 1 ? STRATA_DTYPE_BF16 : STRATA_DTYPE_F32, (i >> 1) & 1,
-                                                             (i >> 2) & 1));
-    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->max_smem)) != cudaSuccess)
-      return cleanup(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
-    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-      return cleanup(cuda_fail(e, "cudaFuncSetAttribute(cluster)"));
-  }
+  if ((e = set_kernel_attributes(c->max_smem)) != cudaSuccess) return cleanup(cuda_fail(e, "cudaFuncSetAttribute"));
   // The largest cluster the device can place with a typical shared-memory footprint.
   c->max_cluster = 8;
   {
@@ -824,8 +881,7 @@ std::mutex g_na_mu;
 
 // Once per device, with that device current: the array's device address, kernel attributes and
 // the identity row-to-slot table.  Runs inside the first call on the device (synchronously).
-int noalloc_setup(int dev, NoallocDevice** out) {
-  std::lock_guard<std::mutex> lock(g_na_mu);
+int noalloc_setup(int dev, NoallocDevice** out) {  // called with g_na_mu held
   NoallocDevice& d = g_na[dev];
   if (!d.ready) {
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.scratch), g_noalloc_scratch);
@@ -836,14 +892,7 @@ int noalloc_setup(int dev, NoallocDevice** out) {
     d.num_sms = prop.multiProcessorCount;
     d.max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
     d.smem_three = smem_for_three(prop);
-    const void* kernels[2] = {reinterpret_cast<const void*>(strata::rows_kernel<0, false>),
-                              reinterpret_cast<const void*>(strata::rows_kernel<1, false>)};
-    for (const void* k : kernels) {
-      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem)) != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute(smem)");
-      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute(cluster)");
-    }
+    if ((e = set_kernel_attributes(d.max_smem)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     d.max_cluster = 8;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(strata::MAX_CS, 1, 1);
@@ -870,12 +919,14 @@ int noalloc_setup(int dev, NoallocDevice** out) {
   return STRATA_OK;
 }
 
-// Host staging of one call's key records and counter words (per thread, no heap).
+// Host staging of one call's key records and counter words: one static buffer, used under
+// g_na_mu from the first write to the return of the copies that read it (a copy from pageable
+// memory returns once the runtime holds the bytes), so host threads take turns.
 struct NoallocStage {
   unsigned char head[NA_CTR + sizeof(unsigned long long) * NA_MAX_ROWS];
   SlotDev slots[NA_MAX_ROWS];
 };
-thread_local NoallocStage g_na_stage;
+NoallocStage g_na_stage;
 
 }  // namespace
 
@@ -905,6 +956,7 @@ extern "C" int strata_sample_rows_noalloc(const void* logits, int dtype, int B, 
   if (dev < 0 || dev >= NA_MAX_DEVICES) return fail(STRATA_ERANGE, "device %d", dev);
 
   // keys and counters of this call, one slot per row
+  std::lock_guard<std::mutex> lock(g_na_mu);
   NoallocStage& st = g_na_stage;
   std::memset(st.head, 0, NA_CTR);  // the device error word starts at zero
   unsigned long long* ctr = reinterpret_cast<unsigned long long*>(st.head + NA_CTR);

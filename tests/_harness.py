@@ -39,6 +39,13 @@ def upload(w):
     return d
 
 
+def shape_hint(kind):
+    """Launch-shape flags of the parametrised tests: 0 the library's default, 1 the concurrency hint
+    (one block per full row), 2 the concurrency hint with resident chunks (STRATA_FLAG_RESIDENT)."""
+    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT, STRATA_FLAG_RESIDENT
+    return (0, STRATA_FLAG_CONCURRENT, STRATA_FLAG_CONCURRENT | STRATA_FLAG_RESIDENT)[kind]
+
+
 def set_slots(sampler, w, counters=None):
     counters = w["counters"] if counters is None else counters
     for s, p in w["slot_params"].items():

@@ -245,14 +245,16 @@ def test_history_graph_replay(sampler, S):
         assert sampler.slot_state(s)[1] == counters[s]
 
 
-@pytest.mark.parametrize("split", [0, 1], ids=["concurrency-hint", "one-cta-per-row"])
+@pytest.mark.parametrize("split", [0, 1, -1], ids=["concurrency-hint", "one-cta-per-row", "resident-hint"])
 def test_history_verify_windows_full_vocab(sampler, S, split):
     """The verify-window shape at V=248,320 fp32 (5 rows: 4 drafts + head, one request, repeat 1.1
-    over 64 ids) for ten consecutive windows, history kept on the device; also forced to one CTA
-    per row and with the concurrency hint (8 CTAs per row for these calls)."""
-    fl = S.STRATA_FLAG_SPLIT(split) if split else S.STRATA_FLAG_CONCURRENT
-    if not split:
+    over 64 ids) for ten consecutive windows, history kept on the device; with the concurrency hint
+    (8 CTAs per row for these calls), forced to one CTA per row, and with resident chunks."""
+    fl = S.STRATA_FLAG_SPLIT(split) if split > 0 else S.STRATA_FLAG_CONCURRENT
+    if split == 0:
         assert sampler.shape(2, 0, 5, synth.V_FULL, 0, S.STRATA_FLAG_HISTORY_RING | fl)["split"] == 8
+    if split < 0:
+        fl |= S.STRATA_FLAG_RESIDENT
     run = synth.DecodeRun(51, 1, synth.V_FULL, rows_per_slot=5, last_ns=(64,), prompt_len=(64, 64),
                           greedy_frac=0.0)
     state, counters = _start(sampler, run)

@@ -7,7 +7,7 @@ import pytest
 import oracle
 import synth
 
-from _harness import compare_sample, gpu_sample, set_slots
+from _harness import shape_hint, compare_sample, gpu_sample, set_slots
 
 pytestmark = pytest.mark.gpu
 
@@ -29,14 +29,13 @@ def _mask_flag():
     return STRATA_FLAG_ALLOWED_MASK
 
 
-@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+@pytest.mark.parametrize("concurrent", [0, 1, 2], ids=["default-shape", "one-cta-per-row", "resident-chunks"])
 def test_mask_config4_fused(sampler, concurrent):
     """Config 4's rows with their 5/100/1000-id lists used as masks (also with the concurrency hint:
     one CTA per row, both id bitmaps as long as the row)."""
-    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT
     w = synth.config4(fused=True)
     set_slots(sampler, w)
-    g = gpu_sample(sampler, w, flags=_mask_flag() | (STRATA_FLAG_CONCURRENT if concurrent else 0))
+    g = gpu_sample(sampler, w, flags=_mask_flag() | shape_hint(concurrent))
     rows, ctr = oracle.sample_call(w, mask_allowed=True)
     compare_sample(w, rows, g)
     off = w["allowed_off"]

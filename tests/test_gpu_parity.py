@@ -11,7 +11,7 @@ import pytest
 import oracle
 import synth
 
-from _harness import Stats, compare_logprobs, compare_sample, gpu_logprobs, gpu_sample, report, set_slots, upload
+from _harness import shape_hint, Stats, compare_logprobs, compare_sample, gpu_logprobs, gpu_sample, report, set_slots, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -60,12 +60,11 @@ def test_config2_verify_windows_counter_persists(sampler):
     report("config2", st)
 
 
-@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+@pytest.mark.parametrize("concurrent", [0, 1, 2], ids=["default-shape", "one-cta-per-row", "resident-chunks"])
 def test_config3_batch_slots_bf16(sampler, concurrent):
-    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT
     w = synth.config3()
     set_slots(sampler, w)
-    g = gpu_sample(sampler, w, top_n=0, chosen_lp=True, flags=STRATA_FLAG_CONCURRENT if concurrent else 0)
+    g = gpu_sample(sampler, w, top_n=0, chosen_lp=True, flags=shape_hint(concurrent))
     rows, ctr = oracle.sample_call(w)
     st = compare_sample(w, rows, g, top_n=0)
     _check_no_errors(sampler)
@@ -83,7 +82,7 @@ def test_config4_logprobs_entry(sampler):
     report("config4 logprobs", st)
 
 
-@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+@pytest.mark.parametrize("concurrent", [0, 1, 2], ids=["default-shape", "one-cta-per-row", "resident-chunks"])
 def test_config4_logprobs_entry_pipelined_own_outputs(sampler, concurrent):
     """strata_logprobs_rows back to back with early loads and own outputs: no call waits for the
     one before it; each call's log-probabilities against the oracle."""
@@ -92,8 +91,7 @@ def test_config4_logprobs_entry_pipelined_own_outputs(sampler, concurrent):
     base = synth.config4(fused=False)
     sampler.errors()  # drained: an earlier late-counter call would make these wait as usual
     fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS
-    if concurrent:
-        fl |= STRATA_FLAG_CONCURRENT
+    fl |= shape_hint(concurrent)
     ws = []
     for c in range(5):
         w = dict(base)
@@ -118,14 +116,13 @@ def test_config4_fused_sample_and_logprobs(sampler):
     report("config4 fused", st)
 
 
-@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+@pytest.mark.parametrize("concurrent", [0, 1, 2], ids=["default-shape", "one-cta-per-row", "resident-chunks"])
 def test_config5_stress_bf16_ties(sampler, concurrent):
     """Heavy ties: with one CTA per row a thread's tied ids at the threshold take the warp-wide
     rescan and the exact rounds over the whole row."""
-    from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT
     w = synth.config5()
     set_slots(sampler, w)
-    g = gpu_sample(sampler, w, flags=STRATA_FLAG_CONCURRENT if concurrent else 0)
+    g = gpu_sample(sampler, w, flags=shape_hint(concurrent))
     rows, ctr = oracle.sample_call(w)
     st = compare_sample(w, rows, g)
     _check_no_errors(sampler)
@@ -161,16 +158,21 @@ def test_random_edge_cases(sampler, seed):
         assert sampler.slot_state(s)[1] == ctr[s]
 
 
-def test_config4_pipelined_calls(sampler):
-    """The launch bench.py times: back-to-back calls with programmatic dependent launch and early
-    loads (few, large chunks per row), no host synchronisation in between; every call's picks,
-    alternatives and log-probabilities against the oracle, the counters advancing call by call."""
-    from request_token_sampling_gb300 import STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL
+@pytest.mark.parametrize("resident", [False, True], ids=["streaming", "resident"])
+def test_config4_pipelined_calls(sampler, resident):
+    """Back-to-back calls with programmatic dependent launch and early loads, no host
+    synchronisation in between; every call's picks, alternatives and log-probabilities against the
+    oracle, the counters advancing call by call.  Streaming chunks take few, large chunks per row for
+    such calls; resident chunks keep their size."""
+    from request_token_sampling_gb300 import STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL, STRATA_FLAG_RESIDENT
     base = synth.config4(fused=True)
     set_slots(sampler, base)
-    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD
-    assert sampler.shape(0, 0, base["B"], base["V"], base["top_n"], fl)["split"] < \
-        sampler.shape(0, 0, base["B"], base["V"], base["top_n"], 0)["split"]
+    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | (STRATA_FLAG_RESIDENT if resident else 0)
+    one = sampler.shape(0, 0, base["B"], base["V"], base["top_n"], fl & STRATA_FLAG_RESIDENT)["split"]
+    if resident:
+        assert sampler.shape(0, 0, base["B"], base["V"], base["top_n"], fl)["split"] == one == 16
+    else:
+        assert sampler.shape(0, 0, base["B"], base["V"], base["top_n"], fl)["split"] < one
     ws, ds, outs = [], [], []
     for c in range(5):
         w = dict(base)
@@ -191,10 +193,10 @@ def test_config4_pipelined_calls(sampler):
     for s in base["slot_params"]:
         assert sampler.slot_state(s)[1] == counters[s]
     _check_no_errors(sampler)
-    report("config4 pipelined", st)
+    report("config4 pipelined" + (" resident" if resident else ""), st)
 
 
-@pytest.mark.parametrize("concurrent", [False, True], ids=["default-shape", "one-cta-per-row"])
+@pytest.mark.parametrize("concurrent", [0, 1, 2], ids=["default-shape", "one-cta-per-row", "resident-chunks"])
 def test_config4_pipelined_own_outputs(sampler, concurrent):
     """Back-to-back calls on one stream that each write their own outputs: no call waits for the
     one before it, each takes its counters at its start, and the draws still follow call order."""
@@ -204,8 +206,7 @@ def test_config4_pipelined_own_outputs(sampler, concurrent):
     set_slots(sampler, base)
     sampler.errors()  # drained: an earlier waiting call would make these take their counters late
     fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_OWN_OUTPUTS
-    if concurrent:
-        fl |= STRATA_FLAG_CONCURRENT
+    fl |= shape_hint(concurrent)
     ws = []
     for c in range(8):
         w = dict(base)
@@ -256,21 +257,22 @@ def test_config5_pipelined_own_outputs_rows_share_slots(sampler):
     report("config5 own outputs", st)
 
 
-def test_config4_concurrent_groups():
+@pytest.mark.parametrize("resident", [False, True], ids=["streaming", "resident"])
+def test_config4_concurrent_groups(resident):
     """Two request groups, each its own context and stream, their pipelined calls interleaved with
-    the concurrency hint (one block per full row): every call of each group matches the oracle,
-    and each group's counters advance by its own calls only."""
+    the concurrency hint (one block per full row; resident chunks: 16 blocks per row): every call of
+    each group matches the oracle, and each group's counters advance by its own calls only."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from request_token_sampling_gb300 import (STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL,
-                                              Sampler)
+                                              STRATA_FLAG_RESIDENT, Sampler)
     base = synth.config4(fused=True)
-    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_CONCURRENT
+    fl = STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD | STRATA_FLAG_CONCURRENT | (STRATA_FLAG_RESIDENT if resident else 0)
     groups = [Sampler(device=0, max_slots=16, max_vocab=synth.V_FULL, max_rows=64) for _ in range(2)]
     try:
         for g in groups:
             set_slots(g, base)
-        assert groups[0].shape(0, 0, base["B"], base["V"], base["top_n"], fl)["split"] == 1
+        assert groups[0].shape(0, 0, base["B"], base["V"], base["top_n"], fl)["split"] == (16 if resident else 1)
         streams = [torch.cuda.Stream() for _ in groups]
         ws, outs = [], []
         for c in range(6):
@@ -294,7 +296,7 @@ def test_config4_concurrent_groups():
             for s in base["slot_params"]:
                 assert g.slot_state(s)[1] == ctr[s]
             _check_no_errors(g)
-        report("config4 concurrent groups", st)
+        report("config4 concurrent groups" + (" resident" if resident else ""), st)
     finally:
         for g in groups:
             g.close()

@@ -68,7 +68,7 @@ def test_verify_window_every_prefix(sampler, accepted):
 @pytest.mark.parametrize("accepted", [0, 2, 4])
 def test_verify_window_concurrency_hint(sampler, accepted):
     """The same windows with the concurrency hint (two CTAs per full row) and pipelined flags, as
-    independent request groups run them; also one CTA per row, forced."""
+    independent request groups run them; also with resident chunks, and one CTA per row, forced."""
     from request_token_sampling_gb300 import STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD, STRATA_FLAG_PDL
     w = synth.config2_window(31 + accepted)
     set_slots(sampler, w)
@@ -78,12 +78,12 @@ def test_verify_window_concurrency_hint(sampler, accepted):
     if accepted < w["B"] - 1:
         drafts[accepted] = (picks[accepted] + 29) % w["V"]
     set_slots(sampler, w)
-    from request_token_sampling_gb300 import STRATA_FLAG_SPLIT
+    from request_token_sampling_gb300 import STRATA_FLAG_RESIDENT, STRATA_FLAG_SPLIT
     fl = STRATA_FLAG_CONCURRENT | STRATA_FLAG_PDL | STRATA_FLAG_EARLY_LOAD
     assert sampler.shape(2, 0, w["B"], w["V"], w["top_n"], fl)["split"] == 2
     rows2, ctr, keep = oracle.verify_call(w, drafts)
     assert keep == {0: accepted + 1}
-    for extra in (0, STRATA_FLAG_SPLIT(1)):
+    for extra in (0, STRATA_FLAG_RESIDENT, STRATA_FLAG_SPLIT(1)):
         set_slots(sampler, w)
         g = _verify(sampler, w, drafts, flags=fl | extra)
         _check(w, rows2, g, drafts)

@@ -1,17 +1,21 @@
-"""The allocation-free entry point gives the same results as the context-based call.
+"""The allocation-free entry point gives the same results as the context-based call and the oracle.
 
 strata_sample_rows_noalloc exists for callers that cannot call cudaMalloc (a framework whose
 allocator owns all device memory, a server that must not grow its device footprint).  It keeps its
 per-row key records, counter words and error word in a static device array instead of a context.
 This test runs the same rows through both entry points, two calls in a row (the caller advances
 the counters of sampled rows between calls, as the context does on the device), and requires equal
-ids and log-probabilities within the tolerance of the other parity tests.  It lives in a file of its
-own, collected last.
+ids and log-probabilities within the tolerance of the other parity tests.  Both calls' rows are also
+checked against the CPU oracle with the counters the test supplies (a greedy row, top_k 64 with
+neutral cuts, top_k 0 meaning 20, a counter above 2^40).  It lives in a file of its own, collected
+last.
 """
 import numpy as np
 import pytest
 
+import oracle
 import synth
+from _harness import Stats, compare_sample
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +79,12 @@ def test_noalloc_matches_context_call_twice():
         got.append({k: v.cpu().numpy() for k, v in out.items()})
         counters = [c + 1 if sm else c for c, sm in zip(counters, sampled)]
 
+    st = Stats()
+    counters = {b: start[b] for b in range(B)}
+    for call in range(2):
+        rows, counters = oracle.sample_call(w, counters=counters)
+        compare_sample(w, rows, got[call], top_n=20, stats=st, debug=False)
+    assert st.rows == 2 * B
     for call in range(2):
         assert np.array_equal(got[call]["ids"], ref[call]["ids"]), call
         assert np.array_equal(got[call]["top_ids"], ref[call]["top_ids"]), call
