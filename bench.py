@@ -83,6 +83,10 @@ DESCRIPTIONS = {
                "over a 64-token history; seeded draft ids; kept rows counted in the launch"),
 }
 DESCRIPTIONS["mask"] = DESCRIPTIONS["fused"] + "; the allowed ids used as a sampling mask (STRATA_FLAG_ALLOWED_MASK)"
+DESCRIPTIONS["sliced"] = ("vocabulary slices: B=8 fp32 rows x V=248,320, N(0,3^2)+1..5 spikes; " + _KEYS1
+                          + "; top_logprobs=20, chosen-token logprob (no allowed subsets); each row split into "
+                          "{G} equal column slices reduced to records (strata_shard_rows, one launch per slice, "
+                          "one after another on one GPU) and merged (strata_merge_shards)")
 DESCRIPTIONS["verify-ring"] = (DESCRIPTIONS["verify"] + "; the 64-token window read from the slot's history kept on "
                                "the device (STRATA_FLAG_HISTORY_RING) and the kept picks appended in the launch")
 KERNEL_SOURCES = ("request_token_sampling_gb300/csrc/strata_kernel.cuh",   # the device code the
@@ -110,6 +114,8 @@ def load_workload(name: str):
         return synth.config5(), "sample"
     if name in ("verify", "verify-ring"):
         return synth.config2_window(0), "verify"
+    if name == "sliced":  # sliced rows carry no allowed subsets
+        return dict(synth.config4(fused=True), allowed=None, allowed_off=None), "sample"
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -117,13 +123,13 @@ def esize(w) -> int:
     return 4 if w["dtype"] == "f32" else 2
 
 
-def algorithmic_bytes(w, kind="sample", ring=False) -> int:
+def algorithmic_bytes(w, kind="sample", ring=False, slices=0) -> int:
     """Bytes a launch must move at least: logits once, the history windows, allowed ids, row
     arrays, slot keys and counters, and every output (verify windows: drafts and the kept count;
     with a kept history its length read and written and the kept picks written, counted as the
-    whole window)."""
+    whole window; vocabulary slices: every slice's records written and read once)."""
     B, V = w["B"], w["V"]
-    n = B * V * esize(w)
+    n = B * V * esize(w) + 2 * slices * B * 1280
     for s in range(w["n_hist_slots"]):
         ln = w["slot_params"][s]["penalty_last_n"]
         n += 4 * min(ln, int(w["hist_off"][s + 1] - w["hist_off"][s]))
@@ -375,7 +381,8 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32(penalty,ranking)+f64",
-            "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": w["B"]},
+            "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.workload].replace("{G}", str(args.slices)),
+                                            "rows_per_step": w["B"]},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{args.steps} timed whole {w['B']}-row calls on 1 host core"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -467,7 +474,7 @@ def run_gpu(args, rank, world):
     import torch.distributed as dist
     from request_token_sampling_gb300 import (STRATA_FLAG_ALLOWED_MASK, STRATA_FLAG_CONCURRENT, STRATA_FLAG_EARLY_LOAD,
                                               STRATA_FLAG_HISTORY_RING, STRATA_FLAG_OWN_OUTPUTS, STRATA_FLAG_PDL,
-                                              STRATA_FLAG_SPLIT, Sampler)
+                                              STRATA_FLAG_SPLIT, STRATA_SHARD_RECORD_BYTES, Sampler)
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -476,6 +483,8 @@ def run_gpu(args, rank, world):
     w, kind = load_workload(args.workload)
     verify = kind == "verify"
     ring = args.workload == "verify-ring"
+    sliced = args.workload == "sliced"
+    G = max(1, args.slices) if sliced else 0
     B, V = w["B"], w["V"]
     dtype_code = 0 if w["dtype"] == "f32" else 1
     step_bytes = B * w["ld"] * esize(w)
@@ -483,6 +492,8 @@ def run_gpu(args, rank, world):
     R = max(2, -(-4 * l2 // step_bytes)) if args.batches <= 0 else args.batches
     W, K = args.warmup, args.steps
     flags = 0 if args.no_pdl else (STRATA_FLAG_PDL | (0 if args.no_early_load else STRATA_FLAG_EARLY_LOAD))
+    if sliced:  # a slice call takes only the launch-shape flags
+        flags = 0
     if args.workload == "mask":
         flags |= STRATA_FLAG_ALLOWED_MASK
     if ring:
@@ -493,7 +504,8 @@ def run_gpu(args, rank, world):
         flags |= STRATA_FLAG_CONCURRENT
     # every call writes its own output buffers (they rotate like the inputs), so no call waits for
     # the one before it; verify windows and kept histories depend on the previous call by nature
-    own = (not args.no_own_outputs and (flags & STRATA_FLAG_EARLY_LOAD) != 0 and not verify and not ring)
+    own = (not args.no_own_outputs and (flags & STRATA_FLAG_EARLY_LOAD) != 0 and not verify and not ring
+           and not sliced)
     if own:
         flags |= STRATA_FLAG_OWN_OUTPUTS
 
@@ -525,9 +537,23 @@ def run_gpu(args, rank, world):
     row_draft = ten(drafts)
     top_n = w["top_n"]
     batches = make_batches(w, R, dev)
+    # vocabulary slices: G equal column ranges (multiples of 8 ids, so every slice starts on a
+    # 16-byte boundary) and one record buffer per group
+    bounds = [min(V, (V * g // max(G, 1) + 7) // 8 * 8) for g in range(G + 1)] if sliced else []
+    recbufs = [torch.empty(G, B, STRATA_SHARD_RECORD_BYTES, dtype=torch.uint8, device=dev) for _ in samplers] \
+        if sliced else []
+
+    def sliced_call(sg, x, rs, rp, h, ho, st, o, fl, debug=False):
+        rec = recbufs[samplers.index(sg)]
+        for g in range(G):
+            a, b = bounds[g], bounds[g + 1]
+            sg.shard(x[:, a:b], rs, a, V=b - a, hist=h, hist_off=ho, top_n=top_n, flags=fl, stream=st, out=rec[g])
+        return sg.merge(rec, rs, rp, top_n=top_n, chosen_lp=True, debug=debug, stream=st, out=o)
 
     def call_on(sg, st, o, fl, i, debug=False):
         x = batches[i % R]
+        if sliced:
+            return sliced_call(sg, x, row_slot, row_pos, hist, hist_off, st, o, fl, debug)
         if verify:
             return sg.verify(x, row_slot, row_pos, row_draft, V=V, hist=hist, hist_off=hist_off, top_n=top_n,
                              chosen_lp=True, flags=fl, stream=st, out=o)
@@ -541,7 +567,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     if any(sg.errors() != 0 for sg in samplers):
         raise RuntimeError("device error bits set")
-    shape = s.shape(2 if verify else 0, dtype_code, B, V, top_n, flags)
+    shape = s.shape(2 if verify else 0, dtype_code, B, bounds[1] if sliced else V, top_n, flags)
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
@@ -701,7 +727,10 @@ def run_gpu(args, rank, world):
         if k >= 2:
             stream.wait_event(st_["ev_out"])     # its results from two steps back have left
         d_small, o_ = st_["small"], st_["out"]
-        if verify:
+        if sliced:
+            sliced_call(s, st_["logits"], d_small["row_slot"], d_small["row_pos"], d_small.get("hist"),
+                        d_small.get("hist_off"), stream, o_, flags_e2e)
+        elif verify:
             s.verify(st_["logits"], d_small["row_slot"], d_small["row_pos"], d_small["row_draft"], V=V,
                      hist=d_small.get("hist"), hist_off=d_small.get("hist_off"), top_n=top_n, chosen_lp=True,
                      flags=flags_e2e, stream=stream, out=o_)
@@ -754,7 +783,7 @@ def run_gpu(args, rank, world):
         for sg in samplers:
             sg.close()
         return
-    alg = algorithmic_bytes(w, kind, ring)
+    alg = algorithmic_bytes(w, kind, ring, G)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
         peak, peak_src = float(json.load(open(peaks_path))["hbm_gbs"]), "measured"
@@ -779,7 +808,7 @@ def run_gpu(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.workload], "rows_per_step": B, "V": V,
+        "config": {"workload": DESCRIPTIONS[args.workload].replace("{G}", str(G)), "rows_per_step": B, "V": V,
                    "logits_dtype": w["dtype"],
                    "l2_policy": (f"inputs rotate over {R} distinct batches ({R * step_bytes / 1e6:.0f} MB, "
                                  f"{R * step_bytes / l2:.1f}x the {l2 / 1e6:.0f} MB L2); the timed steps take "
@@ -790,7 +819,8 @@ def run_gpu(args, rank, world):
                              + (", logit loads start before the previous call ends (inputs resident)"
                                 if flags & 2 else "")
                              + (", each call writes its own output set (no wait for the previous call)"
-                                if flags & STRATA_FLAG_OWN_OUTPUTS else ""),
+                                if flags & STRATA_FLAG_OWN_OUTPUTS else "")
+                             + (f"; a step is {G} slice launches and one merge launch" if sliced else ""),
                    "split": shape["split"], "chunk_elems": shape["chunk"], "smem_bytes": shape["smem"],
                    "grid": shape["grid"], "parallelism": f"replicas x{world}",
                    "streams": S},
@@ -803,7 +833,7 @@ def run_gpu(args, rank, world):
         "single_group": single,
         "single_call_us": single_call,
         "parity": parity,
-        "gpu_launches": K,
+        "gpu_launches": K * (G + 1) if sliced else K,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -835,12 +865,14 @@ def main():
     ap.add_argument("--batches", type=int, default=0,
                     help="distinct input batches to rotate over (0: enough for 4x the L2 size)")
     ap.add_argument("--lone-reps", type=int, default=15, help="gated single calls timed for single_call_us")
+    ap.add_argument("--slices", type=int, default=2, help="sliced workload: column slices per row (1..16)")
     ap.add_argument("--workload", choices=["fused", "config1", "config3", "config5", "verify", "mask",
-                                           "verify-ring"], default="fused",
+                                           "verify-ring", "sliced"], default="fused",
                     help="fused: the logprobs workload fused with sampling (the headline); config1/3/5: those "
                          "workloads at their own shapes; verify: verify windows; mask: the fused workload with "
                          "its allowed ids as a sampling mask; verify-ring: verify windows over histories kept "
-                         "on the device")
+                         "on the device; sliced: the fused rows without allowed subsets over --slices "
+                         "vocabulary slices, merged")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -63,6 +63,8 @@ extern "C" {
 #define STRATA_MAX_PENALTY_LAST_N  4096 /* library limit on the penalty history window           */
 #define STRATA_MAX_VOCAB           524288 /* library limit on V (per-row split over <= 16 SMs)   */
 #define STRATA_HISTORY_CAP         4096 /* ids a slot's kept history holds (its newest ids)      */
+#define STRATA_MAX_SHARDS          16   /* vocabulary slices one strata_merge_shards call merges  */
+#define STRATA_SHARD_RECORD_BYTES  1280 /* bytes of one row's record from one vocabulary slice    */
 
 /* ---- launch flags (strata_sample_rows / strata_logprobs_rows `flags`) --------------------- */
 /* Launch with programmatic dependent launch: the kernel may be scheduled while the previous
@@ -112,14 +114,13 @@ extern "C" {
 #define STRATA_FLAG_OWN_OUTPUTS 0x20u
 /* A launch-shape hint: calls on other streams (of other contexts) run on the GPU at the same time
  * as this one, so whole-GPU throughput matters more than this call's latency.  The call then gives
- * each row one block per STRATA_CONCURRENT_ROW_BYTES of logits (one block for a full fp32 or bf16
- * row of 248,320 ids): fewer blocks per byte, no exchange between blocks, at the price of a longer
- * call (each block streams its row alone).  strata_sample_verify, whose windows wait for the
- * previous window, uses half that, and calls with STRATA_FLAG_HISTORY_RING (which wait for the
- * previous call before their penalties) one block per 128 KiB.  Results are the same as without
- * the flag.  A forced split (STRATA_FLAG_SPLIT) takes precedence.                                */
+ * each row one block per STRATA_CONCURRENT_ROW_BYTES of logits (two blocks for a full fp32 row of
+ * 248,320 ids, one for a bf16 row): fewer blocks per byte and a small exchange between them, at
+ * the price of a longer call.  Calls with STRATA_FLAG_HISTORY_RING (which wait for the previous
+ * call before their penalties) take one block per 128 KiB.  Results are the same as without the
+ * flag.  A forced split (STRATA_FLAG_SPLIT) takes precedence.                                    */
 #define STRATA_FLAG_CONCURRENT  0x10u
-#define STRATA_CONCURRENT_ROW_BYTES (1u << 20)
+#define STRATA_CONCURRENT_ROW_BYTES (1u << 19)
 /* A launch-shape choice: hold each block's chunk whole in shared memory (at most 64 KiB of logits:
  * up to 16 blocks per row) instead of streaming it through a ring of shared-memory slots, with a
  * row threshold exchanged across the row's blocks and candidates read from shared memory.  A row
@@ -305,6 +306,60 @@ int strata_logprobs_rows(strata_ctx *ctx, const void *logits, int dtype, int B, 
                          int top_n, int32_t *top_ids, float *top_lps,
                          const int32_t *allowed, const int32_t *allowed_off, float *allowed_lps,
                          uint32_t flags, void *stream);
+
+/*
+ * Vocabulary-sliced sampling: each row's V ids are split into disjoint slices (for instance one per
+ * GPU holding that slice of the head's output), each slice is reduced to a small record, the
+ * records are exchanged, and a merge of every slice's record gives what strata_sample_rows gives on
+ * the whole row.  The pages split a model across GPUs only by layers, with sampling on the last
+ * stage [P559, "What it adds"]; this pair is a library addition whose result is defined by the
+ * whole-row chain [P19, "min_p and the penalties", "The sampled chain is one block per token"]
+ * and the raw-logit logprobs [P3200, "Approach"]: the row's top_k list is among the union of its
+ * slices' own top_k lists, its top_n raw alternatives among the union of theirs, and its
+ * log-sum-exp is the log of the summed exponentials of theirs.
+ *
+ * strata_shard_rows: one slice of B rows.  logits/dtype/ld as in strata_sample_rows, with V_shard
+ * columns that hold the ids id_offset .. id_offset + V_shard - 1 (id_offset >= 0).  row_slot,
+ * hist, hist_off and n_hist_slots as in strata_sample_rows; history ids are the row's own (whole
+ * vocabulary) ids and the slice counts those inside it.  top_n (0..20) alternatives are kept per
+ * record.  records: device, [B][STRATA_SHARD_RECORD_BYTES], 16-byte aligned (else
+ * STRATA_EALIGN).  Record layout (little-endian 32-bit words):
+ *   word 0: n_pen, entries in the penalised list (<= the row's top_k, 1 for a greedy row,
+ *           0 for a row whose slot is out of range)
+ *   word 1: n_raw, entries in the raw list (<= top_n)
+ *   word 2: float, log of the sum of exp(raw logit) over the slice's ids
+ *   word 3: 0
+ *   bytes 16 .. 16 + 16*64: penalised entries, best first: key low word, key high word, raw logit
+ *           (float), 0
+ *   bytes 1040 .. 1040 + 8*20: raw entries, best first: key low word, key high word
+ *   the rest: unused.
+ * A key is (ord(v) << 32) | (0xFFFFFFFF - id), larger is better: v the entry's (penalised or raw)
+ * logit, ord the order-preserving map of a float to uint32 (sign bit clear: bits | 0x80000000;
+ * set: ~bits; -0.0 as +0.0), id the whole-vocabulary id, so equal values order by lower id.  No
+ * slot state changes: the counters move only in the merge.
+ * flags: STRATA_FLAG_CONCURRENT and STRATA_FLAG_SPLIT only (else STRATA_EINVAL).
+ *
+ * strata_merge_shards: records device, [n_shards][B][STRATA_SHARD_RECORD_BYTES] (slice-major: the
+ * concatenation of every slice's strata_shard_rows output for the same B rows, in any slice
+ * order), 1 <= n_shards <= STRATA_MAX_SHARDS.  The slices must be disjoint and made with the same
+ * context state (slot keys) and the same top_n.  Runs top_k, min_p, top_p, temperature and the
+ * Philox draw on the merged list of each row and writes out_ids, chosen_lp, top_ids/top_lps
+ * (top_n as given to the slices) and the debug outputs topk_ids/topk_vals/kept exactly as
+ * strata_sample_rows does, with row_pos the rows' positions; the counter rule is that of
+ * strata_sample_rows (each slot with a sampled row advances by 1 in this call).  Every GPU that
+ * merges the same records with the same slot state writes the same outputs.  flags: 0 (else
+ * STRATA_EINVAL).  The allowed-subset logprobs, STRATA_FLAG_ALLOWED_MASK, verify windows and kept
+ * histories are not available on sliced rows.
+ */
+int strata_shard_rows(strata_ctx *ctx, const void *logits, int dtype, int B, int V_shard, int64_t ld,
+                      int id_offset, const int32_t *row_slot,
+                      const int32_t *hist, const int32_t *hist_off, int n_hist_slots,
+                      int top_n, void *records, uint32_t flags, void *stream);
+int strata_merge_shards(strata_ctx *ctx, const void *records, int n_shards, int B,
+                        const int32_t *row_slot, const int64_t *row_pos, int32_t *out_ids,
+                        int top_n, float *chosen_lp, int32_t *top_ids, float *top_lps,
+                        int32_t *topk_ids, float *topk_vals, int32_t *kept,
+                        uint32_t flags, void *stream);
 
 /*
  * Kept per-slot histories (STRATA_FLAG_HISTORY_RING).  A slot's history is the ids of its run so

@@ -31,6 +31,8 @@ STRATA_MAX_PENALTY_LAST_N = 4096
 STRATA_MAX_VOCAB = 524288
 STRATA_NOALLOC_MAX_ROWS = 1024
 STRATA_HISTORY_CAP = 4096
+STRATA_MAX_SHARDS = 16
+STRATA_SHARD_RECORD_BYTES = 1280
 
 STRATA_FLAG_PDL = 0x1
 STRATA_FLAG_EARLY_LOAD = 0x2
@@ -39,7 +41,7 @@ STRATA_FLAG_HISTORY_RING = 0x8
 STRATA_FLAG_CONCURRENT = 0x10
 STRATA_FLAG_OWN_OUTPUTS = 0x20
 STRATA_FLAG_RESIDENT = 0x40
-STRATA_CONCURRENT_ROW_BYTES = 1 << 20
+STRATA_CONCURRENT_ROW_BYTES = 1 << 19
 STRATA_FLAG_TEST_STALL = 0x10000
 
 
@@ -60,7 +62,7 @@ EXPORTED = (
     "strata_create", "strata_destroy", "strata_set_slot_params", "strata_get_slot_state",
     "strata_set_slot_state", "strata_sample_rows", "strata_logprobs_rows", "strata_read_errors",
     "strata_launch_shape", "strata_sample_rows_noalloc", "strata_sample_verify", "strata_history_enable",
-    "strata_history_set", "strata_history_get",
+    "strata_history_set", "strata_history_get", "strata_shard_rows", "strata_merge_shards",
 )
 
 
@@ -120,6 +122,8 @@ def _load() -> ctypes.CDLL:
         "strata_history_enable": ([vp], i32),
         "strata_history_set": ([vp, i32, vp, i64, vp], i32),
         "strata_history_get": ([vp, i32, vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i64), vp], i32),
+        "strata_shard_rows": ([vp, vp, i32, i32, i32, i64, i32, vp, vp, vp, i32, i32, vp, u32, vp], i32),
+        "strata_merge_shards": ([vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, u32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -289,6 +293,34 @@ def strata_logprobs_rows(ctx, logits, V=None, chosen=None, chosen_lp=None, top_n
         int(top_n), _typed(top_ids, torch.int32, "top_ids"), _typed(top_lps, torch.float32, "top_lps"),
         _typed(allowed, torch.int32, "allowed"), _typed(allowed_off, torch.int32, "allowed_off"),
         _typed(allowed_lps, torch.float32, "allowed_lps"), int(flags), _stream(stream)))
+
+
+def strata_shard_rows(ctx, logits, row_slot, records, id_offset: int, V=None, hist=None, hist_off=None,
+                      top_n: int = 0, flags: int = 0, stream=None) -> None:
+    """One vocabulary slice of B rows (columns = ids id_offset ..) -> records [B][1280] uint8."""
+    import torch
+    ptr, dt, B, V, ld = _logits_args(logits, V)
+    n_hist = 0 if hist_off is None else int(hist_off.numel()) - 1
+    _check(lib.strata_shard_rows(
+        ctx, ptr, dt, B, V, ld, int(id_offset), _typed(row_slot, torch.int32, "row_slot"),
+        _typed(hist, torch.int32, "hist"), _typed(hist_off, torch.int32, "hist_off"), n_hist,
+        int(top_n), _typed(records, torch.uint8, "records"), int(flags), _stream(stream)))
+
+
+def strata_merge_shards(ctx, records, row_slot, row_pos, out_ids, top_n: int = 0, chosen_lp=None, top_ids=None,
+                        top_lps=None, topk_ids=None, topk_vals=None, kept=None, flags: int = 0,
+                        stream=None) -> None:
+    """Merge records [n_shards][B][1280] uint8 into the rows' samples and logprobs."""
+    import torch
+    if records.dim() != 3 or records.shape[2] != STRATA_SHARD_RECORD_BYTES:
+        raise ValueError("records must be [n_shards, B, STRATA_SHARD_RECORD_BYTES]")
+    _check(lib.strata_merge_shards(
+        ctx, _typed(records, torch.uint8, "records"), int(records.shape[0]), int(records.shape[1]),
+        _typed(row_slot, torch.int32, "row_slot"), _typed(row_pos, torch.int64, "row_pos"),
+        _typed(out_ids, torch.int32, "out_ids"), int(top_n), _typed(chosen_lp, torch.float32, "chosen_lp"),
+        _typed(top_ids, torch.int32, "top_ids"), _typed(top_lps, torch.float32, "top_lps"),
+        _typed(topk_ids, torch.int32, "topk_ids"), _typed(topk_vals, torch.float32, "topk_vals"),
+        _typed(kept, torch.int32, "kept"), int(flags), _stream(stream)))
 
 
 def strata_read_errors(ctx, stream=None) -> int:

@@ -12,6 +12,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libstrata_sample.so")
 SOURCES = [os.path.join(CSRC, "strata_sample.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "strata_kernel.cuh"), os.path.join(CSRC, "strata_device.cuh"),
+                     os.path.join(CSRC, "strata_resident.cuh"), os.path.join(CSRC, "strata_merge.cuh"),
                      os.path.join(ROOT, "include", "strata_sample.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

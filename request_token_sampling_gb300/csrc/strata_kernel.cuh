@@ -54,6 +54,8 @@ constexpr int QW_MAX = 16;                   // thread maxima a warp publishes, 
 constexpr int RANK_LIMIT = 256;              // candidates ranked by counting; beyond: argmax rounds
 constexpr int HASH_CNT_BITS = 13;            // history table entry = (local id << 13) | count
 constexpr uint32_t HASH_EMPTY = 0xFFFFFFFFu;
+constexpr int REC_PEN = 16;                  // a slice record: penalised entries after the header
+constexpr int REC_RAW = REC_PEN + 16 * 64;   // and the raw keys after the penalised entries
 constexpr int MODE_SAMPLE = 0;
 constexpr int MODE_LOGPROBS = 1;
 constexpr uint32_t SLOT_SAMPLED = 1u;
@@ -136,7 +138,15 @@ struct KParams {
   uint32_t* done;            // verify windows / kept histories: per-slot rows done in the current call
   int32_t* ring;             // kept histories: STRATA_HISTORY_CAP ids per slot, or NULL
   unsigned long long* hlen;  // kept histories: per-slot total length
+  int id_off;                // vocabulary slices: the whole-row id of column 0 (0 otherwise)
+  unsigned char* rec;        // vocabulary slices: [B][STRATA_SHARD_RECORD_BYTES] records, or NULL
 };
+
+// A history id relative to the row's first column (a slice's id offset; ids below the slice wrap
+// to values no chunk holds).
+__device__ __forceinline__ int slice_id(int id, int off) {
+  return static_cast<int>(static_cast<uint32_t>(id) - static_cast<uint32_t>(off));
+}
 
 struct Layout {
   uint32_t data, mbar, abits, mbits, hash, hraw, hflag, wkey, red, ctl, xrec;
@@ -563,17 +573,48 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t x, uint64_t* red, int
   return r;
 }
 
+// A threshold key for a thread that owns history ids: the largest order key of min(raw,
+// penalised) over the batch of 16 elements that starts at vector `vb` (vectors vb, vb + NT, ...).
+// Both the raw and the penalised value of that id reach it, so it bounds both candidate lists.
+template <int DT>
+__device__ __noinline__ uint32_t batch_safe_key(const unsigned char* gchunk, int vb, int n_vec, int n_el,
+                                                const uint32_t* htab, int hash_bits, float rep, float freq,
+                                                float pres) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+  constexpr int RB = BATCH_VECS<DT>;
+  uint32_t best = 0u;
+#pragma unroll
+  for (int r = 0; r < RB; ++r) {
+    const int v = vb + r * NT;
+    if (v >= n_vec) continue;
+    float x[EPV];
+    load_vec_g<DT>(gchunk, v, n_el, x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+      if (loc >= static_cast<uint32_t>(n_el)) continue;
+      const uint32_t c = hash_count(htab, hash_bits, loc);
+      const float y = c != 0u ? fminf(x[e], penalize(x[e], c, rep, freq, pres)) : x[e];
+      best = max(best, order_key(y));
+    }
+  }
+  return best;
+}
+
 // Exact argmax rounds over this CTA's chunk: the `need` largest keys in order (penalised values
 // for list 0, raw values for list 1), written to the candidate buffer.  Only taken when more
 // candidates reach the row threshold than the buffer holds (heavy ties); kept out of line so the
-// common path stays small.  Every thread of the CTA calls it.  Returns the number found.
+// common path stays small.  A penalised value needs the history table only for the elements of
+// threads that own a history id (`hflag`; thread t owns vectors t, t + NT, ...).  Every thread of
+// the CTA calls it.  Returns the number found.
 template <int DT>
 __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, int n_el, int lo, int list, int need,
-                                         bool penal, const uint32_t* htab, int hash_bits,
+                                         bool penal, const uint32_t* htab, int hash_bits, const uint32_t* hflag,
                                          float rep, float freq, float pres, uint64_t* red64, uint4* cand_pen,
                                          uint64_t* cand_raw) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool owner = list == 0 && penal && ((hflag[tid >> 5] >> (tid & 31)) & 1u);
   uint64_t prev = ~0ull;
   int got = 0;
   for (int r = 0; r < need; ++r) {
@@ -586,7 +627,7 @@ __device__ __noinline__ int exact_rounds(const unsigned char* data, int n_vec, i
         const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
         if (loc >= static_cast<uint32_t>(n_el)) continue;
         float pv = x[e];
-        if (list == 0 && penal) {
+        if (owner) {
           const uint32_t c = hash_count(htab, hash_bits, loc);
           if (c != 0u) pv = penalize(pv, c, rep, freq, pres);
         }
@@ -665,6 +706,116 @@ __device__ __noinline__ int draw_dw(float wa, float wb, int m2, float u, int lan
   const uint32_t ja = __ballot_sync(FULL_MASK, lane < m2 && !dw_less(td, a));
   const uint32_t jb = __ballot_sync(FULL_MASK, lane + 32 < m2 && !dw_less(td, b));
   return min(__popc(ja) + __popc(jb), m2 - 1);
+}
+
+// The tail of a row on its ordered top_k list (one warp; lane i holds entries i and i + 32).
+struct Tail {
+  uint4 ea, eb;      // the entries: key low word, key high word, raw logit, 0
+  float va, vb;      // their penalised logits
+  float wa, wb;      // tempered weights over the top_p survivors
+  float Ca, Cb;      // and their fp32 prefix sums
+  int m1, m2;        // survivors of min_p, of top_p
+};
+
+// The tail's first half on k_eff > 0 ordered entries: min_p and top_p cuts and the tempered
+// cumulative weights (nothing here depends on the draw counter).  A greedy row keeps its head.
+__device__ __forceinline__ void tail_cuts(const uint4* sorted_pen, int k_eff, bool sampled, const SlotDev& sp,
+                                          int lane, Tail& t) {
+  t.ea = (lane < k_eff) ? sorted_pen[lane] : make_uint4(0, 0, 0, 0);
+  t.eb = (lane + 32 < k_eff) ? sorted_pen[lane + 32] : make_uint4(0, 0, 0, 0);
+  t.va = key_value(t.ea.y);
+  t.vb = key_value(t.eb.y);
+  t.m1 = t.m2 = 1;
+  if (!sampled) return;
+  const float v0 = __shfl_sync(FULL_MASK, t.va, 0);
+  t.m1 = k_eff;
+  if (sp.min_p > 0.0f) {  // min_p in logit space, float32
+    const float thr = __fadd_rn(v0, sp.logminp);
+    const uint32_t ba = __ballot_sync(FULL_MASK, lane < k_eff && t.va >= thr);
+    const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && t.vb >= thr);
+    t.m1 = max(1, __popc(ba) + __popc(bb));
+  }
+  // temperature-1 mass (top_p) and tempered weights (draw) over the min_p survivors.  Prefix sums
+  // in fp32 decide unless a decision lies within 1e-5 of its boundary (the fp32 scan is good to
+  // ~4e-7 relative); then double-word sums (TwoSum) decide.
+  const bool ina = lane < t.m1, inb = lane + 32 < t.m1;
+  // lanes outside the survivors divide a plain zero (a NaN or an infinity would take the
+  // division's slow path)
+  const float da = ina ? __fsub_rn(t.va, v0) : 0.0f, db = inb ? __fsub_rn(t.vb, v0) : 0.0f;
+  const float Tm = sp.temperature;
+  const float qa = ina ? expf(da) : 0.0f, qb = inb ? expf(db) : 0.0f;
+  t.wa = ina ? expf(__fdiv_rn(da, Tm)) : 0.0f;
+  t.wb = inb ? expf(__fdiv_rn(db, Tm)) : 0.0f;
+  const float ca = warp_scan_f(qa, lane);
+  t.Ca = warp_scan_f(t.wa, lane);
+  const float cb = warp_scan_f(qb, lane) + __shfl_sync(FULL_MASK, ca, 31);
+  t.Cb = warp_scan_f(t.wb, lane) + __shfl_sync(FULL_MASK, t.Ca, 31);
+  t.m2 = t.m1;
+  if (!(sp.top_p >= 1.0f)) {
+    if (!(sp.top_p > 0.0f)) {
+      t.m2 = 1;
+    } else {
+      const float tot_q = __shfl_sync(FULL_MASK, cb, 31);
+      const float target = sp.top_p * tot_q, margin = 1e-5f * tot_q;
+      const bool near = __any_sync(FULL_MASK, (ina && fabsf(ca - target) <= margin) ||
+                                                  (inb && fabsf(cb - target) <= margin));
+      if (!near) {
+        const uint32_t la = __ballot_sync(FULL_MASK, ina && ca < target);
+        const uint32_t lb = __ballot_sync(FULL_MASK, inb && cb < target);
+        t.m2 = min(t.m1, __popc(la) + __popc(lb) + 1);
+      } else {
+        t.m2 = top_p_dw(qa, qb, ina, inb, sp.top_p, t.m1, lane);
+      }
+    }
+  }
+}
+
+// The draw: the index of the first survivor whose cumulative tempered weight exceeds u * W (W the
+// sum over the m2 top_p survivors), from the fp32 sums unless a prefix lies within 1e-5 of u * W.
+__device__ __forceinline__ int tail_draw(const Tail& t, uint32_t x0, int lane) {
+  const float u = static_cast<float>(x0 >> 8) * 0x1p-24f;
+  const int last = t.m2 - 1;  // the draw reads prefixes below m2 only; W = C[m2 - 1]
+  const float W = (last < 32) ? __shfl_sync(FULL_MASK, t.Ca, last) : __shfl_sync(FULL_MASK, t.Cb, last - 32);
+  const float tgt = u * W, margin = 1e-5f * W;
+  const bool ia = lane < t.m2, ib = lane + 32 < t.m2;
+  const bool near = __any_sync(FULL_MASK, (ia && fabsf(t.Ca - tgt) <= margin) || (ib && fabsf(t.Cb - tgt) <= margin));
+  if (!near) {
+    const uint32_t ja = __ballot_sync(FULL_MASK, ia && t.Ca <= tgt);
+    const uint32_t jb = __ballot_sync(FULL_MASK, ib && t.Cb <= tgt);
+    return min(__popc(ja) + __popc(jb), t.m2 - 1);
+  }
+  return draw_dw(t.wa, t.wb, t.m2, u, lane);
+}
+
+// Entry j of the tail's list (warp-wide): id and raw logit.
+__device__ __forceinline__ uint32_t tail_id(const Tail& t, int j) {
+  const uint32_t id_a = key_id((static_cast<uint64_t>(t.ea.y) << 32) | t.ea.x);
+  const uint32_t id_b = key_id((static_cast<uint64_t>(t.eb.y) << 32) | t.eb.x);
+  return __shfl_sync(FULL_MASK, j < 32 ? id_a : id_b, j & 31);
+}
+__device__ __forceinline__ float tail_raw(const Tail& t, int j) {
+  return __uint_as_float(__shfl_sync(FULL_MASK, j < 32 ? t.ea.z : t.eb.z, j & 31));
+}
+
+// A vocabulary slice's record of one row (the layout strata_shard_rows documents): the counts and
+// the log-sum-exp, then the ordered penalised entries (key, raw logit) and raw keys, their ids
+// moved from the slice's columns to whole-row ids (a key's low word is the complement of the id,
+// so the id offset is subtracted from it).  Threads 0..63 and 64..83 of the leader write it.
+__device__ __forceinline__ void write_record(unsigned char* rec, const uint4* sorted_pen, int n_pen,
+                                             const uint64_t* sorted_raw, int n_raw, float lse, int id_off, int tid) {
+  static_assert(STRATA_SHARD_RECORD_BYTES >= REC_RAW + STRATA_MAX_TOP_N * 8, "record layout");
+  const uint32_t off = static_cast<uint32_t>(id_off);
+  if (tid == 0)
+    *reinterpret_cast<uint4*>(rec) = make_uint4(static_cast<uint32_t>(n_pen), static_cast<uint32_t>(n_raw),
+                                                __float_as_uint(lse), 0u);
+  if (tid < n_pen) {
+    const uint4 e = sorted_pen[tid];
+    *reinterpret_cast<uint4*>(rec + REC_PEN + 16 * tid) = make_uint4(e.x - off, e.y, e.z, 0u);
+  } else if (tid >= KMAX && tid - KMAX < n_raw) {
+    const uint64_t k = sorted_raw[tid - KMAX];
+    *reinterpret_cast<uint2*>(rec + REC_RAW + 8 * (tid - KMAX)) =
+        make_uint2(static_cast<uint32_t>(k) - off, static_cast<uint32_t>(k >> 32));
+  }
 }
 
 // Entries CTA c stored in list `w` (0: penalised, 1: raw) of the leader, clamped to its slice.
@@ -990,7 +1141,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   // arrival and reads the counter from the returned value, and the row that completes the slot's
   // arrivals also advances the counter and clears them.  Every row of the call sees the value
   // from before the call.  The leader's warp 0 issues it once the candidates are in.
-  const bool ctr_warp = k_row > 0 && wid == 0 && crank == 0 && sampled;
+  const bool ctr_warp = k_row > 0 && wid == 0 && crank == 0 && sampled && P.rec == nullptr;
   const bool ctr_thread = ctr_warp && lane == 0;
   unsigned long long ctr_old = 0ull;
   int rs_pre[2] = {-1, -1};  // row slots of the call, fetched ahead for the count of the slot's rows
@@ -1011,7 +1162,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 #pragma unroll
   for (int j = 0; j < HPRE; ++j) {
     const int i = tid + j * NT;
-    hid[j] = (penal && i < h_len) ? hb[(h_start + static_cast<uint32_t>(i)) & h_mask] : -1;
+    hid[j] = (penal && i < h_len) ? slice_id(hb[(h_start + static_cast<uint32_t>(i)) & h_mask], P.id_off) : -1;
   }
 
   // ---- 1b. first pass as pieces land ----------------------------------------------------------
@@ -1112,16 +1263,28 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
 #pragma unroll
     for (int j = 0; j < HPRE; ++j) add_hist(hid[j], true, hval[j]);
     for (int i = tid + (kept_hist ? 0 : HPRE * NT); i < h_len; i += NT)
-      add_hist(hb[(h_start + static_cast<uint32_t>(i)) & h_mask], false, 0.0f);
+      add_hist(slice_id(hb[(h_start + static_cast<uint32_t>(i)) & h_mask], P.id_off), false, 0.0f);
   }
   __syncthreads();  // history table and owner flags complete
 
-  // ---- 2. this CTA's record: the qw largest thread maxima of each warp (ids without a penalty)
-  // and the (max, sum) pairs.  The candidate test key covers every id of the thread; a threshold
-  // key must be the value of an id without a penalty, so a thread that owns a history id
-  // publishes nothing (a valid, very slightly weaker bound).
+  // ---- 2. this CTA's record: the qw largest thread maxima of each warp and the (max, sum) pairs.
+  // The candidate test key covers every id of the thread.  A threshold key must be a value that
+  // both the raw and the penalised value of one id reach: a thread that owns no history id
+  // publishes its maximum; one that owns some publishes nothing (a slightly weaker bound), unless
+  // its warp has fewer than qw threads without history ids (long windows spread over the row),
+  // in which case it publishes the best min(raw, penalised) over the batch that holds its maximum.
   const uint32_t kall = tid < n_vec ? order_key(mx) : 0u;
-  const uint32_t kthr = (penal && ((hflag[tid >> 5] >> (tid & 31)) & 1u)) ? 0u : kall;
+  uint32_t kthr = kall;
+  if (penal) {
+    const bool flagged = (hflag[tid >> 5] >> (tid & 31)) & 1u;
+    const uint32_t plain = __ballot_sync(FULL_MASK, !flagged);
+    if (flagged) kthr = 0u;
+    if (flagged && kall != 0u && __popc(plain) < P.qw) {
+      constexpr int RB = BATCH_VECS<DT>;
+      const int vb = (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid;
+      kthr = batch_safe_key<DT>(gchunk, vb, n_vec, n_el, htab, P.hash_bits, sp.rep, sp.freq, sp.pres);
+    }
+  }
   {
     uint32_t kk = kthr;
 #pragma unroll 1
@@ -1333,15 +1496,15 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
         np = masked_rounds<DT>(gchunk, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + tid + APRE * NT,
                                a_end, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, red64, cand_pen);
       else
-        np = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
-                              red64, cand_pen, cand_raw);
+        np = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, hflag, sp.rep, sp.freq,
+                              sp.pres, red64, cand_pen, cand_raw);
     } else if (k_row > 0 && np > RANK_LIMIT) {
       np = buffer_rounds(reinterpret_cast<uint32_t*>(cand_pen), 4, np, k_row, reinterpret_cast<uint32_t*>(sorted_pen),
                          red64);
     }
     if (n_row > 0 && nr > cap)
-      nr = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres,
-                            red64, cand_pen, cand_raw);
+      nr = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, hflag, sp.rep, sp.freq,
+                            sp.pres, red64, cand_pen, cand_raw);
     else if (n_row > 0 && nr > RANK_LIMIT)
       nr = buffer_rounds(reinterpret_cast<uint32_t*>(cand_raw), 2, nr, n_row, reinterpret_cast<uint32_t*>(sorted_raw),
                          red64);
@@ -1430,10 +1593,8 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   }
 
   // state of the tail (leader, warp 0)
-  int k_eff = 0, n_eff = 0, m1 = 0, m2 = 0;
-  float Ca = 0.0f, Cb = 0.0f, wa = 0.0f, wb = 0.0f;  // tempered weights and their fp32 prefix sums
-  uint4 ea = make_uint4(0, 0, 0, 0), eb = make_uint4(0, 0, 0, 0);
-  float va = 0.0f, vb = 0.0f;
+  int k_eff = 0, n_eff = 0;
+  Tail tl = {};
 
   // ---- 4. the leader ranks the received keys exactly -------------------------------------------
   if (crank == 0 && (P.flags & STRATA_FLAG_TEST_STALL)) test_stall(&mbar[BAR_STALL], ctl, P.err);
@@ -1529,59 +1690,16 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     k_eff = min(k_row, tot_p);
     n_eff = min(n_row, tot_r);
 
-    // the tail's first half on <= 64 survivors (one warp): min_p and top_p cuts and the
-    // tempered cumulative weights; nothing here depends on the draw counter
-    if (P.mode == MODE_SAMPLE && wid == 0 && valid && k_eff > 0) {
-      ea = (lane < k_eff) ? sorted_pen[lane] : make_uint4(0, 0, 0, 0);
-      eb = (lane + 32 < k_eff) ? sorted_pen[lane + 32] : make_uint4(0, 0, 0, 0);
-      va = key_value(ea.y);
-      vb = key_value(eb.y);
-      m1 = m2 = 1;
-      if (sampled) {
-        const float v0 = __shfl_sync(FULL_MASK, va, 0);
-        m1 = k_eff;
-        if (sp.min_p > 0.0f) {  // min_p in logit space, float32
-          const float thr = __fadd_rn(v0, sp.logminp);
-          const uint32_t ba = __ballot_sync(FULL_MASK, lane < k_eff && va >= thr);
-          const uint32_t bb = __ballot_sync(FULL_MASK, lane + 32 < k_eff && vb >= thr);
-          m1 = max(1, __popc(ba) + __popc(bb));
-        }
-        // temperature-1 mass (top_p) and tempered weights (draw) over the min_p survivors.
-        // Prefix sums in fp32 decide unless a decision lies within 1e-5 of its boundary (the fp32
-        // scan is good to ~4e-7 relative); then double-word sums (TwoSum) decide.
-        const bool ina = lane < m1, inb = lane + 32 < m1;
-        // lanes outside the survivors divide a plain zero (a NaN or an infinity would take the
-        // division's slow path)
-        const float da = ina ? __fsub_rn(va, v0) : 0.0f, db = inb ? __fsub_rn(vb, v0) : 0.0f;
-        const float Tm = sp.temperature;
-        const float qa = ina ? expf(da) : 0.0f, qb = inb ? expf(db) : 0.0f;
-        wa = ina ? expf(__fdiv_rn(da, Tm)) : 0.0f;
-        wb = inb ? expf(__fdiv_rn(db, Tm)) : 0.0f;
-        const float ca = warp_scan_f(qa, lane);
-        Ca = warp_scan_f(wa, lane);
-        const float cb = warp_scan_f(qb, lane) + __shfl_sync(FULL_MASK, ca, 31);
-        Cb = warp_scan_f(wb, lane) + __shfl_sync(FULL_MASK, Ca, 31);
-        m2 = m1;
-        if (!(sp.top_p >= 1.0f)) {
-          if (!(sp.top_p > 0.0f)) {
-            m2 = 1;
-          } else {
-            const float tot_q = __shfl_sync(FULL_MASK, cb, 31);
-            const float target = sp.top_p * tot_q, margin = 1e-5f * tot_q;
-            const bool near = __any_sync(FULL_MASK, (ina && fabsf(ca - target) <= margin) ||
-                                                        (inb && fabsf(cb - target) <= margin));
-            if (!near) {
-              const uint32_t la = __ballot_sync(FULL_MASK, ina && ca < target);
-              const uint32_t lb = __ballot_sync(FULL_MASK, inb && cb < target);
-              m2 = min(m1, __popc(la) + __popc(lb) + 1);
-            } else {
-              m2 = top_p_dw(qa, qb, ina, inb, sp.top_p, m1, lane);
-            }
-          }
-        }
-      }
-    }
+    // the tail's first half on <= 64 survivors (one warp); a vocabulary slice reports its lists
+    // instead
+    if (P.mode == MODE_SAMPLE && wid == 0 && valid && k_eff > 0 && P.rec == nullptr)
+      tail_cuts(sorted_pen, k_eff, sampled, sp, lane, tl);
   }
+
+  // a vocabulary slice: the row's record (its lists with whole-row ids, and its log-sum-exp)
+  if (P.rec != nullptr && crank == 0)
+    write_record(P.rec + static_cast<size_t>(row) * STRATA_SHARD_RECORD_BYTES, sorted_pen, k_eff, sorted_raw, n_eff,
+                 lse, P.id_off, tid);
 
   // ---- outputs (leader only): with early loads the previous kernel owns outputs and counters
   // until it ends, unless this call has its own outputs (its counter was taken at the start) -----
@@ -1641,7 +1759,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       }
     }
     // the tail's second half: Philox(seed, position) at the slot's counter, the pick, the outputs
-    if (P.mode == MODE_SAMPLE && wid == 0) {
+    if (P.mode == MODE_SAMPLE && wid == 0 && P.rec == nullptr) {
       int out = -1;
       float chosen_raw = __int_as_float(0x7FC00000);
       if (!valid) {
@@ -1656,31 +1774,16 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
           uint32_t x0 = 0u;
           if (ctr_thread) x0 = philox_word0(sp.seed, pos, ctr_old >> 16);
           if (!own_out) slot_arrival_done(r_slot, slot, P.ctr, ctr_old, lane);
-          x0 = __shfl_sync(FULL_MASK, x0, 0);
-          const float u = static_cast<float>(x0 >> 8) * 0x1p-24f;
-          const int last = m2 - 1;  // the draw reads prefixes below m2 only; W = C[m2 - 1]
-          const float W = (last < 32) ? __shfl_sync(FULL_MASK, Ca, last) : __shfl_sync(FULL_MASK, Cb, last - 32);
-          const float tgt = u * W, margin = 1e-5f * W;
-          const bool ia = lane < m2, ib = lane + 32 < m2;
-          const bool near = __any_sync(FULL_MASK, (ia && fabsf(Ca - tgt) <= margin) || (ib && fabsf(Cb - tgt) <= margin));
-          if (!near) {
-            const uint32_t ja = __ballot_sync(FULL_MASK, ia && Ca <= tgt);
-            const uint32_t jb = __ballot_sync(FULL_MASK, ib && Cb <= tgt);
-            j = min(__popc(ja) + __popc(jb), m2 - 1);
-          } else {
-            j = draw_dw(wa, wb, m2, u, lane);
-          }
+          j = tail_draw(tl, __shfl_sync(FULL_MASK, x0, 0), lane);
         }
-        const uint32_t id_a = key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x);
-        const uint32_t id_b = key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x);
-        out = static_cast<int>(__shfl_sync(FULL_MASK, j < 32 ? id_a : id_b, j & 31));
-        chosen_raw = __uint_as_float(__shfl_sync(FULL_MASK, j < 32 ? ea.z : eb.z, j & 31));  // raw logit of the pick
+        out = static_cast<int>(tail_id(tl, j));
+        chosen_raw = tail_raw(tl, j);  // raw logit of the pick
       }
       if (lane == 0) {
         P.out_ids[row] = out;
         if (P.kept != nullptr) {
-          P.kept[2 * row] = m1;
-          P.kept[2 * row + 1] = m2;
+          P.kept[2 * row] = tl.m1;
+          P.kept[2 * row + 1] = tl.m2;
         }
         if (P.chosen_lp != nullptr) P.chosen_lp[row] = (out >= 0) ? chosen_raw - lse : __int_as_float(0x7FC00000);
       }
@@ -1689,15 +1792,15 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
       if (P.topk_ids != nullptr) {
         const long long o = static_cast<long long>(row) * KMAX;
         const bool ia = valid && lane < k_eff, ib = valid && lane + 32 < k_eff;
-        P.topk_ids[o + lane] = ia ? static_cast<int32_t>(key_id((static_cast<uint64_t>(ea.y) << 32) | ea.x)) : -1;
-        P.topk_ids[o + lane + 32] = ib ? static_cast<int32_t>(key_id((static_cast<uint64_t>(eb.y) << 32) | eb.x)) : -1;
+        P.topk_ids[o + lane] = ia ? static_cast<int32_t>(key_id((static_cast<uint64_t>(tl.ea.y) << 32) | tl.ea.x)) : -1;
+        P.topk_ids[o + lane + 32] = ib ? static_cast<int32_t>(key_id((static_cast<uint64_t>(tl.eb.y) << 32) | tl.eb.x)) : -1;
         if (P.topk_vals != nullptr) {
-          P.topk_vals[o + lane] = ia ? va : __int_as_float(0x7FC00000);
-          P.topk_vals[o + lane + 32] = ib ? vb : __int_as_float(0x7FC00000);
+          P.topk_vals[o + lane] = ia ? tl.va : __int_as_float(0x7FC00000);
+          P.topk_vals[o + lane + 32] = ib ? tl.vb : __int_as_float(0x7FC00000);
         }
       }
     }
-  } else if (kp == 0 && P.mode == MODE_SAMPLE && crank == 0 && tid == 0) {
+  } else if (kp == 0 && P.mode == MODE_SAMPLE && crank == 0 && tid == 0 && P.rec == nullptr) {
     // no selection in this row: only an out-of-range slot gets here
     P.out_ids[row] = -1;
     if (P.kept != nullptr) {

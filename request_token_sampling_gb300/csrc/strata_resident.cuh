@@ -174,6 +174,29 @@ __device__ __forceinline__ void res_pass_piece(const unsigned char* data, int p,
   }
 }
 
+// A threshold key for a thread that owns history ids: the largest order key of min(raw,
+// penalised) over its elements (vectors tid, tid + NT, ... of the resident chunk).  Both the raw
+// and the penalised value of that id reach it.  The history table is looked up only for elements
+// that could raise the key.
+template <int DT>
+__device__ __noinline__ uint32_t res_safe_key(const unsigned char* data, int n_vec, int n_el, const uint32_t* htab,
+                                              int hash_bits, float rep, float freq, float pres) {
+  constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
+  uint32_t best = 0u;
+  for (int v = threadIdx.x; v < n_vec; v += NT) {
+    float x[EPV];
+    load_vec<DT>(data, v, x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const uint32_t loc = static_cast<uint32_t>(v * EPV + e);
+      if (loc >= static_cast<uint32_t>(n_el) || order_key(x[e]) <= best) continue;
+      const uint32_t c = hash_count(htab, hash_bits, loc);
+      best = max(best, order_key(c != 0u ? fminf(x[e], penalize(x[e], c, rep, freq, pres)) : x[e]));
+    }
+  }
+  return best;
+}
+
 // Exact argmax rounds over the resident chunk: the `need` largest keys in order (list 0: penalised
 // values, with their raw logits, into cand_pen; list 1: raw values into cand_raw).  Only taken when
 // more candidates reach the threshold than the candidate buffer holds (very long runs of ties); out
@@ -564,7 +587,15 @@ __global__ void __launch_bounds__(NT, 3) res_kernel(const KParams P) {
   const uint32_t kall = tid < n_vec ? order_key(mx) : 0u;
   __syncthreads();  // the history table and its owner flags are complete
   const bool own_hist = penal && ((hflag[tid >> 5] >> (tid & 31)) & 1u);
-  const uint32_t kthr = own_hist ? 0u : kall;  // a threshold key must carry no penalty
+  // a threshold key must be a value that both the raw and the penalised value of one id reach: a
+  // thread that owns a history id publishes nothing, unless its warp has fewer than qw threads
+  // without one; then it publishes the best min(raw, penalised) over its elements
+  uint32_t kthr = own_hist ? 0u : kall;
+  if (penal) {
+    const uint32_t plain = __ballot_sync(FULL_MASK, !own_hist);
+    if (own_hist && kall != 0u && __popc(plain) < P.qw)
+      kthr = res_safe_key<DT>(data, n_vec, n_el, htab, P.hash_bits, sp.rep, sp.freq, sp.pres);
+  }
   {
     uint32_t kk = kthr;
 #pragma unroll 1

@@ -21,6 +21,7 @@
 
 #include "../../include/strata_sample.h"
 #include "strata_kernel.cuh"
+#include "strata_merge.cuh"
 #include "strata_resident.cuh"
 
 using strata::KParams;
@@ -307,15 +308,13 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
   // latter wait for the previous call before their penalties): they take the latency split
   const bool pipelined = (flags & STRATA_FLAG_PDL) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u &&
                          (flags & STRATA_FLAG_HISTORY_RING) == 0u && !verify;
-  // the concurrency hint: a plain call's block streams up to STRATA_CONCURRENT_ROW_BYTES; a verify
-  // window waits for the previous window, so its latency stays on its group's chain and it takes
-  // half that; a call that keeps histories waits for the previous call before its penalties and
-  // takes PIPELINED_BYTES (measured at 8 groups: these were the fastest of the splits tried)
+  // the concurrency hint: a block streams up to STRATA_CONCURRENT_ROW_BYTES; a call that keeps
+  // histories waits for the previous call before its penalties and takes PIPELINED_BYTES (measured
+  // with 8 groups in flight: these were the fastest of the splits tried)
   int concurrent_bytes = 0;
   if ((flags & STRATA_FLAG_CONCURRENT) != 0u)
     concurrent_bytes = (flags & STRATA_FLAG_HISTORY_RING) != 0u ? PIPELINED_BYTES
-                       : verify ? static_cast<int>(STRATA_CONCURRENT_ROW_BYTES / 2)
-                                : static_cast<int>(STRATA_CONCURRENT_ROW_BYTES);
+                                                                : static_cast<int>(STRATA_CONCURRENT_ROW_BYTES);
   return shape_for(c->max_cluster, c->max_smem, c->smem_three, c->num_sms, mode, esz, B, V, kmax, top_n_eff,
                    max_lastn_penal(c),
                    with_hist, with_allowed, mask, pipelined, concurrent_bytes,
@@ -840,6 +839,108 @@ int strata_logprobs_rows(strata_ctx* c, const void* logits, int dtype, int B, in
   rc = launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream), "logprobs_rows");
   if (rc == STRATA_OK) c->late_counters_pending = pending_after(c->late_counters_pending, flags, false);
   return rc;
+}
+
+int strata_shard_rows(strata_ctx* c, const void* logits, int dtype, int B, int V_shard, int64_t ld, int id_offset,
+                      const int32_t* row_slot, const int32_t* hist, const int32_t* hist_off, int n_hist_slots,
+                      int top_n, void* records, uint32_t flags, void* stream) {
+  int rc = check_rows_common(c, logits, dtype, B, V_shard, ld, top_n, nullptr, nullptr, nullptr, nullptr, nullptr,
+                             nullptr);
+  if (rc != STRATA_OK) return rc;
+  if (id_offset < 0 || static_cast<long long>(id_offset) + V_shard > 0x7FFFFFFFLL)
+    return fail(STRATA_EINVAL, "id_offset=%d with V_shard=%d outside the int32 id range", id_offset, V_shard);
+  if (B > 0 && (row_slot == nullptr || records == nullptr)) return fail(STRATA_EINVAL, "row_slot and records are required");
+  if ((reinterpret_cast<uintptr_t>(records) & 15u) != 0) return fail(STRATA_EALIGN, "records not 16-byte aligned");
+  if ((flags & ~(STRATA_FLAG_CONCURRENT | STRATA_FLAG_SPLIT(31))) != 0u)
+    return fail(STRATA_EINVAL, "flags 0x%x: a slice call takes only STRATA_FLAG_CONCURRENT and STRATA_FLAG_SPLIT", flags);
+  if (hist_off != nullptr && (hist == nullptr || n_hist_slots < 1))
+    return fail(STRATA_EINVAL, "hist_off needs hist and n_hist_slots >= 1");
+  if (hist_off == nullptr) n_hist_slots = 0;
+  if ((rc = check_device(c)) != STRATA_OK) return rc;
+  if (B == 0) return STRATA_OK;
+  Shape sh;
+  if ((rc = compute_shape(c, strata::MODE_SAMPLE, dtype, B, V_shard, top_n, hist_off != nullptr, false, flags, &sh)) !=
+      STRATA_OK)
+    return rc;
+  KParams P{};
+  P.logits = logits;
+  P.ld = ld;
+  P.B = B;
+  P.V = V_shard;
+  P.cs = sh.cs;
+  P.chunk = sh.chunk;
+  P.mode = strata::MODE_SAMPLE;
+  P.row_slot = row_slot;
+  P.hist = hist;
+  P.hist_off = hist_off;
+  P.n_hist_slots = n_hist_slots;
+  P.top_n = top_n;
+  P.nmax = sh.nmax;
+  P.kmax = sh.kmax;
+  P.slots = c->d_slots;
+  P.ctr = c->d_ctr;
+  P.max_slots = c->max_slots;
+  P.err = c->d_err;
+  P.hash_cap = sh.hash_cap;
+  P.hash_bits = sh.hash_bits;
+  P.nslot = sh.nslot;
+  P.qw = sh.qw;
+  P.flags = flags;
+  P.id_off = id_offset;
+  P.rec = static_cast<unsigned char*>(records);
+  rc = launch(c, P, dtype, sh, flags, static_cast<cudaStream_t>(stream), "shard_rows");
+  if (rc == STRATA_OK) c->late_counters_pending = pending_after(c->late_counters_pending, flags, false);
+  return rc;
+}
+
+int strata_merge_shards(strata_ctx* c, const void* records, int n_shards, int B, const int32_t* row_slot,
+                        const int64_t* row_pos, int32_t* out_ids, int top_n, float* chosen_lp, int32_t* top_ids,
+                        float* top_lps, int32_t* topk_ids, float* topk_vals, int32_t* kept, uint32_t flags,
+                        void* stream) {
+  if (c == nullptr) return fail(STRATA_EINVAL, "null context");
+  if (n_shards < 1 || n_shards > STRATA_MAX_SHARDS)
+    return fail(STRATA_EINVAL, "n_shards=%d outside 1..%d", n_shards, STRATA_MAX_SHARDS);
+  if (B < 0) return fail(STRATA_EINVAL, "B=%d", B);
+  if (B > c->max_rows) return fail(STRATA_ERANGE, "B=%d above max_rows %d", B, c->max_rows);
+  if (top_n < 0 || top_n > STRATA_MAX_TOP_N) return fail(STRATA_EINVAL, "top_n=%d outside 0..%d", top_n, STRATA_MAX_TOP_N);
+  if (top_n > 0 && ((top_ids == nullptr) != (top_lps == nullptr)))
+    return fail(STRATA_EINVAL, "top_ids and top_lps must be given together");
+  if (B > 0 && (records == nullptr || row_slot == nullptr || row_pos == nullptr || out_ids == nullptr))
+    return fail(STRATA_EINVAL, "records, row_slot, row_pos and out_ids are required");
+  if ((reinterpret_cast<uintptr_t>(records) & 15u) != 0) return fail(STRATA_EALIGN, "records not 16-byte aligned");
+  if (flags != 0u) return fail(STRATA_EINVAL, "flags 0x%x: the merge takes none", flags);
+  int rc;
+  if ((rc = check_device(c)) != STRATA_OK) return rc;
+  if (B == 0) return STRATA_OK;
+  strata::MParams M{};
+  M.rec = static_cast<const unsigned char*>(records);
+  M.G = n_shards;
+  M.B = B;
+  M.top_n = top_n;
+  M.row_slot = row_slot;
+  M.row_pos = reinterpret_cast<const long long*>(row_pos);
+  M.out_ids = out_ids;
+  M.chosen_lp = chosen_lp;
+  M.top_ids = top_n > 0 ? top_ids : nullptr;
+  M.top_lps = top_n > 0 ? top_lps : nullptr;
+  M.topk_ids = topk_ids;
+  M.topk_vals = topk_vals;
+  M.kept = kept;
+  M.slots = c->d_slots;
+  M.ctr = c->d_ctr;
+  M.max_slots = c->max_slots;
+  M.err = c->d_err;
+  if (trace_on())
+    std::fprintf(stderr, "strata: merge_shards B=%d shards=%d top_n=%d grid=%d block=%d\n", B, n_shards, top_n, B,
+                 strata::MT);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+  cfg.blockDim = dim3(strata::MT, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, strata::merge_kernel, M);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  c->late_counters_pending = pending_after(c->late_counters_pending, 0u, true);
+  return STRATA_OK;
 }
 
 }  // extern "C"

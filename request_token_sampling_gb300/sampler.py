@@ -114,3 +114,40 @@ class Sampler:
                                allowed_off=allowed_off, allowed_lps=o.get("allowed_lps"), flags=flags,
                                stream=stream)
         return o
+
+    def shard(self, logits, row_slot, id_offset: int, V=None, hist=None, hist_off=None, top_n: int = 0,
+              flags: int = 0, stream=None, out=None):
+        """One vocabulary slice of the rows (its columns hold ids id_offset ..): the rows' records,
+        a [B, STRATA_SHARD_RECORD_BYTES] uint8 tensor."""
+        import torch
+        rows = logits.shape[0]
+        rec = out if out is not None else torch.empty(rows, B.STRATA_SHARD_RECORD_BYTES, dtype=torch.uint8,
+                                                      device=logits.device)
+        B.strata_shard_rows(self.ctx, logits, row_slot, rec, id_offset, V=V, hist=hist, hist_off=hist_off,
+                            top_n=top_n, flags=flags, stream=stream)
+        return rec
+
+    def merge(self, records, row_slot, row_pos, top_n: int = 0, chosen_lp: bool = False, debug: bool = False,
+              stream=None, out=None) -> dict:
+        """Merge every slice's records ([n_shards, B, STRATA_SHARD_RECORD_BYTES] uint8): the same
+        outputs as `sample` on the whole rows."""
+        import torch
+        rows = records.shape[1]
+        dev = records.device
+        o = out if out is not None else {}
+        if "ids" not in o:
+            o["ids"] = torch.empty(rows, dtype=torch.int32, device=dev)
+        if chosen_lp and "chosen_lp" not in o:
+            o["chosen_lp"] = torch.empty(rows, dtype=torch.float32, device=dev)
+        if top_n > 0 and "top_ids" not in o:
+            o["top_ids"] = torch.empty(rows, top_n, dtype=torch.int32, device=dev)
+            o["top_lps"] = torch.empty(rows, top_n, dtype=torch.float32, device=dev)
+        if debug and "topk_ids" not in o:
+            o["topk_ids"] = torch.empty(rows, 64, dtype=torch.int32, device=dev)
+            o["topk_vals"] = torch.empty(rows, 64, dtype=torch.float32, device=dev)
+            o["kept"] = torch.empty(rows, 2, dtype=torch.int32, device=dev)
+        B.strata_merge_shards(self.ctx, records, row_slot, row_pos, o["ids"], top_n=top_n,
+                              chosen_lp=o.get("chosen_lp"), top_ids=o.get("top_ids"), top_lps=o.get("top_lps"),
+                              topk_ids=o.get("topk_ids"), topk_vals=o.get("topk_vals"), kept=o.get("kept"),
+                              stream=stream)
+        return o

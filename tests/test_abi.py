@@ -96,7 +96,18 @@ def test_null_arguments_rejected_without_cuda(S):
     assert S.lib.strata_history_enable(None) == S.STRATA_EINVAL
     assert S.lib.strata_history_set(None, 0, None, 0, None) == S.STRATA_EINVAL
     assert S.lib.strata_history_get(None, 0, None, 0, None, None, None) == S.STRATA_EINVAL
+    assert S.lib.strata_shard_rows(None, None, 0, 1, 10, 10, 0, None, None, None, 0, 0, None, 0, None) == S.STRATA_EINVAL
+    assert S.lib.strata_merge_shards(None, None, 1, 1, None, None, None, 0, None, None, None, None, None, None, 0,
+                                     None) == S.STRATA_EINVAL
     S.lib.strata_destroy(None)
+
+
+def test_record_layout_constants(S):
+    """A slice record holds the header, 64 penalised entries of 16 bytes and 20 raw keys of 8."""
+    from request_token_sampling_gb300 import sharded
+    assert sharded.REC_RAW + 8 * S.STRATA_MAX_TOP_N <= S.STRATA_SHARD_RECORD_BYTES
+    assert sharded.REC_PEN == 16 and sharded.REC_RAW == 16 + 16 * S.STRATA_MAX_TOP_K
+    assert S.STRATA_SHARD_RECORD_BYTES % 16 == 0
 
 
 def test_history_capacity_constants(S):

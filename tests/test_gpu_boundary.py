@@ -269,13 +269,15 @@ torch.cuda.synchronize(); print('counter', s.slot_state(0)[1]); s.close()
 
 def test_launch_shape_modes(sampler):
     """The shape query covers the three entry points (0 sampling, 1 logprobs, 2 verify windows) and
-    refuses any other mode; the concurrency hint gives sampling rows one CTA and verify rows two.
+    refuses any other mode; the concurrency hint gives a full fp32 row two CTAs (512 KiB each) and
+    a bf16 row one.
     Resident chunks (STRATA_FLAG_RESIDENT) hold at most 64 KiB of logits: a full fp32 row takes 16
     blocks, a bf16 row 8 under the concurrency hint."""
     import request_token_sampling_gb300 as S
     fl = S.STRATA_FLAG_PDL | S.STRATA_FLAG_EARLY_LOAD | S.STRATA_FLAG_CONCURRENT
-    assert sampler.shape(0, 0, 8, synth.V_FULL, 20, fl)["split"] == 1
-    assert sampler.shape(1, 0, 8, synth.V_FULL, 20, fl)["split"] == 1
+    assert sampler.shape(0, 0, 8, synth.V_FULL, 20, fl)["split"] == 2
+    assert sampler.shape(0, 1, 8, synth.V_FULL, 20, fl)["split"] == 1
+    assert sampler.shape(1, 0, 8, synth.V_FULL, 20, fl)["split"] == 2
     assert sampler.shape(2, 0, 5, synth.V_FULL, 0, fl)["split"] == 2
     assert sampler.shape(2, 0, 5, synth.V_FULL, 0, fl | S.STRATA_FLAG_HISTORY_RING)["split"] == 8
     rs = fl | S.STRATA_FLAG_RESIDENT

@@ -29,10 +29,10 @@ def _mask_flag():
     return STRATA_FLAG_ALLOWED_MASK
 
 
-@pytest.mark.parametrize("concurrent", [0, 1, 2], ids=["default-shape", "one-cta-per-row", "resident-chunks"])
+@pytest.mark.parametrize("concurrent", [0, 1, 2], ids=["default-shape", "concurrency-hint", "resident-chunks"])
 def test_mask_config4_fused(sampler, concurrent):
     """Config 4's rows with their 5/100/1000-id lists used as masks (also with the concurrency hint:
-    one CTA per row, both id bitmaps as long as the row)."""
+    two CTAs per row, both id bitmaps as long as a half row)."""
     w = synth.config4(fused=True)
     set_slots(sampler, w)
     g = gpu_sample(sampler, w, flags=_mask_flag() | shape_hint(concurrent))
