@@ -1035,7 +1035,7 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   auto load_meta1 = [&]() {
     if (P.mode == MODE_SAMPLE) {
       slot = P.row_slot[row];
-      pos = static_cast<unsigned long long>(P.row_pos[row]);
+      if (P.row_pos != nullptr) pos = static_cast<unsigned long long>(P.row_pos[row]);  // none for a slice
     } else if (P.chosen != nullptr) {
       chosen_id = P.chosen[row];
     }
