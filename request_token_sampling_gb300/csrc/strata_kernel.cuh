@@ -601,6 +601,28 @@ __device__ __noinline__ uint32_t batch_safe_key(const unsigned char* gchunk, int
   return best;
 }
 
+// Published keys above `u` in records c = sub, sub + lpk, ... < cs of the record exchange (Q4 uint4
+// of keys each, record stride 4 * Q4 + 4 words), counted in four independent sums.  The record
+// length is a template constant, so the inner loop is fully unrolled: a runtime trip count there
+// cost several times the loads it makes.
+template <int Q4>
+__device__ __forceinline__ int count_above_recs(const uint32_t* xrec, int sub, int lpk, int cs, uint32_t u) {
+  int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll 1
+  for (int c = sub; c < cs; c += lpk) {
+    const uint4* rk = reinterpret_cast<const uint4*>(xrec + c * (4 * Q4 + 4));
+#pragma unroll
+    for (int j = 0; j < Q4; ++j) {
+      const uint4 v = rk[j];
+      a0 += v.x > u;
+      a1 += v.y > u;
+      a2 += v.z > u;
+      a3 += v.w > u;
+    }
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
 // Exact argmax rounds over this CTA's chunk: the `need` largest keys in order (penalised values
 // for list 0, raw values for list 1), written to the candidate buffer.  Only taken when more
 // candidates reach the row threshold than the buffer holds (heavy ties); kept out of line so the
@@ -984,9 +1006,11 @@ __device__ __noinline__ void slot_window_done(const int32_t* row_slot, const int
 // ------------------------------------------------------------------------------ the kernel
 // DT: 0 fp32 rows, 1 bf16 rows.  MASK: allowed ids restrict the sampling (STRATA_FLAG_ALLOWED_MASK);
 // OWN: a call with own outputs and early loads (STRATA_FLAG_OWN_OUTPUTS).  Separate instantiations
-// so that plain launches carry none of their state or code.
-template <int DT, bool MASK, bool OWN = false>
-__global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
+// so that plain launches carry none of their state or code.  MINB: blocks per SM the registers
+// are budgeted for: 3 (80 registers, some spilled to local memory) where many blocks stream at
+// once, 2 (no spills) for the latency shape, whose few blocks each walk the whole serial chain.
+template <int DT, bool MASK, bool OWN = false, int MINB = 3>
+__global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char sm[];
   constexpr int ESZ = DT == 0 ? 4 : 2;
   constexpr int EPV = 16 / ESZ;
@@ -1366,23 +1390,17 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     for (int base = 0; base < nk * lpk; base += NT) {
       const int i = (base + tid) >> llog;
       uint32_t u = 0xFFFFFFFFu;
-      int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+      int above = 0;
       if (i < nk) {
         u = xrec[(i >> qlog) * XW + (i & (Q - 1))];
-#pragma unroll 1
-        for (int c = sub; c < cs; c += lpk) {
-          const uint4* rk = reinterpret_cast<const uint4*>(xrec + c * XW);
-#pragma unroll 4
-          for (int j = 0; j < (Q >> 2); ++j) {
-            const uint4 v = rk[j];
-            a0 += v.x > u;
-            a1 += v.y > u;
-            a2 += v.z > u;
-            a3 += v.w > u;
-          }
+        switch (P.qw) {  // the record length as a constant: the inner loop fully unrolled
+          case 1: above = count_above_recs<2>(xrec, sub, lpk, cs, u); break;
+          case 2: above = count_above_recs<4>(xrec, sub, lpk, cs, u); break;
+          case 4: above = count_above_recs<8>(xrec, sub, lpk, cs, u); break;
+          case 8: above = count_above_recs<16>(xrec, sub, lpk, cs, u); break;
+          default: above = count_above_recs<32>(xrec, sub, lpk, cs, u); break;
         }
       }
-      int above = (a0 + a1) + (a2 + a3);
       for (int off = 1; off < lpk; off <<= 1) above += __shfl_xor_sync(FULL_MASK, above, off);
       const uint32_t cand = (i < nk && sub == 0 && above < kp) ? u : 0xFFFFFFFFu;
       const uint32_t wmin = __reduce_min_sync(FULL_MASK, cand);
@@ -1601,8 +1619,6 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
   if (kp > 0 && crank == 0) {
     if (cs > 1) wait_bar(&mbar[BAR_X1], ctl, P.err, true);
     if (ctr_warp && !own_out) r_slot = slot_rows(rs_pre[0], rs_pre[1], P.row_slot, P.B, slot, lane);
-    // issued here, consumed by the draw: the merge and the tail's first half hide the latency
-    if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], r_slot == 1 ? (1ull << 16) : 1ull);
     __syncthreads();  // every slice (the leader's own included) is in place
     // slice offsets (every copying warp scans the counts itself), then warp c copies slice c into
     // the dense lists (the candidate buffers, free by now)
@@ -1689,6 +1705,9 @@ __global__ void __launch_bounds__(NT, 3) rows_kernel(const KParams P) {
     __syncthreads();
     k_eff = min(k_row, tot_p);
     n_eff = min(n_row, tot_r);
+    // the draw counter: issued after the block's last barrier (a barrier waits for a global atomic
+    // before it to be performed), consumed by the draw, so the tail's first half hides its latency
+    if (!early && ctr_thread) ctr_old = atomicAdd(&P.ctr[slot], r_slot == 1 ? (1ull << 16) : 1ull);
 
     // the tail's first half on <= 64 survivors (one warp); a vocabulary slice reports its lists
     // instead

@@ -41,9 +41,10 @@ int fail(int code, const char* fmt, ...) {
 }
 
 // The kernel instance for a launch: streaming or resident chunk x logit type x allowed-id mask x
-// own outputs.
+// own outputs; the streaming kernel's latency shape (`two`: few blocks, no call alongside) takes
+// the instance whose registers are budgeted for two blocks per SM.
 using KernelFn = void (*)(strata::KParams);
-KernelFn kernel_for(int dtype, bool mask, bool own, bool resident = false) {
+KernelFn kernel_for(int dtype, bool mask, bool own, bool resident = false, bool two = false) {
   static const KernelFn table[2][2][2][2] = {
       {{{strata::rows_kernel<0, false, false>, strata::rows_kernel<0, false, true>},
         {strata::rows_kernel<0, true, false>, strata::rows_kernel<0, true, true>}},
@@ -53,6 +54,10 @@ KernelFn kernel_for(int dtype, bool mask, bool own, bool resident = false) {
         {strata::res_kernel<0, true, false>, strata::res_kernel<0, true, true>}},
        {{strata::res_kernel<1, false, false>, strata::res_kernel<1, false, true>},
         {strata::res_kernel<1, true, false>, strata::res_kernel<1, true, true>}}}};
+  static const KernelFn two_table[2][2] = {
+      {strata::rows_kernel<0, false, false, 2>, strata::rows_kernel<0, true, false, 2>},
+      {strata::rows_kernel<1, false, false, 2>, strata::rows_kernel<1, true, false, 2>}};
+  if (two && !resident && !own) return two_table[dtype == STRATA_DTYPE_F32 ? 0 : 1][mask ? 1 : 0];
   return table[resident ? 1 : 0][dtype == STRATA_DTYPE_F32 ? 0 : 1][mask ? 1 : 0][own ? 1 : 0];
 }
 
@@ -60,9 +65,10 @@ KernelFn kernel_for(int dtype, bool mask, bool own, bool resident = false) {
 // cluster sizes (up to 16 blocks per row).
 cudaError_t set_kernel_attributes(int max_smem) {
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 16 && e == cudaSuccess; ++i) {
+  for (int i = 0; i < 20 && e == cudaSuccess; ++i) {
     const void* k = reinterpret_cast<const void*>(
-        kernel_for(i & 1 ? STRATA_DTYPE_BF16 : STRATA_DTYPE_F32, (i >> 1) & 1, (i >> 2) & 1, (i >> 3) & 1));
+        i < 16 ? kernel_for(i & 1 ? STRATA_DTYPE_BF16 : STRATA_DTYPE_F32, (i >> 1) & 1, (i >> 2) & 1, (i >> 3) & 1)
+               : kernel_for(i & 1 ? STRATA_DTYPE_BF16 : STRATA_DTYPE_F32, (i >> 1) & 1, false, false, true));
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem)) == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }
@@ -192,6 +198,7 @@ bool pending_after(bool pending, uint32_t flags, bool sampling) {
 struct Shape {
   int cs, chunk, smem, kmax, nmax, hash_cap, hash_bits, nslot, qw;
   bool resident;  // the chunk is held whole in shared memory (res_kernel); else it streams
+  bool two;       // the latency shape: the instance with registers for two blocks per SM
 };
 
 // Keys each warp of a resident block publishes for the row's threshold: enough that the row's
@@ -233,6 +240,7 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
   s->hash_cap = 0;
   s->hash_bits = 0;
   s->resident = false;
+  s->two = !concurrent && !pipelined;
   if (mode == strata::MODE_SAMPLE && with_hist && lastn_max > 0) {
     int bits = 6;
     while ((1 << bits) < 2 * lastn_max) ++bits;
@@ -340,7 +348,7 @@ int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t
                  "strata: %s B=%d V=%d dtype=%s flags=0x%x kernel=%s split=%d chunk=%d ring_slots=%d qw=%d hash=%d "
                  "smem=%d grid=%d\n",
                  entry, P.B, P.V, dtype == STRATA_DTYPE_F32 ? "f32" : "bf16", flags,
-                 sh.resident ? "resident" : "streaming", sh.cs, sh.chunk, sh.nslot, sh.qw, sh.hash_cap, sh.smem,
+                 sh.resident ? "resident" : sh.two ? "streaming-2" : "streaming", sh.cs, sh.chunk, sh.nslot, sh.qw, sh.hash_cap, sh.smem,
                  P.B * sh.cs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(P.B * sh.cs), 1, 1);
@@ -364,7 +372,7 @@ int launch(strata_ctx* c, const KParams& P, int dtype, const Shape& sh, uint32_t
   cudaError_t e;
   const bool mask = P.mode == strata::MODE_SAMPLE && (flags & STRATA_FLAG_ALLOWED_MASK) != 0u && P.allowed_off != nullptr;
   const bool own = (flags & STRATA_FLAG_OWN_OUTPUTS) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u;
-  e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, mask, own, sh.resident), P);
+  e = cudaLaunchKernelEx(&cfg, kernel_for(dtype, mask, own, sh.resident, sh.two), P);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   (void)c;
   return STRATA_OK;
