@@ -177,3 +177,29 @@ def test_slice_argument_checks(sampler):
         sampler.merge(recs, d["row_slot"], d["row_pos"])
     assert e.value.code == STRATA_EINVAL
     assert sampler.errors() == 0
+
+
+def test_out_of_range_slot_row(sampler):
+    """A row whose slot is outside the context: its records carry no penalised entries, the merge
+    writes id -1 (NaN chosen lp) and sets STRATA_DEVERR_SLOT; the other rows are exact."""
+    from request_token_sampling_gb300 import STRATA_DEVERR_SLOT
+    w = synth.config4(fused=True)
+    w = dict(w, allowed=None, allowed_off=None, row_slot=w["row_slot"].copy())
+    w["row_slot"][3] = 1000                      # max_slots is 64
+    sampler.errors()                              # clear earlier bits
+    set_slots(sampler, w)
+    d = upload(w)
+    recs = _slice_records(sampler, w, d, _bounds(w["V"], [w["V"] // 2]), w["top_n"])
+    g = _merge(sampler, recs, d, w["top_n"])
+    assert sampler.errors() == STRATA_DEVERR_SLOT
+    assert int(g["ids"][3]) == -1 and np.isnan(g["chosen_lp"][3])
+    rows, _ = oracle.sample_call(w, with_allowed=False)
+    compare_sample(w, rows, g)
+
+
+def test_greedy_rows_with_penalties(sampler):
+    """Greedy rows whose slots carry penalties (the penalised argmax) over four slices."""
+    w = synth.random_case(11, B=6, V=20011, dtype="f32", ld=20016, sampled_frac=0.0, hist_len=40)
+    for s in w["slot_params"]:
+        w["slot_params"][s] = dict(w["slot_params"][s], penalty_repeat=1.7, penalty_freq=0.4, penalty_present=0.3)
+    _run(sampler, w, [5000, 10000, 15000], "greedy penalised slices")
