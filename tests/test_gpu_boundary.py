@@ -225,13 +225,16 @@ def test_trace_lines_on_stderr():
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     code = ("import sys; sys.path.insert(0, %r); import torch, synth; from _harness import gpu_sample, set_slots; "
-            "from request_token_sampling_gb300 import Sampler; w = synth.config1(); s = Sampler(0, 4, w['V'], 4); "
-            "set_slots(s, w); gpu_sample(s, w); s.close()") % os.path.join(root, "tests")
+            "import request_token_sampling_gb300 as S; w = synth.config1(); s = S.Sampler(0, 4, w['V'], 4); "
+            "set_slots(s, w); gpu_sample(s, w); gpu_sample(s, w, flags=S.STRATA_FLAG_CONCURRENT); "
+            "gpu_sample(s, w, flags=S.STRATA_FLAG_PDL | S.STRATA_FLAG_EARLY_LOAD); s.close()") % os.path.join(root, "tests")
     env = dict(os.environ, STRATA_SAMPLE_DEBUG="1")
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stderr.splitlines() if l.startswith("strata: sample_rows")]
-    assert len(lines) == 1 and "V=32000" in lines[0] and "split=" in lines[0] and "smem=" in lines[0], r.stderr[-2000:]
+    assert len(lines) == 3 and "V=32000" in lines[0] and "split=" in lines[0] and "smem=" in lines[0], r.stderr[-2000:]
+    # the latency shape takes the instance budgeted for two blocks per SM; the others three
+    assert [l.split("kernel=")[1].split()[0] for l in lines] == ["streaming-2", "streaming", "streaming"], lines
 
 
 def test_own_outputs_after_a_waiting_call_take_counters_late():
