@@ -1007,8 +1007,9 @@ __device__ __noinline__ void slot_window_done(const int32_t* row_slot, const int
 // DT: 0 fp32 rows, 1 bf16 rows.  MASK: allowed ids restrict the sampling (STRATA_FLAG_ALLOWED_MASK);
 // OWN: a call with own outputs and early loads (STRATA_FLAG_OWN_OUTPUTS).  Separate instantiations
 // so that plain launches carry none of their state or code.  MINB: blocks per SM the registers
-// are budgeted for: 3 (80 registers, some spilled to local memory) where many blocks stream at
-// once, 2 (no spills) for the latency shape, whose few blocks each walk the whole serial chain.
+// are budgeted for: 3 (80 registers, some spilled to local memory) where calls of independent
+// groups stream at once, 2 (no spills) for one stream of calls, whose blocks each walk the whole
+// serial chain.
 template <int DT, bool MASK, bool OWN = false, int MINB = 3>
 __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char sm[];

@@ -80,11 +80,14 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 // Blocks per row.  Pipelined calls (early loads: the next call's loads overlap this one) are
-// throughput-bound, so a row goes to few blocks that each stream up to PIPELINED_BYTES of logits;
-// otherwise a call is latency-bound, so rows split into blocks of about LATENCY_BYTES, enough of
-// them to fill the GPU (but no block below MIN_CHUNK_ELEMS ids).  With STRATA_FLAG_CONCURRENT a
-// block streams up to STRATA_CONCURRENT_ROW_BYTES.
-constexpr int PIPELINED_BYTES = 128 * 1024;
+// throughput-bound, so a row goes to few blocks that each stream up to PIPELINED_BYTES of logits
+// (one stream of config-4 calls: 3.55 us per call over 20 calls and 2.37 over 200 with 4 blocks per
+// row, against 4.06 and 3.26 with 8); otherwise a call is latency-bound, so rows split into blocks
+// of about LATENCY_BYTES, enough of them to fill the GPU (but no block below MIN_CHUNK_ELEMS ids).
+// With STRATA_FLAG_CONCURRENT a block streams up to STRATA_CONCURRENT_ROW_BYTES, or RING_BYTES for
+// a call that keeps histories (it waits for the previous call before its penalties).
+constexpr int PIPELINED_BYTES = 256 * 1024;
+constexpr int RING_BYTES = 128 * 1024;
 constexpr int LATENCY_BYTES = 64 * 1024;
 constexpr int MIN_CHUNK_ELEMS = 2048;
 constexpr int RING_SLOTS = 4;                 // pieces in flight per CTA when shared memory allows
@@ -240,7 +243,8 @@ int shape_for(int max_cluster, int max_smem, int smem_three, int num_sms, int mo
   s->hash_cap = 0;
   s->hash_bits = 0;
   s->resident = false;
-  s->two = !concurrent && !pipelined;
+  // the register budget: two blocks per SM (no spills) unless calls of other groups stream alongside
+  s->two = !concurrent;
   if (mode == strata::MODE_SAMPLE && with_hist && lastn_max > 0) {
     int bits = 6;
     while ((1 << bits) < 2 * lastn_max) ++bits;
@@ -319,11 +323,11 @@ int compute_shape(const strata_ctx* c, int mode, int dtype, int B, int V, int to
   const bool pipelined = (flags & STRATA_FLAG_PDL) != 0u && (flags & STRATA_FLAG_EARLY_LOAD) != 0u &&
                          (flags & STRATA_FLAG_HISTORY_RING) == 0u && !verify;
   // the concurrency hint: a block streams up to STRATA_CONCURRENT_ROW_BYTES; a call that keeps
-  // histories waits for the previous call before its penalties and takes PIPELINED_BYTES (measured
+  // histories waits for the previous call before its penalties and takes RING_BYTES (measured
   // with 8 groups in flight: these were the fastest of the splits tried)
   int concurrent_bytes = 0;
   if ((flags & STRATA_FLAG_CONCURRENT) != 0u)
-    concurrent_bytes = (flags & STRATA_FLAG_HISTORY_RING) != 0u ? PIPELINED_BYTES
+    concurrent_bytes = (flags & STRATA_FLAG_HISTORY_RING) != 0u ? RING_BYTES
                                                                 : static_cast<int>(STRATA_CONCURRENT_ROW_BYTES);
   return shape_for(c->max_cluster, c->max_smem, c->smem_three, c->num_sms, mode, esz, B, V, kmax, top_n_eff,
                    max_lastn_penal(c),

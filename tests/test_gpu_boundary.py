@@ -233,8 +233,8 @@ def test_trace_lines_on_stderr():
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stderr.splitlines() if l.startswith("strata: sample_rows")]
     assert len(lines) == 3 and "V=32000" in lines[0] and "split=" in lines[0] and "smem=" in lines[0], r.stderr[-2000:]
-    # the latency shape takes the instance budgeted for two blocks per SM; the others three
-    assert [l.split("kernel=")[1].split()[0] for l in lines] == ["streaming-2", "streaming", "streaming"], lines
+    # one stream of calls takes the instance budgeted for two blocks per SM; the concurrency hint three
+    assert [l.split("kernel=")[1].split()[0] for l in lines] == ["streaming-2", "streaming", "streaming-2"], lines
 
 
 def test_own_outputs_after_a_waiting_call_take_counters_late():
