@@ -353,3 +353,45 @@ def test_logprobs_edge_cases(sampler):
         ref = oracle.logprobs_call(w)
         compare_logprobs(w, ref, g)
         assert sampler.errors() == 0x02 | 0x04     # out-of-range allowed and chosen ids flagged
+
+
+def _boundary_case():
+    """Rows built to sit on a top_p or draw boundary: the kernel's double-word fallbacks decide.
+
+    Row 0: two equal logits, top_p 0.5 (the first prefix reaches it exactly).  Row 1: three equal
+    logits, top_p = float32(2/3).  Rows 2-3: two survivors whose first cumulative weight equals the
+    row's Philox uniform u (temperature 1, then 0.7): d = T * ln(1/u - 1), rounded to float32, for a
+    position whose u is above 1/2 (the first survivor carries more than half the weight).
+    """
+    V, B = 1024, 4
+    logits = np.full((B, V), -100.0, np.float32)
+    logits[0, 10] = logits[0, 20] = 0.0
+    logits[1, 10] = logits[1, 20] = logits[1, 30] = 1.5
+    prm = {0: synth.make_params(temperature=1.0, top_k=8, top_p=0.5, seed=7),
+           1: synth.make_params(temperature=1.0, top_k=8, top_p=float(np.float32(2.0 / 3.0)), seed=8)}
+    pos = [100, 200, 0, 0]
+    for b, (T, seed) in ((2, (1.0, 9)), (3, (0.7, 10))):
+        p = 0
+        while oracle.row_uniform(seed, p, 0) <= 0.5:
+            p += 1
+        u = oracle.row_uniform(seed, p, 0)
+        pos[b] = p
+        logits[b, 10] = 0.0
+        logits[b, 20] = np.float32(T * np.log(1.0 / u - 1.0))
+        prm[b] = synth.make_params(temperature=T, top_k=2, seed=seed)
+    return synth._workload("boundary_rows", "f32", V, logits, prm, [0, 1, 2, 3], pos, [[], [], [], []], 3)
+
+
+def test_rows_on_a_boundary_take_the_exact_fallback(sampler):
+    """Every row sits within 1e-6 of a top_p or draw boundary (the oracle flags it): the kernel's
+    fp32 decision is within 1e-5 of the boundary, so its double-word sums decide, and the pick must
+    be one the oracle's draw makes for a top_p and a uniform within 1e-6 of the row's."""
+    w = _boundary_case()
+    set_slots(sampler, w)
+    rows, _ = oracle.sample_call(w)
+    assert all(r["flag_top_p"] or r["flag_draw"] for r in rows), [(r["flag_top_p"], r["flag_draw"]) for r in rows]
+    g = gpu_sample(sampler, w, with_allowed=False)
+    st = compare_sample(w, rows, g)
+    _check_no_errors(sampler)
+    assert st.flagged == 4
+    report("boundary rows", st)

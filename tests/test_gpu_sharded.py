@@ -203,3 +203,10 @@ def test_greedy_rows_with_penalties(sampler):
     for s in w["slot_params"]:
         w["slot_params"][s] = dict(w["slot_params"][s], penalty_repeat=1.7, penalty_freq=0.4, penalty_present=0.3)
     _run(sampler, w, [5000, 10000, 15000], "greedy penalised slices")
+
+
+def test_one_slice_is_the_whole_row(sampler):
+    """A single slice holding the whole vocabulary merges to the whole-row result (config 3's bf16
+    slots, greedy and sampled)."""
+    w = synth.config3()
+    _run(sampler, w, [], "config3 one slice")
