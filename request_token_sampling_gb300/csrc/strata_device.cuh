@@ -9,6 +9,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// Branch hints for the rarely taken fallbacks of the post-pass: the compiler lays the common path
+// out in one run, so a block fetches its instructions with fewer jumps.
+#define STRATA_LIKELY(x) __builtin_expect(!!(x), 1)
+#define STRATA_UNLIKELY(x) __builtin_expect(!!(x), 0)
+
 namespace strata {
 
 constexpr uint32_t FULL_MASK = 0xFFFFFFFFu;

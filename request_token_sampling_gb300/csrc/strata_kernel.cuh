@@ -366,14 +366,16 @@ template <int DT>
 constexpr int BATCH_VECS = DT == 0 ? 4 : 2;  // 16 elements
 
 // First pass over this thread's vectors of one piece, a batch of 16 elements at a time: the
-// running max `mx`, the batch `bmx` that holds it and the largest max `mx2` of the thread's other
+// running max `mx`, the batch `bmx` that holds it, the second batch maximum `mx2` and its batch
+// `bmx2`, the largest max `mx3` of the thread's other
 // batches, and the sum of exp(x - ref) in two partial sums.  The reference `ref` moves to the piece's max only when that
 // exceeds it by LAZY_SHIFT (or on the first finite piece), so the common piece costs one compare.
 // `slot` holds piece p (vectors p * PIECE_VECS ...) for the vectors below n_full; the ragged last
 // vector (n_full, when the chunk's bytes are not a multiple of 16) comes from global memory.
 template <int DT>
 __device__ __forceinline__ void pass1_piece(const unsigned char* slot, const unsigned char* gchunk, int p, int n_full,
-                                            int n_vec, int n_el, float& ref, float& mx, float& mx2, int& bmx, float& s0,
+                                            int n_vec, int n_el, float& ref, float& mx, float& mx2, float& mx3, int& bmx,
+                                            int& bmx2, float& s0,
                                             float& s1) {
   constexpr int EPV = 16 / (DT == 0 ? 4 : 2);
   constexpr int RB = BATCH_VECS<DT>;  // vectors held at once: one batch of 16 elements
@@ -398,12 +400,18 @@ __device__ __forceinline__ void pass1_piece(const unsigned char* slot, const uns
     for (int r = 0; r < RB; ++r)
 #pragma unroll
       for (int e = 0; e < EPV; ++e) pm = fmaxf(pm, x[r][e]);
-    if (pm > mx) {  // the batch holding the thread's max, and the best max of its other batches
+    if (pm > mx) {  // the two batches holding the thread's largest maxima, and the best of the rest
+      mx3 = mx2;
       mx2 = mx;
+      bmx2 = bmx;
       mx = pm;
       bmx = p * (VR / RB) + r0 / RB;
+    } else if (pm > mx2) {
+      mx3 = mx2;
+      mx2 = pm;
+      bmx2 = p * (VR / RB) + r0 / RB;
     } else {
-      mx2 = fmaxf(mx2, pm);
+      mx3 = fmaxf(mx3, pm);
     }
     if (pm > ref + LAZY_SHIFT) {
       const float f = (ref == -INFINITY) ? 0.0f : ex2_approx((ref - pm) * LOG2E);
@@ -1191,8 +1199,8 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
   }
 
   // ---- 1b. first pass as pieces land ----------------------------------------------------------
-  float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
-  int bmx = 0;
+  float ref = -INFINITY, mx = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY, s0 = 0.0f, s1 = 0.0f;
+  int bmx = 0, bmx2 = 0;
   // logits of this thread's first allowed and history ids, fetched once their ids have landed
   // (after the first piece) and used after the pass
   float aval[APRE], hval[HPRE];
@@ -1218,7 +1226,8 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
 #pragma unroll 1
     for (int p = 0; p < n_iter; ++p) {
       if (p < n_pieces) wait_bar(&mbar[si], ctl, P.err, false, ph);
-      pass1_piece<DT>(data + si * PIECE_BYTES, gchunk, p, n_full, n_vec, n_el, ref, mx, mx2, bmx, s0, s1);
+      pass1_piece<DT>(data + si * PIECE_BYTES, gchunk, p, n_full, n_vec, n_el, ref, mx, mx2, mx3, bmx, bmx2, s0,
+                      s1);
       if (p + nslot < n_pieces) {
         __syncwarp();
         if (lane == 0) {
@@ -1438,12 +1447,16 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
     const bool masked = mask_launch && a_end > a_beg && k_row > 0;
     const bool pen_from_t = k_row > 0 && !masked;
     const bool want = kall != 0u && kall >= T && (n_row > 0 || pen_from_t);
-    const bool whole = want && order_key(mx2) >= T;  // another batch also reaches T: a full rescan
-    if (want && !whole) {
+    const bool whole = want && order_key(mx3) >= T;  // a third batch also reaches T: a full rescan
+    const int n_bat = (want && !whole) ? (order_key(mx2) >= T ? 2 : 1) : 0;
+#pragma unroll 1
+    for (int q = 0; q < n_bat; ++q) {
       constexpr int RB = BATCH_VECS<DT>;
-      // every element at or above T sits in the batch that holds the max: scan its 16 elements
-      // straight-line (independent loads), then append the hits
-      const int vb = (bmx / (VR / RB)) * PIECE_VECS + (bmx % (VR / RB)) * RB * NT + tid;
+      // every element at or above T sits in the batch that holds the max (and the second batch,
+      // when its maximum reaches T): scan its 16 elements straight-line (independent loads), then
+      // append the hits
+      const int bq = q == 0 ? bmx : bmx2;
+      const int vb = (bq / (VR / RB)) * PIECE_VECS + (bq % (VR / RB)) * RB * NT + tid;
       uint32_t hit = 0u;
       float xf[RB * EPV];
 #pragma unroll
@@ -1474,7 +1487,7 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
       }
     }
     const uint32_t need = __ballot_sync(FULL_MASK, whole);
-    if (need != 0u)
+    if (STRATA_UNLIKELY(need != 0u))
       warp_rescan<DT>(gchunk, need, __ballot_sync(FULL_MASK, own_hist), wid, lane, n_vec, n_el, lo, Tf, htab,
                       P.hash_bits, ctl, cand_pen, cand_raw, cap, n_row > 0, pen_from_t);
     if (penal) {  // penalised ids: raw value for the raw list, penalised value for the other
@@ -1510,21 +1523,21 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
     // more candidates than the buffer holds (extreme ties): exact argmax rounds over the chunk
     // write its best k_row / n_row in order into the candidate buffers; more than RANK_LIMIT in
     // the buffer: argmax rounds over the buffer keep the best ones at its head
-    if (k_row > 0 && np > cap) {
+    if (STRATA_UNLIKELY(k_row > 0 && np > cap)) {
       if (MASK && masked)
         np = masked_rounds<DT>(gchunk, lo, hi, aid[0], aid[1], aid[2], aid[3], P.allowed, a_beg + tid + APRE * NT,
                                a_end, k_row, penal, htab, P.hash_bits, sp.rep, sp.freq, sp.pres, red64, cand_pen);
       else
         np = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 0, k_row, penal, htab, P.hash_bits, hflag, sp.rep, sp.freq,
                               sp.pres, red64, cand_pen, cand_raw);
-    } else if (k_row > 0 && np > RANK_LIMIT) {
+    } else if (STRATA_UNLIKELY(k_row > 0 && np > RANK_LIMIT)) {
       np = buffer_rounds(reinterpret_cast<uint32_t*>(cand_pen), 4, np, k_row, reinterpret_cast<uint32_t*>(sorted_pen),
                          red64);
     }
-    if (n_row > 0 && nr > cap)
+    if (STRATA_UNLIKELY(n_row > 0 && nr > cap))
       nr = exact_rounds<DT>(gchunk, n_vec, n_el, lo, 1, n_row, penal, htab, P.hash_bits, hflag, sp.rep, sp.freq,
                             sp.pres, red64, cand_pen, cand_raw);
-    else if (n_row > 0 && nr > RANK_LIMIT)
+    else if (STRATA_UNLIKELY(n_row > 0 && nr > RANK_LIMIT))
       nr = buffer_rounds(reinterpret_cast<uint32_t*>(cand_raw), 2, nr, n_row, reinterpret_cast<uint32_t*>(sorted_raw),
                          red64);
     if (k_row == 0) np = 0;
@@ -1668,7 +1681,7 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
       for (int f = half; f < tot_p; f += NT / 2) {
         uint4 ent;
         int rank;
-        if (tot_p <= cap - 8) {
+        if (STRATA_LIKELY(tot_p <= cap - 8)) {
           ent = cand_pen[f];
           rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_pen), 4, (tot_p + 7) & ~7,
                            (static_cast<uint64_t>(ent.y) << 32) | ent.x);
@@ -1688,7 +1701,7 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
       for (int f = half; f < tot_r; f += NT / 2) {
         uint64_t key;
         int rank;
-        if (tot_r <= cap - 8) {
+        if (STRATA_LIKELY(tot_r <= cap - 8)) {
           key = cand_raw[f];
           rank = rank_desc(reinterpret_cast<const uint32_t*>(cand_raw), 2, (tot_r + 7) & ~7, key);
         } else {
@@ -1835,7 +1848,7 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
     if (P.topk_vals != nullptr) P.topk_vals[static_cast<long long>(row) * KMAX + tid] = __int_as_float(0x7FC00000);
   }
   if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
-  if (ctl[CTL_TIMEOUT] != 0u) {
+  if (STRATA_UNLIKELY(ctl[CTL_TIMEOUT] != 0u)) {
     // a wait ran out: a copy, or another CTA's stores into this one, may still be on the way, so
     // wait for each once more (bounded) before the CTA leaves
     for (int si = 0; si < min(nslot, n_pieces); ++si) {
