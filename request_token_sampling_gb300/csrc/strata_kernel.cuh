@@ -149,7 +149,7 @@ __device__ __forceinline__ int slice_id(int id, int off) {
 }
 
 struct Layout {
-  uint32_t data, mbar, abits, mbits, hash, hraw, hflag, wkey, red, ctl, xrec;
+  uint32_t data, mbar, abits, mbits, hash, hraw, hflag, wkey, red, ctl, sps, xrec;
   uint32_t cand_pen, cand_raw, recv_cnt, recv_pkey, recv_praw, recv_raw, sorted_pen, sorted_raw, total;
   int cand_cap;  // entries of each candidate list (they live in the ring once the first pass is done)
 };
@@ -190,6 +190,8 @@ __host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, i
   L.ctl = o;
   o += CTL_WORDS * 4;
   o = align_up(o, 16);
+  L.sps = o;  // the row's slot keys: one copy for the block instead of registers in every thread
+  o += static_cast<uint32_t>(sizeof(SlotDev));
   L.xrec = o;
   o += static_cast<uint32_t>(cs * xrec_words(qw)) * 4;
   L.recv_cnt = o;
@@ -211,7 +213,7 @@ __host__ __device__ inline Layout make_layout(int chunk, int hash_cap, int cs, i
 
 // Every region starts on a 16-byte boundary (vector and bulk accesses rely on it).
 __host__ __device__ inline bool layout_aligned(const Layout& L) {
-  const uint32_t r[] = {L.data, L.mbar, L.abits, L.mbits, L.hash, L.hraw, L.hflag, L.wkey, L.red, L.ctl, L.xrec,
+  const uint32_t r[] = {L.data, L.mbar, L.abits, L.mbits, L.hash, L.hraw, L.hflag, L.wkey, L.red, L.ctl, L.sps, L.xrec,
                         L.cand_pen, L.cand_raw, L.recv_cnt, L.recv_pkey, L.recv_praw, L.recv_raw, L.sorted_pen,
                         L.sorted_raw};
   for (uint32_t x : r)
@@ -1134,18 +1136,31 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
   cluster_arrive_relaxed();  // this CTA is running (remote stores wait for every CTA, below)
 
   // ---- row metadata, second level ------------------------------------------------------------
+  // the slot's keys: the three the set-up needs in registers, the rest read from the block's one
+  // copy in shared memory (written by thread 0, read after the next barrier)
   bool valid = true;
-  SlotDev sp{};
+  uint32_t sp_flags = 0u;
+  int sp_k = 0, sp_last_n = 0;
+  SlotDev* const sps = reinterpret_cast<SlotDev*>(sm + L.sps);
   if (P.mode == MODE_SAMPLE) {
     valid = static_cast<unsigned>(slot) < static_cast<unsigned>(P.max_slots);
-    if (valid) sp = P.slots[slot];
+    if (valid) {
+      const SlotDev* g = P.slots + slot;
+      sp_flags = g->flags;
+      sp_k = g->k;
+      sp_last_n = g->last_n;
+      if (tid == 0) *sps = *g;
+    } else if (tid == 0) {
+      *sps = SlotDev{};
+    }
   }
-  const bool sampled = valid && (sp.flags & SLOT_SAMPLED);
-  const int k_row = (P.mode == MODE_SAMPLE && valid) ? min(max(sp.k, 1), P.kmax) : 0;
+  const SlotDev& sp = *sps;
+  const bool sampled = valid && (sp_flags & SLOT_SAMPLED);
+  const int k_row = (P.mode == MODE_SAMPLE && valid) ? min(max(sp_k, 1), P.kmax) : 0;
   const int n_row = P.nmax;
   const int kp = max(k_row, n_row);
   const bool kept_hist = P.ring != nullptr;
-  const bool penal = (P.mode == MODE_SAMPLE) && valid && (sp.flags & SLOT_PENAL) && P.hash_cap > 0 &&
+  const bool penal = (P.mode == MODE_SAMPLE) && valid && (sp_flags & SLOT_PENAL) && P.hash_cap > 0 &&
                      (kept_hist || (P.hist_off != nullptr && slot < P.n_hist_slots));
   // the window: ids hb[(h_start + i) & h_mask] for i < h_len (a caller's CSR row, or the slot's ring)
   int h_len = 0;
@@ -1158,7 +1173,7 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
       h_mask = STRATA_HISTORY_CAP - 1;
     } else {
       const int hs = P.hist_off[slot], he = P.hist_off[slot + 1];
-      h_len = min(sp.last_n, max(0, he - hs));
+      h_len = min(sp_last_n, max(0, he - hs));
       h_start = static_cast<uint32_t>(he - h_len);
     }
   }
@@ -1280,7 +1295,7 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
   if (penal && kept_hist) {
     if (early) grid_dep_wait();
     const unsigned long long n = P.hlen[slot];
-    h_len = static_cast<int>(min(static_cast<unsigned long long>(sp.last_n), n));
+    h_len = static_cast<int>(min(static_cast<unsigned long long>(sp_last_n), n));
     h_start = static_cast<uint32_t>(n - static_cast<unsigned long long>(h_len)) & h_mask;
   }
   if (penal) {
@@ -1847,7 +1862,7 @@ __global__ void __launch_bounds__(NT, MINB) rows_kernel(const KParams P) {
     P.topk_ids[static_cast<long long>(row) * KMAX + tid] = -1;
     if (P.topk_vals != nullptr) P.topk_vals[static_cast<long long>(row) * KMAX + tid] = __int_as_float(0x7FC00000);
   }
-  if (P.mode == MODE_SAMPLE && valid && sp.k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
+  if (P.mode == MODE_SAMPLE && valid && sp_k > P.kmax && crank == 0 && tid == 0) atomicOr(P.err, STRATA_DEVERR_SHAPE);
   if (STRATA_UNLIKELY(ctl[CTL_TIMEOUT] != 0u)) {
     // a wait ran out: a copy, or another CTA's stores into this one, may still be on the way, so
     // wait for each once more (bounded) before the CTA leaves
