@@ -116,6 +116,84 @@ def test_record_exchange_gloo_world2():
         assert abs(chosen_lp - r["chosen_lp"]) <= 1e-5
 
 
+class _OracleSlices:
+    """A stand-in for a rank's Sampler on CPU: `shard` packs the oracle's records of the rank's slice
+    in the library's layout, `merge` reads the gathered records back and merges them with the
+    oracle, so `sample_sliced` runs its real exchange between the two."""
+
+    def __init__(self, w):
+        self.w = w
+
+    def shard(self, logits, row_slot, id_offset, hist=None, hist_off=None, top_n=0, flags=0, stream=None):
+        import oracle
+        import torch
+        from request_token_sampling_gb300 import STRATA_SHARD_RECORD_BYTES
+        w = self.w
+        out = np.zeros((w["B"], STRATA_SHARD_RECORD_BYTES), np.uint8)
+        for b in range(w["B"]):
+            s = int(w["row_slot"][b])
+            p = oracle.Params.from_dict(w["slot_params"][s])
+            raw = np.asarray(logits[b].numpy(), np.float32)
+            rec = oracle.shard_record(raw, id_offset, p, oracle.sampling._slot_history(w, s),
+                                      1 if p.greedy else p.k, top_n)
+            out[b] = np.frombuffer(pack_record(rec, STRATA_SHARD_RECORD_BYTES), np.uint8)
+        return torch.from_numpy(out)
+
+    def merge(self, allrec, row_slot, row_pos, top_n=0, chosen_lp=False, stream=None):
+        import oracle
+        from request_token_sampling_gb300.sharded import unpack_record
+        w, a = self.w, allrec.numpy()
+        ids = []
+        for b in range(w["B"]):
+            s = int(w["row_slot"][b])
+            p = oracle.Params.from_dict(w["slot_params"][s])
+            recs = [unpack_record(a[g, b].tobytes()) for g in range(a.shape[0])]
+            ids.append(oracle.merge_records(recs, p, int(w["row_pos"][b]), int(w["counters"].get(s, 0)), top_n)["id"])
+        return {"ids": ids}
+
+
+def _sliced_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import synth
+    from request_token_sampling_gb300.sharded import sample_sliced
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = synth.config3()                       # bf16 batch slots, greedy and sampled
+        import oracle
+        raw = np.stack([oracle.widen(w["logits"][b, :w["V"]], w["dtype"]) for b in range(w["B"])])
+        cut = [0, 100000, w["V"]]
+        part = torch.from_numpy(np.ascontiguousarray(raw[:, cut[rank]:cut[rank + 1]]))
+        out = sample_sliced(_OracleSlices(w), part, cut[rank], None, None, top_n=w["top_n"])
+        q.put((rank, [int(x) for x in out["ids"]]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sample_sliced_over_gloo_world2():
+    """`sample_sliced` on two gloo ranks, each holding part of config 3's rows: both ranks return
+    the whole-row oracle's picks."""
+    _build()
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_sliced_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=300) for _ in procs), key=lambda r: r[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    rows, _ = oracle.sample_call(synth.config3(), with_allowed=False)
+    assert res[0][1] == res[1][1] == [r["id"] for r in rows]
+
+
 def test_pack_unpack_round_trip():
     """The package's reader inverts the documented layout, -0.0 read as +0.0, for every sign."""
     _build()
