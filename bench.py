@@ -382,7 +382,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32(penalty,ranking)+f64",
             "data": "synthetic", "config": {"workload": DESCRIPTIONS[args.workload].replace("{G}", str(args.slices)),
-                                            "rows_per_step": w["B"]},
+                                            "rows_per_step": w["B"], "V": w["V"], "logits_dtype": w["dtype"]},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{args.steps} timed whole {w['B']}-row calls on 1 host core"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -59,3 +59,25 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "3", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_line_on_rank0():
+    """Rank 0 of the reference arm times whole calls of the oracle and prints one JSON line with the
+    GPU arm's metric, unit and workload keys, a cpu_baseline that is the line itself, and an e2e
+    object that moves no bytes."""
+    import json
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "config1",
+                        "--steps", "3", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["config"]["rows_per_step"] == 1 and d["config"]["V"] == 32000 and d["config"]["logits_dtype"] == "f32"
+    assert d["value"] > 0 and abs(d["value"] - 3 / (d["ms_per_step"] * 3 / 1e3)) / d["value"] < 1e-9
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
