@@ -34,10 +34,17 @@ def sample_sliced(sampler, logits, id_offset: int, row_slot, row_pos, hist=None,
                   chosen_lp: bool = False, group=None, flags: int = 0, stream=None) -> dict:
     """One sampling step over rows whose vocabulary is split across the group's ranks: this rank's
     columns hold ids id_offset .. id_offset + logits.shape[1] - 1.  Returns the merged outputs
-    (identical on every rank)."""
+    (identical on every rank).  `stream` (a torch CUDA stream or a raw cudaStream_t handle; None:
+    the current stream) orders the slice launch, the all-gather and the merge one after another."""
     rec = sampler.shard(logits, row_slot, id_offset, hist=hist, hist_off=hist_off, top_n=top_n, flags=flags,
                         stream=stream)
-    allrec = gather_records(rec, group)
+    if stream is None:
+        allrec = gather_records(rec, group)
+    else:
+        import torch
+        ts = torch.cuda.ExternalStream(stream) if isinstance(stream, int) else stream
+        with torch.cuda.stream(ts):     # the collective waits for the slice launch on this stream
+            allrec = gather_records(rec, group)
     return sampler.merge(allrec, row_slot, row_pos, top_n=top_n, chosen_lp=chosen_lp, stream=stream)
 
 
