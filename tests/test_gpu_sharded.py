@@ -210,3 +210,40 @@ def test_one_slice_is_the_whole_row(sampler):
     slots, greedy and sampled)."""
     w = synth.config3()
     _run(sampler, w, [], "config3 one slice")
+
+
+def test_sample_sliced_one_rank_nccl(sampler):
+    """`sharded.sample_sliced` through a one-rank NCCL group on a side stream: the slice launch,
+    the all-gather and the merge run in order on the GPU, and the picks and log-probabilities equal
+    the whole-row call's (config 4's rows, the whole vocabulary as the one slice)."""
+    import os
+    import torch.distributed as dist
+    from request_token_sampling_gb300.sharded import sample_sliced
+    if not dist.is_available() or not dist.is_nccl_available():
+        pytest.skip("torch.distributed without NCCL")
+    w = synth.config4(fused=True)
+    V, top_n = w["V"], w["top_n"]
+    set_slots(sampler, w)
+    d = upload(w)
+    whole = sampler.sample(d["logits"], d["row_slot"], d["row_pos"], V=V, hist=d["hist"], hist_off=d["hist_off"],
+                           top_n=top_n, chosen_lp=True)
+    torch.cuda.synchronize()
+    whole = {k: v.cpu().numpy() for k, v in whole.items()}
+    set_slots(sampler, w)
+    os.environ["NCCL_NVLS_ENABLE"] = "0"
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1)
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        out = sample_sliced(sampler, d["logits"][:, :V], 0, d["row_slot"], d["row_pos"], hist=d["hist"],
+                            hist_off=d["hist_off"], top_n=top_n, chosen_lp=True, stream=side)
+        side.synchronize()
+        got = {k: v.cpu().numpy() for k, v in out.items()}
+    finally:
+        dist.destroy_process_group()
+    assert sampler.errors() == 0
+    assert got["ids"].tolist() == whole["ids"].tolist()
+    assert got["top_ids"].tolist() == whole["top_ids"].tolist()
+    assert np.max(np.abs(got["top_lps"] - whole["top_lps"])) <= 2 * LP_TOL
+    assert np.max(np.abs(got["chosen_lp"] - whole["chosen_lp"])) <= 2 * LP_TOL
