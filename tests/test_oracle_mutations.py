@@ -59,6 +59,18 @@ MUTATIONS = [
     ("sampling.py", "pen = sorted((e for r in records for e in r[\"pen\"]), key=lambda e: (-e[0], e[1]))",
      "pen = sorted((e for r in records for e in r[\"pen\"]), key=lambda e: (-e[0], -e[1]))"),
     ("sampling.py", "            if t >= v0:\n                counts[t - v0] = c", "            if t >= v0:\n                counts[t - v0] = 1"),
+    ("sampling.py", "res.update(id=int(order[0]), topk_ids=order[:1].copy()",
+     "res.update(id=int(rank_order(raw32)[0]), topk_ids=order[:1].copy()"),
+    ("sampling.py", "    if tp <= 0.0:\n        return 1, False", "    if tp <= 0.0:\n        return m1, False"),
+    ("sampling.py", "lse_a = m + np.log(np.sum(np.exp(l[uniq] - m)))", "lse_a = m + np.log(np.sum(np.exp(l - m)))"),
+    ("sampling.py", "        if 0 <= t < V:\n            counts[t]", "        if t < V:\n            counts[t]"),
+    ("sampling.py", "np.float32(p.penalty_repeat) == 1 and np.float32(p.penalty_freq) == 0",
+     "np.float32(p.penalty_repeat) == 1 or np.float32(p.penalty_freq) == 0"),
+    ("sampling.py", "return dict(pen=[(float(pen[i]), v0 + int(i), float(raw[i])) for i in op],",
+     "return dict(pen=[(float(pen[i]), int(i), float(raw[i])) for i in op],"),
+    ("sampling.py", "    orr = rank_order(raw)[:top_n]", "    orr = rank_order(pen)[:top_n]"),
+    ("sampling.py", "    order = rank_order(raw32)[:n]", "    order = rank_order(raw32)[1:n + 1]"),
+    ("sampling.py", "    k = min(p.k, order.size)", "    k = min(p.k, order.size) - 1"),
 ]
 
 
