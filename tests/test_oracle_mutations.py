@@ -71,6 +71,13 @@ MUTATIONS = [
     ("sampling.py", "    orr = rank_order(raw)[:top_n]", "    orr = rank_order(pen)[:top_n]"),
     ("sampling.py", "    order = rank_order(raw32)[:n]", "    order = rank_order(raw32)[1:n + 1]"),
     ("sampling.py", "    k = min(p.k, order.size)", "    k = min(p.k, order.size) - 1"),
+    ("sampling.py", "        if not p.greedy:\n            sampled_slots.add(s)", "        sampled_slots.add(s)"),
+    ("sampling.py", "int(w[\"row_pos\"][b]), counters.get(s, 0), mask)", "int(w[\"row_pos\"][b]), counters.get(s, 0) + b, mask)"),
+    ("sampling.py", "        if d < 0 or t < 0 or t != d:", "        if t != d:"),
+    ("sampling.py", "float(lp[chosen]) if 0 <= chosen < V else", "float(lp[chosen]) if chosen < V else"),
+    ("sampling.py", "m = min(len(h), HISTORY_RING_CAP, max(0, int(max_n)))", "m = min(len(h), max(0, int(max_n)))"),
+    ("sampling.py", "    m = np.max(l)\n    lse = m + np.log(np.sum(np.exp(l - m)))\n    return l - lse",
+     "    m = np.max(l)\n    lse = m + np.log(np.sum(np.exp(l - m)))\n    return l - m"),
 ]
 
 

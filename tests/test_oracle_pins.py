@@ -348,6 +348,17 @@ def test_logprobs_top_n_padding():
     assert np.isneginf(res["top_lps"][3:]).all()
 
 
+def test_logprobs_chosen_outside_the_vocabulary():
+    """An id outside [0, V) is no vocabulary entry and has no log-probability (NaN), at either end;
+    the ends inside have the closed form log(e^l / sum e^l)."""
+    row = np.array([1.0, 2.0, 3.0], f32)
+    for c in (-1, -3, 3, 10):
+        assert math.isnan(oracle.logprobs_row(row, c, 0)["chosen_lp"])
+    z = math.log(math.e + math.e ** 2 + math.e ** 3)
+    assert abs(oracle.logprobs_row(row, 0, 0)["chosen_lp"] - (1.0 - z)) < 1e-12
+    assert abs(oracle.logprobs_row(row, 2, 0)["chosen_lp"] - (3.0 - z)) < 1e-12
+
+
 # ----------------------------------------------------------------------------- full chain
 def test_feature_visibility_config1():
     """Each feature of the single-row request changes the oracle's answer when it is switched on."""
@@ -725,6 +736,8 @@ def test_history_tail_capacity():
     assert oracle.HISTORY_RING_CAP == 4096
     t, n = oracle.history_tail(st, 0, 10)
     assert t.tolist() == list(range(4990, 5000))
+    t, n = oracle.history_tail(st, 0, 10 ** 6)                   # a ring of 4096 ids holds no more
+    assert n == 5000 and t.tolist() == list(range(5000 - 4096, 5000))
     assert oracle.history_tail(st, 1)[0].tolist() == [3, 4]
     assert oracle.history_tail(st, 5)[0].size == 0 and oracle.history_tail(st, 5)[1] == 0
     assert oracle.history_tail(st, 1, 0)[0].size == 0
