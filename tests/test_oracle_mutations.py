@@ -39,6 +39,10 @@ MUTATIONS = [
     ("philox.py", "(position & MASK32, position >> 32, counter & MASK32, counter >> 32)",
      "(counter & MASK32, counter >> 32, position & MASK32, position >> 32)"),
     ("philox.py", "return (out[0] >> 8) * (2.0 ** -24)", "return (out[1] >> 8) * (2.0 ** -24)"),
+    ("philox.py", "    for _ in range(10):", "    for _ in range(9):"),
+    ("philox.py", "(seed & MASK32, seed >> 32))", "(seed >> 32, seed & MASK32))"),
+    ("philox.py", "        k1 = (k1 + PHILOX_W32_1) & MASK32", "        k1 = (k1 + PHILOX_W32_0) & MASK32"),
+    ("philox.py", "return (out[0] >> 8) * (2.0 ** -24)", "return (out[0] & 0xFFFFFF) * (2.0 ** -24)"),
     ("sampling.py", "        if not open_[s]:\n            continue\n", ""),
     ("sampling.py", "        keep[s] += 1\n        if d < 0 or t < 0 or t != d:\n            open_[s] = False",
      "        if d < 0 or t < 0 or t != d:\n            open_[s] = False\n        else:\n            keep[s] += 1"),
