@@ -75,6 +75,11 @@ MUTATIONS = [
     ("sampling.py", "    orr = rank_order(raw)[:top_n]", "    orr = rank_order(pen)[:top_n]"),
     ("sampling.py", "    order = rank_order(raw32)[:n]", "    order = rank_order(raw32)[1:n + 1]"),
     ("sampling.py", "    k = min(p.k, order.size)", "    k = min(p.k, order.size) - 1"),
+    ("sampling.py", "lse = float(m + np.log(np.sum(np.exp(l - m)))) if n and",
+     "lse = float(np.log(np.sum(np.exp(l - m)))) if n and"),
+    ("sampling.py", "raw = sorted((e for r in records for e in r[\"raw\"]), key=lambda e: (-e[0], e[1]))",
+     "raw = sorted((e for r in records for e in r[\"raw\"]), key=lambda e: (e[0], e[1]))"),
+    ("sampling.py", "k = 1 if p.greedy else min(p.k, len(pen))", "k = min(p.k, len(pen))"),
     ("sampling.py", "        if not p.greedy:\n            sampled_slots.add(s)", "        sampled_slots.add(s)"),
     ("sampling.py", "int(w[\"row_pos\"][b]), counters.get(s, 0), mask)", "int(w[\"row_pos\"][b]), counters.get(s, 0) + b, mask)"),
     ("sampling.py", "        if d < 0 or t < 0 or t != d:", "        if t != d:"),
