@@ -5,6 +5,7 @@ or extra term, a flipped sign or comparison, a wrong index or word, the cuts in 
 The test copies ``oracle/``, ``synth/`` and ``tests/`` to a temporary folder, plants one mistake,
 runs ``test_oracle_pins.py`` there and requires it to fail.  Nothing here touches a GPU.
 """
+import concurrent.futures
 import os
 import shutil
 import subprocess
@@ -90,16 +91,34 @@ MUTATIONS = [
 ]
 
 
-@pytest.mark.parametrize("fn,old,new", MUTATIONS, ids=[f"{m[0]}:{i}" for i, m in enumerate(MUTATIONS)])
-def test_planted_mistake_is_caught(tmp_path, fn, old, new):
-    for d in ("oracle", "synth", "tests"):
-        shutil.copytree(os.path.join(ROOT, d), tmp_path / d,
-                        ignore=shutil.ignore_patterns("__pycache__", "*.pyc"))
-    target = tmp_path / "oracle" / fn
+def _run_mutant(base, i):
+    """Plant mutation i in a fresh copy and run the pin suite there: (anchor found, exit code)."""
+    fn, old, new = MUTATIONS[i]
+    d = base / f"m{i}"
+    for sub in ("oracle", "synth", "tests"):
+        shutil.copytree(os.path.join(ROOT, sub), d / sub, ignore=shutil.ignore_patterns("__pycache__", "*.pyc"))
+    target = d / "oracle" / fn
     src = target.read_text()
-    assert old in src, "mutation anchor vanished from the oracle"
+    if old not in src:
+        return False, None
     target.write_text(src.replace(old, new))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        str(tmp_path / "tests" / "test_oracle_pins.py")],
-                       cwd=tmp_path, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"planted mistake survived: {new!r}"
+                        str(d / "tests" / "test_oracle_pins.py")],
+                       cwd=d, capture_output=True, text=True, timeout=600)
+    return True, r.returncode
+
+
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """Every mutant's outcome, the pin suites run a few at a time (each is its own process)."""
+    base = tmp_path_factory.mktemp("mutants")
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(lambda i: _run_mutant(base, i), range(len(MUTATIONS))))
+
+
+@pytest.mark.parametrize("i", range(len(MUTATIONS)), ids=[f"{m[0]}:{i}" for i, m in enumerate(MUTATIONS)])
+def test_planted_mistake_is_caught(outcomes, i):
+    found, rc = outcomes[i]
+    assert found, "mutation anchor vanished from the oracle"
+    assert rc != 0, f"planted mistake survived: {MUTATIONS[i][2]!r}"
